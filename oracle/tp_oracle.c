@@ -1,0 +1,475 @@
+/*
+ * tp_oracle.c - plain, slow fp64 CPU oracle for the tensor-parallel MLP.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline / reference leg load this library.  It shares no code with the
+ * CUDA path and the CUDA path never calls it.
+ *
+ * What it computes, and where the pages state it:
+ *   - Column-parallel first layer: W1 split along its output (column)
+ *     dimension, Y_i = act(X W1_i), X replicated, no exchange afterwards
+ *     ("Tensor Parallelism in Action: Megatron-LM Matrix Splitting",
+ *     section 1, "Column Parallel (W1)"; "Tensor parallelism" guide, section
+ *     "Concept").
+ *   - The activation is applied per shard because it is elementwise:
+ *     GeLU([y1 | y2]) = [GeLU(y1) | GeLU(y2)] ("Tensor Parallelism in
+ *     Action", section 2, interview question 2).
+ *   - Row-parallel second layer: W2 split along its input (row) dimension,
+ *     Z_i = Y_i W2_i are partial products ("Tensor Parallelism in Action",
+ *     section 1, "Row Parallel (W2)"; "Slice the matrix itself", section
+ *     "Column-Parallel & Row-Parallel GEMMs").
+ *   - All-reduce-sum of the partials, Z = sum_i Z_i ("Slice the matrix
+ *     itself", section "Mathematical formulation - row-parallel matrix
+ *     multiplication summation"; "Tensor Parallelism in Action", section 1,
+ *     "Output Combination").
+ *   - Attention: heads are sharded across ranks ("Tensor parallelism" guide,
+ *     section "Walking through a transformer block"), so the QKV projection
+ *     is column-parallel by head and the output projection row-parallel.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - GeLU is the exact form 0.5 y (1 + erf(y / sqrt 2)).
+ *   - SwiGLU ("Gate/Up" in "Slice the matrix itself") is SiLU(g) * u with
+ *     SiLU(g) = g / (1 + exp(-g)); W1 is given as [Wg | Wu] ([H x 2F], gate
+ *     first) and shard i takes the SAME columns of Wg and of Wu.
+ *   - QKV weights are [Wq | Wk | Wv], each [H x H], head h in columns
+ *     [h*hd, (h+1)*hd); shard i takes heads [i*nh/T, (i+1)*nh/T) of all three.
+ *   - Shards are equal: F % T == 0 and n_heads % T == 0, else an error.
+ *   - The all-reduce sum runs over shards in ascending order, left to right.
+ *
+ * Everything is fp64 on the exact input values: float32 and bfloat16 inputs
+ * are widened exactly.  Loops are the plain definitions; OpenMP only splits
+ * independent output rows between threads.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+#define ORC_GELU 0
+#define ORC_SWIGLU 1
+#define ORC_IDENTITY 2
+
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_INDIVISIBLE 2
+#define ORC_ERR_OOM 5
+
+/* ---- element access ---------------------------------------------------- */
+
+size_t orc_elem_bytes(int dt) { return dt == ORC_BF16 ? 2u : 4u; }
+
+/* Exact value of element idx of an array of float32 or bfloat16 (the upper
+ * 16 bits of a float32). */
+double orc_value(const void *base, int64_t idx, int dt)
+{
+    float f;
+    if (dt == ORC_F32) {
+        f = ((const float *)base)[idx];
+    } else {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+        memcpy(&f, &bits, sizeof f);
+    }
+    return (double)f;
+}
+
+/* ---- activations ------------------------------------------------------- */
+
+/* GeLU(y) = y * Phi(y), Phi the standard normal CDF, via erf. */
+double orc_gelu(double y) { return 0.5 * y * (1.0 + erf(y / sqrt(2.0))); }
+
+/* SiLU(g) = g * sigmoid(g). */
+double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ---- shard partition (bit copies) -------------------------------------- */
+
+/* Column block i of W1 (which = 0), or, for SwiGLU, of the gate half
+ * (which = 0) or the up half (which = 1), as a row-major [H x F/T] array.
+ * W1 is [H x F] (GeLU, identity) or [H x 2F] = [Wg | Wu] (SwiGLU). */
+int orc_shard_w1(const void *W1, int dt, int64_t H, int64_t F, int T, int act,
+                 int i, int which, void *out)
+{
+    if (!W1 || !out || H <= 0 || F <= 0 || T <= 0 || i < 0 || i >= T)
+        return ORC_ERR_ARG;
+    if (F % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (which != 0 && !(act == ORC_SWIGLU && which == 1))
+        return ORC_ERR_ARG;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t Fs = F / T;
+    const int64_t ld = (act == ORC_SWIGLU) ? 2 * F : F;
+    const int64_t col0 = (int64_t)which * F + (int64_t)i * Fs;
+    for (int64_t k = 0; k < H; ++k)
+        for (int64_t c = 0; c < Fs; ++c)
+            memcpy((char *)out + (size_t)(k * Fs + c) * eb,
+                   (const char *)W1 + (size_t)(k * ld + col0 + c) * eb, eb);
+    return ORC_OK;
+}
+
+/* Row block i of W2 ([F x H]) as a row-major [F/T x H] array. */
+int orc_shard_w2(const void *W2, int dt, int64_t F, int64_t H, int T, int i, void *out)
+{
+    if (!W2 || !out || H <= 0 || F <= 0 || T <= 0 || i < 0 || i >= T)
+        return ORC_ERR_ARG;
+    if (F % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t Fs = F / T;
+    for (int64_t r = 0; r < Fs; ++r)
+        for (int64_t c = 0; c < H; ++c)
+            memcpy((char *)out + (size_t)(r * H + c) * eb,
+                   (const char *)W2 + (size_t)((i * Fs + r) * H + c) * eb, eb);
+    return ORC_OK;
+}
+
+/* Heads of shard i from each of Wq, Wk, Wv: Wqkv is [H x 3H] = [Wq|Wk|Wv];
+ * out is [H x 3*W] with W = (n_heads/T)*head_dim, holding the Wq columns,
+ * then the Wk columns, then the Wv columns of those heads. */
+int orc_shard_wqkv(const void *Wqkv, int dt, int64_t H, int n_heads, int head_dim,
+                   int T, int i, void *out)
+{
+    if (!Wqkv || !out || H <= 0 || n_heads <= 0 || head_dim <= 0 || T <= 0 ||
+        i < 0 || i >= T || (int64_t)n_heads * head_dim != H)
+        return ORC_ERR_ARG;
+    if (n_heads % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t W = (int64_t)(n_heads / T) * head_dim;
+    for (int64_t k = 0; k < H; ++k)
+        for (int p = 0; p < 3; ++p)
+            for (int64_t c = 0; c < W; ++c)
+                memcpy((char *)out + (size_t)(k * 3 * W + p * W + c) * eb,
+                       (const char *)Wqkv + (size_t)(k * 3 * H + p * H + i * W + c) * eb, eb);
+    return ORC_OK;
+}
+
+/* Rows of Wo ([H x H], input dim = heads side by side) that belong to the
+ * heads of shard i: out is [W x H], W = (n_heads/T)*head_dim. */
+int orc_shard_wo(const void *Wo, int dt, int64_t H, int n_heads, int head_dim,
+                 int T, int i, void *out)
+{
+    if (!Wo || !out || H <= 0 || n_heads <= 0 || head_dim <= 0 || T <= 0 ||
+        i < 0 || i >= T || (int64_t)n_heads * head_dim != H)
+        return ORC_ERR_ARG;
+    if (n_heads % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t W = (int64_t)(n_heads / T) * head_dim;
+    memcpy(out, (const char *)Wo + (size_t)(i * W * H) * eb, (size_t)(W * H) * eb);
+    return ORC_OK;
+}
+
+/* ---- dense building blocks --------------------------------------------- */
+
+/* One output row of a plain linear layer: out[c] = sum_k a[k] * W[k][c],
+ * W row-major [K x N] with leading dimension ldw, starting at column col0.
+ * a is a row of A (element offset a0, element type dt). */
+static void row_times_matrix(const void *A, int64_t a0, int dt, int64_t K,
+                             const void *W, int64_t ldw, int64_t col0, int64_t N,
+                             double *out)
+{
+    for (int64_t c = 0; c < N; ++c)
+        out[c] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = orc_value(A, a0 + k, dt);
+        for (int64_t c = 0; c < N; ++c)
+            out[c] += a * orc_value(W, k * ldw + col0 + c, dt);
+    }
+}
+
+/* Same, with the row given as fp64 values. */
+static void drow_times_matrix(const double *a, int64_t K, const void *W, int dt,
+                              int64_t N, double *out)
+{
+    for (int64_t c = 0; c < N; ++c)
+        out[c] = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t c = 0; c < N; ++c)
+            out[c] += a[k] * orc_value(W, k * N + c, dt);
+}
+
+static int check_rows(const int64_t *rows, int64_t n_rows, int64_t M)
+{
+    if (n_rows < 0 || (n_rows > 0 && !rows))
+        return ORC_ERR_ARG;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= M)
+            return ORC_ERR_ARG;
+    return ORC_OK;
+}
+
+/* Activation of one row of first-layer products y (F values, or 2F = [g|u]
+ * for SwiGLU) into h (F values). */
+static void activate_row(const double *y, int64_t F, int act, double *h)
+{
+    for (int64_t c = 0; c < F; ++c) {
+        if (act == ORC_GELU)
+            h[c] = orc_gelu(y[c]);
+        else if (act == ORC_SWIGLU)
+            h[c] = orc_silu(y[c]) * y[F + c];
+        else
+            h[c] = y[c];
+    }
+}
+
+/* Plain linear layer on selected rows: out[r][c] = sum_k A[rows[r]][k] W[k][c],
+ * A [M x K], W [K x N]. */
+int orc_linear(const void *A, const void *W, int dt, int64_t M, int64_t K, int64_t N,
+               const int64_t *rows, int64_t n_rows, double *out)
+{
+    if (!A || !W || !out || M <= 0 || K <= 0 || N <= 0)
+        return ORC_ERR_ARG;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r)
+        row_times_matrix(A, rows[r] * K, dt, K, W, N, 0, N, out + r * N);
+    return ORC_OK;
+}
+
+/* ---- the MLP ----------------------------------------------------------- */
+
+/* Unsharded first layer on selected rows: Y[r] = act(X[rows[r]] W1), F values
+ * per row (for SwiGLU, SiLU(X Wg) * (X Wu)). */
+int orc_colpar_full(const void *X, const void *W1, int dt, int64_t M, int64_t H,
+                    int64_t F, int act, const int64_t *rows, int64_t n_rows, double *Y)
+{
+    if (!X || !W1 || !Y || M <= 0 || H <= 0 || F <= 0 || act < 0 || act > 2)
+        return ORC_ERR_ARG;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const int64_t ncols = (act == ORC_SWIGLU) ? 2 * F : F;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        double *y = (double *)malloc((size_t)ncols * sizeof(double));
+        if (!y) {
+#pragma omp atomic write
+            err = ORC_ERR_OOM;
+            continue;
+        }
+        row_times_matrix(X, rows[r] * H, dt, H, W1, ncols, 0, ncols, y);
+        activate_row(y, F, act, Y + r * F);
+        free(y);
+    }
+    return err;
+}
+
+/* First layer of shard i alone, from the oracle's own copy of the shard:
+ * Y_i[r] = act(X[rows[r]] W1_i), F/T values per row. */
+int orc_colpar_shard(const void *X, const void *W1, int dt, int64_t M, int64_t H,
+                     int64_t F, int T, int act, int i, const int64_t *rows,
+                     int64_t n_rows, double *Yi)
+{
+    if (!X || !W1 || !Yi || M <= 0 || H <= 0 || F <= 0 || T <= 0 || i < 0 || i >= T ||
+        act < 0 || act > 2)
+        return ORC_ERR_ARG;
+    if (F % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t Fs = F / T;
+    const int nparts = (act == ORC_SWIGLU) ? 2 : 1;
+    /* shard copy: [H x Fs] per part, parts side by side -> [H x nparts*Fs]
+       so that the SwiGLU shard reads as [Wg_i | Wu_i]. */
+    void *part = malloc((size_t)(H * Fs) * eb);
+    void *w1i = malloc((size_t)(H * Fs * nparts) * eb);
+    if (!part || !w1i) {
+        free(part);
+        free(w1i);
+        return ORC_ERR_OOM;
+    }
+    for (int p = 0; p < nparts; ++p) {
+        int e = orc_shard_w1(W1, dt, H, F, T, act, i, p, part);
+        if (e) {
+            free(part);
+            free(w1i);
+            return e;
+        }
+        for (int64_t k = 0; k < H; ++k)
+            memcpy((char *)w1i + (size_t)(k * nparts * Fs + p * Fs) * eb,
+                   (char *)part + (size_t)(k * Fs) * eb, (size_t)Fs * eb);
+    }
+    free(part);
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        double *y = (double *)malloc((size_t)(nparts * Fs) * sizeof(double));
+        if (!y) {
+#pragma omp atomic write
+            err = ORC_ERR_OOM;
+            continue;
+        }
+        row_times_matrix(X, rows[r] * H, dt, H, w1i, nparts * Fs, 0, nparts * Fs, y);
+        activate_row(y, Fs, act, Yi + r * Fs);
+        free(y);
+    }
+    free(w1i);
+    return err;
+}
+
+/* Unsharded MLP on selected rows: Z[r] = act(X[rows[r]] W1) W2, H values per
+ * row.  This is the dense result that the sharded computation must equal. */
+int orc_mlp_unsharded(const void *X, const void *W1, const void *W2, int dt, int64_t M,
+                      int64_t H, int64_t F, int act, const int64_t *rows, int64_t n_rows,
+                      double *Z)
+{
+    if (!W2 || !Z)
+        return ORC_ERR_ARG;
+    if (n_rows == 0)
+        return check_rows(rows, n_rows, M);
+    double *Y = (double *)malloc((size_t)(n_rows * F) * sizeof(double));
+    if (!Y)
+        return ORC_ERR_OOM;
+    int e = orc_colpar_full(X, W1, dt, M, H, F, act, rows, n_rows, Y);
+    if (e) {
+        free(Y);
+        return e;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r)
+        drow_times_matrix(Y + r * F, F, W2, dt, H, Z + r * H);
+    free(Y);
+    return ORC_OK;
+}
+
+/* Sharded MLP: for each shard i (ascending), Y_i = act(X W1_i) and the
+ * partial product Z_i = Y_i W2_i from the oracle's own shard copies; then
+ * Z = sum_i Z_i (the all-reduce-sum).  Same rows and layout as above. */
+int orc_mlp_sharded(const void *X, const void *W1, const void *W2, int dt, int64_t M,
+                    int64_t H, int64_t F, int T, int act, const int64_t *rows,
+                    int64_t n_rows, double *Z)
+{
+    if (!X || !W1 || !W2 || !Z || M <= 0 || H <= 0 || F <= 0 || T <= 0)
+        return ORC_ERR_ARG;
+    if (F % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t Fs = F / T;
+    double *Yi = (double *)malloc((size_t)(n_rows * Fs + 1) * sizeof(double));
+    double *Zi = (double *)malloc((size_t)(n_rows * H + 1) * sizeof(double));
+    void *w2i = malloc((size_t)(Fs * H) * eb);
+    if (!Yi || !Zi || !w2i) {
+        free(Yi);
+        free(Zi);
+        free(w2i);
+        return ORC_ERR_OOM;
+    }
+    for (int64_t e = 0; e < n_rows * H; ++e)
+        Z[e] = 0.0;
+    int err = ORC_OK;
+    for (int i = 0; i < T && !err; ++i) {
+        err = orc_colpar_shard(X, W1, dt, M, H, F, T, act, i, rows, n_rows, Yi);
+        if (!err)
+            err = orc_shard_w2(W2, dt, F, H, T, i, w2i);
+        if (err)
+            break;
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r)
+            drow_times_matrix(Yi + r * Fs, Fs, w2i, dt, H, Zi + r * H);
+        for (int64_t e = 0; e < n_rows * H; ++e)
+            Z[e] += Zi[e];
+    }
+    free(Yi);
+    free(Zi);
+    free(w2i);
+    return err;
+}
+
+/* ---- attention projections --------------------------------------------- */
+
+/* QKV projection of shard i: out[r] = X[rows[r]] Wqkv_i, 3*W values per row
+ * ([Q_i | K_i | V_i]), from the oracle's own copy of the shard. */
+int orc_qkv_shard(const void *X, const void *Wqkv, int dt, int64_t M, int64_t H,
+                  int n_heads, int head_dim, int T, int i, const int64_t *rows,
+                  int64_t n_rows, double *out)
+{
+    if (!X || !Wqkv || !out || M <= 0 || T <= 0 || n_heads <= 0 ||
+        (int64_t)n_heads * head_dim != H)
+        return ORC_ERR_ARG;
+    if (n_heads % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t W = (int64_t)(n_heads / T) * head_dim;
+    void *wi = malloc((size_t)(H * 3 * W) * eb);
+    if (!wi)
+        return ORC_ERR_OOM;
+    int e = orc_shard_wqkv(Wqkv, dt, H, n_heads, head_dim, T, i, wi);
+    if (!e)
+        e = orc_linear(X, wi, dt, M, H, 3 * W, rows, n_rows, out);
+    free(wi);
+    return e;
+}
+
+/* Row-parallel output projection: Z = sum_i A_i Wo_i over shards in
+ * ascending order, A [M x H] with the heads side by side (A_i = the columns
+ * of shard i's heads), Wo_i the matching rows of Wo. */
+int orc_oproj_sharded(const void *A, const void *Wo, int dt, int64_t M, int64_t H,
+                      int n_heads, int head_dim, int T, const int64_t *rows,
+                      int64_t n_rows, double *Z)
+{
+    if (!A || !Wo || !Z || M <= 0 || T <= 0 || n_heads <= 0 ||
+        (int64_t)n_heads * head_dim != H)
+        return ORC_ERR_ARG;
+    if (n_heads % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const size_t eb = orc_elem_bytes(dt);
+    const int64_t W = (int64_t)(n_heads / T) * head_dim;
+    void *woi = malloc((size_t)(W * H) * eb);
+    double *zi = (double *)malloc((size_t)(n_rows * H + 1) * sizeof(double));
+    if (!woi || !zi) {
+        free(woi);
+        free(zi);
+        return ORC_ERR_OOM;
+    }
+    for (int64_t e = 0; e < n_rows * H; ++e)
+        Z[e] = 0.0;
+    for (int i = 0; i < T; ++i) {
+        orc_shard_wo(Wo, dt, H, n_heads, head_dim, T, i, woi);
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r)
+            row_times_matrix(A, rows[r] * H + i * W, dt, W, woi, H, 0, H, zi + r * H);
+        for (int64_t e = 0; e < n_rows * H; ++e)
+            Z[e] += zi[e];
+    }
+    free(woi);
+    free(zi);
+    return ORC_OK;
+}
+
+/* ---- the all-reduce-sum arithmetic ------------------------------------- */
+
+/* Z[k] = ((P[0][k] + P[1][k]) + ...) + P[T-1][k] in float32, shards in
+ * ascending order; P is [T x n].  This fixes the bits the device shard-sum
+ * must reproduce. */
+void orc_partial_sum_f32(const float *P, int T, int64_t n, float *Z)
+{
+    for (int64_t k = 0; k < n; ++k) {
+        float s = P[k];
+        for (int i = 1; i < T; ++i)
+            s = s + P[(int64_t)i * n + k];
+        Z[k] = s;
+    }
+}
+
+/* Threads the OpenMP runtime would use. */
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

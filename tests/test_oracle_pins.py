@@ -1,0 +1,335 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code (CPU only).
+
+Each test names the fact it pins.  Together they are chosen so that a
+plausible slip in the oracle (a dropped term of GeLU, the gate and up halves
+swapped, a transposed operand, an off-by-one shard index, a dropped partial)
+fails at least one of them.
+"""
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+from scipy import special
+
+import oracle
+from synth import attn_inputs, f32_to_bf16_bits, mlp_inputs
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _kv(name):
+    out = {}
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = (s.strip() for s in line.split("=", 1))
+        out[k] = float(v)
+    return out
+
+
+def _table(name):
+    rows = []
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(tuple(float(t) for t in line.split()))
+    return rows
+
+
+def _decode(a):
+    """Exact values of float32 / bfloat16-bit arrays, decoded here without the oracle."""
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _normwise(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# --- element decoding --------------------------------------------------------
+
+@pytest.mark.parametrize("bits,val", [
+    (0x3F80, 1.0), (0xC000, -2.0), (0x3FC0, 1.5), (0x4049, 3.140625),
+    (0x0001, 2.0 ** -133), (0x8000, -0.0), (0x7F7F, 3.3895313892515355e38),
+    (0x3E80, 0.25),
+])
+def test_bf16_values_exact(bits, val):
+    """bfloat16 is the upper half of an IEEE float32: known bit patterns."""
+    a = np.array([bits], dtype=np.uint16)
+    assert oracle.value(a, 0) == val
+    assert math.copysign(1.0, oracle.value(a, 0)) == math.copysign(1.0, val)
+
+
+# --- activations --------------------------------------------------------------
+
+@pytest.mark.parametrize("x,phi", _table("gelu_normal_cdf.txt"))
+def test_gelu_is_x_times_normal_cdf(x, phi):
+    """GeLU(x) = x Phi(x) at tabulated Phi values (a dropped 0.5, a missing
+    1/sqrt(2) or the tanh approximation all fail here).  In the left tail
+    1 + erf(x/sqrt 2) cancels, so the bound there is absolute: |x| times a
+    few units of fp64 rounding."""
+    assert oracle.gelu(x) == pytest.approx(x * phi, rel=2e-15, abs=4e-16 * abs(x))
+
+
+def test_silu_closed_forms():
+    """SiLU(g) = g sigmoid(g): SiLU(1) = 1/(1+e^-1), SiLU(-1) = -1/(1+e), SiLU(0) = 0."""
+    assert oracle.silu(1.0) == pytest.approx(0.7310585786300049, rel=1e-15)
+    assert oracle.silu(-1.0) == pytest.approx(-0.2689414213699951, rel=1e-15)
+    assert oracle.silu(0.0) == 0.0
+    for g in np.linspace(-30, 30, 61):
+        assert oracle.silu(g) == pytest.approx(g * special.expit(g), rel=1e-14, abs=1e-300)
+
+
+# --- the hand-worked example --------------------------------------------------
+
+def test_one_sigma_two_shard_mlp():
+    """Two shards, X = [1, -1], W1 = I, W2 = [[1, 0], [1, 0]]:
+    Z = [GeLU(1) + GeLU(-1), 0] = [erf(1/sqrt 2), 0]."""
+    g = _kv("one_sigma_mlp.txt")
+    X = np.array([[1.0, -1.0]], dtype=np.float32)
+    W1 = np.eye(2, dtype=np.float32)
+    W2 = np.array([[1.0, 0.0], [1.0, 0.0]], dtype=np.float32)
+    for Z in (oracle.mlp_unsharded(X, W1, W2, "gelu"), oracle.mlp_sharded(X, W1, W2, 2, "gelu")):
+        assert Z[0, 0] == pytest.approx(g["Z0"], rel=1e-15)
+        assert Z[0, 1] == g["Z1"]
+
+
+def test_shape_mismatch_rejected():
+    X = np.zeros((1, 2), dtype=np.float32)
+    with pytest.raises(ValueError):
+        oracle.mlp_unsharded(X, np.eye(2, dtype=np.float32), np.ones((2, 1), np.float32), "gelu")
+
+
+# --- the column-parallel identity (act per shard) ----------------------------
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
+@pytest.mark.parametrize("T", [1, 2, 4])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_activation_concatenation_identity(act, T, dtype):
+    """act([y_1 | ... | y_T]) = [act(y_1) | ... | act(y_T)] exactly: the
+    per-shard first layer, concatenated, equals the unsharded one bit for bit."""
+    d = mlp_inputs(M=5, H=24, F=32, act=act, dtype=dtype, seed=3)
+    full = oracle.colpar_full(d["X"], d["W1"], 32, act)
+    parts = [oracle.colpar_shard(d["X"], d["W1"], 32, T, act, i) for i in range(T)]
+    assert np.array_equal(np.concatenate(parts, axis=1), full)
+
+
+# --- sharded == unsharded -----------------------------------------------------
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sharded_equals_unsharded(act, T, dtype):
+    """Sum over shards of act(X W1_i) W2_i equals act(X W1) W2 (the all-reduce
+    reconstructs the dense output) to fp64 rounding."""
+    d = mlp_inputs(M=7, H=32, F=64, act=act, dtype=dtype, seed=11)
+    zu = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    zs = oracle.mlp_sharded(d["X"], d["W1"], d["W2"], T, act)
+    assert _normwise(zs, zu) <= 1e-12
+
+
+def test_sharded_equals_unsharded_with_outlier_rows():
+    d = mlp_inputs(M=64, H=32, F=64, act="swiglu", dtype="bf16", seed=0,
+                   outlier_frac=0.05, outlier_scale=20.0)
+    assert d["outlier_rows"].size == 3
+    zu = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu")
+    zs = oracle.mlp_sharded(d["X"], d["W1"], d["W2"], 8, "swiglu")
+    assert _normwise(zs, zu) <= 1e-12
+
+
+# --- special cases that reduce to library routines ---------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_identity_activation_is_associative_product(dtype):
+    """With no activation, Z = X (W1 W2): checks operand order and transposes
+    of both GEMMs against a library matmul on the exact input values."""
+    d = mlp_inputs(M=6, H=16, F=40, act="identity", dtype=dtype, seed=5)
+    X, W1, W2 = (_decode(d[k]) for k in ("X", "W1", "W2"))
+    ref = X @ (W1 @ W2)
+    for T in (1, 2, 4, 8):
+        assert _normwise(oracle.mlp_sharded(d["X"], d["W1"], d["W2"], T, "identity"), ref) <= 1e-13
+    assert _normwise(oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "identity"), ref) <= 1e-13
+
+
+def test_permutation_weights_give_gelu_of_input():
+    """W1 = P, W2 = P^T (P a permutation): Z = GeLU(X) elementwise, checked
+    against x * Phi(x) from scipy's normal CDF."""
+    rng = np.random.default_rng(1)
+    n = 16
+    perm = rng.permutation(n)
+    P = np.zeros((n, n), dtype=np.float32)
+    P[np.arange(n), perm] = 1.0
+    X = rng.standard_normal((4, n)).astype(np.float32) * 2
+    ref = X.astype(np.float64) * special.ndtr(X.astype(np.float64))
+    # erf-form cancellation in the left tail: absolute bound |x| * 4 ulp(1)
+    bound = 1e-14 * np.abs(ref) + 4e-16 * np.abs(X.astype(np.float64))
+    for T in (1, 2, 4):
+        Z = oracle.mlp_sharded(X, P, np.ascontiguousarray(P.T), T, "gelu")
+        assert np.all(np.abs(Z - ref) <= bound)
+    Zi = oracle.mlp_unsharded(X, P, np.ascontiguousarray(P.T), "identity")
+    assert np.array_equal(Zi, X.astype(np.float64))
+
+
+def test_swiglu_gate_is_first_half():
+    """W1 = [Wg | Wu] with Wg = I, Wu = diag(d), W2 = I: Z = SiLU(x) * d * x.
+    Swapping the halves gives SiLU(d x) * x instead, which differs."""
+    rng = np.random.default_rng(2)
+    n = 8
+    d = rng.uniform(0.5, 2.0, n).astype(np.float32)
+    X = rng.standard_normal((3, n)).astype(np.float32)
+    I = np.eye(n, dtype=np.float32)
+    W1 = np.concatenate([I, np.diag(d)], axis=1)
+    Xd = X.astype(np.float64)
+    ref = Xd * special.expit(Xd) * d * Xd
+    for T in (1, 2, 4):
+        np.testing.assert_allclose(oracle.mlp_sharded(X, W1, I, T, "swiglu"), ref, rtol=1e-14)
+    swapped = np.concatenate([np.diag(d), I], axis=1)
+    assert not np.allclose(oracle.mlp_unsharded(X, swapped, I, "swiglu"), ref, rtol=1e-6)
+
+
+# --- the partition layout (bit exact, brute force) ---------------------------
+
+def _ids(shape):
+    return np.arange(int(np.prod(shape)), dtype=np.uint32).astype(np.uint16).reshape(shape)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_w1_column_blocks(act, T):
+    """Element (k, c) of W1 (of Wg, Wu for SwiGLU) lands in shard c // (F/T)
+    at local column c % (F/T), and every element lands exactly once."""
+    H, F = 12, 64
+    ncols = 2 * F if act == "swiglu" else F
+    W1 = _ids((H, ncols))
+    Fs = F // T
+    seen = np.zeros(W1.size, dtype=np.int64)
+    for i in range(T):
+        for which in ((0, 1) if act == "swiglu" else (0,)):
+            s = oracle.shard_w1(W1, F, T, act, i, which)
+            assert s.shape == (H, Fs)
+            for k in range(H):
+                for c in range(Fs):
+                    src = which * F + i * Fs + c
+                    assert s[k, c] == W1[k, src]
+                    seen[k * ncols + src] += 1
+    assert np.all(seen == 1)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_w2_row_blocks(T):
+    """Row r of W2 lands in shard r // (F/T) at local row r % (F/T), once."""
+    F, H = 64, 12
+    W2 = _ids((F, H))
+    Fs = F // T
+    seen = np.zeros(W2.size, dtype=np.int64)
+    for i in range(T):
+        s = oracle.shard_w2(W2, T, i)
+        assert s.shape == (Fs, H)
+        for r in range(Fs):
+            assert np.array_equal(s[r], W2[i * Fs + r])
+            seen[(i * Fs + r) * H:(i * Fs + r + 1) * H] += 1
+    assert np.all(seen == 1)
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_qkv_head_aligned_shards(T):
+    """Shard i holds heads [i*nh/T, (i+1)*nh/T) of each of Wq, Wk, Wv; Wo's
+    rows of those heads; every column / row exactly once."""
+    nh, hd = 8, 4
+    H = nh * hd
+    Wqkv = _ids((H, 3 * H))
+    Wo = _ids((H, H))
+    hps = nh // T
+    W = hps * hd
+    seen = np.zeros(3 * H, dtype=np.int64)
+    for i in range(T):
+        s = oracle.shard_wqkv(Wqkv, nh, hd, T, i)
+        assert s.shape == (H, 3 * W)
+        for p in range(3):
+            for c in range(W):
+                head = i * hps + c // hd
+                src = p * H + head * hd + c % hd
+                assert np.array_equal(s[:, p * W + c], Wqkv[:, src])
+                seen[src] += 1
+        o = oracle.shard_wo(Wo, nh, hd, T, i)
+        assert np.array_equal(o, Wo[i * W:(i + 1) * W])
+    assert np.all(seen == 1)
+
+
+def test_indivisible_shards_rejected():
+    W1 = np.zeros((4, 10), dtype=np.float32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.shard_w1(W1, 10, 4, "gelu", 0)
+    assert e.value.code == oracle.ERR_INDIVISIBLE
+    X = np.zeros((2, 4), dtype=np.float32)
+    W2 = np.zeros((10, 4), dtype=np.float32)
+    with pytest.raises(oracle.OracleError):
+        oracle.mlp_sharded(X, W1, W2, 3, "gelu")
+
+
+# --- attention projections ----------------------------------------------------
+
+def test_qkv_shards_are_dense_columns_and_oproj_sum_is_dense():
+    """Head-sharded QKV equals the matching columns of the dense X Wqkv bit
+    for bit; the row-parallel output projection summed over shards equals
+    the dense A Wo."""
+    nh, hd, T, M = 8, 8, 4, 5
+    d = attn_inputs(M=M, H=nh * hd, n_heads=nh, head_dim=hd, seed=4)
+    H = nh * hd
+    dense = oracle.linear(d["X"], d["Wqkv"])
+    W = nh // T * hd
+    for i in range(T):
+        s = oracle.qkv_shard(d["X"], d["Wqkv"], nh, hd, T, i)
+        cols = np.concatenate([np.arange(p * H + i * W, p * H + (i + 1) * W) for p in range(3)])
+        assert np.array_equal(s, dense[:, cols])
+    ref = _decode(d["A"]) @ _decode(d["Wo"])
+    assert _normwise(oracle.oproj_sharded(d["A"], d["Wo"], nh, hd, T), ref) <= 1e-13
+
+
+# --- row sampling -------------------------------------------------------------
+
+def test_row_subset_matches_full_rows():
+    """A row of Z depends only on that row of X: the sampled-row oracle (used at
+    full sizes) returns exactly the rows of the full computation."""
+    d = mlp_inputs(M=20, H=16, F=32, act="swiglu", dtype="bf16", seed=9)
+    full = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu")
+    rows = np.array([19, 0, 7, 7])
+    sub = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu", rows=rows)
+    assert np.array_equal(sub, full[rows])
+
+
+# --- the all-reduce-sum arithmetic -------------------------------------------
+
+def test_partial_sum_integers_exact():
+    """Integer-valued partials sum exactly in float32: each shard counted once."""
+    rng = np.random.default_rng(0)
+    P = rng.integers(-1000, 1000, size=(8, 257)).astype(np.float32)
+    assert np.array_equal(oracle.partial_sum_f32(P), P.astype(np.int64).sum(0).astype(np.float32))
+
+
+def test_partial_sum_order_is_ascending_left_to_right():
+    """(a + b) + c in float32 with a = 1, b = 2^-24, c = 2^-24 gives 1, while
+    a + (b + c) gives 1 + 2^-23: the order is ascending shard index, left to right."""
+    P = np.array([[1.0], [2.0 ** -24], [2.0 ** -24]], dtype=np.float32)
+    assert oracle.partial_sum_f32(P)[0] == np.float32(1.0)
+    P2 = P[::-1].copy()
+    assert oracle.partial_sum_f32(P2)[0] == np.float32(1.0 + 2.0 ** -23)
+
+
+def test_partial_sum_within_float32_bound():
+    rng = np.random.default_rng(1)
+    P = rng.standard_normal((8, 4096)).astype(np.float32)
+    exact = P.astype(np.float64).sum(0)
+    bound = 8 * 2.0 ** -24 * np.abs(P.astype(np.float64)).sum(0)
+    assert np.all(np.abs(oracle.partial_sum_f32(P) - exact) <= bound)
+
+
+def test_synth_bf16_encoding_round_to_nearest_even():
+    """The shared input encoder: ties go to the even bfloat16, others to nearest."""
+    v = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9, -2.5], dtype=np.float32)
+    bits = f32_to_bf16_bits(v)
+    assert list(bits) == [0x3F80, 0x3F82, 0x3F80, 0xC020]
