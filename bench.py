@@ -1,0 +1,526 @@
+#!/usr/bin/env python
+"""Benchmark of the tensor-parallel MLP hot path on GB300.
+
+One step = one pass of the whole path over one batch: the column-parallel
+GEMM with the fused activation (all T shards), the row-parallel GEMM and the
+all-reduce-sum, on the prefill workload (M = 2048 tokens, H = 4096,
+F = 16384, T = 4, erf-GeLU, bf16 inputs, float32 accumulation).  Prints one
+JSON line.  Under torchrun each rank runs an independent replica on its own
+GPU (the path has no cross-GPU exchange: all shards live on one GPU), so the
+scaling is weak and the value is the sum over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TP-sharded MLP fwd TFLOP/s and % BF16 peak; shard-sum/decode HBM GB/s %"
+WORKLOAD = "prefill_gelu_m2048_h4096_f16384_t4"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE = os.path.join(ROOT, "profiles", "colpar_gemm_gelu_prefill_m2048_h4096_f16384_t4.md")
+GEMM_SOURCES = [os.path.join(ROOT, "linear_sharding_gb300", "csrc", f)
+                for f in ("tp_gemm.cu", "tp_device.cuh", "tp_internal.h")]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--variant", choices=("auto", "partials", "tmem_acc"), default="auto")
+    p.add_argument("--extras", choices=("none", "default", "full"), default="default",
+                   help="secondary measurements at N=1: decode + shard-sum (default), "
+                        "plus attention projections and the large SwiGLU prefill (full)")
+    p.add_argument("--cpu-rows", type=int, default=64, help="rows of the oracle CPU-baseline sample")
+    return p.parse_args(argv)
+
+
+# ---- distributed plumbing (replicas) ------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def _reduce(value: float, op: str, device) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def reduce_max(value: float, device="cpu") -> float:
+    return _reduce(value, "max", device)
+
+
+def reduce_sum(value: float, device="cpu") -> float:
+    return _reduce(value, "sum", device)
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate(elapsed_s: float, units_per_rank: float, device="cpu"):
+    """Whole-job throughput of replicas: the units all ranks processed over
+    the slowest rank's time.  Returns (units/s, max elapsed)."""
+    t = reduce_max(elapsed_s, device)
+    units = reduce_sum(units_per_rank, device)
+    return units / t, t
+
+
+# ---- clocks ------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                    "-i", str(gpu_index), "-lms", str(period_ms)]
+        self.proc = None
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, mx, pw = [], [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [c for c, p in zip(sm, pw) if p >= 0.3 * max(pw)] or sm
+        loaded.sort()
+        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# ---- roofline bookkeeping ------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the column-parallel GEMM from the committed ncu
+    summary, or None if absent or taken on different kernel source."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not sha or sha.group(1) != gemm_source_sha():
+        return None
+    return float(m.group(1))
+
+
+# ---- our implementation ---------------------------------------------------------
+
+def _dev(a, device):
+    import numpy as np
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def cpu_baseline(w: dict, rows: int) -> dict:
+    """The fp64 oracle as it stands, on a seeded sample of rows of the same
+    workload, on this host's cores."""
+    import numpy as np
+    import oracle
+    from synth import mlp_inputs
+    oracle.build()
+    d = mlp_inputs(M=w["M"], H=w["H"], F=w["F"], act=w["act"], dtype=w["dtype"], seed=0)
+    sample = np.sort(np.random.default_rng(1).choice(w["M"], size=rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.mlp_sharded(d["X"], d["W1"], d["W2"], w["T"], w["act"], rows=sample)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * rows * w["H"] * w["F"]
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{rows} of {w['M']} rows (seeded), sharded fp64 oracle, {dt:.2f} s; "
+                      f"full M extrapolates to {dt * w['M'] / rows:.0f} s"}
+
+
+def run_ours(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    import linear_sharding_gb300 as tp
+    from synth import WORKLOADS, mlp_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    tp.load_library()
+
+    w = WORKLOADS[WORKLOAD]
+    M, H, F, T, act = w["M"], w["H"], w["F"], w["T"], w["act"]
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=rank)
+    s = tp.tp_shard_weights(_dev(d["W1"], device), _dev(d["W2"], device), T, act)
+    X = _dev(d["X"], device)
+    Y = torch.empty((T, M, F // T), dtype=torch.bfloat16, device=device)
+    Z = torch.empty((M, H), dtype=torch.float32, device=device)
+    ws_col = tp.tp_colpar_workspace_bytes(s, M)
+    ws_row = tp.tp_rowpar_workspace_bytes(s, M, args.variant)
+    wcol = torch.empty(max(ws_col, 1), dtype=torch.uint8, device=device)
+    wrow = torch.empty(max(ws_row, 1), dtype=torch.uint8, device=device)
+    launches_per_step = 1 + 1 + (1 if ws_row > 0 else 0)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tp.tp_colpar_forward(s, X, Y, workspace=wcol)
+        tp.tp_rowpar_forward(s, Y, args.variant, Z, workspace=wrow)
+
+    clocks = ClockSampler(physical_gpu_index(local)).start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if tp.tp_last_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        e0[i].record(stream)
+        tp.tp_colpar_forward(s, X, Y, workspace=wcol)
+        e1[i].record(stream)
+        tp.tp_rowpar_forward(s, Y, args.variant, Z, workspace=wrow)
+        e2[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(device)
+    clk = clocks.stop()
+    status = tp.tp_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    elapsed = start.elapsed_time(end) / 1e3
+    flops_step = 4.0 * M * H * F
+    value, t_max = aggregate(elapsed, flops_step * K, device)
+    col_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K
+    row_ms = sum(e1[i].elapsed_time(e2[i]) for i in range(K)) / K
+
+    # end to end through the public host-buffer call: pinned X in, Z out
+    Xh = torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    Zh = torch.empty((M, H), dtype=torch.float32).pin_memory()
+    wsh = torch.empty(tp.tp_mlp_host_workspace_bytes(s, M, args.variant), dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        tp.tp_mlp_forward_host(s, Xh, Zh, wsh, args.variant)
+    barrier(device)
+    torch.cuda.synchronize()
+    hs, he = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hs.record(stream)
+    for _ in range(K):
+        tp.tp_mlp_forward_host(s, Xh, Zh, wsh, args.variant)
+    he.record(stream)
+    torch.cuda.synchronize()
+    barrier(device)
+    e2e_value, _ = aggregate(hs.elapsed_time(he) / 1e3, flops_step * K, device)
+
+    peaks, peak_src = measured_peaks()
+    sustained = elapsed > 1.0
+    peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    achieved = 2.0 * M * H * F / (col_ms / 1e3) / 1e12
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max * 1e3 / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) X, N(0,1/fan_in) weights, bf16)",
+        "config": {"workload": WORKLOAD, "M": M, "H": H, "F": F, "T": T, "act": "erf-gelu",
+                   "variant": args.variant, "accumulate": "fp32", "output": "fp32",
+                   "parallelism": f"{world} independent replica(s); T={T} shards per GPU",
+                   "l2": "inputs larger than L2 (256 MiB of weights read per step)"},
+        "pct_bf16_peak": round(100.0 * value / 1e12 / world / peak, 1),
+        "roofline": {"kernel": "tp_gemm_kernel<256, GELU> (column-parallel GEMM + GeLU)",
+                     "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+                     "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
+                     "traffic": traffic, "avg_launch_ms": round(col_ms, 5)},
+        "rowpar_ms": round(row_ms, 5),
+        "e2e": {"value": round(e2e_value / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 4},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "context": {"ring_allreduce_bytes_per_rank_if_T_gpus": tp.ring_allreduce_bytes(M * H, T, 4)},
+    }
+    if world == 1 and rank == 0:
+        if args.extras != "none":
+            line["extras"] = extras(args, tp, device, peaks, full=args.extras == "full")
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+    s.close()
+    return line if rank == 0 else None
+
+
+def _time_calls(fn, reps: int, warm: int = 3) -> float:
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / reps
+
+
+def extras(args, tp, device, peaks, full: bool) -> dict:
+    """Secondary measurements (N = 1): the memory-bound decode shapes and the
+    standalone shard-sum against HBM bandwidth; with `full`, the attention
+    projections and the large SwiGLU prefill against tensor peak.  Inputs
+    for these timing-only runs are drawn on the device with a seeded
+    generator (same distributions as the parity workloads)."""
+    import torch
+    from synth import WORKLOADS
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+
+    def randn(shape, std, dtype=torch.bfloat16):
+        return (torch.randn(shape, generator=gen, device=device) * std).to(dtype)
+
+    w = WORKLOADS["decode_swiglu_h8192_f28672_t8"]
+    H, F, T = w["H"], w["F"], w["T"]
+    W1 = randn((H, 2 * F), 1 / math.sqrt(H))
+    W2 = randn((F, H), 1 / math.sqrt(F))
+    s = tp.tp_shard_weights(W1, W2, T, "swiglu")
+    del W1, W2
+    dec = {}
+    for M in w["decode_m"]:
+        X = randn((M, H), 1.0)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, "auto"), 1), dtype=torch.uint8, device=device)
+        t = _time_calls(lambda: tp.tp_mlp_forward(s, X, "auto", Z, ws), 50)
+        byts = 3 * H * F * 2 + M * H * (2 + 4)
+        dec[f"M{M}"] = {"us": round(t * 1e6, 1), "GB/s": round(byts / t / 1e9, 1),
+                        "frac_hbm": round(byts / t / 1e9 / hbm, 3)}
+    s.close()
+    torch.cuda.empty_cache()
+    out["decode_swiglu_h8192_f28672_t8"] = dec
+
+    ss = {}
+    for name, T, n in (("prefill_gelu", 4, 2048 * 4096), ("attn_proj", 8, 4096 * 4096),
+                       ("prefill_swiglu_large", 8, 8192 * 8192)):
+        P = [torch.randn(n, generator=gen, device=device) for _ in range(T)]
+        Zs = torch.empty(n, dtype=torch.float32, device=device)
+        t = _time_calls(lambda: tp.tp_partial_sum(P, Zs), 20)
+        byts = (T + 1) * n * 4
+        ss[f"{name}_T{T}_n{n}"] = {"us": round(t * 1e6, 1), "GB/s": round(byts / t / 1e9, 1),
+                                   "frac_hbm": round(byts / t / 1e9 / hbm, 3)}
+        del P, Zs
+        torch.cuda.empty_cache()
+    out["shard_sum"] = ss
+    out["hbm_peak_gbs"] = hbm
+
+    if full:
+        w = WORKLOADS["attn_proj_m4096_h4096_32x128_t8"]
+        M, H, T, nh, hd = w["M"], w["H"], w["T"], w["n_heads"], w["head_dim"]
+        s = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                    nh, hd, T)
+        X, A = randn((M, H), 1.0), randn((M, H), 1.0)
+        QKV = torch.empty((T, M, 3 * H // T), dtype=torch.bfloat16, device=device)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        res = {}
+        for v in ("auto", "partials", "tmem_acc"):
+            ws = torch.empty(max(tp.tp_attn_proj_workspace_bytes(s, M, v), 1), dtype=torch.uint8,
+                             device=device)
+            t_qkv = _time_calls(lambda: tp.tp_attn_proj_forward(s, X=X, variant=v, QKV=QKV), 20)
+            t_o = _time_calls(lambda: tp.tp_attn_proj_forward(s, A=A, variant=v, Z=Z, workspace=ws), 20)
+            res[v] = {"qkv_TFLOP/s": round(2 * M * H * 3 * H / t_qkv / 1e12, 1),
+                      "oproj_TFLOP/s": round(2 * M * H * H / t_o / 1e12, 1),
+                      "us_qkv": round(t_qkv * 1e6, 1), "us_oproj": round(t_o * 1e6, 1)}
+        out["attn_proj_m4096_h4096_32x128_t8"] = res
+        s.close()
+        torch.cuda.empty_cache()
+
+        w = WORKLOADS["prefill_swiglu_m8192_h8192_f28672_t8_outliers"]
+        M, H, F, T = w["M"], w["H"], w["F"], w["T"]
+        s = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                                "swiglu")
+        X = randn((M, H), 1.0)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        res = {}
+        for v in ("auto", "partials", "tmem_acc"):
+            ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, v), 1), dtype=torch.uint8, device=device)
+            t = _time_calls(lambda: tp.tp_mlp_forward(s, X, v, Z, ws), 5)
+            res[v] = {"ms": round(t * 1e3, 3), "TFLOP/s": round(6 * M * H * F / t / 1e12, 1)}
+            del ws
+        out["prefill_swiglu_m8192_h8192_f28672_t8"] = res
+        s.close()
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---- reference arm: the oracle on the host cores ----------------------------------
+
+def run_reference(args) -> dict | None:
+    import numpy as np
+
+    import oracle
+    from synth import WORKLOADS, mlp_inputs
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    oracle.build()
+    w = WORKLOADS[WORKLOAD]
+    M, H, F, T, act = w["M"], w["H"], w["F"], w["T"], w["act"]
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=0)
+    rows_per_step = 16
+    rng = np.random.default_rng(2)
+
+    def step():
+        rows = np.sort(rng.choice(M, size=rows_per_step, replace=False))
+        oracle.mlp_sharded(d["X"], d["W1"], d["W2"], T, act, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 4.0 * rows_per_step * H * F * args.steps
+    value = flops / dt / 1e12
+    cores = oracle.max_threads()
+    sample = f"{rows_per_step} seeded rows of {M} per step (sharded fp64 oracle)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same inputs as the GPU arm)",
+        "config": {"workload": WORKLOAD, "M": M, "H": H, "F": F, "T": T, "act": "erf-gelu",
+                   "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps >= 1 and --warmup >= 0")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,288 @@
+/*
+ * tp_mlp.h - C ABI of libtpmlp.so, the tensor-parallel transformer MLP on
+ * one GB300 (sm_103a).
+ *
+ * The method (Megatron-style tensor parallelism):
+ *   - the first linear layer is column-parallel: W1 is split along its output
+ *     dimension into T column blocks W1_i, X is replicated, Y_i = act(X W1_i)
+ *     ("Tensor Parallelism in Action: Megatron-LM Matrix Splitting", section
+ *     1, "Column Parallel (W1)"; "Slice the matrix itself", section
+ *     "Column-Parallel & Row-Parallel GEMMs");
+ *   - the activation needs no exchange because it is elementwise
+ *     ("Tensor Parallelism in Action", section 2, question 2);
+ *   - the second linear layer is row-parallel: W2 is split along its input
+ *     dimension into T row blocks W2_i, giving partial products
+ *     Z_i = Y_i W2_i ("Tensor Parallelism in Action", section 1, "Row
+ *     Parallel (W2)");
+ *   - one all-reduce-sum completes it, Z = sum_i Z_i ("Slice the matrix
+ *     itself", section "Mathematical formulation - row-parallel matrix
+ *     multiplication summation"; "Tensor parallelism" guide, section
+ *     "Concept").
+ * Here all T shards are partitions on ONE GPU and the all-reduce-sum is
+ * arithmetic in device memory (or in the tensor-core accumulator): there is
+ * no collective and nothing crosses GPUs.
+ *
+ * Conventions for every call:
+ *   - Every call returns a tp_status_t (or a size); none aborts or throws.
+ *   - Matrices are row-major.  The pages' convention Y = X W is used, so W1 is
+ *     [H x F] (in x out) and W2 is [F x H].
+ *   - Pointers are DEVICE pointers unless the name ends in _host / host_dst.
+ *     Device pointers must be 16-byte aligned.  The caller owns every buffer
+ *     it passes; the library owns only what a tp_shards_t holds and its own
+ *     per-device status word.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued on it and the call returns without waiting, except where a
+ *     call says otherwise.  Argument errors are returned synchronously;
+ *     device-side errors (a wait that ran out, a failed device check) are
+ *     reported by tp_last_device_status().
+ *   - The calling thread's current CUDA device is used; it must be sm_103
+ *     (GB300) or the call returns TP_ERR_ARCH.
+ *   - Shapes are int64_t.  T (shards) is 1..64.
+ */
+#ifndef TP_MLP_H
+#define TP_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TP_ABI_VERSION 1
+
+/* Exported symbols of libtpmlp.so (the library hides everything else). */
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_ARG = 1,          /* null pointer, bad size, misaligned pointer, bad enum */
+    TP_ERR_INDIVISIBLE = 2,  /* F % T != 0 or n_heads % T != 0 (shards must be equal) */
+    TP_ERR_DTYPE = 3,        /* element type not supported for this call */
+    TP_ERR_ARCH = 4,         /* current device is not sm_103 */
+    TP_ERR_OOM = 5,          /* device or host allocation failed */
+    TP_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed */
+    TP_ERR_TIMEOUT = 7,      /* a device-side wait ran past its limit (kernel returned early) */
+    TP_ERR_DEVICE_CHECK = 8, /* a device-side check failed */
+    TP_ERR_UNSUPPORTED = 9,  /* shape outside what the kernels tile (see each call) */
+    TP_ERR_WORKSPACE = 10    /* workspace smaller than the *_workspace_bytes() figure */
+} tp_status_t;
+
+typedef enum {
+    TP_ACT_GELU_ERF = 0,  /* GeLU(y) = 0.5 y (1 + erf(y / sqrt 2)) */
+    TP_ACT_SWIGLU = 1,    /* h = SiLU(X Wg) * (X Wu), SiLU(g) = g / (1 + exp(-g)) */
+    TP_ACT_IDENTITY = 2   /* no activation */
+} tp_act_t;
+
+typedef enum {
+    TP_F32 = 0,   /* float32 in, float32 FMA (CUDA cores), float32 out */
+    TP_BF16 = 1   /* bfloat16 in, float32 accumulate (tensor cores), float32 out */
+} tp_dtype_t;
+
+typedef enum {
+    TP_VAR_AUTO = 0,      /* the library picks per shape */
+    TP_VAR_PARTIALS = 1,  /* row-parallel GEMM writes T float32 partials, then the shard-sum */
+    TP_VAR_TMEM_ACC = 2   /* one accumulator sums all shards' K ranges; partials never reach memory */
+} tp_variant_t;
+
+/* Opaque, library-owned sharded weights. */
+typedef struct tp_shards *tp_shards_t;
+
+/* Human-readable name of a status; never NULL. */
+TP_API const char *tp_status_str(tp_status_t s);
+
+/* TP_ABI_VERSION of the loaded library. */
+TP_API int tp_abi_version(void);
+
+/*
+ * tp_shard_weights - the shard layout (column blocks of W1, row blocks of W2).
+ * Pages: "Tensor Parallelism in Action", section 1 (W1 = [W1_1 | W1_2],
+ * W2 = [W2_1; W2_2]); "Slice the matrix itself" ("First linear layer
+ * (Gate/Up) is split column-wise ... Second linear layer (Down) is split
+ * row-wise").
+ *
+ *   W1   [H x F] (GELU_ERF, IDENTITY) or [H x 2F] = [Wg | Wu] (SWIGLU, gate
+ *        first), element type dt.
+ *   W2   [F x H], element type dt.
+ *   Shard i holds columns [i F/T, (i+1) F/T) of W1 (for SWIGLU the SAME
+ *   columns of Wg and of Wu) and rows [i F/T, (i+1) F/T) of W2.  The copies
+ *   are bit-exact; the device layout is K-major (each shard's W1_i and W2_i
+ *   stored transposed, [out x in]) for the tensor-core GEMMs.
+ *   W1 and W2 are only read; the caller may free them once `stream` has
+ *   reached the end of this call's work.
+ *   Errors: F % T != 0 -> TP_ERR_INDIVISIBLE; for TP_BF16, H % 128 != 0 or
+ *   F/T % 128 != 0 -> TP_ERR_UNSUPPORTED (the tensor-core tiles are 128
+ *   rows by 64 K); SWIGLU with F/T % 128 != 0 -> TP_ERR_UNSUPPORTED;
+ *   allocation -> TP_ERR_OOM.
+ *   *out receives a handle to free with tp_shards_destroy().
+ */
+TP_API tp_status_t tp_shard_weights(const void *W1, const void *W2, int64_t H, int64_t F, int T,
+                             tp_act_t act, tp_dtype_t dt, void *stream, tp_shards_t *out);
+
+/*
+ * tp_shard_weights_qkv - head-sharded attention projections ("Tensor
+ * parallelism" guide, section "Walking through a transformer block": shard
+ * heads across ranks; the output projection is row-parallel and ends in an
+ * all-reduce, "Slice the matrix itself", section "All-Reduce Synchronization").
+ *
+ *   Wqkv [H x 3H] = [Wq | Wk | Wv], head h in columns [h hd, (h+1) hd) of
+ *        each; bfloat16.
+ *   Wo   [H x H], input rows grouped by head the same way; bfloat16.
+ *   Shard i holds heads [i nh/T, (i+1) nh/T): those columns of Wq, Wk and
+ *   Wv (3 W columns, W = nh/T * hd) and those W rows of Wo.
+ *   Errors: n_heads * head_dim != H -> TP_ERR_ARG; n_heads % T != 0 ->
+ *   TP_ERR_INDIVISIBLE; H % 128, W % 64 or 3W % 128 != 0 ->
+ *   TP_ERR_UNSUPPORTED.
+ */
+TP_API tp_status_t tp_shard_weights_qkv(const void *Wqkv, const void *Wo, int64_t H, int n_heads,
+                                 int head_dim, int T, void *stream, tp_shards_t *out);
+
+/*
+ * tp_shard_get - copy the LOGICAL shard i to host memory, row-major, for
+ * bit-exact layout checks.  Synchronous (waits for the device).
+ *   MLP shards: which = 0 -> W1_i (Wg_i for SWIGLU) [H x F/T];
+ *               which = 1 -> Wu_i [H x F/T] (SWIGLU only);
+ *               which = 2 -> W2_i [F/T x H].
+ *   QKV shards: which = 0 -> Wqkv_i [H x 3W] (= [Wq_i | Wk_i | Wv_i]);
+ *               which = 2 -> Wo_i [W x H].
+ *   host_dst must hold that many elements of the shards' element type.
+ */
+TP_API tp_status_t tp_shard_get(tp_shards_t s, int i, int which, void *host_dst);
+
+/* Shape of a handle: any pointer may be NULL.  kind: 0 = MLP, 1 = QKV. */
+TP_API tp_status_t tp_shard_info(tp_shards_t s, int *kind, int64_t *H, int64_t *F, int *T,
+                          int *act, int *dtype);
+
+/* Free a handle and its device buffers (synchronises the device first). */
+TP_API void tp_shards_destroy(tp_shards_t s);
+
+/*
+ * tp_mlp_workspace_bytes - device workspace tp_mlp_forward needs for M
+ * tokens and variant v: Y (T x M x F/T, element type of the shards) plus,
+ * for the partials variant and for decode, the float32 partials.
+ */
+TP_API size_t tp_mlp_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+
+/*
+ * tp_mlp_forward - Z = sum_i act(X W1_i) W2_i for all T shards on this GPU.
+ *   X  [M x H] device, element type of the shards (replicated input).
+ *   Z  [M x H] float32 device, written in full (caller-owned).
+ *   act must be the activation the shards were made for (GELU_ERF and
+ *   IDENTITY are interchangeable for non-SwiGLU shards).
+ *   workspace: device buffer of at least tp_mlp_workspace_bytes(s, M, v)
+ *   bytes, or NULL to let the library allocate it stream-ordered
+ *   (cudaMallocAsync/cudaFreeAsync on `stream`).
+ *   Steps (bf16): column-parallel GEMM with the activation fused into its
+ *   epilogue, Y_i stored as bfloat16; row-parallel GEMM; the all-reduce-sum
+ *   (shard-sum kernel over float32 partials in ascending shard order, or the
+ *   tensor-memory accumulator over all shards' K ranges).  M <= 16 uses the
+ *   memory-bound decode kernels (weights as the 128-row MMA operand).
+ *   M == 0 is a no-op.  Asynchronous on `stream`.
+ */
+TP_API tp_status_t tp_mlp_forward(tp_shards_t s, const void *X, int64_t M, tp_act_t act,
+                           tp_variant_t v, float *Z, void *workspace, size_t ws_bytes,
+                           void *stream);
+
+/*
+ * tp_colpar_forward - the column-parallel layer alone (step 1 of
+ * tp_mlp_forward): Y_i = act(X W1_i) for every shard i ("Tensor Parallelism
+ * in Action", section 1, "Column Parallel (W1)": no exchange after it).
+ *   X  [M x H] device, element type of the shards.
+ *   Y  [T x M x F/T] device out, element type of the shards: shard i's
+ *      block Y_i is contiguous (the rank-local layout).
+ *   workspace: tp_colpar_workspace_bytes(s, M) bytes (0 except for the
+ *   decode shapes, M <= 16), or NULL to allocate stream-ordered.
+ *   Asynchronous on `stream`.
+ */
+TP_API size_t tp_colpar_workspace_bytes(tp_shards_t s, int64_t M);
+TP_API tp_status_t tp_colpar_forward(tp_shards_t s, const void *X, int64_t M, tp_act_t act,
+                                     void *Y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * tp_rowpar_forward - the row-parallel layer and its all-reduce-sum (steps 2
+ * and 3 of tp_mlp_forward): Z = sum_i Y_i W2_i ("Tensor Parallelism in
+ * Action", section 1, "Row Parallel (W2)" and "Output Combination").
+ *   Y  [T x M x F/T] device, as tp_colpar_forward writes it.
+ *   Z  [M x H] float32 device out.
+ *   workspace: tp_rowpar_workspace_bytes(s, M, v) bytes (the float32
+ *   partials when the plan uses them), or NULL to allocate stream-ordered.
+ *   Asynchronous on `stream`.
+ */
+TP_API size_t tp_rowpar_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+TP_API tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp_variant_t v,
+                                     float *Z, void *workspace, size_t ws_bytes, void *stream);
+
+/* Device workspace tp_mlp_forward_host needs: X and Z staging plus
+ * tp_mlp_workspace_bytes(). */
+TP_API size_t tp_mlp_host_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+
+/*
+ * tp_mlp_forward_host - the same computation from HOST buffers: copies
+ * X_host ([M x H], element type of the shards) to the device, runs
+ * tp_mlp_forward and copies Z back to Z_host ([M x H] float32), all on
+ * `stream`.  Pinned host memory makes the copies asynchronous; the call
+ * returns once the work is enqueued (synchronise `stream` before reading
+ * Z_host).  workspace as above, sized by tp_mlp_host_workspace_bytes().
+ */
+TP_API tp_status_t tp_mlp_forward_host(tp_shards_t s, const void *X_host, int64_t M, tp_act_t act,
+                                tp_variant_t v, float *Z_host, void *workspace,
+                                size_t ws_bytes, void *stream);
+
+/* Device workspace tp_attn_proj_forward needs (float32 partials for the
+ * partials variant; 0 for the accumulator variant). */
+TP_API size_t tp_attn_proj_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+
+/*
+ * tp_attn_proj_forward - the head-sharded attention projections.
+ *   X   [M x H] bfloat16 (replicated input).
+ *   QKV [T x M x 3W] bfloat16 out: QKV_i = X Wqkv_i = [Q_i | K_i | V_i], each
+ *       shard's block contiguous (rank-local layout).  May be NULL to skip.
+ *   A   [M x H] bfloat16: the attention output, heads side by side (A_i =
+ *       the W columns of shard i's heads).  May be NULL (with Z) to skip.
+ *   Z   [M x H] float32 out: Z = sum_i A_i Wo_i (row-parallel + all-reduce).
+ *   Asynchronous on `stream`.
+ */
+TP_API tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void *A, int64_t M,
+                                 tp_variant_t v, void *QKV, float *Z, void *workspace,
+                                 size_t ws_bytes, void *stream);
+
+/*
+ * tp_partial_sum - the all-reduce-sum arithmetic on one GPU ("Slice the
+ * matrix itself", section "Mathematical formulation": Y = sum_i X_i W_i, then
+ * All-Reduce-Sum).
+ *   Zi  host array of T device pointers, each to n float32 values.
+ *   Z   n float32 out: Z[k] = ((Zi[0][k] + Zi[1][k]) + ...) + Zi[T-1][k],
+ *       float32, shards in ascending order (deterministic, no atomics).
+ *       Z may be Zi[0] (in place); any other overlap is an error.
+ *   n == 0 is a no-op.  Asynchronous on `stream`.
+ */
+TP_API tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream);
+
+/*
+ * tp_last_device_status - synchronise `stream`, then return and clear the
+ * current device's status word: TP_OK, TP_ERR_TIMEOUT (a kernel's bounded
+ * wait ran out and it returned early; its outputs are undefined) or
+ * TP_ERR_DEVICE_CHECK.  The word collects every kernel of this library on
+ * the device since the last call.  A CUDA error from the stream is returned
+ * as TP_ERR_CUDA.
+ */
+TP_API tp_status_t tp_last_device_status(void *stream);
+
+/*
+ * tp_set_wait_limit_ns - limit on every device-side wait (default 2 s) in
+ * kernels launched after this call, process-wide.  0 restores the default.
+ * A limit of 1 ns makes the waits run out on purpose so that the timeout
+ * path can be tested; the kernels then return early with TP_ERR_TIMEOUT
+ * without faulting or hanging.
+ */
+TP_API tp_status_t tp_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_MLP_H */

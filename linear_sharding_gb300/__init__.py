@@ -1,0 +1,314 @@
+"""Tensor-parallel transformer MLP on one GB300: Python binding of libtpmlp.so.
+
+Argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; PyTorch provides device memory and the current stream.  There is no
+CPU fallback: if the library is missing, loading it raises.
+
+The functions keep the C names (see include/tp_mlp.h for the contract):
+``tp_shard_weights``, ``tp_shard_weights_qkv``, ``tp_shard_get``,
+``tp_mlp_forward``, ``tp_mlp_forward_host``, ``tp_attn_proj_forward``,
+``tp_partial_sum``, ``tp_last_device_status``, ``tp_set_wait_limit_ns``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .volume import ring_allreduce_bytes  # noqa: F401  (host arithmetic, no GPU)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
+
+ACT = {"gelu": 0, "swiglu": 1, "identity": 2}
+DTYPE = {"f32": 0, "bf16": 1}
+VARIANT = {"auto": 0, "partials": 1, "tmem_acc": 2}
+STATUS = {
+    0: "TP_OK", 1: "TP_ERR_ARG", 2: "TP_ERR_INDIVISIBLE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_ARCH",
+    5: "TP_ERR_OOM", 6: "TP_ERR_CUDA", 7: "TP_ERR_TIMEOUT", 8: "TP_ERR_DEVICE_CHECK",
+    9: "TP_ERR_UNSUPPORTED", 10: "TP_ERR_WORKSPACE",
+}
+EXPORTS = (
+    "tp_status_str", "tp_abi_version", "tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get",
+    "tp_shard_info", "tp_shards_destroy", "tp_mlp_workspace_bytes", "tp_mlp_forward",
+    "tp_mlp_host_workspace_bytes", "tp_mlp_forward_host", "tp_attn_proj_workspace_bytes",
+    "tp_attn_proj_forward", "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
+    "tp_colpar_workspace_bytes", "tp_colpar_forward", "tp_rowpar_workspace_bytes",
+    "tp_rowpar_forward",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TPError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtpmlp.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32, sz, u64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t,
+                                 ctypes.c_uint64)
+        lib.tp_status_str.restype = ctypes.c_char_p
+        lib.tp_status_str.argtypes = [i32]
+        lib.tp_abi_version.restype = i32
+        lib.tp_shard_weights.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.tp_shard_weights_qkv.argtypes = [vp, vp, i64, i32, i32, i32, vp, ctypes.POINTER(vp)]
+        lib.tp_shard_get.argtypes = [vp, i32, i32, vp]
+        lib.tp_shard_info.argtypes = [vp] + [vp] * 6
+        lib.tp_shards_destroy.restype = None
+        lib.tp_shards_destroy.argtypes = [vp]
+        lib.tp_mlp_workspace_bytes.restype = sz
+        lib.tp_mlp_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_mlp_forward.argtypes = [vp, vp, i64, i32, i32, vp, vp, sz, vp]
+        lib.tp_mlp_host_workspace_bytes.restype = sz
+        lib.tp_mlp_host_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_mlp_forward_host.argtypes = [vp, vp, i64, i32, i32, vp, vp, sz, vp]
+        lib.tp_attn_proj_workspace_bytes.restype = sz
+        lib.tp_attn_proj_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_attn_proj_forward.argtypes = [vp, vp, vp, i64, i32, vp, vp, vp, sz, vp]
+        lib.tp_partial_sum.argtypes = [ctypes.POINTER(vp), i32, i64, vp, vp]
+        lib.tp_last_device_status.argtypes = [vp]
+        lib.tp_set_wait_limit_ns.argtypes = [u64]
+        lib.tp_colpar_workspace_bytes.restype = sz
+        lib.tp_colpar_workspace_bytes.argtypes = [vp, i64]
+        lib.tp_colpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
+        lib.tp_rowpar_workspace_bytes.restype = sz
+        lib.tp_rowpar_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_rowpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
+        for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
+                     "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
+                     "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
+                     "tp_colpar_forward", "tp_rowpar_forward"):
+            getattr(lib, name).restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise TPError(code, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype_name(t) -> str:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return "bf16"
+    if t.dtype == torch.float32:
+        return "f32"
+    raise TypeError(f"element type {t.dtype} is not supported (bfloat16 or float32)")
+
+
+class Shards:
+    """Library-owned sharded weights (a tp_shards_t handle)."""
+
+    def __init__(self, handle: int, kind: str, H: int, F: int, T: int, act: str, dtype: str,
+                 n_heads: int = 0, head_dim: int = 0):
+        self.handle = ctypes.c_void_p(handle)
+        self.kind, self.H, self.F, self.T, self.act, self.dtype = kind, H, F, T, act, dtype
+        self.n_heads, self.head_dim = n_heads, head_dim
+
+    @property
+    def Fs(self) -> int:
+        return self.F // self.T
+
+    def close(self) -> None:
+        if self.handle and self.handle.value:
+            load_library().tp_shards_destroy(self.handle)
+            self.handle = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tp_shard_weights(W1, W2, T: int, act: str = "gelu", stream=None) -> Shards:
+    """Shard W1 [H x F] (or [H x 2F] = [Wg | Wu] for SwiGLU) by columns and
+    W2 [F x H] by rows into T shards on W1's device."""
+    lib = load_library()
+    dt = _dtype_name(W1)
+    if W2.dtype != W1.dtype:
+        raise TypeError("W1 and W2 must share one element type")
+    W1, W2 = W1.contiguous(), W2.contiguous()
+    F, H = W2.shape
+    out = ctypes.c_void_p()
+    _check(lib.tp_shard_weights(_ptr(W1), _ptr(W2), H, F, T, ACT[act], DTYPE[dt], _stream(stream),
+                                ctypes.byref(out)), "tp_shard_weights")
+    return Shards(out.value, "mlp", H, F, T, act, dt)
+
+
+def tp_shard_weights_qkv(Wqkv, Wo, n_heads: int, head_dim: int, T: int, stream=None) -> Shards:
+    """Shard [Wq | Wk | Wv] ([H x 3H]) and Wo ([H x H]) by heads into T shards."""
+    lib = load_library()
+    if _dtype_name(Wqkv) != "bf16" or Wo.dtype != Wqkv.dtype:
+        raise TypeError("attention projections take bfloat16 weights")
+    Wqkv, Wo = Wqkv.contiguous(), Wo.contiguous()
+    H = Wo.shape[0]
+    out = ctypes.c_void_p()
+    _check(lib.tp_shard_weights_qkv(_ptr(Wqkv), _ptr(Wo), H, n_heads, head_dim, T, _stream(stream),
+                                    ctypes.byref(out)), "tp_shard_weights_qkv")
+    return Shards(out.value, "qkv", H, H, T, "identity", "bf16", n_heads, head_dim)
+
+
+def tp_shard_get(s: Shards, i: int, which: int):
+    """The logical shard i as a host numpy array (bfloat16 as uint16 bits):
+    which 0 = W1_i / Wg_i / Wqkv_i, 1 = Wu_i, 2 = W2_i / Wo_i."""
+    import numpy as np
+    lib = load_library()
+    W = s.Fs
+    if which == 2:
+        shape = (W, s.H)
+    elif s.kind == "qkv":
+        shape = (s.H, 3 * W)
+    else:
+        shape = (s.H, W)
+    out = np.empty(shape, dtype=np.uint16 if s.dtype == "bf16" else np.float32)
+    _check(lib.tp_shard_get(s.handle, i, which, out.ctypes.data_as(ctypes.c_void_p)), "tp_shard_get")
+    return out
+
+
+def tp_mlp_workspace_bytes(s: Shards, M: int, variant: str = "auto") -> int:
+    return int(load_library().tp_mlp_workspace_bytes(s.handle, M, VARIANT[variant]))
+
+
+def tp_mlp_forward(s: Shards, X, variant: str = "auto", Z=None, workspace=None, act=None,
+                   stream=None):
+    """Z = sum_i act(X W1_i) W2_i ([M x H] float32) on X's device."""
+    torch = _torch()
+    lib = load_library()
+    if X.dim() != 2 or X.shape[1] != s.H or _dtype_name(X) != s.dtype:
+        raise ValueError("X must be [M x H] with the shards' element type")
+    X = X.contiguous()
+    M = X.shape[0]
+    if Z is None:
+        Z = torch.empty((M, s.H), dtype=torch.float32, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_mlp_forward(s.handle, _ptr(X), M, ACT[act or s.act], VARIANT[variant], _ptr(Z),
+                              _ptr(workspace), ws_bytes, _stream(stream)), "tp_mlp_forward")
+    return Z
+
+
+def tp_colpar_workspace_bytes(s: Shards, M: int) -> int:
+    return int(load_library().tp_colpar_workspace_bytes(s.handle, M))
+
+
+def tp_colpar_forward(s: Shards, X, Y=None, workspace=None, act=None, stream=None):
+    """Y_i = act(X W1_i) for every shard: Y is [T x M x F/T] (shard blocks contiguous)."""
+    torch = _torch()
+    lib = load_library()
+    X = X.contiguous()
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((s.T, M, s.Fs), dtype=X.dtype, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_colpar_forward(s.handle, _ptr(X), M, ACT[act or s.act], _ptr(Y), _ptr(workspace),
+                                 ws_bytes, _stream(stream)), "tp_colpar_forward")
+    return Y
+
+
+def tp_rowpar_workspace_bytes(s: Shards, M: int, variant: str = "auto") -> int:
+    return int(load_library().tp_rowpar_workspace_bytes(s.handle, M, VARIANT[variant]))
+
+
+def tp_rowpar_forward(s: Shards, Y, variant: str = "auto", Z=None, workspace=None, stream=None):
+    """Z = sum_i Y_i W2_i ([M x H] float32), the row-parallel layer and its all-reduce-sum."""
+    torch = _torch()
+    lib = load_library()
+    M = Y.shape[1]
+    if Z is None:
+        Z = torch.empty((M, s.H), dtype=torch.float32, device=Y.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_rowpar_forward(s.handle, _ptr(Y), M, VARIANT[variant], _ptr(Z), _ptr(workspace),
+                                 ws_bytes, _stream(stream)), "tp_rowpar_forward")
+    return Z
+
+
+def tp_mlp_host_workspace_bytes(s: Shards, M: int, variant: str = "auto") -> int:
+    return int(load_library().tp_mlp_host_workspace_bytes(s.handle, M, VARIANT[variant]))
+
+
+def tp_mlp_forward_host(s: Shards, X_host, Z_host, workspace, variant: str = "auto", stream=None):
+    """The forward pass from host buffers (pinned CPU tensors): copies X in,
+    computes, copies Z back, all enqueued on the stream."""
+    lib = load_library()
+    M = X_host.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.tp_mlp_forward_host(s.handle, _ptr(X_host), M, ACT[s.act], VARIANT[variant],
+                                   _ptr(Z_host), _ptr(workspace), ws_bytes, _stream(stream)),
+           "tp_mlp_forward_host")
+    return Z_host
+
+
+def tp_attn_proj_workspace_bytes(s: Shards, M: int, variant: str = "auto") -> int:
+    return int(load_library().tp_attn_proj_workspace_bytes(s.handle, M, VARIANT[variant]))
+
+
+def tp_attn_proj_forward(s: Shards, X=None, A=None, variant: str = "auto", QKV=None, Z=None,
+                         workspace=None, stream=None):
+    """QKV_i = X Wqkv_i ([T x M x 3W] bf16) and Z = sum_i A_i Wo_i ([M x H] float32)."""
+    torch = _torch()
+    lib = load_library()
+    ref = X if X is not None else A
+    M = ref.shape[0]
+    W = s.Fs
+    if X is not None and QKV is None:
+        QKV = torch.empty((s.T, M, 3 * W), dtype=torch.bfloat16, device=ref.device)
+    if A is not None and Z is None:
+        Z = torch.empty((M, s.H), dtype=torch.float32, device=ref.device)
+    X = X.contiguous() if X is not None else None
+    A = A.contiguous() if A is not None else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_attn_proj_forward(s.handle, _ptr(X), _ptr(A), M, VARIANT[variant],
+                                    _ptr(QKV if X is not None else None),
+                                    _ptr(Z if A is not None else None), _ptr(workspace), ws_bytes,
+                                    _stream(stream)), "tp_attn_proj_forward")
+    return QKV, Z
+
+
+def tp_partial_sum(parts, Z=None, stream=None):
+    """Z = ((parts[0] + parts[1]) + ...) + parts[T-1], float32, on the GPU."""
+    torch = _torch()
+    lib = load_library()
+    T = len(parts)
+    n = parts[0].numel()
+    if Z is None:
+        Z = torch.empty_like(parts[0])
+    arr = (ctypes.c_void_p * T)(*[p.data_ptr() for p in parts])
+    _check(lib.tp_partial_sum(arr, T, n, _ptr(Z), _stream(stream)), "tp_partial_sum")
+    return Z
+
+
+def tp_last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load_library().tp_last_device_status(_stream(stream)))
+
+
+def tp_set_wait_limit_ns(ns: int) -> None:
+    _check(load_library().tp_set_wait_limit_ns(int(ns)), "tp_set_wait_limit_ns")

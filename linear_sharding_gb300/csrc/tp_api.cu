@@ -1,0 +1,831 @@
+// tp_api.cu - the C ABI of libtpmlp.so (declared in include/tp_mlp.h):
+// argument checks, the shard handles, TMA tensor maps, the per-shape launch
+// plan and the order of the kernels of one forward pass.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "tp_internal.h"
+
+using namespace tp;
+
+struct tp_shards {
+  int kind = 0;  // 0 = MLP, 1 = QKV
+  int device = 0;
+  int64_t H = 0, F = 0, Fs = 0;  // QKV: F = H, Fs = W (head columns per shard)
+  int T = 0;
+  tp_act_t act = TP_ACT_GELU_ERF;
+  tp_dtype_t dt = TP_BF16;
+  int n_heads = 0, head_dim = 0;
+  int64_t R1 = 0;  // packed first-layer rows per shard (Fs, 2 Fs for SwiGLU, 3 W for QKV)
+  void *w1p = nullptr;  // [T][R1][H]
+  void *w2p = nullptr;  // [T][H][Fs]
+  int bn1 = 256, bn2 = 256;
+  CUtensorMap map_w1_b, map_w1_a, map_w2_b, map_w2_a;
+};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxShards = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+constexpr int kDecodeMaxM = 16;
+
+struct DevState {
+  bool ready = false;
+  int sms = 0;
+  unsigned int *status = nullptr;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+tp_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TP_OK;
+  if (e == cudaErrorMemoryAllocation) return TP_ERR_OOM;
+  return TP_ERR_CUDA;
+}
+
+#define TP_TRY(expr)                      \
+  do {                                    \
+    const tp_status_t _st = (expr);       \
+    if (_st != TP_OK) return _st;         \
+  } while (0)
+
+#define TP_CUDA(expr) TP_TRY(cuda_status(expr))
+
+// Per-device state: SM count and the status word, created on first use.
+tp_status_t dev_state(DevState **out, int *dev_out = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return TP_ERR_CUDA;
+    if (major != 10 || minor != 3) return TP_ERR_ARCH;
+    unsigned int *st = nullptr;
+    if (cudaMalloc(&st, 256) != cudaSuccess) return TP_ERR_OOM;
+    if (cudaMemset(st, 0, 256) != cudaSuccess) {
+      cudaFree(st);
+      return TP_ERR_CUDA;
+    }
+    d.sms = sms;
+    d.status = st;
+    d.ready = true;
+  }
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return TP_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map, dims {d0 (contiguous), d1, d2}, byte strides {s1, s2},
+// box {64, box1, 1}, 128-byte swizzle, zero fill out of bounds.
+tp_status_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t s1, uint64_t s2, uint32_t box1) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return TP_ERR_CUDA;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {64, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                       strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TP_OK : TP_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t esize(tp_dtype_t dt) { return dt == TP_BF16 ? 2 : 4; }
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+GemmArgs base_args(const DevState *d) {
+  GemmArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.group_m = 16;
+  g.status = d->status;
+  g.wait_limit_ns = g_wait_ns.load();
+  return g;
+}
+
+// ---- planning ---------------------------------------------------------------
+
+// Number of accumulation slots of a row-parallel GEMM with `tiles` output
+// tiles of `kt_total` k-tiles, split into slots that each cover whole shard
+// groups (divisors of T) or, when `sub_ok`, also sub-ranges of a shard.
+// Cost = waves x k-tiles per unit (compute or weight streaming) plus the
+// float32 partial traffic (written once, read by the shard-sum) expressed in
+// k-tile units.
+int choose_slots(int64_t tiles, int T, int kt_per_seg, int sms, double ktile_per_partial_byte,
+                 int64_t partial_bytes, bool sub_ok) {
+  int best = 1;
+  double best_cost = 1e300;
+  auto consider = [&](int S) {
+    const int64_t kt_total = static_cast<int64_t>(T) * kt_per_seg;
+    if (kt_total % S) return;
+    const int64_t units = tiles * S;
+    const int64_t waves = cdiv(units, sms);
+    double cost = static_cast<double>(waves) * static_cast<double>(kt_total / S);
+    if (S > 1) cost += ktile_per_partial_byte * static_cast<double>(partial_bytes) * (2.0 * S + 1.0) / sms;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = S;
+    }
+  };
+  for (int S = 1; S <= T; ++S)
+    if (T % S == 0) consider(S);
+  if (sub_ok)
+    for (int sub = 2; sub <= 8; ++sub)
+      if (kt_per_seg % sub == 0 && T * sub <= kMaxShards) consider(T * sub);
+  return best;
+}
+
+struct MlpPlan {
+  bool simt = false, decode = false;
+  int slots1 = 1;  // decode: split-K slots of the first layer
+  int slots2 = 1;  // second layer accumulation slots (1 = all shards in one accumulator)
+  size_t y_bytes = 0;    // Y, T x M x Fs elements
+  size_t col_bytes = 0;  // first-layer scratch (decode split-K partials)
+  size_t row_bytes = 0;  // second-layer scratch (float32 partials)
+  size_t total() const { return round256(y_bytes) + round256(col_bytes) + round256(row_bytes); }
+};
+
+tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, int sms, MlpPlan *p) {
+  *p = MlpPlan();
+  const int64_t H = s->H, Fs = s->Fs, T = s->T, R1 = s->R1;
+  const size_t eb = esize(s->dt);
+  p->y_bytes = static_cast<size_t>(T * M * Fs) * eb;
+  if (s->dt == TP_F32) {
+    p->simt = true;
+    p->slots2 = (v == TP_VAR_PARTIALS) ? static_cast<int>(T) : 1;
+  } else if (M <= kDecodeMaxM) {
+    p->decode = true;
+    const int kps = static_cast<int>(Fs / 64);
+    // Weight streaming: one 128 x 64 bf16 A tile (16 KiB) per k-tile.
+    const double per_byte = 1.0 / (128.0 * 64.0 * 2.0);
+    p->slots1 = choose_slots((T * R1) / 128, 1, static_cast<int>(H / 64), sms, per_byte,
+                             static_cast<int64_t>(M * T * R1 * 4), true);
+    if (v == TP_VAR_TMEM_ACC)
+      p->slots2 = 1;
+    else if (v == TP_VAR_PARTIALS)
+      p->slots2 = static_cast<int>(T);
+    else
+      p->slots2 = choose_slots(H / 128, static_cast<int>(T), kps, sms, per_byte,
+                               static_cast<int64_t>(M * H * 4), true);
+    p->col_bytes = static_cast<size_t>(p->slots1 * M * T * R1) * 4;
+  } else {
+    const int kps = static_cast<int>(Fs / 64);
+    if (v == TP_VAR_TMEM_ACC)
+      p->slots2 = 1;
+    else if (v == TP_VAR_PARTIALS)
+      p->slots2 = static_cast<int>(T);
+    else {
+      // Tensor-bound: one k-tile of a 128 x bn2 tile is 2*128*bn2*64 flop; a
+      // partial byte costs (peak flop/s per SM) / (HBM bytes/s per SM).
+      const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
+      const double per_byte = (1.9e15 / 6.5e12) / flop_per_ktile;
+      p->slots2 = choose_slots(cdiv(M, 128) * (H / s->bn2), static_cast<int>(T), kps, sms, per_byte,
+                               static_cast<int64_t>(M * H * 4), false);
+    }
+  }
+  p->row_bytes = p->slots2 > 1 ? static_cast<size_t>(p->slots2 * M * H) * 4 : 0;
+  return TP_OK;
+}
+
+// ---- forward passes ---------------------------------------------------------
+
+Epi act_epi(tp_act_t act) {
+  return act == TP_ACT_GELU_ERF ? EPI_GELU_BF16 : act == TP_ACT_SWIGLU ? EPI_SWIGLU_BF16 : EPI_IDENT_BF16;
+}
+
+GemmCfg cfg_for(int bn) { return bn == 256 ? CFG_N256 : CFG_N128; }
+
+// Row-parallel GEMM over T shards into Z, with `slots` accumulation slots
+// (slots > 1: float32 partials in P, then the shard-sum).
+tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &mapA, int a_seg,
+                      int64_t M, int slots, float *P, float *Z, cudaStream_t st) {
+  const int64_t H = s->H;
+  GemmArgs g = base_args(d);
+  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.n_tiles = static_cast<int>(H / s->bn2);
+  g.slots = slots;
+  g.kt_per_seg = static_cast<int>(s->Fs / 64);
+  g.kt_total = s->T * g.kt_per_seg;
+  g.kt_per_slot = g.kt_total / slots;
+  g.a_seg = a_seg;
+  g.b_seg = 1;
+  g.rows_valid = static_cast<int>(M);
+  g.cols_valid = static_cast<int>(H);
+  g.out = slots > 1 ? static_cast<void *>(P) : static_cast<void *>(Z);
+  g.ld_out = H;
+  g.slot_stride = M * H;
+  TP_CUDA(launch_gemm(cfg_for(s->bn2), EPI_F32, mapA, s->map_w2_b, g, d->sms, st));
+  if (slots > 1) TP_CUDA(launch_shard_sum_strided(P, slots, M * H, M * H, Z, d->sms, st));
+  return TP_OK;
+}
+
+// Column-parallel GEMM of all shards: out[shard][M][shard_cols] bf16.
+tp_status_t colpar_tc(const tp_shards *s, const DevState *d, const void *X, int64_t M, Epi epi,
+                      void *out, int64_t shard_cols, cudaStream_t st) {
+  const int64_t H = s->H;
+  CUtensorMap mx;
+  TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
+  GemmArgs g = base_args(d);
+  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.n_tiles = static_cast<int>(s->T * s->R1 / s->bn1);
+  g.slots = 1;
+  g.kt_total = static_cast<int>(H / 64);
+  g.kt_per_seg = g.kt_total;
+  g.kt_per_slot = g.kt_total;
+  g.rows_valid = static_cast<int>(M);
+  g.cols_valid = static_cast<int>(s->T * shard_cols);
+  g.out = out;
+  g.ld_out = shard_cols;
+  g.shard_stride = M * shard_cols;
+  g.shard_cols = static_cast<int>(shard_cols);
+  TP_CUDA(launch_gemm(cfg_for(s->bn1), epi, mx, s->map_w1_b, g, d->sms, st));
+  return TP_OK;
+}
+
+// Decode first layer: operands swapped (weight rows x tokens), split-K
+// float32 partials P1, then the activation into Y.
+tp_status_t colpar_decode(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *X,
+                          int64_t M, tp_act_t act, void *Y, float *P1, cudaStream_t st) {
+  const int64_t H = s->H, T = s->T, Fs = s->Fs, rows1 = T * s->R1;
+  CUtensorMap mxb;
+  TP_TRY(make_map(&mxb, X, H, M, 1, H * 2, M * H * 2, 16));
+  GemmArgs g = base_args(d);
+  g.m_tiles = static_cast<int>(rows1 / 128);
+  g.n_tiles = 1;
+  g.slots = p.slots1;
+  g.kt_total = static_cast<int>(H / 64);
+  g.kt_per_seg = g.kt_total;
+  g.kt_per_slot = g.kt_total / p.slots1;
+  g.group_m = 1;
+  g.rows_valid = static_cast<int>(rows1);
+  g.cols_valid = static_cast<int>(M);
+  g.out = P1;
+  g.ld_out = rows1;
+  g.slot_stride = M * rows1;
+  TP_CUDA(launch_gemm(CFG_N16, EPI_F32_T, s->map_w1_a, mxb, g, d->sms, st));
+  TP_CUDA(launch_decode_act(P1, p.slots1, M * rows1, rows1, static_cast<int>(M), static_cast<int>(T),
+                            static_cast<int>(Fs), act, act == TP_ACT_SWIGLU, Y, st));
+  return TP_OK;
+}
+
+// Decode second layer: W2 rows x tokens, per-shard (and split) slots, then
+// the shard-sum.
+tp_status_t rowpar_decode(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *Y,
+                          int64_t M, float *Z, float *P2, cudaStream_t st) {
+  const int64_t H = s->H, T = s->T, Fs = s->Fs;
+  CUtensorMap myb;
+  TP_TRY(make_map(&myb, Y, Fs, M, T, Fs * 2, M * Fs * 2, 16));
+  GemmArgs g = base_args(d);
+  g.m_tiles = static_cast<int>(H / 128);
+  g.n_tiles = 1;
+  g.slots = p.slots2;
+  g.kt_per_seg = static_cast<int>(Fs / 64);
+  g.kt_total = static_cast<int>(T) * g.kt_per_seg;
+  g.kt_per_slot = g.kt_total / p.slots2;
+  g.a_seg = 1;
+  g.b_seg = 1;
+  g.group_m = 1;
+  g.rows_valid = static_cast<int>(H);
+  g.cols_valid = static_cast<int>(M);
+  g.out = p.slots2 > 1 ? static_cast<void *>(P2) : static_cast<void *>(Z);
+  g.ld_out = H;
+  g.slot_stride = M * H;
+  TP_CUDA(launch_gemm(CFG_N16, EPI_F32_T, s->map_w2_a, myb, g, d->sms, st));
+  if (p.slots2 > 1) TP_CUDA(launch_shard_sum_strided(P2, p.slots2, M * H, M * H, Z, d->sms, st));
+  return TP_OK;
+}
+
+tp_status_t colpar_simt(const tp_shards *s, const void *X, int64_t M, tp_act_t act, void *Y,
+                        cudaStream_t st) {
+  const int64_t H = s->H, T = s->T, Fs = s->Fs;
+  SimtArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.A = static_cast<const float *>(X);
+  a.B = static_cast<const float *>(s->w1p);
+  a.lda = H;
+  a.ldb = H;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(T * s->R1);
+  a.k_seg = static_cast<int>(H);
+  a.nseg = 1;
+  a.segs_per_slot = 1;
+  a.epi = act_epi(act);
+  a.out = static_cast<float *>(Y);
+  a.ld_out = Fs;
+  a.shard_stride = M * Fs;
+  a.shard_cols = static_cast<int>(Fs);
+  TP_CUDA(launch_simt_gemm(a, st));
+  return TP_OK;
+}
+
+tp_status_t rowpar_simt(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *Y,
+                        int64_t M, float *Z, float *P, cudaStream_t st) {
+  const int64_t H = s->H, T = s->T, Fs = s->Fs;
+  SimtArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.A = static_cast<const float *>(Y);
+  a.B = static_cast<const float *>(s->w2p);
+  a.lda = Fs;
+  a.ldb = Fs;
+  a.a_seg = M * Fs;
+  a.b_seg = H * Fs;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(H);
+  a.k_seg = static_cast<int>(Fs);
+  a.nseg = static_cast<int>(T);
+  a.segs_per_slot = p.slots2 > 1 ? static_cast<int>(T) / p.slots2 : static_cast<int>(T);
+  a.epi = EPI_F32;
+  a.out = p.slots2 > 1 ? P : Z;
+  a.ld_out = H;
+  a.slot_stride = M * H;
+  TP_CUDA(launch_simt_gemm(a, st));
+  if (p.slots2 > 1) TP_CUDA(launch_shard_sum_strided(P, p.slots2, M * H, M * H, Z, d->sms, st));
+  return TP_OK;
+}
+
+tp_status_t colpar_any(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *X,
+                       int64_t M, tp_act_t act, void *Y, char *ws_col, cudaStream_t st) {
+  if (p.simt) return colpar_simt(s, X, M, act, Y, st);
+  if (p.decode) return colpar_decode(s, d, p, X, M, act, Y, reinterpret_cast<float *>(ws_col), st);
+  return colpar_tc(s, d, X, M, act_epi(act), Y, s->Fs, st);
+}
+
+tp_status_t rowpar_any(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *Y,
+                       int64_t M, float *Z, char *ws_row, cudaStream_t st) {
+  float *P = reinterpret_cast<float *>(ws_row);
+  if (p.simt) return rowpar_simt(s, d, p, Y, M, Z, P, st);
+  if (p.decode) return rowpar_decode(s, d, p, Y, M, Z, P, st);
+  CUtensorMap my;
+  TP_TRY(make_map(&my, Y, s->Fs, M, s->T, s->Fs * 2, M * s->Fs * 2, 128));
+  return rowpar_tc(s, d, my, 1, M, p.slots2, P, Z, st);
+}
+
+tp_status_t check_handle(const tp_shards *s, int kind, DevState **d) {
+  if (!s || s->kind != kind) return TP_ERR_ARG;
+  int dev = 0;
+  TP_TRY(dev_state(d, &dev));
+  if (dev != s->device) return TP_ERR_ARG;
+  return TP_OK;
+}
+
+bool valid_variant(tp_variant_t v) {
+  return v == TP_VAR_AUTO || v == TP_VAR_PARTIALS || v == TP_VAR_TMEM_ACC;
+}
+
+// Workspace: the caller's, or one allocated stream-ordered for this call.
+struct Workspace {
+  char *ptr = nullptr;
+  bool owned = false;
+  cudaStream_t st = nullptr;
+  ~Workspace() {
+    if (owned && ptr) cudaFreeAsync(ptr, st);
+  }
+};
+
+tp_status_t get_ws(Workspace *w, void *given, size_t given_bytes, size_t need, cudaStream_t st) {
+  w->st = st;
+  if (given) {
+    if (given_bytes < need) return TP_ERR_WORKSPACE;
+    if (!aligned16(given)) return TP_ERR_ARG;
+    w->ptr = static_cast<char *>(given);
+    return TP_OK;
+  }
+  if (need == 0) return TP_OK;
+  void *p = nullptr;
+  if (cudaMallocAsync(&p, need, st) != cudaSuccess) return TP_ERR_OOM;
+  w->ptr = static_cast<char *>(p);
+  w->owned = true;
+  return TP_OK;
+}
+
+bool act_ok(const tp_shards *s, tp_act_t act) {
+  if (act == s->act) return true;
+  return s->act != TP_ACT_SWIGLU && (act == TP_ACT_GELU_ERF || act == TP_ACT_IDENTITY);
+}
+
+tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
+                             float *Z, void *workspace, size_t ws_bytes, cudaStream_t st) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (M < 0 || !valid_variant(v) || !act_ok(s, act)) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!X || !Z || !aligned16(X) || !aligned16(Z)) return TP_ERR_ARG;
+  if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
+  MlpPlan p;
+  TP_TRY(plan_mlp(s, M, v, d->sms, &p));
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
+  char *Y = w.ptr;
+  char *ws_col = Y + round256(p.y_bytes);
+  char *ws_row = ws_col + round256(p.col_bytes);
+  TP_TRY(colpar_any(s, d, p, X, M, act, Y, ws_col, st));
+  return rowpar_any(s, d, p, Y, M, Z, ws_row, st);
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+
+extern "C" {
+
+const char *tp_status_str(tp_status_t s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_ARG: return "TP_ERR_ARG: invalid argument";
+    case TP_ERR_INDIVISIBLE: return "TP_ERR_INDIVISIBLE: dimension not divisible by the shard count";
+    case TP_ERR_DTYPE: return "TP_ERR_DTYPE: element type not supported";
+    case TP_ERR_ARCH: return "TP_ERR_ARCH: current device is not sm_103 (GB300)";
+    case TP_ERR_OOM: return "TP_ERR_OOM: allocation failed";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA: CUDA call failed";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT: a device-side wait ran out";
+    case TP_ERR_DEVICE_CHECK: return "TP_ERR_DEVICE_CHECK: a device-side check failed";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: shape not supported by the kernels";
+    case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace too small";
+  }
+  return "unknown tp_status_t";
+}
+
+int tp_abi_version(void) { return TP_ABI_VERSION; }
+
+tp_status_t tp_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+  return TP_OK;
+}
+
+tp_status_t tp_shard_weights(const void *W1, const void *W2, int64_t H, int64_t F, int T,
+                             tp_act_t act, tp_dtype_t dt, void *stream, tp_shards_t *out) {
+  if (!out) return TP_ERR_ARG;
+  *out = nullptr;
+  if (!W1 || !W2 || H <= 0 || F <= 0 || T < 1 || T > kMaxShards) return TP_ERR_ARG;
+  if (act != TP_ACT_GELU_ERF && act != TP_ACT_SWIGLU && act != TP_ACT_IDENTITY) return TP_ERR_ARG;
+  if (dt != TP_F32 && dt != TP_BF16) return TP_ERR_DTYPE;
+  if (F % T != 0) return TP_ERR_INDIVISIBLE;
+  const int64_t Fs = F / T;
+  const size_t eb = esize(dt);
+  if ((reinterpret_cast<uintptr_t>(W1) | reinterpret_cast<uintptr_t>(W2)) % eb) return TP_ERR_ARG;
+  if (dt == TP_BF16 && (H % 128 != 0 || Fs % 128 != 0)) return TP_ERR_UNSUPPORTED;
+  if (act == TP_ACT_SWIGLU && Fs % kSwigluGranule != 0) return TP_ERR_UNSUPPORTED;
+  if (H > (1LL << 31) || F > (1LL << 31)) return TP_ERR_UNSUPPORTED;
+  DevState *d = nullptr;
+  int dev = 0;
+  TP_TRY(dev_state(&d, &dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  tp_shards *s = new (std::nothrow) tp_shards();
+  if (!s) return TP_ERR_OOM;
+  s->kind = 0;
+  s->device = dev;
+  s->H = H;
+  s->F = F;
+  s->Fs = Fs;
+  s->T = T;
+  s->act = act;
+  s->dt = dt;
+  s->R1 = act == TP_ACT_SWIGLU ? 2 * Fs : Fs;
+  const size_t b1 = static_cast<size_t>(T * s->R1 * H) * eb, b2 = static_cast<size_t>(T * H * Fs) * eb;
+  if (cudaMalloc(&s->w1p, b1) != cudaSuccess || cudaMalloc(&s->w2p, b2) != cudaSuccess) {
+    tp_shards_destroy(s);
+    return TP_ERR_OOM;
+  }
+  tp_status_t r = cuda_status(launch_pack(act == TP_ACT_SWIGLU ? PACK_W1_SWIGLU : PACK_W1, W1,
+                                          act == TP_ACT_SWIGLU ? 2 * F : F, s->w1p, T, s->R1, H,
+                                          static_cast<int>(eb), F, 0, Fs, st));
+  if (r == TP_OK)
+    r = cuda_status(launch_pack(PACK_ROWS, W2, H, s->w2p, T, H, Fs, static_cast<int>(eb), 0, 0, 0, st));
+  if (r == TP_OK && dt == TP_BF16) {
+    s->bn1 = (act == TP_ACT_SWIGLU || Fs % 256 == 0) ? 256 : 128;
+    s->bn2 = (H % 256 == 0) ? 256 : 128;
+    const int64_t rows1 = T * s->R1;
+    r = make_map(&s->map_w1_b, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, s->bn1);
+    if (r == TP_OK) r = make_map(&s->map_w1_a, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, 128);
+    if (r == TP_OK) r = make_map(&s->map_w2_b, s->w2p, Fs, H, T, Fs * 2, H * Fs * 2, s->bn2);
+    if (r == TP_OK) r = make_map(&s->map_w2_a, s->w2p, Fs, H, T, Fs * 2, H * Fs * 2, 128);
+  }
+  if (r != TP_OK) {
+    tp_shards_destroy(s);
+    return r;
+  }
+  *out = s;
+  return TP_OK;
+}
+
+tp_status_t tp_shard_weights_qkv(const void *Wqkv, const void *Wo, int64_t H, int n_heads,
+                                 int head_dim, int T, void *stream, tp_shards_t *out) {
+  if (!out) return TP_ERR_ARG;
+  *out = nullptr;
+  if (!Wqkv || !Wo || H <= 0 || n_heads <= 0 || head_dim <= 0 || T < 1 || T > kMaxShards)
+    return TP_ERR_ARG;
+  if (static_cast<int64_t>(n_heads) * head_dim != H) return TP_ERR_ARG;
+  if (n_heads % T != 0) return TP_ERR_INDIVISIBLE;
+  const int64_t W = static_cast<int64_t>(n_heads / T) * head_dim;
+  if ((reinterpret_cast<uintptr_t>(Wqkv) | reinterpret_cast<uintptr_t>(Wo)) % 2) return TP_ERR_ARG;
+  if (H % 128 != 0 || W % 64 != 0 || (3 * W) % 128 != 0) return TP_ERR_UNSUPPORTED;
+  DevState *d = nullptr;
+  int dev = 0;
+  TP_TRY(dev_state(&d, &dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  tp_shards *s = new (std::nothrow) tp_shards();
+  if (!s) return TP_ERR_OOM;
+  s->kind = 1;
+  s->device = dev;
+  s->H = H;
+  s->F = H;
+  s->Fs = W;
+  s->T = T;
+  s->act = TP_ACT_IDENTITY;
+  s->dt = TP_BF16;
+  s->n_heads = n_heads;
+  s->head_dim = head_dim;
+  s->R1 = 3 * W;
+  const size_t b1 = static_cast<size_t>(T * s->R1 * H) * 2, b2 = static_cast<size_t>(T * H * W) * 2;
+  if (cudaMalloc(&s->w1p, b1) != cudaSuccess || cudaMalloc(&s->w2p, b2) != cudaSuccess) {
+    tp_shards_destroy(s);
+    return TP_ERR_OOM;
+  }
+  tp_status_t r = cuda_status(launch_pack(PACK_QKV, Wqkv, 3 * H, s->w1p, T, s->R1, H, 2, 0, H, W, st));
+  if (r == TP_OK) r = cuda_status(launch_pack(PACK_ROWS, Wo, H, s->w2p, T, H, W, 2, 0, 0, 0, st));
+  if (r == TP_OK) {
+    s->bn1 = ((3 * W) % 256 == 0) ? 256 : 128;
+    s->bn2 = (H % 256 == 0) ? 256 : 128;
+    const int64_t rows1 = T * s->R1;
+    r = make_map(&s->map_w1_b, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, s->bn1);
+    if (r == TP_OK) r = make_map(&s->map_w1_a, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, 128);
+    if (r == TP_OK) r = make_map(&s->map_w2_b, s->w2p, W, H, T, W * 2, H * W * 2, s->bn2);
+    if (r == TP_OK) r = make_map(&s->map_w2_a, s->w2p, W, H, T, W * 2, H * W * 2, 128);
+  }
+  if (r != TP_OK) {
+    tp_shards_destroy(s);
+    return r;
+  }
+  *out = s;
+  return TP_OK;
+}
+
+tp_status_t tp_shard_get(tp_shards_t s, int i, int which, void *host_dst) {
+  if (!s || !host_dst || i < 0 || i >= s->T) return TP_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (dev != s->device) return TP_ERR_ARG;
+  const size_t eb = esize(s->dt);
+  PackMode mode;
+  const void *packed;
+  int64_t R, K, W, elems;
+  int wh = 0;
+  if (which == 2) {
+    mode = PACK_ROWS;
+    packed = s->w2p;
+    R = s->H;
+    K = s->Fs;
+    W = 0;
+    elems = s->Fs * s->H;
+  } else if (which == 0 || which == 1) {
+    if (s->kind == 1) {
+      if (which != 0) return TP_ERR_ARG;
+      mode = PACK_QKV;
+      elems = s->H * 3 * s->Fs;
+    } else {
+      if (which == 1 && s->act != TP_ACT_SWIGLU) return TP_ERR_ARG;
+      mode = s->act == TP_ACT_SWIGLU ? PACK_W1_SWIGLU : PACK_W1;
+      elems = s->H * s->Fs;
+      wh = which;
+    }
+    packed = s->w1p;
+    R = s->R1;
+    K = s->H;
+    W = s->Fs;
+  } else {
+    return TP_ERR_ARG;
+  }
+  void *tmp = nullptr;
+  if (cudaMalloc(&tmp, static_cast<size_t>(elems) * eb) != cudaSuccess) return TP_ERR_OOM;
+  tp_status_t r = cuda_status(launch_unpack(mode, packed, tmp, i, wh, R, K, static_cast<int>(eb), W, 0));
+  if (r == TP_OK) r = cuda_status(cudaMemcpy(host_dst, tmp, static_cast<size_t>(elems) * eb,
+                                             cudaMemcpyDeviceToHost));
+  cudaFree(tmp);
+  return r;
+}
+
+tp_status_t tp_shard_info(tp_shards_t s, int *kind, int64_t *H, int64_t *F, int *T, int *act,
+                          int *dtype) {
+  if (!s) return TP_ERR_ARG;
+  if (kind) *kind = s->kind;
+  if (H) *H = s->H;
+  if (F) *F = s->F;
+  if (T) *T = s->T;
+  if (act) *act = s->act;
+  if (dtype) *dtype = s->dt;
+  return TP_OK;
+}
+
+void tp_shards_destroy(tp_shards_t s) {
+  if (!s) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != s->device) cudaSetDevice(s->device);
+  cudaDeviceSynchronize();
+  if (s->w1p) cudaFree(s->w1p);
+  if (s->w2p) cudaFree(s->w2p);
+  if (prev >= 0 && prev != s->device) cudaSetDevice(prev);
+  delete s;
+}
+
+size_t tp_mlp_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
+  MlpPlan p;
+  if (plan_mlp(s, M, v, d->sms, &p) != TP_OK) return 0;
+  return p.total();
+}
+
+size_t tp_colpar_workspace_bytes(tp_shards_t s, int64_t M) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || dev_state(&d) != TP_OK) return 0;
+  MlpPlan p;
+  if (plan_mlp(s, M, TP_VAR_AUTO, d->sms, &p) != TP_OK) return 0;
+  return p.col_bytes;
+}
+
+tp_status_t tp_colpar_forward(tp_shards_t s, const void *X, int64_t M, tp_act_t act, void *Y,
+                              void *workspace, size_t ws_bytes, void *stream) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (M < 0 || !act_ok(s, act)) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!X || !Y || !aligned16(X) || !aligned16(Y)) return TP_ERR_ARG;
+  if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MlpPlan p;
+  TP_TRY(plan_mlp(s, M, TP_VAR_AUTO, d->sms, &p));
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.col_bytes, st));
+  return colpar_any(s, d, p, X, M, act, Y, w.ptr, st);
+}
+
+size_t tp_rowpar_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
+  MlpPlan p;
+  if (plan_mlp(s, M, v, d->sms, &p) != TP_OK) return 0;
+  return p.row_bytes;
+}
+
+tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp_variant_t v, float *Z,
+                              void *workspace, size_t ws_bytes, void *stream) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (M < 0 || !valid_variant(v)) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!Y || !Z || !aligned16(Y) || !aligned16(Z)) return TP_ERR_ARG;
+  if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MlpPlan p;
+  TP_TRY(plan_mlp(s, M, v, d->sms, &p));
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.row_bytes, st));
+  return rowpar_any(s, d, p, Y, M, Z, w.ptr, st);
+}
+
+tp_status_t tp_mlp_forward(tp_shards_t s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
+                           float *Z, void *workspace, size_t ws_bytes, void *stream) {
+  return mlp_forward_impl(s, X, M, act, v, Z, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t tp_mlp_host_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  if (!s || s->kind != 0 || M <= 0) return 0;
+  const size_t inner = tp_mlp_workspace_bytes(s, M, v);
+  if (inner == 0) return 0;
+  return round256(static_cast<size_t>(M * s->H) * esize(s->dt)) + round256(static_cast<size_t>(M * s->H) * 4) +
+         inner;
+}
+
+tp_status_t tp_mlp_forward_host(tp_shards_t s, const void *X_host, int64_t M, tp_act_t act,
+                                tp_variant_t v, float *Z_host, void *workspace, size_t ws_bytes,
+                                void *stream) {
+  if (!s || s->kind != 0 || M < 0) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!X_host || !Z_host) return TP_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = tp_mlp_host_workspace_bytes(s, M, v);
+  if (need == 0) return TP_ERR_ARG;
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, need, st));
+  const size_t xb = static_cast<size_t>(M * s->H) * esize(s->dt), zb = static_cast<size_t>(M * s->H) * 4;
+  char *Xd = w.ptr;
+  float *Zd = reinterpret_cast<float *>(w.ptr + round256(xb));
+  char *inner = w.ptr + round256(xb) + round256(zb);
+  TP_CUDA(cudaMemcpyAsync(Xd, X_host, xb, cudaMemcpyHostToDevice, st));
+  TP_TRY(mlp_forward_impl(s, Xd, M, act, v, Zd, inner, need - round256(xb) - round256(zb), st));
+  TP_CUDA(cudaMemcpyAsync(Z_host, Zd, zb, cudaMemcpyDeviceToHost, st));
+  return TP_OK;
+}
+
+size_t tp_attn_proj_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 1 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
+  int slots = 1;
+  if (v == TP_VAR_PARTIALS) slots = s->T;
+  if (v == TP_VAR_AUTO) {
+    const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
+    slots = choose_slots(cdiv(M, 128) * (s->H / s->bn2), s->T, static_cast<int>(s->Fs / 64), d->sms,
+                         (1.9e15 / 6.5e12) / flop_per_ktile, M * s->H * 4, false);
+  }
+  return slots > 1 ? round256(static_cast<size_t>(slots * M * s->H) * 4) : 0;
+}
+
+tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void *A, int64_t M,
+                                 tp_variant_t v, void *QKV, float *Z, void *workspace,
+                                 size_t ws_bytes, void *stream) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 1, &d));
+  if (M < 0 || !valid_variant(v)) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if ((QKV && !X) || (Z && !A) || (!QKV && !Z)) return TP_ERR_ARG;
+  if ((X && !aligned16(X)) || (A && !aligned16(A)) || (QKV && !aligned16(QKV)) || (Z && !aligned16(Z)))
+    return TP_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (QKV) TP_TRY(colpar_tc(s, d, X, M, EPI_IDENT_BF16, QKV, s->R1, st));
+  if (Z) {
+    int slots = 1;
+    if (v == TP_VAR_PARTIALS) slots = s->T;
+    if (v == TP_VAR_AUTO) {
+      const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
+      slots = choose_slots(cdiv(M, 128) * (s->H / s->bn2), s->T, static_cast<int>(s->Fs / 64), d->sms,
+                           (1.9e15 / 6.5e12) / flop_per_ktile, M * s->H * 4, false);
+    }
+    const size_t need = slots > 1 ? round256(static_cast<size_t>(slots * M * s->H) * 4) : 0;
+    Workspace w;
+    TP_TRY(get_ws(&w, workspace, ws_bytes, need, st));
+    CUtensorMap ma;
+    TP_TRY(make_map(&ma, A, s->H, M, 1, s->H * 2, M * s->H * 2, 128));
+    TP_TRY(rowpar_tc(s, d, ma, 0, M, slots, reinterpret_cast<float *>(w.ptr), Z, st));
+  }
+  return TP_OK;
+}
+
+tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {
+  if (!Zi || !Z || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
+  for (int t = 0; t < T; ++t)
+    if (!Zi[t]) return TP_ERR_ARG;
+  if (n == 0) return TP_OK;
+  if ((reinterpret_cast<uintptr_t>(Z) & 3u) != 0) return TP_ERR_ARG;
+  const uintptr_t z0 = reinterpret_cast<uintptr_t>(Z), z1 = z0 + static_cast<uintptr_t>(n) * 4;
+  for (int t = 0; t < T; ++t) {
+    if ((reinterpret_cast<uintptr_t>(Zi[t]) & 3u) != 0) return TP_ERR_ARG;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(Zi[t]), a1 = a0 + static_cast<uintptr_t>(n) * 4;
+    const bool overlap = a0 < z1 && z0 < a1;
+    if (overlap && !(t == 0 && a0 == z0)) return TP_ERR_ARG;
+  }
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  return cuda_status(launch_shard_sum(Zi, T, n, Z, d->sms, static_cast<cudaStream_t>(stream)));
+}
+
+tp_status_t tp_last_device_status(void *stream) {
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TP_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return TP_ERR_CUDA;
+  if (word != 0 && cudaMemset(d->status, 0, sizeof word) != cudaSuccess) return TP_ERR_CUDA;
+  if (word & kDevTimeout) return TP_ERR_TIMEOUT;
+  if (word & kDevCheck) return TP_ERR_DEVICE_CHECK;
+  return TP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// tp_internal.h - declarations shared by the C ABI (tp_api.cu) and the
+// kernel files.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tp_mlp.h"
+
+namespace tp {
+
+// Bits of the per-device status word the kernels report into.
+constexpr unsigned kDevTimeout = 1u;
+constexpr unsigned kDevCheck = 2u;
+
+// Epilogues of the tensor-core GEMM.
+enum Epi : int {
+  EPI_GELU_BF16 = 0,    // Y = bf16(GeLU(acc)), written to the per-shard Y buffers
+  EPI_SWIGLU_BF16 = 1,  // accumulator columns [0, BN/2) gate, [BN/2, BN) up -> bf16(SiLU(g) u)
+  EPI_IDENT_BF16 = 2,   // Y = bf16(acc)
+  EPI_F32 = 3,          // out[slot][row][col] = acc (float32 partials or the final Z)
+  EPI_F32_T = 4         // swapped operands: acc[feature][token] -> out[slot][token][feature]
+};
+
+// Packed rows of a SwiGLU shard alternate 128 gate rows and 128 up rows, so
+// one 256-row B tile (or two 128-row A tiles) carries matching gate/up columns.
+constexpr int kSwigluGranule = 128;
+
+// Work description of one tensor-core GEMM launch: D[m][n] = sum_k A[m][k] B[n][k]
+// over units (slot, m-tile, n-tile).  The virtual K axis is `kt_total` tiles
+// of 64, made of segments (shards) of `kt_per_seg` tiles.  A segmented
+// operand (a_seg / b_seg = 1) is a 3-D tensor map [segments][rows][K per
+// segment] and k-tile kt reads coordinate (kt % kt_per_seg * 64, row,
+// kt / kt_per_seg); a flat operand (0) is [1][rows][K] and reads (kt * 64,
+// row, 0).  Slot s covers k-tiles [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
+struct GemmArgs {
+  int m_tiles, n_tiles, slots;
+  int kt_total, kt_per_seg, kt_per_slot;
+  int a_seg, b_seg;
+  int group_m;          // raster: m-tiles per group (L2 reuse of B tiles)
+  int rows_valid;       // valid output rows along A (M, or features when swapped)
+  int cols_valid;       // valid output columns along B (N, or tokens when swapped)
+  void *out;
+  long long ld_out;        // elements between output rows
+  long long slot_stride;   // elements between slots (EPI_F32, EPI_F32_T)
+  long long shard_stride;  // elements between per-shard Y buffers (bf16 epilogues)
+  int shard_cols;          // output columns per shard (bf16 epilogues)
+  unsigned int *status;
+  unsigned long long wait_limit_ns;
+};
+
+// Tile configurations the GEMM is instantiated for.
+enum GemmCfg : int {
+  CFG_N256 = 0,  // BM 128 x BN 256, prefill
+  CFG_N128 = 1,  // BM 128 x BN 128, prefill when the shard width is not a multiple of 256
+  CFG_N16 = 2    // BM 128 x BN 16, decode (weights as A, tokens as B)
+};
+
+// Launch the tensor-core GEMM.  Returns cudaSuccess or the launch error.
+cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
+                        const GemmArgs &args, int num_sms, cudaStream_t stream);
+
+// Float32 CUDA-core GEMM: D[m][n] = sum_k A[m][k] B[n][k], same work model
+// as the tensor-core path but with plain row-major pointers.  A rows have
+// stride lda; segments (shards) of A and B along K are `a_seg`/`b_seg`
+// elements apart; K per segment is `k_seg`, `segs_per_slot` segments per
+// output slot.
+struct SimtArgs {
+  const float *A;
+  const float *B;
+  long long lda, ldb, a_seg, b_seg;
+  int M, N, k_seg, nseg, segs_per_slot;
+  int epi;              // EPI_GELU_BF16/EPI_SWIGLU_BF16/EPI_IDENT_BF16 write float32 here
+  float *out;
+  long long ld_out, slot_stride, shard_stride;
+  int shard_cols;
+};
+cudaError_t launch_simt_gemm(const SimtArgs &a, cudaStream_t stream);
+
+// Z[k] = sum over i ascending of P_i[k] (float32).
+cudaError_t launch_shard_sum(const float *const *parts, int T, long long n, float *Z, int num_sms,
+                             cudaStream_t stream);
+
+// Shard-sum of `slots` float32 partials laid out `slot_stride` apart.
+cudaError_t launch_shard_sum_strided(const float *P, int slots, long long slot_stride, long long n,
+                                     float *Z, int num_sms, cudaStream_t stream);
+
+// Packing of weights into the K-major per-shard layout.
+enum PackMode : int {
+  PACK_W1 = 0,         // dst[s][r][k] = W1[k][s*Fs + r]
+  PACK_W1_SWIGLU = 1,  // dst[s][r][k] = W1[k][gate/up column of packed row r]
+  PACK_QKV = 2,        // dst[s][r][k] = Wqkv[k][(r / W) * H + s*W + r % W]
+  PACK_ROWS = 3        // dst[s][n][k] = W2[s*Ks + k][n]
+};
+// dst is [S][R][K]; src is row-major with leading dimension src_ld; esize is
+// 2 or 4 bytes; `F` is the width of one half of [Wg | Wu], `H` the QKV
+// hidden size, `W` the per-shard width (Fs or head columns).
+cudaError_t launch_pack(PackMode mode, const void *src, long long src_ld, void *dst, int S,
+                        long long R, long long K, int esize, long long F, long long H, long long W,
+                        cudaStream_t stream);
+// Inverse: the logical shard s (row-major [H x W] for W1-like modes and
+// `which` = 0/1 gate/up; [W x N] for PACK_ROWS) from the packed buffer.
+cudaError_t launch_unpack(PackMode mode, const void *packed, void *dst, int s, int which, long long R,
+                          long long K, int esize, long long W, cudaStream_t stream);
+
+// Decode finalize: h[s][t][j] = bf16(act(sum over slots of P[slot][t][row(s, j)])) for
+// SwiGLU (gate and up rows) or GeLU/identity.
+cudaError_t launch_decode_act(const float *P, int slots, long long slot_stride, long long ldp,
+                              int M, int T, int Fs, int act, bool swiglu_rows, void *h,
+                              cudaStream_t stream);
+
+}  // namespace tp

@@ -1,0 +1,42 @@
+"""Helpers for the GPU parity tests: moving seeded inputs to the device and
+the error measures the tolerances are stated in."""
+import numpy as np
+
+
+def to_device(a: np.ndarray):
+    """numpy float32 or bfloat16 bits (uint16) -> CUDA tensor of that type."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def bf16_bits(t) -> np.ndarray:
+    """bfloat16 CUDA tensor -> uint16 bit patterns on the host."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rowwise_rms_error(Z: np.ndarray, Zref: np.ndarray) -> float:
+    """max over (r, c) of |Z - Zref| / RMS(Zref[r, :]): the bf16 tolerance
+    measure, normalised per output row (token)."""
+    rms = np.sqrt(np.mean(np.asarray(Zref, np.float64) ** 2, axis=1, keepdims=True))
+    return float(np.max(np.abs(np.asarray(Z, np.float64) - Zref) / np.maximum(rms, 1e-300)))
+
+
+def global_rms_error(Z: np.ndarray, Zref: np.ndarray) -> float:
+    """max |Z - Zref| / RMS(Zref) over the whole output (reported, not gated)."""
+    rms = np.sqrt(np.mean(np.asarray(Zref, np.float64) ** 2))
+    return float(np.max(np.abs(np.asarray(Z, np.float64) - Zref)) / max(rms, 1e-300))
+
+
+def normwise_error(Z: np.ndarray, Zref: np.ndarray) -> float:
+    """max |Z - Zref| / max |Zref|: the float32 tolerance measure."""
+    return float(np.max(np.abs(np.asarray(Z, np.float64) - Zref)) / max(np.max(np.abs(Zref)), 1e-300))
+
+
+# Tolerances (stated for the path): bf16 inputs with float32 accumulation,
+# bf16 intermediate Y: max-abs error over the output row's RMS <= 2e-2;
+# float32 inputs: normwise relative error <= 1e-4.
+TOL_BF16_ROW_RMS = 2e-2
+TOL_F32_NORMWISE = 1e-4

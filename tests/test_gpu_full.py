@@ -1,0 +1,111 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times, on sampled output rows (a row of Z depends only on that
+row of X, so the oracle computes the sampled rows alone).  Tolerance: bf16
+row-RMS measure (tests/gpu_util.py); the global-RMS figure is printed."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import WORKLOADS, attn_inputs, mlp_inputs
+from tests.gpu_util import (TOL_BF16_ROW_RMS, bf16_bits, global_rms_error, rowwise_rms_error,
+                            to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import linear_sharding_gb300 as tp
+    tp.load_library()
+    return tp
+
+
+def _sample_rows(M, k, seed, must=()):
+    rng = np.random.default_rng(seed)
+    rows = set(int(r) for r in must) | {0, M - 1}
+    rest = [int(r) for r in rng.choice(M, size=min(M, k), replace=False)]
+    for r in rest:
+        if len(rows) >= k:
+            break
+        rows.add(r)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _mlp_check(tp, name, variants, k_rows=24):
+    import torch
+    w = WORKLOADS[name]
+    d = mlp_inputs(M=w["M"], H=w["H"], F=w["F"], act=w["act"], dtype=w["dtype"], seed=0,
+                   outlier_frac=w.get("outlier_frac", 0.0), outlier_scale=w.get("outlier_scale", 20.0))
+    W1, W2 = to_device(d["W1"]), to_device(d["W2"])
+    s = tp.tp_shard_weights(W1, W2, w["T"], w["act"])
+    del W1, W2
+    X = to_device(d["X"])
+    out = d["outlier_rows"]
+    rows = _sample_rows(w["M"], k_rows, seed=1, must=out[: min(8, out.size)])
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], w["act"], rows=rows)
+    for v in variants:
+        Z = tp.tp_mlp_forward(s, X, variant=v)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0
+        Zs = Z[torch.from_numpy(rows).cuda()].cpu().numpy()
+        err = rowwise_rms_error(Zs, Zref)
+        print(f"{name} {v}: row-RMS err {err:.3e}, global-RMS err {global_rms_error(Zs, Zref):.3e}")
+        assert err <= TOL_BF16_ROW_RMS
+    return d, s
+
+
+def test_prefill_gelu_full(tp):
+    _mlp_check(tp, "prefill_gelu_m2048_h4096_f16384_t4", ["auto", "partials", "tmem_acc"])
+
+
+def test_large_prefill_swiglu_full(tp):
+    name = "prefill_swiglu_m8192_h8192_f28672_t8_outliers"
+    d, s = _mlp_check(tp, name, ["auto", "partials"], k_rows=24)
+    w = WORKLOADS[name]
+    assert d["outlier_rows"].size == 82
+    # shard layout bit exact at full size, first and last shard
+    for i in (0, w["T"] - 1):
+        assert np.array_equal(tp.tp_shard_get(s, i, 0), oracle.shard_w1(d["W1"], w["F"], w["T"], "swiglu", i, 0))
+        assert np.array_equal(tp.tp_shard_get(s, i, 1), oracle.shard_w1(d["W1"], w["F"], w["T"], "swiglu", i, 1))
+        assert np.array_equal(tp.tp_shard_get(s, i, 2), oracle.shard_w2(d["W2"], w["T"], i))
+
+
+def test_decode_swiglu_full(tp):
+    """Every row at M in {1, 4, 16}, one set of weights."""
+    import torch
+    w = WORKLOADS["decode_swiglu_h8192_f28672_t8"]
+    d = mlp_inputs(M=16, H=w["H"], F=w["F"], act="swiglu", dtype="bf16", seed=0, x_rows=16)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), w["T"], "swiglu")
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu")
+    for M in w["decode_m"]:
+        X = to_device(d["X"][:M])
+        for v in ("auto", "partials"):
+            Z = tp.tp_mlp_forward(s, X, variant=v)
+            torch.cuda.synchronize()
+            assert tp.tp_last_device_status() == 0
+            err = rowwise_rms_error(Z.cpu().numpy(), Zref[:M])
+            print(f"decode M={M} {v}: row-RMS err {err:.3e}")
+            assert err <= TOL_BF16_ROW_RMS
+
+
+def test_attn_proj_full(tp):
+    import torch
+    w = WORKLOADS["attn_proj_m4096_h4096_32x128_t8"]
+    d = attn_inputs(M=w["M"], H=w["H"], n_heads=w["n_heads"], head_dim=w["head_dim"], seed=0)
+    s = tp.tp_shard_weights_qkv(to_device(d["Wqkv"]), to_device(d["Wo"]), w["n_heads"], w["head_dim"], w["T"])
+    X, A = to_device(d["X"]), to_device(d["A"])
+    rows = _sample_rows(w["M"], 24, seed=2)
+    Zref = oracle.oproj_sharded(d["A"], d["Wo"], w["n_heads"], w["head_dim"], w["T"], rows=rows)
+    ridx = torch.from_numpy(rows).cuda()
+    for v in ("auto", "partials", "tmem_acc"):
+        QKV, Z = tp.tp_attn_proj_forward(s, X=X, A=A, variant=v)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0
+        err = rowwise_rms_error(Z[ridx].cpu().numpy(), Zref)
+        print(f"attn o-proj {v}: row-RMS err {err:.3e}")
+        assert err <= TOL_BF16_ROW_RMS
+    q = bf16_bits(QKV[:, ridx])
+    for i in range(w["T"]):
+        ref = oracle.qkv_shard(d["X"], d["Wqkv"], w["n_heads"], w["head_dim"], w["T"], i, rows=rows)
+        got = (q[i].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert rowwise_rms_error(got, ref) <= TOL_BF16_ROW_RMS

@@ -1,0 +1,266 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases are compared element by element at sizes that span several
+128 x 256 tiles and a ragged tail; the full-size workloads are compared on
+sampled output rows (each row of Z depends only on that row of X).  The
+shard layout and the shard-sum are bit exact; outputs are within the stated
+tolerances (tests/gpu_util.py)."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import WORKLOADS, attn_inputs, mlp_inputs, partials_inputs
+from tests.gpu_util import (TOL_BF16_ROW_RMS, TOL_F32_NORMWISE, bf16_bits, global_rms_error,
+                            normwise_error, rowwise_rms_error, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import torch
+    import linear_sharding_gb300 as tp
+    tp.load_library()
+    assert torch.cuda.is_available()
+    return tp
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+# ---- shard layout (bit exact) ---------------------------------------------------
+
+@pytest.mark.parametrize("act,dtype,T", [("gelu", "bf16", 4), ("swiglu", "bf16", 2),
+                                         ("identity", "f32", 2), ("gelu", "f32", 8),
+                                         ("swiglu", "f32", 1)])
+def test_shard_layout_bit_exact(tp, act, dtype, T):
+    H, F = 256, 128 * T * 2
+    d = mlp_inputs(M=1, H=H, F=F, act=act, dtype=dtype, seed=1)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    for i in range(T):
+        assert np.array_equal(tp.tp_shard_get(s, i, 0), oracle.shard_w1(d["W1"], F, T, act, i, 0))
+        if act == "swiglu":
+            assert np.array_equal(tp.tp_shard_get(s, i, 1), oracle.shard_w1(d["W1"], F, T, act, i, 1))
+        assert np.array_equal(tp.tp_shard_get(s, i, 2), oracle.shard_w2(d["W2"], T, i))
+
+
+def test_qkv_shard_layout_bit_exact(tp):
+    nh, hd, T, H = 8, 64, 4, 512
+    d = attn_inputs(M=1, H=H, n_heads=nh, head_dim=hd, seed=2)
+    s = tp.tp_shard_weights_qkv(to_device(d["Wqkv"]), to_device(d["Wo"]), nh, hd, T)
+    for i in range(T):
+        assert np.array_equal(tp.tp_shard_get(s, i, 0), oracle.shard_wqkv(d["Wqkv"], nh, hd, T, i))
+        assert np.array_equal(tp.tp_shard_get(s, i, 2), oracle.shard_wo(d["Wo"], nh, hd, T, i))
+
+
+# ---- shard-sum (bit exact against the ascending-order float32 sum) -------------
+
+@pytest.mark.parametrize("T,n", [(1, 1000), (2, 4099), (3, 77777), (4, 1 << 20), (5, 12345),
+                                 (8, 1000003), (16, 65536), (11, 3)])
+def test_partial_sum_bit_exact(tp, T, n):
+    P = partials_inputs(T, n, seed=T)
+    parts = [to_device(P[t]) for t in range(T)]
+    Z = tp.tp_partial_sum(parts)
+    _sync()
+    assert np.array_equal(Z.cpu().numpy(), oracle.partial_sum_f32(P))
+    # in place into the first partial
+    tp.tp_partial_sum(parts, Z=parts[0])
+    _sync()
+    assert np.array_equal(parts[0].cpu().numpy(), oracle.partial_sum_f32(P))
+
+
+def test_partial_sum_unaligned_scalar_path(tp):
+    """Pointers that are 4- but not 16-byte aligned take the scalar path."""
+    import torch
+    T, n = 4, 5001
+    P = partials_inputs(T, n + 1, seed=7)
+    parts = [to_device(P[t])[1:] for t in range(T)]
+    Z = torch.empty(n + 1, dtype=torch.float32, device="cuda")[1:]
+    tp.tp_partial_sum(parts, Z=Z)
+    _sync()
+    assert np.array_equal(Z.cpu().numpy(), oracle.partial_sum_f32(P[:, 1:]))
+
+
+def test_partial_sum_empty_is_noop(tp):
+    import torch
+    z = torch.full((4,), 7.0, device="cuda")
+    tp.tp_partial_sum([z[:0], z[:0]], Z=z[:0])
+    _sync()
+    assert torch.all(z == 7.0)
+
+
+# ---- MLP parity, small shapes (every element) ------------------------------------
+
+def _run_mlp(tp, d, T, act, variant, M=None):
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    X = to_device(d["X"])
+    Z = tp.tp_mlp_forward(s, X, variant=variant)
+    _sync()
+    assert tp.tp_last_device_status() == 0
+    return Z.cpu().numpy()
+
+
+@pytest.mark.parametrize("variant", ["partials", "tmem_acc", "auto"])
+@pytest.mark.parametrize("act,M,H,F,T", [
+    ("gelu", 300, 512, 2048, 4),      # ragged M (300 = 2 x 128 + 44), 2 x 2 x 4 tiles
+    ("swiglu", 200, 512, 2048, 8),    # Fs = 256: one gate/up tile per shard
+    ("identity", 129, 256, 1024, 2),  # one row into the second M tile
+    ("gelu", 517, 384, 1152, 3),      # T = 3, 128-wide tiles in both GEMMs (Fs = H = 384)
+])
+def test_mlp_bf16_small(tp, variant, act, M, H, F, T):
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=M)
+    Z = _run_mlp(tp, d, T, act, variant)
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    assert rowwise_rms_error(Z, Zref) <= TOL_BF16_ROW_RMS
+
+
+@pytest.mark.parametrize("variant", ["partials", "tmem_acc", "auto"])
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_mlp_bf16_decode_small(tp, variant, act, M):
+    """M <= 16 takes the decode kernels (weights as the 128-row MMA operand)."""
+    H, F, T = 512, 2048, 4
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=100 + M, x_rows=16)
+    Z = _run_mlp(tp, d, T, act, variant)
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    assert rowwise_rms_error(Z, Zref) <= TOL_BF16_ROW_RMS
+
+
+@pytest.mark.parametrize("variant", ["partials", "tmem_acc"])
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
+def test_mlp_f32_tiny(tp, variant, act):
+    """The float32 path (CUDA-core FMA) at the tiny workload's shape."""
+    w = WORKLOADS["tiny_fp32_gelu"]
+    F = w["F"] if act != "swiglu" else 256
+    d = mlp_inputs(M=w["M"], H=w["H"], F=F, act=act, dtype="f32", seed=0)
+    Z = _run_mlp(tp, d, w["T"], act, variant)
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    assert normwise_error(Z, Zref) <= TOL_F32_NORMWISE
+
+
+def test_tiny_fp32_workload_exact_recipe(tp):
+    """X[8x64], W1[64x256], W2[256x64], T = 2, erf-GeLU, seed 0; also checks
+    sharded == unsharded on the oracle side."""
+    w = WORKLOADS["tiny_fp32_gelu"]
+    d = mlp_inputs(M=w["M"], H=w["H"], F=w["F"], act="gelu", dtype="f32", seed=0)
+    Zu = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")
+    Zs = oracle.mlp_sharded(d["X"], d["W1"], d["W2"], w["T"], "gelu")
+    assert normwise_error(Zs, Zu) <= 1e-12
+    for variant in ("partials", "tmem_acc", "auto"):
+        Z = _run_mlp(tp, d, w["T"], "gelu", variant)
+        assert normwise_error(Z, Zu) <= TOL_F32_NORMWISE
+
+
+def test_mlp_f32_ragged_general(tp):
+    M, H, F, T = 37, 96, 240, 3
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="f32", seed=5)
+    for variant in ("partials", "tmem_acc"):
+        Z = _run_mlp(tp, d, T, "gelu", variant)
+        assert normwise_error(Z, oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")) <= TOL_F32_NORMWISE
+
+
+def test_attn_proj_small(tp):
+    M, nh, hd, T = 300, 8, 64, 4
+    H = nh * hd
+    d = attn_inputs(M=M, H=H, n_heads=nh, head_dim=hd, seed=3)
+    s = tp.tp_shard_weights_qkv(to_device(d["Wqkv"]), to_device(d["Wo"]), nh, hd, T)
+    X, A = to_device(d["X"]), to_device(d["A"])
+    Zref = oracle.oproj_sharded(d["A"], d["Wo"], nh, hd, T)
+    for variant in ("partials", "tmem_acc", "auto"):
+        QKV, Z = tp.tp_attn_proj_forward(s, X=X, A=A, variant=variant)
+        _sync()
+        assert tp.tp_last_device_status() == 0
+        assert rowwise_rms_error(Z.cpu().numpy(), Zref) <= TOL_BF16_ROW_RMS
+        q = bf16_bits(QKV)
+        for i in range(T):
+            ref = oracle.qkv_shard(d["X"], d["Wqkv"], nh, hd, T, i)
+            got = (q[i].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            assert rowwise_rms_error(got, ref) <= TOL_BF16_ROW_RMS
+
+
+# ---- edge cases ---------------------------------------------------------------------
+
+def test_mlp_edge_cases(tp):
+    import torch
+    H, F, T = 256, 1024, 4
+    d = mlp_inputs(M=8, H=H, F=F, act="gelu", dtype="bf16", seed=9)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
+    # M = 0 is a no-op
+    Z0 = tp.tp_mlp_forward(s, to_device(d["X"])[:0])
+    assert Z0.shape == (0, H)
+    # workspace too small
+    X = to_device(d["X"])
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_mlp_forward(s, X, variant="partials", workspace=ws)
+    assert e.value.code == 10
+    # the activation must match the shards' packing
+    with pytest.raises(tp.TPError):
+        tp.tp_mlp_forward(s, X, act="swiglu")
+    # an explicit workspace of the stated size works and matches
+    need = tp.tp_mlp_workspace_bytes(s, X.shape[0], "partials")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    Z = tp.tp_mlp_forward(s, X, variant="partials", workspace=ws)
+    _sync()
+    assert rowwise_rms_error(Z.cpu().numpy(),
+                             oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")) <= TOL_BF16_ROW_RMS
+    # indivisible and unsupported shapes
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), 3, "gelu")
+    assert e.value.code == 2
+
+
+def test_variants_agree_and_are_deterministic(tp):
+    """Both all-reduce variants are correct; each is run-to-run bit identical."""
+    M, H, F, T = 256, 512, 2048, 4
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=21)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
+    X = to_device(d["X"])
+    outs = {}
+    for v in ("partials", "tmem_acc"):
+        a = tp.tp_mlp_forward(s, X, variant=v).cpu().numpy()
+        b = tp.tp_mlp_forward(s, X, variant=v).cpu().numpy()
+        assert np.array_equal(a, b)
+        outs[v] = a
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")
+    for v in outs:
+        assert rowwise_rms_error(outs[v], Zref) <= TOL_BF16_ROW_RMS
+
+
+def test_host_buffer_forward(tp):
+    """tp_mlp_forward_host: pinned host X in, host Z out, same result."""
+    import torch
+    M, H, F, T = 64, 256, 1024, 2
+    d = mlp_inputs(M=M, H=H, F=F, act="swiglu", dtype="bf16", seed=4)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "swiglu")
+    Xh = torch.from_numpy(d["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    Zh = torch.empty((M, H), dtype=torch.float32).pin_memory()
+    ws = torch.empty(tp.tp_mlp_host_workspace_bytes(s, M), dtype=torch.uint8, device="cuda")
+    tp.tp_mlp_forward_host(s, Xh, Zh, ws)
+    _sync()
+    Zd = tp.tp_mlp_forward(s, to_device(d["X"])).cpu().numpy()
+    assert np.array_equal(Zh.numpy(), Zd)
+
+
+def test_wait_timeout_reports_and_recovers(tp):
+    """A wait limit of 1 ns makes the GEMM's waits run out: the kernels return
+    early, the status says TP_ERR_TIMEOUT, nothing faults, and the next call
+    with the default limit is correct."""
+    M, H, F, T = 256, 512, 2048, 4
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=8)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
+    X = to_device(d["X"])
+    assert tp.tp_last_device_status() == 0
+    try:
+        tp.tp_set_wait_limit_ns(1)
+        tp.tp_mlp_forward(s, X, variant="tmem_acc")
+        assert tp.tp_last_device_status() == 7
+    finally:
+        tp.tp_set_wait_limit_ns(0)
+    Z = tp.tp_mlp_forward(s, X, variant="tmem_acc")
+    _sync()
+    assert tp.tp_last_device_status() == 0
+    assert rowwise_rms_error(Z.cpu().numpy(),
+                             oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")) <= TOL_BF16_ROW_RMS
