@@ -799,10 +799,11 @@ tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void *A, in
 }
 
 tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {
-  if (!Zi || !Z || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
+  if (!Zi || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
+  if (n == 0) return TP_OK;
+  if (!Z) return TP_ERR_ARG;
   for (int t = 0; t < T; ++t)
     if (!Zi[t]) return TP_ERR_ARG;
-  if (n == 0) return TP_OK;
   if ((reinterpret_cast<uintptr_t>(Z) & 3u) != 0) return TP_ERR_ARG;
   const uintptr_t z0 = reinterpret_cast<uintptr_t>(Z), z1 = z0 + static_cast<uintptr_t>(n) * 4;
   for (int t = 0; t < T; ++t) {

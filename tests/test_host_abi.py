@@ -64,6 +64,10 @@ def test_argument_errors_are_status_codes(lib):
     assert lib.tp_partial_sum(arr, 0, 16, dummy, None) == 1
     assert lib.tp_partial_sum(arr, 65, 16, dummy, None) == 1
     assert lib.tp_partial_sum(None, 2, 16, dummy, None) == 1
+    assert lib.tp_partial_sum(arr, 2, 16, None, None) == 1
+    nulls = (ctypes.c_void_p * 2)(None, None)
+    assert lib.tp_partial_sum(nulls, 2, 16, dummy, None) == 1
+    assert lib.tp_partial_sum(nulls, 2, 0, None, None) == 0  # n == 0: no-op, pointers unused
     assert lib.tp_partial_sum(arr, 2, -1, dummy, None) == 1
     overlap = (ctypes.c_void_p * 2)(256, 4096)
     assert lib.tp_partial_sum(overlap, 2, 16, ctypes.c_void_p(4096 + 32), None) == 1
