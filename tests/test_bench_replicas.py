@@ -1,0 +1,57 @@
+"""The N > 1 host path of bench.py on CPU: world size 2 over gloo.  Each rank
+is an independent replica; the job's throughput is the units of all ranks
+over the slowest rank's time, with barriers on both sides."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    import bench
+    w, r, local = bench.dist_env()
+    assert (w, r, local) == (world, rank, rank)
+    bench.dist_init(w, "gloo")
+    bench.barrier()
+    elapsed = 1.0 + rank          # rank 1 is the slow one
+    units = 10.0 * (rank + 1)     # 10 + 20 units in total
+    value, t = bench.aggregate(elapsed, units)
+    out[rank] = (value, t, bench.reduce_max(float(rank)), bench.reduce_sum(1.0))
+    bench.barrier()
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_replicas_aggregate_over_gloo():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    for rank in range(world):
+        value, t, mx, n = res[rank]
+        assert t == pytest.approx(2.0)
+        assert value == pytest.approx(30.0 / 2.0)
+        assert mx == 1.0 and n == 2.0
+
+
+def test_single_process_aggregate_is_local():
+    import bench
+    value, t = bench.aggregate(2.0, 8.0)
+    assert (value, t) == (4.0, 2.0)
+
+
+def test_bench_arguments_default_to_one_gpu():
+    import bench
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3 and a.steps >= 1
