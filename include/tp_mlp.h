@@ -216,6 +216,32 @@ TP_API size_t tp_rowpar_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v
 TP_API tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp_variant_t v,
                                      float *Z, void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * tp_mlp_forward_noalloc - tp_mlp_forward (variant AUTO) that allocates no
+ * memory at all.  The pages have no counterpart to this call: it exists for
+ * callers that cannot allocate device memory while they run the MLP, such as
+ * a decode loop captured into a CUDA graph or driven by a real-time
+ * scheduler that forbids allocator calls (cudaMalloc can synchronise the
+ * device and take unbounded time), or a host runtime that hands out all
+ * device memory itself and has none to lend as workspace.
+ *   Its scratch is a fixed 16 MiB device array inside the library, which
+ *   every GPU that loads the library holds until the process exits.  Calls
+ *   whose workspace (tp_mlp_workspace_bytes(s, M, TP_VAR_AUTO)) exceeds
+ *   16 MiB are rejected with TP_ERR_WORKSPACE; the memory-bound decode
+ *   shapes (M <= 16 tokens) of an H = 8192, F = 28672, T = 8 MLP fit.
+ *   The first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   `s` must have been made on the current device (else TP_ERR_ARG), and
+ *   X, Z are as for tp_mlp_forward.
+ *   All calls share the one scratch array and it keeps the last call's
+ *   contents; every byte a call reads from it is written earlier in the same
+ *   call, so nothing needs clearing.  Calls that overlap on the GPU (on
+ *   different streams, or from several threads without ordering) race on the
+ *   scratch and give wrong results: order them on one stream.
+ */
+TP_API tp_status_t tp_mlp_forward_noalloc(tp_shards_t s, const void *X, int64_t M, tp_act_t act,
+                                          float *Z, void *stream);
+
 /* Device workspace tp_mlp_forward_host needs: X and Z staging plus
  * tp_mlp_workspace_bytes(). */
 TP_API size_t tp_mlp_host_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);

@@ -34,7 +34,7 @@ EXPORTS = (
     "tp_mlp_host_workspace_bytes", "tp_mlp_forward_host", "tp_attn_proj_workspace_bytes",
     "tp_attn_proj_forward", "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
     "tp_colpar_workspace_bytes", "tp_colpar_forward", "tp_rowpar_workspace_bytes",
-    "tp_rowpar_forward",
+    "tp_rowpar_forward", "tp_mlp_forward_noalloc",
 )
 
 _lock = threading.Lock()
@@ -86,10 +86,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_rowpar_workspace_bytes.restype = sz
         lib.tp_rowpar_workspace_bytes.argtypes = [vp, i64, i32]
         lib.tp_rowpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
+        lib.tp_mlp_forward_noalloc.argtypes = [vp, vp, i64, i32, vp, vp]
         for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
                      "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
                      "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
-                     "tp_colpar_forward", "tp_rowpar_forward"):
+                     "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib

@@ -458,6 +458,14 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
 
 }  // namespace
 
+bool tp::handle_ready_on_current_device(const tp_shards *s) {
+  int dev = 0;
+  if (!s || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (dev != s->device) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_dev[dev].ready;
+}
+
 // ============================================================================
 // C ABI
 // ============================================================================

@@ -110,4 +110,8 @@ cudaError_t launch_decode_act(const float *P, int slots, long long slot_stride, 
                               int M, int T, int Fs, int act, bool swiglu_rows, void *h,
                               cudaStream_t stream);
 
+// True when `s` was made on the current device and that device's library
+// state already exists (checked without creating it, so without allocating).
+bool handle_ready_on_current_device(const tp_shards *s);
+
 }  // namespace tp
