@@ -229,13 +229,18 @@ Epi act_epi(tp_act_t act) {
 
 GemmCfg cfg_for(int bn) { return bn == 256 ? CFG_N256 : CFG_N128; }
 
+// 256-wide tiles over more than one 128-row block of tokens run on CTA pairs
+// (cta_group::2): half the B-tile traffic per SM and a deeper stage ring.
+bool use_pair(int bn, int64_t M) { return bn == 256 && M > 128; }
+
 // Row-parallel GEMM over T shards into Z, with `slots` accumulation slots
 // (slots > 1: float32 partials in P, then the shard-sum).
 tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &mapA, int a_seg,
                       int64_t M, int slots, float *P, float *Z, cudaStream_t st) {
   const int64_t H = s->H;
+  const bool pair = use_pair(s->bn2, M);
   GemmArgs g = base_args(d);
-  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.m_tiles = static_cast<int>(cdiv(M, pair ? 256 : 128));
   g.n_tiles = static_cast<int>(H / s->bn2);
   g.slots = slots;
   g.kt_per_seg = static_cast<int>(s->Fs / 64);
@@ -248,7 +253,10 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
   g.out = slots > 1 ? static_cast<void *>(P) : static_cast<void *>(Z);
   g.ld_out = H;
   g.slot_stride = M * H;
-  TP_CUDA(launch_gemm(cfg_for(s->bn2), EPI_F32, mapA, s->map_w2_b, g, d->sms, st));
+  if (pair)
+    TP_CUDA(launch_gemm(CFG_PAIR_N256, EPI_F32, mapA, s->map_w2_a, g, d->sms, st));
+  else
+    TP_CUDA(launch_gemm(cfg_for(s->bn2), EPI_F32, mapA, s->map_w2_b, g, d->sms, st));
   if (slots > 1) TP_CUDA(launch_shard_sum_strided(P, slots, M * H, M * H, Z, d->sms, st));
   return TP_OK;
 }
@@ -259,8 +267,9 @@ tp_status_t colpar_tc(const tp_shards *s, const DevState *d, const void *X, int6
   const int64_t H = s->H;
   CUtensorMap mx;
   TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
+  const bool pair = use_pair(s->bn1, M);
   GemmArgs g = base_args(d);
-  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.m_tiles = static_cast<int>(cdiv(M, pair ? 256 : 128));
   g.n_tiles = static_cast<int>(s->T * s->R1 / s->bn1);
   g.slots = 1;
   g.kt_total = static_cast<int>(H / 64);
@@ -272,7 +281,10 @@ tp_status_t colpar_tc(const tp_shards *s, const DevState *d, const void *X, int6
   g.ld_out = shard_cols;
   g.shard_stride = M * shard_cols;
   g.shard_cols = static_cast<int>(shard_cols);
-  TP_CUDA(launch_gemm(cfg_for(s->bn1), epi, mx, s->map_w1_b, g, d->sms, st));
+  if (pair)
+    TP_CUDA(launch_gemm(CFG_PAIR_N256, epi, mx, s->map_w1_a, g, d->sms, st));
+  else
+    TP_CUDA(launch_gemm(cfg_for(s->bn1), epi, mx, s->map_w1_b, g, d->sms, st));
   return TP_OK;
 }
 

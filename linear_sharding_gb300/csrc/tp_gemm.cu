@@ -118,17 +118,17 @@ __device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (
 }
 
 // Epilogue of one tile by the 128 epilogue threads: each thread owns TMEM
-// lane `row_in_tile` (one row of the tile); `tb` addresses that lane's
-// quarter at the accumulator's first column.
+// lane `row_in_tile`, i.e. output row row0 + row_in_tile; `tb` addresses that
+// lane's quarter at the accumulator's first column.
 template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int row_in_tile,
+__device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int row0, int row_in_tile,
                                               const GemmArgs &g) {
   if constexpr (EPI == EPI_F32_T) {
     static_assert(BN == 16, "swapped epilogue is the N = 16 decode tile");
     uint32_t r[16];
     tmem_ld16(tb, r);
     tmem_ld_wait();
-    const int feat = t.m * BM + row_in_tile;
+    const int feat = row0 + row_in_tile;
     if (feat < g.rows_valid) {
       float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride + feat;
 #pragma unroll
@@ -136,7 +136,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
         if (j < g.cols_valid) out[j * g.ld_out] = __uint_as_float(r[j]);
     }
   } else if constexpr (EPI == EPI_F32) {
-    const int row = t.m * BM + row_in_tile;
+    const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
     float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
                  static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
@@ -155,7 +155,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     }
   } else if constexpr (EPI == EPI_SWIGLU_BF16) {
     constexpr int HALF = BN / 2;
-    const int row = t.m * BM + row_in_tile;
+    const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * HALF;
     const long long shard = col0 / g.shard_cols;
@@ -177,7 +177,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
       }
     }
   } else {  // EPI_GELU_BF16, EPI_IDENT_BF16
-    const int row = t.m * BM + row_in_tile;
+    const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * BN;
     const long long shard = col0 / g.shard_cols;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, EPI>(tb, t, row_in_tile, g);
+      epilogue_tile<BN, EPI>(tb, t, t.m * BM, row_in_tile, g);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (++acc == kAcc) {
@@ -362,6 +362,259 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// ---- CTA-pair variant ------------------------------------------------------
+//
+// Cluster of 2 CTAs on a 256 x 256 output tile.  CTA r loads rows
+// [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
+// tile into its own shared memory (32 KiB per stage, 6 stages); one thread of
+// CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both
+// CTAs' tiles and leaves rows [128 r, 128 r + 128) x 256 columns in CTA r's
+// tensor memory.  Each CTA's copies complete on its own barrier; in CTA 1 a
+// relay thread forwards "stage full" to CTA 0, so every CTA can always wait
+// for its own copies.  Commits are multicast to both CTAs' barriers; the
+// epilogue warps of both CTAs release an accumulator on CTA 0's barrier.
+constexpr int kPairStages = 6;
+constexpr int kPairBN = 256;
+
+// The B ring is followed by one spare half-tile (16 KiB) so that an MMA
+// operand read of a full B tile from the last stage stays inside this CTA's
+// shared memory.
+constexpr size_t kPairPad = (kPairBN / 2) * BK * 2;
+
+__host__ __device__ constexpr size_t pair_smem_bytes() {
+  return 1024 + static_cast<size_t>(kPairStages) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) +
+         kPairPad + 512;
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tp_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
+                        const __grid_constant__ CUtensorMap mapB, const GemmArgs g) {
+  constexpr int STAGES = kPairStages;
+  constexpr int BN = kPairBN;
+  constexpr uint32_t A_BYTES = 128 * BK * 2;
+  constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
+  constexpr uint32_t TMEM_COLS = 512;
+  constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
+  constexpr int kReleaseArrivals = 8;  // 4 epilogue warps in each CTA
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES + kPairPad);
+  // barriers: full[S] | pfull[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * kAcc + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto pfull_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + kAcc + a); };
+  const uint32_t drain = bar0 + 8u * (3 * STAGES + 2 * kAcc);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(pfull_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kAcc; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), kReleaseArrivals);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mapA);
+    prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
+  const int units = g.slots * g.m_tiles * g.n_tiles;
+  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer (both CTAs, own half of each tile) ----
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < units && ok; u += nclusters) {
+        const Unit t = decode_unit(u, g);
+        const int arow = t.m * 256 + 128 * static_cast<int>(rank);
+        const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
+        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+          if (!wait_bar_cluster(empty_bar(stage), phase ^ 1u, w)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          const int seg = kt / g.kt_per_seg;
+          const int kk = (kt - seg * g.kt_per_seg) * BK;
+          if (g.a_seg)
+            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kk, arow, seg);
+          else
+            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kt * BK, arow, 0);
+          if (g.b_seg)
+            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kk, brow, seg);
+          else
+            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kt * BK, brow, 0);
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) drain_bar(full_bar(s), (last_par >> s) & 1u, g.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---- MMA issuer (CTA 0 only) ----
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < units && ok; u += nclusters) {
+        const Unit t = decode_unit(u, g);
+        if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+          if (!wait_bar(full_bar(stage), phase, w) || !wait_bar_cluster(pfull_bar(stage), phase, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kt > t.kt0 || k > 0) ? 1u : 0u);
+          tc_commit2_multicast(empty_bar(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit2_multicast(tfull_bar(acc), 0x3);
+        if (++acc == kAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      tc_commit2(drain);
+      drain_bar(drain, 0u, g.status);
+    } else if (lane == 0) {
+      // ---- relay (CTA 1): this CTA's stage has landed -> tell CTA 0 ----
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < units && ok; u += nclusters) {
+        const Unit t = decode_unit(u, g);
+        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+          if (!wait_bar(full_bar(stage), phase, w)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(map_to_rank(pfull_bar(stage), 0));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue (warps 2..5 of both CTAs) ----
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = cluster_id; u < units; u += nclusters) {
+      const Unit t = decode_unit(u, g);
+      const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(acc * BN);
+      epilogue_tile<BN, EPI>(tb, t, t.m * 256 + 128 * static_cast<int>(rank), row_in_tile, g);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+      if (++acc == kAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
+                        cudaStream_t stream) {
+  constexpr size_t smem = pair_smem_bytes();
+  auto kern = tp_gemm_pair_kernel<EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
+  if (units <= 0) return cudaSuccess;
+  // Clusters that fit on the GPU at once (pairs of SMs with room for one CTA each).
+  static int max_clusters[64][4];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &mc = max_clusters[dev & 63][EPI & 3];
+  if (mc <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = num_sms / 2;
+    }
+    mc = n;
+  }
+  const int clusters = static_cast<int>(units < mc ? units : mc);
+  kern<<<2 * clusters, kThreads, smem, stream>>>(a, b, g);
+  return cudaGetLastError();
 }
 
 template <int BN, int EPI>
@@ -403,6 +656,15 @@ cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUt
       break;
     case CFG_N16:
       if (epi == EPI_F32_T) return launch_impl<16, EPI_F32_T>(mapA, mapB, args, num_sms, stream);
+      break;
+    case CFG_PAIR_N256:
+      switch (epi) {
+        case EPI_GELU_BF16: return launch_pair<EPI_GELU_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_SWIGLU_BF16: return launch_pair<EPI_SWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_IDENT_BF16: return launch_pair<EPI_IDENT_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32: return launch_pair<EPI_F32>(mapA, mapB, args, num_sms, stream);
+        default: break;
+      }
       break;
   }
   return cudaErrorInvalidValue;

@@ -54,7 +54,9 @@ struct GemmArgs {
 enum GemmCfg : int {
   CFG_N256 = 0,  // BM 128 x BN 256, prefill
   CFG_N128 = 1,  // BM 128 x BN 128, prefill when the shard width is not a multiple of 256
-  CFG_N16 = 2    // BM 128 x BN 16, decode (weights as A, tokens as B)
+  CFG_N16 = 2,   // BM 128 x BN 16, decode (weights as A, tokens as B)
+  CFG_PAIR_N256 = 3  // CTA pair (cta_group::2): 256 x 256 tile, m_tiles count 256 rows,
+                     // B tensor map box 128 rows (each CTA loads half of the B tile)
 };
 
 // Launch the tensor-core GEMM.  Returns cudaSuccess or the launch error.
