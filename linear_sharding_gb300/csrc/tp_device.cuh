@@ -56,13 +56,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same, with cluster-scope acquire: for barriers that receive arrivals from
-// the peer CTA of a cluster.
+// Same test, for barriers that receive arrivals from the peer CTA of a
+// cluster (kept separate so the two kinds of wait can be told apart).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -71,10 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // Arrive on a barrier given by its shared::cluster address (possibly in the
-// peer CTA), releasing this thread's prior writes at cluster scope.
+// peer CTA).  Default (CTA-scope release) semantics: a cluster-scope release
+// here would fence every stage of the pipeline.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // shared::cluster address of the variable at `smem_addr` in CTA `rank` of this cluster.
