@@ -289,6 +289,34 @@ TP_API tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void
 TP_API tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream);
 
 /*
+ * The other collectives of tensor parallelism, on one GPU ("Tensor
+ * Parallelism in Action", section 2, question 3: AllReduce, AllGather,
+ * ReduceScatter; the ring all-reduce's 2 (T - 1) / T * H * B bytes in the
+ * "Tensor parallelism" guide, section "Walking through a transformer block",
+ * are its reduce-scatter half plus its all-gather half).
+ *
+ * tp_reduce_scatter - rank i keeps block i of the sum: with nb = n / T,
+ *   out[i][k] = ((Zi[0][i nb + k] + Zi[1][i nb + k]) + ...) + Zi[T-1][i nb + k],
+ *   float32, ranks in ascending order.  Zi: T device pointers to n floats;
+ *   out: T device pointers to nb floats each, overlapping neither each other
+ *   nor any Zi.  n % T != 0 -> TP_ERR_INDIVISIBLE.  Asynchronous on `stream`.
+ *
+ * tp_all_gather - out = parts[0] | parts[1] | ... | parts[T-1], each part
+ *   n_per elements of elem_bytes bytes, in rank order.  A part that already
+ *   sits at its place in `out` (the in-place form) is left as it is; any
+ *   other overlap -> TP_ERR_ARG.  Asynchronous on `stream`.
+ *
+ * tp_partial_sum_bf16 - the all-reduce-sum of tp_partial_sum, rounded once
+ *   to bfloat16 (nearest, ties to even): Z is n bfloat16 values and must not
+ *   overlap the inputs.  Asynchronous on `stream`.
+ */
+TP_API tp_status_t tp_reduce_scatter(const float *const *Zi, int T, int64_t n, float *const *out,
+                                     void *stream);
+TP_API tp_status_t tp_all_gather(const void *const *parts, int T, int64_t n_per, int elem_bytes,
+                                 void *out, void *stream);
+TP_API tp_status_t tp_partial_sum_bf16(const float *const *Zi, int T, int64_t n, void *Z, void *stream);
+
+/*
  * tp_last_device_status - synchronise `stream`, then return and clear the
  * current device's status word: TP_OK, TP_ERR_TIMEOUT (a kernel's bounded
  * wait ran out and it returned early; its outputs are undefined) or
@@ -301,9 +329,12 @@ TP_API tp_status_t tp_last_device_status(void *stream);
 /*
  * tp_set_wait_limit_ns - limit on every device-side wait (default 2 s) in
  * kernels launched after this call, process-wide.  0 restores the default.
- * A limit of 1 ns makes the waits run out on purpose so that the timeout
- * path can be tested; the kernels then return early with TP_ERR_TIMEOUT
- * without faulting or hanging.
+ * A limit below 1 ms is a test limit: the tensor-core kernels then first
+ * wait on a barrier that nothing ever completes, so their waits run out on
+ * purpose and the timeout path (abort, let issued copies and MMAs finish,
+ * release tensor memory, return) is exercised; the call's results are
+ * undefined and tp_last_device_status() reports TP_ERR_TIMEOUT.  Nothing
+ * faults or hangs.
  */
 TP_API tp_status_t tp_set_wait_limit_ns(uint64_t ns);
 

@@ -34,7 +34,8 @@ EXPORTS = (
     "tp_mlp_host_workspace_bytes", "tp_mlp_forward_host", "tp_attn_proj_workspace_bytes",
     "tp_attn_proj_forward", "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
     "tp_colpar_workspace_bytes", "tp_colpar_forward", "tp_rowpar_workspace_bytes",
-    "tp_rowpar_forward", "tp_mlp_forward_noalloc",
+    "tp_rowpar_forward", "tp_mlp_forward_noalloc", "tp_reduce_scatter", "tp_all_gather",
+    "tp_partial_sum_bf16",
 )
 
 _lock = threading.Lock()
@@ -87,10 +88,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_rowpar_workspace_bytes.argtypes = [vp, i64, i32]
         lib.tp_rowpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
         lib.tp_mlp_forward_noalloc.argtypes = [vp, vp, i64, i32, vp, vp]
+        lib.tp_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, ctypes.POINTER(vp), vp]
+        lib.tp_all_gather.argtypes = [ctypes.POINTER(vp), i32, i64, i32, vp, vp]
+        lib.tp_partial_sum_bf16.argtypes = [ctypes.POINTER(vp), i32, i64, vp, vp]
         for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
                      "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
                      "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
-                     "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc"):
+                     "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
+                     "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -303,6 +308,43 @@ def tp_partial_sum(parts, Z=None, stream=None):
         Z = torch.empty_like(parts[0])
     arr = (ctypes.c_void_p * T)(*[p.data_ptr() for p in parts])
     _check(lib.tp_partial_sum(arr, T, n, _ptr(Z), _stream(stream)), "tp_partial_sum")
+    return Z
+
+
+def _ptr_array(tensors):
+    return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def tp_reduce_scatter(parts, out=None, stream=None):
+    """Rank i keeps block i of the sum: out[i] = sum_t parts[t][i*nb:(i+1)*nb]."""
+    torch = _torch()
+    T, n = len(parts), parts[0].numel()
+    if out is None:
+        out = [torch.empty(n // T, dtype=torch.float32, device=parts[0].device) for _ in range(T)]
+    _check(load_library().tp_reduce_scatter(_ptr_array(parts), T, n, _ptr_array(out), _stream(stream)),
+           "tp_reduce_scatter")
+    return out
+
+
+def tp_all_gather(parts, out=None, stream=None):
+    """out = concatenation of the T parts (same element type and size)."""
+    torch = _torch()
+    T, n = len(parts), parts[0].numel()
+    if out is None:
+        out = torch.empty(T * n, dtype=parts[0].dtype, device=parts[0].device)
+    _check(load_library().tp_all_gather(_ptr_array(parts), T, n, parts[0].element_size(), _ptr(out),
+                                        _stream(stream)), "tp_all_gather")
+    return out
+
+
+def tp_partial_sum_bf16(parts, Z=None, stream=None):
+    """The all-reduce-sum rounded once to bfloat16."""
+    torch = _torch()
+    n = parts[0].numel()
+    if Z is None:
+        Z = torch.empty(n, dtype=torch.bfloat16, device=parts[0].device)
+    _check(load_library().tp_partial_sum_bf16(_ptr_array(parts), len(parts), n, _ptr(Z), _stream(stream)),
+           "tp_partial_sum_bf16")
     return Z
 
 

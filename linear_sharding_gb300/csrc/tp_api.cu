@@ -837,6 +837,66 @@ tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, v
   return cuda_status(launch_shard_sum(Zi, T, n, Z, d->sms, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+bool ranges_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+}  // namespace
+
+tp_status_t tp_reduce_scatter(const float *const *Zi, int T, int64_t n, float *const *out, void *stream) {
+  if (!Zi || !out || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
+  if (n % T != 0) return TP_ERR_INDIVISIBLE;
+  if (n == 0) return TP_OK;
+  const size_t bytes = static_cast<size_t>(n) * 4, bb = bytes / T;
+  for (int t = 0; t < T; ++t) {
+    if (!Zi[t] || !out[t] || (reinterpret_cast<uintptr_t>(Zi[t]) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out[t]) & 3u))
+      return TP_ERR_ARG;
+  }
+  for (int i = 0; i < T; ++i) {
+    for (int t = 0; t < T; ++t)
+      if (ranges_overlap(out[i], bb, Zi[t], bytes)) return TP_ERR_ARG;
+    for (int j = i + 1; j < T; ++j)
+      if (ranges_overlap(out[i], bb, out[j], bb)) return TP_ERR_ARG;
+  }
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  return cuda_status(launch_reduce_scatter(Zi, T, n, out, d->sms, static_cast<cudaStream_t>(stream)));
+}
+
+tp_status_t tp_all_gather(const void *const *parts, int T, int64_t n_per, int elem_bytes, void *out,
+                          void *stream) {
+  if (!parts || T < 1 || T > kMaxShards || n_per < 0 || elem_bytes < 1 || elem_bytes > 16)
+    return TP_ERR_ARG;
+  if (n_per == 0) return TP_OK;
+  if (!out) return TP_ERR_ARG;
+  const size_t bb = static_cast<size_t>(n_per) * static_cast<size_t>(elem_bytes);
+  char *o = static_cast<char *>(out);
+  for (int t = 0; t < T; ++t) {
+    if (!parts[t]) return TP_ERR_ARG;
+    const bool in_place = parts[t] == o + static_cast<size_t>(t) * bb;
+    if (!in_place && ranges_overlap(parts[t], bb, out, bb * T)) return TP_ERR_ARG;
+  }
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  return cuda_status(launch_all_gather(parts, T, static_cast<long long>(bb), out, d->sms,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+tp_status_t tp_partial_sum_bf16(const float *const *Zi, int T, int64_t n, void *Z, void *stream) {
+  if (!Zi || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
+  if (n == 0) return TP_OK;
+  if (!Z || (reinterpret_cast<uintptr_t>(Z) & 1u)) return TP_ERR_ARG;
+  for (int t = 0; t < T; ++t) {
+    if (!Zi[t] || (reinterpret_cast<uintptr_t>(Zi[t]) & 3u)) return TP_ERR_ARG;
+    if (ranges_overlap(Zi[t], static_cast<size_t>(n) * 4, Z, static_cast<size_t>(n) * 2)) return TP_ERR_ARG;
+  }
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  return cuda_status(launch_shard_sum_bf16(Zi, T, n, Z, d->sms, static_cast<cudaStream_t>(stream)));
+}
+
 tp_status_t tp_last_device_status(void *stream) {
   DevState *d = nullptr;
   TP_TRY(dev_state(&d));

@@ -56,16 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Same test, for barriers that receive arrivals from the peer CTA of a
-// cluster (kept separate so the two kinds of wait can be told apart).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+// try_wait with a suspend-time hint: the thread sleeps at most ~hint_ns
+// before the probe returns, so short wait limits are honoured.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -103,14 +103,24 @@ struct WaitCtl {
   unsigned long long limit_ns;   // per-wait limit
 };
 
+// Limits below this are test limits: each probe then also carries a suspend
+// hint so that a wait can run out before the awaited event happens.
+constexpr unsigned long long kShortLimitNs = 1000000ull;
+
+__device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+  if (w.limit_ns < kShortLimitNs)
+    return mbar_try_wait_hint(bar, parity, static_cast<uint32_t>(w.limit_ns) | 1u);
+  return mbar_try_wait(bar, parity);
+}
+
 // Wait for the phase with the given parity to complete.  Returns false if
 // the CTA is aborting or the wait ran past its limit (then it raises the
 // abort flag and the timeout bit).  Never loops without bound.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl &w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (probe(bar, parity, w)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe(bar, parity, w)) return true;
     if ((i & 15u) == 0u) {
       if (*w.abort) return false;
       if (globaltimer_ns() - t0 > w.limit_ns) {
@@ -124,19 +134,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
 
 // wait_bar for barriers that the peer CTA arrives on.
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const WaitCtl &w) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 15u) == 0u) {
-      if (*w.abort) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        *w.abort = 1;
-        atomicOr(w.status, kDevTimeout);
-        return false;
-      }
-    }
-  }
+  return wait_bar(bar, parity, w);
 }
 
 // Clean-up wait: ignores the abort flag, bounded by kDrainLimitNs.

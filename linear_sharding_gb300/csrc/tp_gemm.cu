@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  // barriers: full[STAGES] | empty[STAGES] | tfull[kAcc] | tempty[kAcc] | drain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2 * kAcc + 1);
+  // barriers: full[STAGES] | empty[STAGES] | tfull[kAcc] | tempty[kAcc] | drain | never
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2 * kAcc + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 2 * kAcc);
+  const uint32_t never = drain + 8u;  // nothing ever arrives here (timeout test)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), kEpiThreads);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -298,7 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- MMA issuer ----
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
+      // Under a test wait limit, first wait for an event that never happens,
+      // so that the timeout path runs with copies in flight.
+      bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, g);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
@@ -368,25 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Cluster of 2 CTAs on a 256 x 256 output tile.  CTA r loads rows
 // [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
-// tile into its own shared memory (32 KiB per stage, 6 stages); one thread of
+// tile into its own shared memory (32 KiB per stage, 7 stages); one thread of
 // CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both
 // CTAs' tiles and leaves rows [128 r, 128 r + 128) x 256 columns in CTA r's
 // tensor memory.  Each CTA's copies complete on its own barrier; in CTA 1 a
 // relay thread forwards "stage full" to CTA 0, so every CTA can always wait
 // for its own copies.  Commits are multicast to both CTAs' barriers; the
 // epilogue warps of both CTAs release an accumulator on CTA 0's barrier.
-constexpr int kPairStages = 6;
+#ifndef TP_PAIR_STAGES
+#define TP_PAIR_STAGES 7
+#endif
+constexpr int kPairStages = TP_PAIR_STAGES;
 constexpr int kPairBN = 256;
 
-// The B ring is followed by one spare half-tile (16 KiB) so that an MMA
-// operand read of a full B tile from the last stage stays inside this CTA's
-// shared memory.
-constexpr size_t kPairPad = (kPairBN / 2) * BK * 2;
-
 __host__ __device__ constexpr size_t pair_smem_bytes() {
-  return 1024 + static_cast<size_t>(kPairStages) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) +
-         kPairPad + 512;
+  return 1024 + static_cast<size_t>(kPairStages) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) + 512;
 }
+static_assert(pair_smem_bytes() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
 
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -405,9 +407,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES + kPairPad);
-  // barriers: full[S] | pfull[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * kAcc + 1);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  // barriers: full[S] | pfull[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain | never
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * kAcc + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -417,6 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + kAcc + a); };
   const uint32_t drain = bar0 + 8u * (3 * STAGES + 2 * kAcc);
+  const uint32_t never = drain + 8u;  // nothing ever arrives here (timeout test)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -433,6 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), kReleaseArrivals);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -500,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- MMA issuer (CTA 0 only) ----
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
+      bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = cluster_id; u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
         if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;

@@ -88,6 +88,17 @@ cudaError_t launch_shard_sum(const float *const *parts, int T, long long n, floa
 cudaError_t launch_shard_sum_strided(const float *P, int slots, long long slot_stride, long long n,
                                      float *Z, int num_sms, cudaStream_t stream);
 
+// Reduce-scatter: out[i][k] = sum over t ascending of parts[t][i n/T + k].
+cudaError_t launch_reduce_scatter(const float *const *parts, int T, long long n, float *const *out,
+                                  int num_sms, cudaStream_t stream);
+// All-gather: out = parts[0] | parts[1] | ... (nb_bytes each); a part already
+// at its place in `out` is left alone.
+cudaError_t launch_all_gather(const void *const *parts, int T, long long nb_bytes, void *out,
+                              int num_sms, cudaStream_t stream);
+// Shard-sum rounded once to bfloat16.
+cudaError_t launch_shard_sum_bf16(const float *const *parts, int T, long long n, void *Z, int num_sms,
+                                  cudaStream_t stream);
+
 // Packing of weights into the K-major per-shard layout.
 enum PackMode : int {
   PACK_W1 = 0,         // dst[s][r][k] = W1[k][s*Fs + r]

@@ -85,6 +85,109 @@ __global__ void shard_sum_scalar(const PartList L, int T, long long first, long 
   }
 }
 
+// ---- reduce-scatter, all-gather, bf16 all-reduce ----------------------------
+
+struct OutList {
+  float *p[kMaxParts];
+};
+
+// out[i][k] = sum over t ascending of P_t[i nb + k], 16-byte groups
+// (nb4 = nb / 4 groups per block).
+__global__ void __launch_bounds__(256) reduce_scatter_vec(const PartList L, int T, const OutList O,
+                                                          long long nb4, long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += stride) {
+    float4 s = __ldcs(reinterpret_cast<const float4 *>(L.p[0]) + i);
+    for (int t0 = 1; t0 < T; t0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (t0 + j < T) v[j] = __ldcs(reinterpret_cast<const float4 *>(L.p[t0 + j]) + i);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (t0 + j < T) add4(s, v[j]);
+    }
+    const long long blk = i / nb4;
+    __stcs(reinterpret_cast<float4 *>(O.p[blk]) + (i - blk * nb4), s);
+  }
+}
+
+__global__ void reduce_scatter_scalar(const PartList L, int T, const OutList O, long long nb,
+                                      long long n) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    float s = L.p[0][i];
+    for (int t = 1; t < T; ++t) s += L.p[t][i];
+    const long long blk = i / nb;
+    O.p[blk][i - blk * nb] = s;
+  }
+}
+
+struct ConstList {
+  const uint8_t *p[kMaxParts];
+};
+
+// out[i nb_bytes + k] = parts[i][k]; 16-byte vectors when every block allows.
+__global__ void all_gather_vec(const ConstList L, int T, long long nb16, uint4 *out) {
+  const long long n16 = nb16 * T;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += stride) {
+    const long long blk = i / nb16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(L.p[blk]);
+    if (src == out + blk * nb16) continue;  // this block is already in place
+    out[i] = __ldcs(src + (i - blk * nb16));
+  }
+}
+
+__global__ void all_gather_bytes(const ConstList L, int T, long long nb_bytes, uint8_t *out) {
+  const long long n = nb_bytes * T;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const long long blk = i / nb_bytes;
+    if (L.p[blk] == out + blk * nb_bytes) continue;
+    out[i] = L.p[blk][i - blk * nb_bytes];
+  }
+}
+
+// Z[k] = bf16(sum over t ascending of P_t[k]), 4 values per thread step.
+__global__ void __launch_bounds__(256) shard_sum_bf16_vec(const PartList L, int T, long long n4,
+                                                          __nv_bfloat16 *Z) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += stride) {
+    float4 s = __ldcs(reinterpret_cast<const float4 *>(L.p[0]) + i);
+    for (int t0 = 1; t0 < T; t0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (t0 + j < T) v[j] = __ldcs(reinterpret_cast<const float4 *>(L.p[t0 + j]) + i);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (t0 + j < T) add4(s, v[j]);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(Z)[i] = pk;
+  }
+}
+
+__global__ void shard_sum_bf16_scalar(const PartList L, int T, long long first, long long n,
+                                      __nv_bfloat16 *Z) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = first + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    float s = L.p[0][i];
+    for (int t = 1; t < T; ++t) s += L.p[t][i];
+    Z[i] = __float2bfloat16_rn(s);
+  }
+}
+
 // ---- packing ------------------------------------------------------------
 
 template <typename E>
@@ -293,6 +396,70 @@ cudaError_t launch_shard_sum_strided(const float *P, int slots, long long slot_s
   const float *parts[kMaxParts];
   for (int s = 0; s < slots; ++s) parts[s] = P + s * slot_stride;
   return launch_shard_sum(parts, slots, n, Z, num_sms, stream);
+}
+
+cudaError_t launch_reduce_scatter(const float *const *parts, int T, long long n, float *const *out,
+                                  int num_sms, cudaStream_t stream) {
+  if (T < 1 || T > kMaxParts || n % T != 0) return cudaErrorInvalidValue;
+  if (n <= 0) return cudaSuccess;
+  PartList L{};
+  OutList O{};
+  const long long nb = n / T;
+  bool vec = nb % 4 == 0;
+  for (int t = 0; t < T; ++t) {
+    L.p[t] = parts[t];
+    O.p[t] = out[t];
+    vec = vec && ((reinterpret_cast<uintptr_t>(parts[t]) | reinterpret_cast<uintptr_t>(out[t])) & 15u) == 0;
+  }
+  constexpr int threads = 256;
+  if (vec) {
+    reduce_scatter_vec<<<grid_for(n / 4, threads, num_sms, 8), threads, 0, stream>>>(L, T, O, nb / 4,
+                                                                                    n / 4);
+  } else {
+    reduce_scatter_scalar<<<grid_for(n, threads, num_sms, 8), threads, 0, stream>>>(L, T, O, nb, n);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_all_gather(const void *const *parts, int T, long long nb_bytes, void *out,
+                              int num_sms, cudaStream_t stream) {
+  if (T < 1 || T > kMaxParts || nb_bytes < 0) return cudaErrorInvalidValue;
+  if (nb_bytes == 0) return cudaSuccess;
+  ConstList L{};
+  bool vec = nb_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  for (int t = 0; t < T; ++t) {
+    L.p[t] = static_cast<const uint8_t *>(parts[t]);
+    vec = vec && (reinterpret_cast<uintptr_t>(parts[t]) & 15u) == 0;
+  }
+  constexpr int threads = 256;
+  if (vec)
+    all_gather_vec<<<grid_for(nb_bytes / 16 * T, threads, num_sms, 8), threads, 0, stream>>>(
+        L, T, nb_bytes / 16, static_cast<uint4 *>(out));
+  else
+    all_gather_bytes<<<grid_for(nb_bytes * T, threads, num_sms, 8), threads, 0, stream>>>(
+        L, T, nb_bytes, static_cast<uint8_t *>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_sum_bf16(const float *const *parts, int T, long long n, void *Z, int num_sms,
+                                  cudaStream_t stream) {
+  if (T < 1 || T > kMaxParts) return cudaErrorInvalidValue;
+  if (n <= 0) return cudaSuccess;
+  PartList L{};
+  bool aligned = (reinterpret_cast<uintptr_t>(Z) & 7u) == 0;
+  for (int t = 0; t < T; ++t) {
+    L.p[t] = parts[t];
+    aligned = aligned && ((reinterpret_cast<uintptr_t>(parts[t]) & 15u) == 0);
+  }
+  constexpr int threads = 256;
+  const long long n4 = aligned ? n / 4 : 0;
+  __nv_bfloat16 *z = static_cast<__nv_bfloat16 *>(Z);
+  if (n4 > 0)
+    shard_sum_bf16_vec<<<grid_for(n4, threads, num_sms, 8), threads, 0, stream>>>(L, T, n4, z);
+  if (n4 * 4 < n)
+    shard_sum_bf16_scalar<<<grid_for(n - n4 * 4, threads, num_sms, 8), threads, 0, stream>>>(
+        L, T, n4 * 4, n, z);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_pack(PackMode mode, const void *src, long long src_ld, void *dst, int S, long long R,

@@ -75,6 +75,14 @@ def _load():
         lib.orc_partial_sum_f32.restype = None
         lib.orc_partial_sum_f32.argtypes = [vp, i32, i64, vp]
         lib.orc_max_threads.restype = i32
+        lib.orc_reduce_scatter_f32.restype = i32
+        lib.orc_reduce_scatter_f32.argtypes = [vp, i32, i64, vp]
+        lib.orc_all_gather.restype = i32
+        lib.orc_all_gather.argtypes = [vp, i32, i64, i32, vp]
+        lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+        lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.orc_partial_sum_bf16.restype = None
+        lib.orc_partial_sum_bf16.argtypes = [vp, i32, i64, vp]
         for name in ("orc_shard_w1", "orc_shard_w2", "orc_shard_wqkv", "orc_shard_wo",
                      "orc_linear", "orc_colpar_full", "orc_colpar_shard",
                      "orc_mlp_unsharded", "orc_mlp_sharded", "orc_qkv_shard",
@@ -290,4 +298,38 @@ def partial_sum_f32(P: np.ndarray) -> np.ndarray:
     T, n = P.shape
     out = np.empty(n, dtype=np.float32)
     _load().orc_partial_sum_f32(_ptr(P), T, n, _ptr(out))
+    return out
+
+
+def reduce_scatter_f32(P: np.ndarray) -> np.ndarray:
+    """Reduce-scatter of float32 partials [T x n]: row i of the [T x n/T]
+    result is block i of the ascending-order sum."""
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    T, n = P.shape
+    if n % T:
+        raise OracleError(ERR_INDIVISIBLE, "reduce_scatter_f32")
+    out = np.empty((T, n // T), dtype=np.float32)
+    _check(_load().orc_reduce_scatter_f32(_ptr(P), T, n, _ptr(out)), "reduce_scatter_f32")
+    return out
+
+
+def all_gather(parts: np.ndarray) -> np.ndarray:
+    """All-gather of T blocks [T x nb] into one array of T * nb elements."""
+    parts = np.ascontiguousarray(parts)
+    T, nb = parts.shape
+    out = np.empty(T * nb, dtype=parts.dtype)
+    _check(_load().orc_all_gather(_ptr(parts), T, nb, parts.dtype.itemsize, _ptr(out)), "all_gather")
+    return out
+
+
+def f32_to_bf16(x: float) -> int:
+    return int(_load().orc_f32_to_bf16(float(x)))
+
+
+def partial_sum_bf16(P: np.ndarray) -> np.ndarray:
+    """All-reduce-sum of float32 partials [T x n] rounded once to bfloat16 (bits)."""
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    T, n = P.shape
+    out = np.empty(n, dtype=np.uint16)
+    _load().orc_partial_sum_bf16(_ptr(P), T, n, _ptr(out))
     return out

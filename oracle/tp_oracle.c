@@ -473,3 +473,61 @@ int orc_max_threads(void)
     return 1;
 #endif
 }
+
+/* ---- the other collectives named for tensor parallelism ------------------
+ * "Tensor Parallelism in Action", section 2, question 3 names AllReduce,
+ * AllGather and ReduceScatter; the "Tensor parallelism" guide's ring byte
+ * count 2 (T - 1) / T * H * B is a reduce-scatter half followed by an
+ * all-gather half.  With all T ranks on one device: */
+
+/* Reduce-scatter: rank i receives block i (n/T values) of the sum over ranks,
+ * out[i][k] = ((P[0][i nb + k] + P[1][i nb + k]) + ...) in float32. */
+int orc_reduce_scatter_f32(const float *P, int T, int64_t n, float *out)
+{
+    if (!P || !out || T <= 0 || n < 0)
+        return ORC_ERR_ARG;
+    if (n % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    const int64_t nb = n / T;
+    for (int i = 0; i < T; ++i)
+        for (int64_t k = 0; k < nb; ++k) {
+            float s = P[i * nb + k];
+            for (int j = 1; j < T; ++j)
+                s = s + P[(int64_t)j * n + i * nb + k];
+            out[(int64_t)i * nb + k] = s;
+        }
+    return ORC_OK;
+}
+
+/* All-gather: the T blocks of nb elements each, concatenated in rank order. */
+int orc_all_gather(const void *parts, int T, int64_t nb, int elem_bytes, void *out)
+{
+    if (!parts || !out || T <= 0 || nb < 0 || elem_bytes <= 0)
+        return ORC_ERR_ARG;
+    memcpy(out, parts, (size_t)(T * nb) * (size_t)elem_bytes);
+    return ORC_OK;
+}
+
+/* float32 -> bfloat16 bits, round to nearest, ties to even (finite inputs). */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* All-reduce-sum with a bfloat16 result: the float32 ascending-order sum,
+ * rounded once to bfloat16. */
+void orc_partial_sum_bf16(const float *P, int T, int64_t n, uint16_t *Z)
+{
+    for (int64_t k = 0; k < n; ++k) {
+        float s = P[k];
+        for (int i = 1; i < T; ++i)
+            s = s + P[(int64_t)i * n + k];
+        Z[k] = orc_f32_to_bf16(s);
+    }
+}

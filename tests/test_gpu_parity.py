@@ -244,12 +244,13 @@ def test_host_buffer_forward(tp):
     assert np.array_equal(Zh.numpy(), Zd)
 
 
-def test_wait_timeout_reports_and_recovers(tp):
+@pytest.mark.parametrize("M", [256, 64, 4])  # CTA-pair tiles, single-CTA tiles, decode
+def test_wait_timeout_reports_and_recovers(tp, M):
     """A wait limit of 1 ns makes the GEMM's waits run out: the kernels return
     early, the status says TP_ERR_TIMEOUT, nothing faults, and the next call
     with the default limit is correct."""
-    M, H, F, T = 256, 512, 2048, 4
-    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=8)
+    H, F, T = 512, 2048, 4
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=8, x_rows=max(M, 16))
     s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
     X = to_device(d["X"])
     assert tp.tp_last_device_status() == 0
@@ -264,3 +265,89 @@ def test_wait_timeout_reports_and_recovers(tp):
     assert tp.tp_last_device_status() == 0
     assert rowwise_rms_error(Z.cpu().numpy(),
                              oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")) <= TOL_BF16_ROW_RMS
+
+
+# ---- guard bands: no write outside the output buffers -----------------------------
+
+@pytest.mark.parametrize("act,M,H,F,T,variant", [
+    ("gelu", 300, 512, 2048, 4, "partials"),   # CTA-pair tiles with a ragged last tile
+    ("gelu", 300, 512, 2048, 4, "tmem_acc"),
+    ("swiglu", 100, 512, 2048, 8, "auto"),     # single-CTA tiles, ragged
+    ("swiglu", 3, 512, 2048, 4, "auto"),       # decode kernels
+    ("gelu", 37, 96, 240, 3, "partials"),      # float32 path
+])
+def test_outputs_stay_inside_their_buffers(tp, act, M, H, F, T, variant):
+    """Y, Z and the workspace sit between canary bands; after the forward
+    pass every canary word is intact and Z is still correct."""
+    import torch
+    dtype = "f32" if H == 96 else "bf16"
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype=dtype, seed=77, x_rows=max(M, 16))
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    X = to_device(d["X"])
+    G = 4096  # canary words on each side
+    canary = 0x7F7FDEAD
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+
+    def guarded(n_bytes):
+        n_words = (n_bytes + 3) // 4
+        buf = torch.full((G + n_words + G,), canary, dtype=torch.int32, device="cuda")
+        return buf, buf[G:G + n_words]
+
+    zbuf, zwords = guarded(M * H * 4)
+    ybuf, ywords = guarded(T * M * (F // T) * (2 if dtype == "bf16" else 4))
+    ws_col = tp.tp_colpar_workspace_bytes(s, M)
+    ws_row = tp.tp_rowpar_workspace_bytes(s, M, variant)
+    cbuf, cwords = guarded(max(ws_col, 16))
+    rbuf, rwords = guarded(max(ws_row, 16))
+    Z = zwords.view(torch.float32).view(M, H)
+    Y = ywords.view(tdt).view(T, M, F // T)
+    tp.tp_colpar_forward(s, X, Y, workspace=cwords.view(torch.uint8))
+    tp.tp_rowpar_forward(s, Y, variant, Z, workspace=rwords.view(torch.uint8))
+    _sync()
+    assert tp.tp_last_device_status() == 0
+    for buf in (zbuf, ybuf, cbuf, rbuf):
+        assert torch.all(buf[:G] == canary) and torch.all(buf[-G:] == canary)
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    if dtype == "bf16":
+        assert rowwise_rms_error(Z.cpu().numpy(), Zref) <= TOL_BF16_ROW_RMS
+    else:
+        assert normwise_error(Z.cpu().numpy(), Zref) <= TOL_F32_NORMWISE
+
+
+# ---- reduce-scatter, all-gather, bf16 all-reduce (bit exact) -----------------------
+
+@pytest.mark.parametrize("T,n", [(2, 4096), (4, 1 << 20), (8, 8 * 1001), (3, 3 * 77), (8, 8 * 4096)])
+def test_reduce_scatter_all_gather_bit_exact(tp, T, n):
+    import torch
+    P = partials_inputs(T, n, seed=40 + T)
+    parts = [to_device(P[t]) for t in range(T)]
+    rs = tp.tp_reduce_scatter(parts)
+    _sync()
+    ref = oracle.reduce_scatter_f32(P)
+    for i in range(T):
+        assert np.array_equal(rs[i].cpu().numpy(), ref[i])
+    ag = tp.tp_all_gather(rs)
+    _sync()
+    assert np.array_equal(ag.cpu().numpy(), oracle.partial_sum_f32(P))
+    # in-place all-gather: the parts already live in the output
+    buf = torch.zeros(n, dtype=torch.float32, device="cuda")
+    nb = n // T
+    views = [buf[i * nb:(i + 1) * nb] for i in range(T)]
+    for i in range(T):
+        views[i].copy_(rs[i])
+    tp.tp_all_gather(views, out=buf)
+    _sync()
+    assert np.array_equal(buf.cpu().numpy(), ag.cpu().numpy())
+    # bf16 elements, odd sizes (byte path)
+    parts16 = [torch.arange(i * 7, i * 7 + 7, device="cuda").to(torch.bfloat16) for i in range(T)]
+    g16 = tp.tp_all_gather(parts16)
+    _sync()
+    assert torch.equal(g16.float().cpu(), torch.arange(7 * T).float())
+
+
+@pytest.mark.parametrize("T,n", [(4, 1 << 20), (8, 12345), (1, 7)])
+def test_partial_sum_bf16_bit_exact(tp, T, n):
+    P = partials_inputs(T, n, seed=60 + T)
+    Z = tp.tp_partial_sum_bf16([to_device(P[t]) for t in range(T)])
+    _sync()
+    assert np.array_equal(bf16_bits(Z), oracle.partial_sum_bf16(P))

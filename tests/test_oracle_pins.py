@@ -333,3 +333,45 @@ def test_synth_bf16_encoding_round_to_nearest_even():
     v = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9, -2.5], dtype=np.float32)
     bits = f32_to_bf16_bits(v)
     assert list(bits) == [0x3F80, 0x3F82, 0x3F80, 0xC020]
+
+
+# --- the other collectives: reduce-scatter, all-gather, bf16 all-reduce -------
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_reduce_scatter_then_all_gather_is_the_all_reduce(T):
+    """The ring all-reduce is a reduce-scatter followed by an all-gather (the
+    2 (T-1)/T byte count of the ring): the composition equals the all-reduce
+    bit for bit, and each block is the sum of that block over ranks."""
+    rng = np.random.default_rng(T)
+    n = 64 * T
+    P = rng.standard_normal((T, n)).astype(np.float32)
+    rs = oracle.reduce_scatter_f32(P)
+    assert rs.shape == (T, n // T)
+    assert np.array_equal(oracle.all_gather(rs), oracle.partial_sum_f32(P))
+    Pi = rng.integers(-50, 50, size=(T, n)).astype(np.float32)
+    exact = Pi.astype(np.int64).sum(0).reshape(T, n // T).astype(np.float32)
+    assert np.array_equal(oracle.reduce_scatter_f32(Pi), exact)
+
+
+def test_all_gather_is_concatenation():
+    parts = np.arange(24, dtype=np.uint16).reshape(4, 6)
+    assert np.array_equal(oracle.all_gather(parts), np.arange(24, dtype=np.uint16))
+
+
+def test_reduce_scatter_rejects_uneven_blocks():
+    with pytest.raises(oracle.OracleError):
+        oracle.reduce_scatter_f32(np.zeros((3, 10), dtype=np.float32))
+
+
+def test_bf16_rounding_matches_the_input_encoder_and_ties_to_even():
+    """Two independent implementations of round-to-nearest-even agree; ties
+    go to the even neighbour."""
+    rng = np.random.default_rng(3)
+    v = np.concatenate([rng.standard_normal(5000).astype(np.float32) * 100,
+                        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 0.0, -0.0,
+                                  3.3895314e38], dtype=np.float32)])
+    assert [oracle.f32_to_bf16(x) for x in v] == list(f32_to_bf16_bits(v))
+    assert oracle.f32_to_bf16(1 + 2 ** -8) == 0x3F80
+    assert oracle.f32_to_bf16(1 + 3 * 2 ** -8) == 0x3F82
+    P = rng.standard_normal((4, 999)).astype(np.float32)
+    assert np.array_equal(oracle.partial_sum_bf16(P), f32_to_bf16_bits(oracle.partial_sum_f32(P)))
