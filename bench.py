@@ -340,7 +340,8 @@ def run_ours(args) -> dict | None:
                    "parallelism": f"{world} independent replica(s); T={T} shards per GPU",
                    "l2": "inputs larger than L2 (256 MiB of weights read per step)"},
         "pct_bf16_peak": round(100.0 * value / 1e12 / world / peak, 1),
-        "roofline": {"kernel": "tp_gemm_kernel<256, GELU> (column-parallel GEMM + GeLU)",
+        "roofline": {"kernel": "tp_gemm_pair_kernel<EPI_GELU_BF16> (column-parallel GEMM + GeLU, "
+                               "CTA-pair 256x256 tiles)",
                      "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
                      "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
