@@ -47,6 +47,11 @@ def parse_args(argv=None):
                    help="secondary measurements at N=1: decode + shard-sum (default), "
                         "plus attention projections and the large SwiGLU prefill (full)")
     p.add_argument("--cpu-rows", type=int, default=64, help="rows of the oracle CPU-baseline sample")
+    p.add_argument("--case", choices=("prefill", "decode", "shard_sum"), default="prefill",
+                   help="prefill: the headline step (default); decode / shard_sum: time only the "
+                        "memory-bound decode MLP (H=8192, F=28672, T=8, SwiGLU, --decode-m tokens) "
+                        "or the standalone shard-sum (T=8, n=8192*8192), for profiling")
+    p.add_argument("--decode-m", type=int, default=16)
     return p.parse_args(argv)
 
 
@@ -508,10 +513,60 @@ def run_reference(args) -> dict | None:
     }
 
 
+def run_case(args) -> dict:
+    """One memory-bound case on its own (N = 1): the decode MLP or the
+    standalone shard-sum, timed over --steps calls after --warmup calls."""
+    import torch
+
+    import linear_sharding_gb300 as tp
+    from synth import WORKLOADS
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    tp.load_library()
+    peaks, peak_src = measured_peaks()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+
+    def randn(shape, std, dtype=torch.bfloat16):
+        return (torch.randn(shape, generator=gen, device=device) * std).to(dtype)
+
+    if args.case == "decode":
+        w = WORKLOADS["decode_swiglu_h8192_f28672_t8"]
+        H, F, T, M = w["H"], w["F"], w["T"], args.decode_m
+        s = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                                "swiglu")
+        X = randn((M, H), 1.0)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, args.variant), 1), dtype=torch.uint8,
+                         device=device)
+        fn = lambda: tp.tp_mlp_forward(s, X, args.variant, Z, ws)  # noqa: E731
+        byts = 3 * H * F * 2 + M * H * (2 + 4)
+        cfg = {"workload": "decode_swiglu_h8192_f28672_t8", "M": M, "H": H, "F": F, "T": T,
+               "variant": args.variant}
+    else:
+        T, n = 8, 8192 * 8192
+        P = [torch.randn(n, generator=gen, device=device) for _ in range(T)]
+        Z = torch.empty(n, dtype=torch.float32, device=device)
+        fn = lambda: tp.tp_partial_sum(P, Z)  # noqa: E731
+        byts = (T + 1) * n * 4
+        cfg = {"workload": "shard_sum_t8_n67108864", "T": T, "n": n}
+    t = _time_calls(fn, args.steps, warm=args.warmup)
+    if tp.tp_last_device_status() != 0:
+        raise RuntimeError("device status error")
+    gbs = byts / t / 1e9
+    return {"metric": f"{args.case} HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "us_per_call": round(t * 1e6, 2), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3),
+            "peak_source": peak_src, "steps": args.steps, "warmup": args.warmup, "config": cfg,
+            "algorithmic_bytes": byts, "l2": "inputs larger than L2"}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps >= 1 and --warmup >= 0")
+    if args.case != "prefill" and args.impl == "ours":
+        print(json.dumps(run_case(args)), flush=True)
+        return
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
