@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tp_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 ACTS = {"gelu": 0, "swiglu": 1, "identity": 2}
 OK, ERR_ARG, ERR_INDIVISIBLE, ERR_OOM = 0, 1, 2, 5
 
@@ -75,6 +75,14 @@ def _load():
         lib.orc_partial_sum_f32.restype = None
         lib.orc_partial_sum_f32.argtypes = [vp, i32, i64, vp]
         lib.orc_max_threads.restype = i32
+        lib.orc_gelu_grad.restype = ctypes.c_double
+        lib.orc_gelu_grad.argtypes = [ctypes.c_double]
+        lib.orc_silu_grad.restype = ctypes.c_double
+        lib.orc_silu_grad.argtypes = [ctypes.c_double]
+        lib.orc_mlp_backward_dx.restype = i32
+        lib.orc_mlp_backward_dx.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp]
+        lib.orc_mlp_backward_dw.restype = i32
+        lib.orc_mlp_backward_dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp, dp]
         lib.orc_reduce_scatter_f32.restype = i32
         lib.orc_reduce_scatter_f32.argtypes = [vp, i32, i64, vp]
         lib.orc_all_gather.restype = i32
@@ -108,7 +116,9 @@ def _dt(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle inputs are float32 or bfloat16 bits (uint16), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle inputs are float32, float64 or bfloat16 bits (uint16), got {a.dtype}")
 
 
 def _c(a: np.ndarray) -> np.ndarray:
@@ -333,3 +343,41 @@ def partial_sum_bf16(P: np.ndarray) -> np.ndarray:
     out = np.empty(n, dtype=np.uint16)
     _load().orc_partial_sum_bf16(_ptr(P), T, n, _ptr(out))
     return out
+
+
+def gelu_grad(y: float) -> float:
+    return float(_load().orc_gelu_grad(float(y)))
+
+
+def silu_grad(g: float) -> float:
+    return float(_load().orc_silu_grad(float(g)))
+
+
+def mlp_backward_dx(X, W1, W2, dZ, act: str, rows=None) -> np.ndarray:
+    """dX = dP W1^T on the selected token rows, [rows x H] (fp64)."""
+    X, W1, W2, dZ = _c(X), _c(W1), _c(W2), _c(dZ)
+    M, H, F = _mlp_shapes(X, W1, W2, act)
+    if dZ.shape != (M, H) or dZ.dtype != X.dtype:
+        raise ValueError("dZ must be [M x H] like X")
+    r = _rows(rows, M)
+    out = np.empty((r.size, H), dtype=np.float64)
+    _check(_load().orc_mlp_backward_dx(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dZ), _dt(X), M, H, F,
+                                       ACTS[act], _ptr(r), r.size, _ptr(out)), "mlp_backward_dx")
+    return out
+
+
+def mlp_backward_dw(X, W1, W2, dZ, act: str, fcols=None):
+    """(dW1 columns, dW2 rows) at the selected FFN indices f: dW1 [H x n]
+    (SwiGLU [H x 2n]: gate columns then up columns), dW2 [n x H] (fp64)."""
+    X, W1, W2, dZ = _c(X), _c(W1), _c(W2), _c(dZ)
+    M, H, F = _mlp_shapes(X, W1, W2, act)
+    if dZ.shape != (M, H) or dZ.dtype != X.dtype:
+        raise ValueError("dZ must be [M x H] like X")
+    f = _rows(fcols, F)
+    n = f.size
+    nparts = 2 if act == "swiglu" else 1
+    dW1 = np.empty((H, nparts * n), dtype=np.float64)
+    dW2 = np.empty((n, H), dtype=np.float64)
+    _check(_load().orc_mlp_backward_dw(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dZ), _dt(X), M, H, F,
+                                       ACTS[act], _ptr(f), n, _ptr(dW1), _ptr(dW2)), "mlp_backward_dw")
+    return dW1, dW2

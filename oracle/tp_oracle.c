@@ -50,6 +50,7 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_F64 2 /* test inputs for finite differences */
 
 #define ORC_GELU 0
 #define ORC_SWIGLU 1
@@ -62,13 +63,15 @@
 
 /* ---- element access ---------------------------------------------------- */
 
-size_t orc_elem_bytes(int dt) { return dt == ORC_BF16 ? 2u : 4u; }
+size_t orc_elem_bytes(int dt) { return dt == ORC_BF16 ? 2u : dt == ORC_F64 ? 8u : 4u; }
 
 /* Exact value of element idx of an array of float32 or bfloat16 (the upper
  * 16 bits of a float32). */
 double orc_value(const void *base, int64_t idx, int dt)
 {
     float f;
+    if (dt == ORC_F64)
+        return ((const double *)base)[idx];
     if (dt == ORC_F32) {
         f = ((const float *)base)[idx];
     } else {
@@ -530,4 +533,163 @@ void orc_partial_sum_bf16(const float *P, int T, int64_t n, uint16_t *Z)
             s = s + P[(int64_t)i * n + k];
         Z[k] = orc_f32_to_bf16(s);
     }
+}
+
+/* ---- backward of the tensor-parallel MLP -------------------------------
+ * "Slice the matrix itself", section "Strict NVLink Domain Constraint": the
+ * all-reduces run on every layer's forward AND backward pass; the duoan.github.io
+ * teaser: a layer contract says "which gradient path communicates".  For
+ * Z = act(X W1) W2 and an upstream gradient dZ, with P = X W1 the
+ * pre-activation and Hh = act(P):
+ *   dH = dZ W2^T            (per shard: dH_i = dZ W2_i^T, no exchange)
+ *   dP = dH * act'(P)        (elementwise; SwiGLU: dG = dH u SiLU'(g), dU = dH SiLU(g))
+ *   dW2 = Hh^T dZ            (row block i = Hh_i^T dZ, local)
+ *   dW1 = X^T dP             (column block i = X^T dP_i, local)
+ *   dX = dP W1^T = sum_i dP_i W1_i^T   (the backward all-reduce-sum)
+ * GeLU'(y) = Phi(y) + y phi(y); SiLU'(g) = s (1 + g (1 - s)), s = 1/(1+e^-g). */
+
+double orc_gelu_grad(double y)
+{
+    const double pi = 3.14159265358979323846;
+    return 0.5 * (1.0 + erf(y / sqrt(2.0))) + y * exp(-0.5 * y * y) / sqrt(2.0 * pi);
+}
+
+double orc_silu_grad(double g)
+{
+    const double s = 1.0 / (1.0 + exp(-g));
+    return s * (1.0 + g * (1.0 - s));
+}
+
+/* For one token row r: P (ncols = F or 2F values), dH (F values), and
+ * dP (ncols values: for SwiGLU [dG | dU]) and Hh (F values). */
+static void token_backward(const void *X, const void *W1, const void *W2, const void *dZ, int dt,
+                           int64_t H, int64_t F, int act, int64_t r, double *P, double *dH,
+                           double *dP, double *Hh)
+{
+    const int64_t ncols = (act == ORC_SWIGLU) ? 2 * F : F;
+    row_times_matrix(X, r * H, dt, H, W1, ncols, 0, ncols, P);
+    /* dH[f] = sum_h dZ[r][h] W2[f][h] */
+    for (int64_t f = 0; f < F; ++f) {
+        double acc = 0.0;
+        for (int64_t h = 0; h < H; ++h)
+            acc += orc_value(dZ, r * H + h, dt) * orc_value(W2, f * H + h, dt);
+        dH[f] = acc;
+    }
+    for (int64_t f = 0; f < F; ++f) {
+        if (act == ORC_GELU) {
+            dP[f] = dH[f] * orc_gelu_grad(P[f]);
+            Hh[f] = orc_gelu(P[f]);
+        } else if (act == ORC_SWIGLU) {
+            const double g = P[f], u = P[F + f];
+            dP[f] = dH[f] * u * orc_silu_grad(g);
+            dP[F + f] = dH[f] * orc_silu(g);
+            Hh[f] = orc_silu(g) * u;
+        } else {
+            dP[f] = dH[f];
+            Hh[f] = P[f];
+        }
+    }
+}
+
+/* dX on selected token rows: dX[r][h] = sum_c dP[r][c] W1[h][c]. */
+int orc_mlp_backward_dx(const void *X, const void *W1, const void *W2, const void *dZ, int dt,
+                        int64_t M, int64_t H, int64_t F, int act, const int64_t *rows,
+                        int64_t n_rows, double *dX)
+{
+    if (!X || !W1 || !W2 || !dZ || !dX || M <= 0 || H <= 0 || F <= 0 || act < 0 || act > 2)
+        return ORC_ERR_ARG;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const int64_t ncols = (act == ORC_SWIGLU) ? 2 * F : F;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        double *buf = (double *)malloc((size_t)(ncols * 2 + F * 2) * sizeof(double));
+        if (!buf) {
+#pragma omp atomic write
+            err = ORC_ERR_OOM;
+            continue;
+        }
+        double *P = buf, *dP = buf + ncols, *dH = buf + 2 * ncols, *Hh = dH + F;
+        token_backward(X, W1, W2, dZ, dt, H, F, act, rows[i], P, dH, dP, Hh);
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < ncols; ++c)
+                acc += dP[c] * orc_value(W1, h * ncols + c, dt);
+            dX[i * H + h] = acc;
+        }
+        free(buf);
+    }
+    return err;
+}
+
+/* Weight gradients on selected FFN columns f (for SwiGLU, f names the pair
+ * gate column f / up column F + f):
+ *   dW1c[k][j] = sum_m X[m][k] dP[m][f_j]    (and dW1c_up for the up column),
+ *   dW2r[j][h] = sum_m Hh[m][f_j] dZ[m][h].
+ * dW1c is [H x n] (SwiGLU: [H x 2n], gate columns then up columns),
+ * dW2r is [n x H].  Every token contributes. */
+int orc_mlp_backward_dw(const void *X, const void *W1, const void *W2, const void *dZ, int dt,
+                        int64_t M, int64_t H, int64_t F, int act, const int64_t *fcols,
+                        int64_t n, double *dW1c, double *dW2r)
+{
+    if (!X || !W1 || !W2 || !dZ || !dW1c || !dW2r || M <= 0 || H <= 0 || F <= 0 || act < 0 ||
+        act > 2 || n < 0 || (n > 0 && !fcols))
+        return ORC_ERR_ARG;
+    for (int64_t j = 0; j < n; ++j)
+        if (fcols[j] < 0 || fcols[j] >= F)
+            return ORC_ERR_ARG;
+    const int64_t ncols = (act == ORC_SWIGLU) ? 2 * F : F;
+    const int nparts = (act == ORC_SWIGLU) ? 2 : 1;
+    /* per token, the values of dP and Hh at the selected columns */
+    double *dPs = (double *)calloc((size_t)(M * n * nparts + 1), sizeof(double));
+    double *Hs = (double *)calloc((size_t)(M * n + 1), sizeof(double));
+    if (!dPs || !Hs) {
+        free(dPs);
+        free(Hs);
+        return ORC_ERR_OOM;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j < n; ++j) {
+            const int64_t f = fcols[j];
+            double p[2] = {0.0, 0.0}, dh = 0.0;
+            for (int part = 0; part < nparts; ++part)
+                for (int64_t k = 0; k < H; ++k)
+                    p[part] += orc_value(X, m * H + k, dt) * orc_value(W1, k * ncols + part * F + f, dt);
+            for (int64_t h = 0; h < H; ++h)
+                dh += orc_value(dZ, m * H + h, dt) * orc_value(W2, f * H + h, dt);
+            if (act == ORC_GELU) {
+                dPs[(m * n + j) * nparts] = dh * orc_gelu_grad(p[0]);
+                Hs[m * n + j] = orc_gelu(p[0]);
+            } else if (act == ORC_SWIGLU) {
+                dPs[(m * n + j) * 2] = dh * p[1] * orc_silu_grad(p[0]);
+                dPs[(m * n + j) * 2 + 1] = dh * orc_silu(p[0]);
+                Hs[m * n + j] = orc_silu(p[0]) * p[1];
+            } else {
+                dPs[m * n + j] = dh;
+                Hs[m * n + j] = p[0];
+            }
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t k = 0; k < H; ++k)
+        for (int part = 0; part < nparts; ++part)
+            for (int64_t j = 0; j < n; ++j) {
+                double acc = 0.0;
+                for (int64_t m = 0; m < M; ++m)
+                    acc += orc_value(X, m * H + k, dt) * dPs[(m * n + j) * nparts + part];
+                dW1c[k * n * nparts + part * n + j] = acc;
+            }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n; ++j)
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                acc += Hs[m * n + j] * orc_value(dZ, m * H + h, dt);
+            dW2r[j * H + h] = acc;
+        }
+    free(dPs);
+    free(Hs);
+    return ORC_OK;
 }

@@ -375,3 +375,82 @@ def test_bf16_rounding_matches_the_input_encoder_and_ties_to_even():
     assert oracle.f32_to_bf16(1 + 3 * 2 ** -8) == 0x3F82
     P = rng.standard_normal((4, 999)).astype(np.float32)
     assert np.array_equal(oracle.partial_sum_bf16(P), f32_to_bf16_bits(oracle.partial_sum_f32(P)))
+
+
+# --- backward of the MLP ------------------------------------------------------
+
+def _loss(X, W1, W2, G, act):
+    """L = sum(Z * G) with the oracle's forward; dL/dZ = G."""
+    return float(np.sum(oracle.mlp_unsharded(X, W1, W2, act) * G))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
+def test_backward_matches_central_differences(act):
+    """Every gradient (dX, dW1, dW2) equals the central difference of the
+    forward loss sum(Z * dZ) on fp64 inputs: a pin independent of the
+    backward's own formulas."""
+    rng = np.random.default_rng(12)
+    M, H, F = 3, 4, 6
+    ncols = 2 * F if act == "swiglu" else F
+    X = rng.standard_normal((M, H))
+    W1 = rng.standard_normal((H, ncols)) * 0.7
+    W2 = rng.standard_normal((F, H)) * 0.7
+    G = rng.standard_normal((M, H))
+    eps = 1e-6
+    dX = oracle.mlp_backward_dx(X, W1, W2, G, act)
+    dW1, dW2 = oracle.mlp_backward_dw(X, W1, W2, G, act)
+    nparts = 2 if act == "swiglu" else 1
+
+    def fd(arr, idx):
+        a, b = arr.copy(), arr.copy()
+        a[idx] += eps
+        b[idx] -= eps
+        if arr is X:
+            return (_loss(a, W1, W2, G, act) - _loss(b, W1, W2, G, act)) / (2 * eps)
+        if arr is W1:
+            return (_loss(X, a, W2, G, act) - _loss(X, b, W2, G, act)) / (2 * eps)
+        return (_loss(X, W1, a, G, act) - _loss(X, W1, b, G, act)) / (2 * eps)
+
+    for idx in np.ndindex(X.shape):
+        assert dX[idx] == pytest.approx(fd(X, idx), rel=1e-6, abs=1e-8)
+    for k, c in np.ndindex(W1.shape):
+        part, f = divmod(c, F)
+        got = dW1[k, part * F + f] if nparts == 2 else dW1[k, c]
+        assert got == pytest.approx(fd(W1, (k, c)), rel=1e-6, abs=1e-8)
+    for idx in np.ndindex(W2.shape):
+        assert dW2[idx] == pytest.approx(fd(W2, idx), rel=1e-6, abs=1e-8)
+
+
+def test_activation_derivatives_closed_forms():
+    """GeLU'(0) = 1/2, GeLU'(1) = Phi(1) + phi(1); SiLU'(0) = 1/2."""
+    from math import exp, pi, sqrt
+    assert oracle.gelu_grad(0.0) == pytest.approx(0.5, rel=1e-15)
+    assert oracle.gelu_grad(1.0) == pytest.approx(0.8413447460685429 + exp(-0.5) / sqrt(2 * pi), rel=1e-14)
+    assert oracle.silu_grad(0.0) == pytest.approx(0.5, rel=1e-15)
+    for g in (-3.0, -0.5, 0.7, 4.0):
+        h = 1e-6
+        assert oracle.silu_grad(g) == pytest.approx((oracle.silu(g + h) - oracle.silu(g - h)) / (2 * h), rel=1e-8)
+        assert oracle.gelu_grad(g) == pytest.approx((oracle.gelu(g + h) - oracle.gelu(g - h)) / (2 * h), rel=1e-8)
+
+
+def test_identity_backward_is_transposed_products():
+    """act = identity: dX = dZ W2^T W1^T, dW1 = X^T dZ W2^T, dW2 = (X W1)^T dZ."""
+    d = mlp_inputs(M=5, H=8, F=16, act="identity", dtype="f32", seed=6)
+    rng = np.random.default_rng(7)
+    G = rng.standard_normal((5, 8)).astype(np.float32)
+    X, W1, W2 = (_decode(d[k]) for k in ("X", "W1", "W2"))
+    Gd = G.astype(np.float64)
+    assert _normwise(oracle.mlp_backward_dx(d["X"], d["W1"], d["W2"], G, "identity"), Gd @ W2.T @ W1.T) <= 1e-13
+    dW1, dW2 = oracle.mlp_backward_dw(d["X"], d["W1"], d["W2"], G, "identity")
+    assert _normwise(dW1, X.T @ (Gd @ W2.T)) <= 1e-13
+    assert _normwise(dW2, (X @ W1).T @ Gd) <= 1e-13
+
+
+def test_backward_column_subset_matches_full():
+    d = mlp_inputs(M=6, H=8, F=16, act="swiglu", dtype="bf16", seed=2)
+    G = f32_to_bf16_bits(np.random.default_rng(1).standard_normal((6, 8)).astype(np.float32))
+    full1, full2 = oracle.mlp_backward_dw(d["X"], d["W1"], d["W2"], G, "swiglu")
+    cols = np.array([3, 11, 0])
+    s1, s2 = oracle.mlp_backward_dw(d["X"], d["W1"], d["W2"], G, "swiglu", fcols=cols)
+    assert np.array_equal(s1[:, :3], full1[:, cols]) and np.array_equal(s1[:, 3:], full1[:, 16 + cols])
+    assert np.array_equal(s2, full2[cols])
