@@ -33,7 +33,7 @@ WORKLOAD = "prefill_gelu_m2048_h4096_f16384_t4"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE = os.path.join(ROOT, "profiles", "colpar_gemm_gelu_prefill_m2048_h4096_f16384_t4.md")
 GEMM_SOURCES = [os.path.join(ROOT, "linear_sharding_gb300", "csrc", f)
-                for f in ("tp_gemm.cu", "tp_device.cuh", "tp_internal.h")]
+                for f in ("tp_gemm_impl.cuh", "tp_gemm.cu", "tp_device.cuh", "tp_internal.h")]
 
 
 def parse_args(argv=None):

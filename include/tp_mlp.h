@@ -258,6 +258,50 @@ TP_API tp_status_t tp_mlp_forward_host(tp_shards_t s, const void *X_host, int64_
                                 tp_variant_t v, float *Z_host, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/*
+ * Training: the forward pass that keeps what the backward pass needs, and
+ * the backward pass.  The pages say the tensor-parallel all-reduces run "on
+ * every single layer forward/backward pass" ("Slice the matrix itself",
+ * section "Strict NVLink Domain Constraint") and that each layer contract
+ * fixes "which gradient path communicates" (the duoan.github.io post on
+ * ColumnParallelLinear / RowParallelLinear).  With P = X W1 (the
+ * pre-activation), Hh = act(P) and the upstream gradient dZ:
+ *   dH_i = dZ W2_i^T, dP_i = dH_i * act'(P_i)   (per shard, no exchange)
+ *   dW2_i = Hh_i^T dZ, dW1_i = X^T dP_i          (per shard, local)
+ *   dX = sum_i dP_i W1_i^T                      (the backward all-reduce-sum)
+ * bfloat16 shards only.
+ *
+ * tp_shards_enable_backward - give a handle the weights in the caller's
+ *   layout (W1 [H x F] or [H x 2F], W2 [F x H], the same matrices that were
+ *   sharded), which the backward GEMMs read K-major.  The handle keeps
+ *   copies (device memory: one more set of weights).
+ *
+ * tp_mlp_forward_train - tp_mlp_forward that also keeps, for the backward
+ *   pass, Hsave = act(X W1_i) as [T x M x F/T] bfloat16 (it is also the
+ *   row-parallel layer's input) and Psave = the pre-activations: GeLU
+ *   [T x M x F/T], SwiGLU [2 x T x M x F/T] (gate, then up); unused (may be
+ *   NULL) for IDENTITY.  Always uses the tensor-core prefill tiles, any M.
+ *   workspace: tp_mlp_train_workspace_bytes(s, M, v) bytes or NULL.
+ *
+ * tp_mlp_backward - from X [M x H], Hsave, Psave and dZ [M x H] (bfloat16,
+ *   device), writes dX [M x H], dW1 [H x F] (SwiGLU [H x 2F] = [dWg | dWu])
+ *   and dW2 [F x H], float32, in the caller's weight layout.  Requires
+ *   tp_shards_enable_backward.  v chooses how dX's sum over shards is done
+ *   (TMEM accumulation, or float32 partials + shard-sum).  workspace:
+ *   tp_mlp_backward_workspace_bytes(s, M, v) bytes or NULL.  Asynchronous.
+ */
+TP_API tp_status_t tp_shards_enable_backward(tp_shards_t s, const void *W1, const void *W2,
+                                             void *stream);
+TP_API size_t tp_mlp_train_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+TP_API tp_status_t tp_mlp_forward_train(tp_shards_t s, const void *X, int64_t M, tp_act_t act,
+                                        tp_variant_t v, float *Z, void *Hsave, void *Psave,
+                                        void *workspace, size_t ws_bytes, void *stream);
+TP_API size_t tp_mlp_backward_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);
+TP_API tp_status_t tp_mlp_backward(tp_shards_t s, const void *X, const void *Hsave,
+                                   const void *Psave, const void *dZ, int64_t M, tp_variant_t v,
+                                   float *dX, float *dW1, float *dW2, void *workspace,
+                                   size_t ws_bytes, void *stream);
+
 /* Device workspace tp_attn_proj_forward needs (float32 partials for the
  * partials variant; 0 for the accumulator variant). */
 TP_API size_t tp_attn_proj_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v);

@@ -35,7 +35,8 @@ EXPORTS = (
     "tp_attn_proj_forward", "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
     "tp_colpar_workspace_bytes", "tp_colpar_forward", "tp_rowpar_workspace_bytes",
     "tp_rowpar_forward", "tp_mlp_forward_noalloc", "tp_reduce_scatter", "tp_all_gather",
-    "tp_partial_sum_bf16",
+    "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
+    "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
 )
 
 _lock = threading.Lock()
@@ -91,11 +92,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, ctypes.POINTER(vp), vp]
         lib.tp_all_gather.argtypes = [ctypes.POINTER(vp), i32, i64, i32, vp, vp]
         lib.tp_partial_sum_bf16.argtypes = [ctypes.POINTER(vp), i32, i64, vp, vp]
+        lib.tp_shards_enable_backward.argtypes = [vp, vp, vp, vp]
+        lib.tp_mlp_train_workspace_bytes.restype = sz
+        lib.tp_mlp_train_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_mlp_forward_train.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+        lib.tp_mlp_backward_workspace_bytes.restype = sz
+        lib.tp_mlp_backward_workspace_bytes.argtypes = [vp, i64, i32]
+        lib.tp_mlp_backward.argtypes = [vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, vp, sz, vp]
         for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
                      "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
                      "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
                      "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
-                     "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16"):
+                     "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16",
+                     "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -346,6 +355,46 @@ def tp_partial_sum_bf16(parts, Z=None, stream=None):
     _check(load_library().tp_partial_sum_bf16(_ptr_array(parts), len(parts), n, _ptr(Z), _stream(stream)),
            "tp_partial_sum_bf16")
     return Z
+
+
+def tp_shards_enable_backward(s: Shards, W1, W2, stream=None) -> None:
+    """Give the handle W1/W2 in the caller's layout for the backward GEMMs."""
+    _check(load_library().tp_shards_enable_backward(s.handle, _ptr(W1.contiguous()), _ptr(W2.contiguous()),
+                                                    _stream(stream)), "tp_shards_enable_backward")
+
+
+def tp_mlp_forward_train(s: Shards, X, variant: str = "auto", stream=None):
+    """Forward pass keeping (Hsave, Psave) for the backward; returns (Z, Hsave, Psave)."""
+    torch = _torch()
+    lib = load_library()
+    X = X.contiguous()
+    M = X.shape[0]
+    Z = torch.empty((M, s.H), dtype=torch.float32, device=X.device)
+    Hs = torch.empty((s.T, M, s.Fs), dtype=torch.bfloat16, device=X.device)
+    nP = 2 if s.act == "swiglu" else 1
+    Ps = torch.empty((nP, s.T, M, s.Fs), dtype=torch.bfloat16, device=X.device)
+    ws = torch.empty(max(lib.tp_mlp_train_workspace_bytes(s.handle, M, VARIANT[variant]), 1),
+                     dtype=torch.uint8, device=X.device)
+    _check(lib.tp_mlp_forward_train(s.handle, _ptr(X), M, ACT[s.act], VARIANT[variant], _ptr(Z), _ptr(Hs),
+                                    _ptr(Ps), _ptr(ws), ws.numel(), _stream(stream)), "tp_mlp_forward_train")
+    return Z, Hs, Ps
+
+
+def tp_mlp_backward(s: Shards, X, Hsave, Psave, dZ, variant: str = "auto", stream=None):
+    """Gradients (dX [M x H], dW1 [H x F or 2F], dW2 [F x H]), float32."""
+    torch = _torch()
+    lib = load_library()
+    M = X.shape[0]
+    ncols = 2 * s.F if s.act == "swiglu" else s.F
+    dX = torch.empty((M, s.H), dtype=torch.float32, device=X.device)
+    dW1 = torch.empty((s.H, ncols), dtype=torch.float32, device=X.device)
+    dW2 = torch.empty((s.F, s.H), dtype=torch.float32, device=X.device)
+    ws = torch.empty(max(lib.tp_mlp_backward_workspace_bytes(s.handle, M, VARIANT[variant]), 1),
+                     dtype=torch.uint8, device=X.device)
+    _check(lib.tp_mlp_backward(s.handle, _ptr(X.contiguous()), _ptr(Hsave), _ptr(Psave), _ptr(dZ.contiguous()),
+                               M, VARIANT[variant], _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(ws), ws.numel(),
+                               _stream(stream)), "tp_mlp_backward")
+    return dX, dW1, dW2
 
 
 def tp_last_device_status(stream=None) -> int:

@@ -24,6 +24,11 @@ struct tp_shards {
   void *w2p = nullptr;  // [T][H][Fs]
   int bn1 = 256, bn2 = 256;
   CUtensorMap map_w1_b, map_w1_a, map_w2_b, map_w2_a;
+  // backward operands: W1 [H x ncols] and W2 [F x H] in the caller's layout
+  bool backward = false;
+  void *w1o = nullptr, *w2o = nullptr;
+  int bn_dh = 256;  // tile width of dH = dZ W2^T (its N is F, tiles stay inside a shard)
+  CUtensorMap map_w2o_bn, map_w2o_128, map_w1o_bn, map_w1o_128;
 };
 
 namespace {
@@ -444,6 +449,240 @@ tp_status_t get_ws(Workspace *w, void *given, size_t given_bytes, size_t need, c
   return TP_OK;
 }
 
+// One tensor-core GEMM D[rows x N] over a K axis of nseg segments of kps
+// k-tiles: picks CTA-pair or single-CTA tiles and fills the work fields.
+struct GemmCall {
+  const CUtensorMap *a = nullptr;
+  int a_seg = 0;
+  const CUtensorMap *b_bn = nullptr, *b_128 = nullptr;  // B maps with box bn rows / 128 rows
+  int b_seg = 0;
+  int64_t rows = 0, N = 0;
+  int bn = 256, kps = 0, nseg = 1, slots = 1;
+  Epi epi = EPI_F32;
+};
+
+tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStream_t st) {
+  const bool pair = use_pair(c.bn, c.rows);
+  g.m_tiles = static_cast<int>(cdiv(c.rows, pair ? 256 : 128));
+  g.n_tiles = static_cast<int>(c.N / c.bn);
+  g.slots = c.slots;
+  g.kt_per_seg = c.kps;
+  g.kt_total = c.nseg * c.kps;
+  g.kt_per_slot = g.kt_total / c.slots;
+  g.a_seg = c.a_seg;
+  g.b_seg = c.b_seg;
+  g.rows_valid = static_cast<int>(c.rows);
+  g.cols_valid = static_cast<int>(c.N);
+  if (pair) TP_CUDA(launch_gemm(CFG_PAIR_N256, c.epi, *c.a, *c.b_128, g, d->sms, st));
+  else TP_CUDA(launch_gemm(cfg_for(c.bn), c.epi, *c.a, *c.b_bn, g, d->sms, st));
+  return TP_OK;
+}
+
+int bn_for(int64_t n) { return n % 256 == 0 ? 256 : 128; }
+
+int64_t round64(int64_t m) { return (m + 63) / 64 * 64; }
+
+struct TrainPlan {
+  int slots2 = 1;       // forward row-parallel slots
+  int slots_dx = 1;     // backward dX slots
+  int nseg = 1;         // segments of dP (T, or 2T for SwiGLU: dG shards then dU shards)
+  int64_t Mp = 0;       // tokens padded to a multiple of 64 (K of the weight gradients)
+  size_t fwd_row = 0;   // forward: row-parallel partials
+  size_t dP = 0, xt = 0, dzt = 0, ht = 0, dpt = 0, dx_part = 0;
+  size_t fwd_total() const { return round256(fwd_row); }
+  size_t bwd_total() const {
+    return round256(dP) + round256(xt) + round256(dzt) + round256(ht) + round256(dpt) + round256(dx_part);
+  }
+};
+
+void plan_train(const tp_shards *s, int64_t M, tp_variant_t v, int sms, TrainPlan *p) {
+  *p = TrainPlan();
+  const int64_t H = s->H, Fs = s->Fs, T = s->T, F = s->F;
+  MlpPlan fp;
+  plan_mlp(s, M > kDecodeMaxM ? M : kDecodeMaxM + 1, v, sms, &fp);
+  p->slots2 = fp.slots2;
+  p->fwd_row = p->slots2 > 1 ? static_cast<size_t>(p->slots2 * M * H) * 4 : 0;
+  p->nseg = static_cast<int>(s->act == TP_ACT_SWIGLU ? 2 * T : T);
+  p->slots_dx = (v == TP_VAR_PARTIALS) ? p->nseg : 1;
+  p->Mp = round64(M);
+  p->dP = static_cast<size_t>(p->nseg * M * Fs) * 2;
+  p->xt = static_cast<size_t>(H * p->Mp) * 2;
+  p->dzt = p->xt;
+  p->ht = static_cast<size_t>(F * p->Mp) * 2;
+  p->dpt = static_cast<size_t>(p->nseg * Fs * p->Mp) * 2;
+  p->dx_part = p->slots_dx > 1 ? static_cast<size_t>(p->slots_dx * M * H) * 4 : 0;
+}
+
+tp_status_t mlp_forward_train_impl(tp_shards *s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
+                                   float *Z, void *Hsave, void *Psave, void *workspace, size_t ws_bytes,
+                                   cudaStream_t st) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (s->dt != TP_BF16) return TP_ERR_DTYPE;
+  if (M < 0 || !valid_variant(v) || act != s->act) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!X || !Z || !Hsave || !aligned16(X) || !aligned16(Z) || !aligned16(Hsave)) return TP_ERR_ARG;
+  if (act != TP_ACT_IDENTITY && (!Psave || !aligned16(Psave))) return TP_ERR_ARG;
+  if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
+  TrainPlan p;
+  plan_train(s, M, v, d->sms, &p);
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.fwd_total(), st));
+  const int64_t H = s->H, T = s->T, Fs = s->Fs;
+  CUtensorMap mx;
+  TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
+  GemmArgs g = base_args(d);
+  g.out = Hsave;
+  g.ld_out = Fs;
+  g.shard_stride = M * Fs;
+  g.shard_cols = static_cast<int>(Fs);
+  GemmCall c;
+  c.a = &mx;
+  c.b_bn = &s->map_w1_b;
+  c.b_128 = &s->map_w1_a;
+  c.rows = M;
+  c.N = T * s->R1;
+  c.bn = s->bn1;
+  c.kps = static_cast<int>(H / 64);
+  if (act == TP_ACT_GELU_ERF) {
+    c.epi = EPI_GELU_SAVE_BF16;
+    g.out2 = Psave;
+  } else if (act == TP_ACT_SWIGLU) {
+    c.epi = EPI_SWIGLU_SAVE_BF16;
+    g.out2 = Psave;
+    g.out3 = static_cast<char *>(Psave) + static_cast<size_t>(T * M * Fs) * 2;
+  } else {
+    c.epi = EPI_IDENT_BF16;
+  }
+  TP_TRY(run_gemm(d, c, g, st));
+  CUtensorMap mh;
+  TP_TRY(make_map(&mh, Hsave, Fs, M, T, Fs * 2, M * Fs * 2, 128));
+  return rowpar_tc(s, d, mh, 1, M, p.slots2, reinterpret_cast<float *>(w.ptr), Z, st);
+}
+
+tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, const void *Psave,
+                              const void *dZ, int64_t M, tp_variant_t v, float *dX, float *dW1, float *dW2,
+                              void *workspace, size_t ws_bytes, cudaStream_t st) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (!s->backward) return TP_ERR_ARG;
+  if (M < 0 || !valid_variant(v)) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  for (const void *ptr : {X, Hsave, dZ, static_cast<const void *>(dX), static_cast<const void *>(dW1),
+                          static_cast<const void *>(dW2)})
+    if (!ptr || !aligned16(ptr)) return TP_ERR_ARG;
+  if (s->act != TP_ACT_IDENTITY && (!Psave || !aligned16(Psave))) return TP_ERR_ARG;
+  if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
+  TrainPlan p;
+  plan_train(s, M, v, d->sms, &p);
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.bwd_total(), st));
+  const int64_t H = s->H, T = s->T, Fs = s->Fs, F = s->F, Mp = p.Mp;
+  const int64_t ncols = p.nseg * Fs;
+  char *dP = w.ptr;
+  char *xt = dP + round256(p.dP);
+  char *dzt = xt + round256(p.xt);
+  char *ht = dzt + round256(p.dzt);
+  char *dpt = ht + round256(p.ht);
+  float *dxp = reinterpret_cast<float *>(dpt + round256(p.dpt));
+
+  // 1. dH = dZ W2^T for every shard, times the activation's derivative -> dP
+  CUtensorMap mdz;
+  TP_TRY(make_map(&mdz, dZ, H, M, 1, H * 2, M * H * 2, 128));
+  {
+    GemmArgs g = base_args(d);
+    g.out = dP;
+    g.ld_out = Fs;
+    g.shard_stride = M * Fs;
+    g.shard_cols = static_cast<int>(Fs);
+    GemmCall c;
+    c.a = &mdz;
+    c.b_bn = &s->map_w2o_bn;
+    c.b_128 = &s->map_w2o_128;
+    c.rows = M;
+    c.N = F;
+    c.bn = s->bn_dh;
+    c.kps = static_cast<int>(H / 64);
+    if (s->act == TP_ACT_GELU_ERF) {
+      c.epi = EPI_DGELU_BF16;
+      g.aux = Psave;
+    } else if (s->act == TP_ACT_SWIGLU) {
+      c.epi = EPI_DSWIGLU_BF16;
+      g.out2 = dP + static_cast<size_t>(T * M * Fs) * 2;
+      g.aux = Psave;
+      g.aux2 = static_cast<const char *>(Psave) + static_cast<size_t>(T * M * Fs) * 2;
+    } else {
+      c.epi = EPI_IDENT_BF16;
+    }
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  // 2. dX = sum over shards of dP_i W1_i^T (the backward all-reduce-sum)
+  CUtensorMap mdp;
+  TP_TRY(make_map(&mdp, dP, Fs, M, p.nseg, Fs * 2, M * Fs * 2, 128));
+  {
+    GemmArgs g = base_args(d);
+    g.out = p.slots_dx > 1 ? static_cast<void *>(dxp) : static_cast<void *>(dX);
+    g.ld_out = H;
+    g.slot_stride = M * H;
+    GemmCall c;
+    c.a = &mdp;
+    c.a_seg = 1;
+    c.b_bn = &s->map_w1o_bn;
+    c.b_128 = &s->map_w1o_128;
+    c.rows = M;
+    c.N = H;
+    c.bn = s->bn2;
+    c.kps = static_cast<int>(Fs / 64);
+    c.nseg = p.nseg;
+    c.slots = p.slots_dx;
+    TP_TRY(run_gemm(d, c, g, st));
+    if (p.slots_dx > 1) TP_CUDA(launch_shard_sum_strided(dxp, p.slots_dx, M * H, M * H, dX, d->sms, st));
+  }
+  // 3. K-major operands for the weight gradients (K = tokens, padded to Mp)
+  TP_CUDA(launch_transpose_pad(X, M, H, H, 0, xt, Mp, 0, 1, st));
+  TP_CUDA(launch_transpose_pad(dZ, M, H, H, 0, dzt, Mp, 0, 1, st));
+  TP_CUDA(launch_transpose_pad(Hsave, M, Fs, Fs, M * Fs, ht, Mp, Fs * Mp, static_cast<int>(T), st));
+  TP_CUDA(launch_transpose_pad(dP, M, Fs, Fs, M * Fs, dpt, Mp, Fs * Mp, p.nseg, st));
+  // 4. dW2 = H^T dZ  [F x H];  5. dW1 = X^T dP  [H x ncols]
+  const int bnh = bn_for(H), bnc = bn_for(ncols);
+  CUtensorMap m_ht, m_xt, m_dzt_bn, m_dzt_128, m_dpt_bn, m_dpt_128;
+  TP_TRY(make_map(&m_ht, ht, Mp, F, 1, Mp * 2, F * Mp * 2, 128));
+  TP_TRY(make_map(&m_xt, xt, Mp, H, 1, Mp * 2, H * Mp * 2, 128));
+  TP_TRY(make_map(&m_dzt_bn, dzt, Mp, H, 1, Mp * 2, H * Mp * 2, bnh));
+  TP_TRY(make_map(&m_dzt_128, dzt, Mp, H, 1, Mp * 2, H * Mp * 2, 128));
+  TP_TRY(make_map(&m_dpt_bn, dpt, Mp, ncols, 1, Mp * 2, ncols * Mp * 2, bnc));
+  TP_TRY(make_map(&m_dpt_128, dpt, Mp, ncols, 1, Mp * 2, ncols * Mp * 2, 128));
+  {
+    GemmArgs g = base_args(d);
+    g.out = dW2;
+    g.ld_out = H;
+    GemmCall c;
+    c.a = &m_ht;
+    c.b_bn = &m_dzt_bn;
+    c.b_128 = &m_dzt_128;
+    c.rows = F;
+    c.N = H;
+    c.bn = bnh;
+    c.kps = static_cast<int>(Mp / 64);
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  {
+    GemmArgs g = base_args(d);
+    g.out = dW1;
+    g.ld_out = ncols;
+    GemmCall c;
+    c.a = &m_xt;
+    c.b_bn = &m_dpt_bn;
+    c.b_128 = &m_dpt_128;
+    c.rows = H;
+    c.N = ncols;
+    c.bn = bnc;
+    c.kps = static_cast<int>(Mp / 64);
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  return TP_OK;
+}
+
 bool act_ok(const tp_shards *s, tp_act_t act) {
   if (act == s->act) return true;
   return s->act != TP_ACT_SWIGLU && (act == TP_ACT_GELU_ERF || act == TP_ACT_IDENTITY);
@@ -681,8 +920,62 @@ void tp_shards_destroy(tp_shards_t s) {
   cudaDeviceSynchronize();
   if (s->w1p) cudaFree(s->w1p);
   if (s->w2p) cudaFree(s->w2p);
+  if (s->w1o) cudaFree(s->w1o);
+  if (s->w2o) cudaFree(s->w2o);
   if (prev >= 0 && prev != s->device) cudaSetDevice(prev);
   delete s;
+}
+
+tp_status_t tp_shards_enable_backward(tp_shards_t s, const void *W1, const void *W2, void *stream) {
+  if (!s || s->kind != 0 || !W1 || !W2) return TP_ERR_ARG;
+  if (s->dt != TP_BF16) return TP_ERR_DTYPE;
+  if (!aligned16(W1) || !aligned16(W2)) return TP_ERR_ARG;
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t H = s->H, F = s->F, ncols = s->act == TP_ACT_SWIGLU ? 2 * F : F;
+  const size_t b1 = static_cast<size_t>(H * ncols) * 2, b2 = static_cast<size_t>(F * H) * 2;
+  if (!s->w1o && cudaMalloc(&s->w1o, b1) != cudaSuccess) return TP_ERR_OOM;
+  if (!s->w2o && cudaMalloc(&s->w2o, b2) != cudaSuccess) return TP_ERR_OOM;
+  TP_CUDA(cudaMemcpyAsync(s->w1o, W1, b1, cudaMemcpyDeviceToDevice, st));
+  TP_CUDA(cudaMemcpyAsync(s->w2o, W2, b2, cudaMemcpyDeviceToDevice, st));
+  s->bn_dh = s->Fs % 256 == 0 ? 256 : 128;
+  TP_TRY(make_map(&s->map_w2o_bn, s->w2o, H, F, 1, H * 2, F * H * 2, s->bn_dh));
+  TP_TRY(make_map(&s->map_w2o_128, s->w2o, H, F, 1, H * 2, F * H * 2, 128));
+  TP_TRY(make_map(&s->map_w1o_bn, s->w1o, ncols, H, 1, ncols * 2, H * ncols * 2, s->bn2));
+  TP_TRY(make_map(&s->map_w1o_128, s->w1o, ncols, H, 1, ncols * 2, H * ncols * 2, 128));
+  s->backward = true;
+  return TP_OK;
+}
+
+size_t tp_mlp_train_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
+  TrainPlan p;
+  plan_train(s, M, v, d->sms, &p);
+  return p.fwd_total();
+}
+
+tp_status_t tp_mlp_forward_train(tp_shards_t s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
+                                 float *Z, void *Hsave, void *Psave, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  return mlp_forward_train_impl(s, X, M, act, v, Z, Hsave, Psave, workspace, ws_bytes,
+                                static_cast<cudaStream_t>(stream));
+}
+
+size_t tp_mlp_backward_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
+  TrainPlan p;
+  plan_train(s, M, v, d->sms, &p);
+  return p.bwd_total();
+}
+
+tp_status_t tp_mlp_backward(tp_shards_t s, const void *X, const void *Hsave, const void *Psave,
+                            const void *dZ, int64_t M, tp_variant_t v, float *dX, float *dW1, float *dW2,
+                            void *workspace, size_t ws_bytes, void *stream) {
+  return mlp_backward_impl(s, X, Hsave, Psave, dZ, M, v, dX, dW1, dW2, workspace, ws_bytes,
+                           static_cast<cudaStream_t>(stream));
 }
 
 size_t tp_mlp_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {

@@ -1,645 +1,16 @@
-// tp_gemm.cu - the tensor-core GEMM of the tensor-parallel MLP on sm_103a.
-//
-// One persistent, warp-specialised kernel serves every GEMM of the path:
-//   - the column-parallel first layer Y_i = act(X W1_i) for all shards at
-//     once, with GeLU / SwiGLU / identity fused into the epilogue and Y_i
-//     stored as bfloat16 in shard i's own buffer ("Tensor Parallelism in
-//     Action: Megatron-LM Matrix Splitting", section 1 "Column Parallel";
-//     section 2, question 2, for why the activation stays local);
-//   - the row-parallel second layer Z_i = Y_i W2_i, either as T float32
-//     partials (one output slot per shard, summed afterwards by the
-//     shard-sum kernel) or with one TMEM accumulator running over every
-//     shard's K range, so that the all-reduce-sum happens inside the
-//     accumulator ("Slice the matrix itself", section "Mathematical
-//     formulation - row-parallel matrix multiplication summation");
-//   - the memory-bound decode shapes with the operands swapped: the weight
-//     rows are the 128-row MMA operand, the (<= 16) tokens the N = 16 one.
-//
-// Roles (192 threads): warp 0 issues TMA loads into a STAGES-deep ring of
-// shared-memory tiles (128-byte swizzle); warp 1 allocates tensor memory and
-// one of its threads issues tcgen05.mma (bf16 x bf16 -> fp32 in TMEM); warps
-// 2..5 drain a finished accumulator (tcgen05.ld), apply the epilogue and
-// store, while the MMA warp already fills the other accumulator.  Every wait
-// is bounded (see tp_device.cuh): a wait that runs out sets the device
-// status word and the CTA returns after letting its in-flight copies and
-// MMAs finish and releasing its tensor memory.
-#include <cuda_bf16.h>
-
-#include "tp_device.cuh"
-#include "tp_internal.h"
+// tp_gemm.cu - launches of the tensor-core GEMM (tp_gemm_impl.cuh) for the
+// forward epilogues: activations fused into the column-parallel GEMM,
+// float32 partials / accumulated outputs of the row-parallel GEMM, and the
+// swapped-operand decode tile.
+#include "tp_gemm_impl.cuh"
 
 namespace tp {
-namespace {
 
-constexpr int BM = 128;          // MMA M (rows of A per tile)
-constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
-
-template <int BN>
-struct Traits;
-template <>
-struct Traits<256> {
-  static constexpr int STAGES = 4;
-};
-template <>
-struct Traits<128> {
-  static constexpr int STAGES = 6;
-};
-template <>
-struct Traits<16> {
-  static constexpr int STAGES = 8;
-};
-
-constexpr int kAcc = 2;  // TMEM accumulators (double buffer)
-
-template <int BN>
-__host__ __device__ constexpr uint32_t tmem_cols() {
-  return kAcc * BN <= 32 ? 32 : kAcc * BN <= 64 ? 64 : kAcc * BN <= 128 ? 128
-         : kAcc * BN <= 256 ? 256 : 512;
-}
-
-template <int BN>
-__host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + static_cast<size_t>(Traits<BN>::STAGES) * (BM * BK * 2 + BN * BK * 2) + 256;
-}
-
-struct Unit {
-  int slot, m, n, kt0, kt1;
-};
-
-// Unit u -> (slot, m-tile, n-tile, k range).  Inside a slot, tiles run in
-// groups of `group_m` m-tiles with m fastest, so the CTAs working at the
-// same time share B tiles (and A rows) through L2.
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
-  Unit r;
-  const int per_slot = g.m_tiles * g.n_tiles;
-  r.slot = u / per_slot;
-  const int t = u - r.slot * per_slot;
-  const int per_group = g.group_m * g.n_tiles;
-  const int grp = t / per_group;
-  const int first_m = grp * g.group_m;
-  const int gm = min(g.group_m, g.m_tiles - first_m);
-  const int in = t - grp * per_group;
-  r.m = first_m + in % gm;
-  r.n = in / gm;
-  r.kt0 = r.slot * g.kt_per_slot;
-  r.kt1 = min(g.kt_total, r.kt0 + g.kt_per_slot);
-  return r;
-}
-
-__device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// 32 float32 values of one row -> activation -> 32 bf16 at dst (16 B aligned).
-template <int EPI>
-__device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
-  uint32_t p[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-    if (EPI == EPI_GELU_BF16) {
-      a = gelu_erf(a);
-      b = gelu_erf(b);
-    }
-    p[j] = pack_bf16x2(a, b);
-  }
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-}
-
-// Epilogue of one tile by the 128 epilogue threads: each thread owns TMEM
-// lane `row_in_tile`, i.e. output row row0 + row_in_tile; `tb` addresses that
-// lane's quarter at the accumulator's first column.
-template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int row0, int row_in_tile,
-                                              const GemmArgs &g) {
-  if constexpr (EPI == EPI_F32_T) {
-    static_assert(BN == 16, "swapped epilogue is the N = 16 decode tile");
-    uint32_t r[16];
-    tmem_ld16(tb, r);
-    tmem_ld_wait();
-    const int feat = row0 + row_in_tile;
-    if (feat < g.rows_valid) {
-      float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride + feat;
-#pragma unroll
-      for (int j = 0; j < BN; ++j)
-        if (j < g.cols_valid) out[j * g.ld_out] = __uint_as_float(r[j]);
-    }
-  } else if constexpr (EPI == EPI_F32) {
-    const int row = row0 + row_in_tile;
-    const bool valid = row < g.rows_valid;
-    float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
-                 static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tb + c * 32, r);
-      tmem_ld_wait();
-      if (valid) {
-        float4 *d = reinterpret_cast<float4 *>(out + c * 32);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      }
-    }
-  } else if constexpr (EPI == EPI_SWIGLU_BF16) {
-    constexpr int HALF = BN / 2;
-    const int row = row0 + row_in_tile;
-    const bool valid = row < g.rows_valid;
-    const long long col0 = static_cast<long long>(t.n) * HALF;
-    const long long shard = col0 / g.shard_cols;
-    const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
-                         static_cast<long long>(row) * g.ld_out + lc;
-#pragma unroll 1
-    for (int c = 0; c < HALF / 32; ++c) {
-      uint32_t gr[32], ur[32];
-      tmem_ld32(tb + c * 32, gr);
-      tmem_ld32(tb + HALF + c * 32, ur);
-      tmem_ld_wait();
-      if (valid) {
-        uint32_t h[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          h[j] = __float_as_uint(silu(__uint_as_float(gr[j])) * __uint_as_float(ur[j]));
-        store_act32<EPI_IDENT_BF16>(out + c * 32, h);
-      }
-    }
-  } else {  // EPI_GELU_BF16, EPI_IDENT_BF16
-    const int row = row0 + row_in_tile;
-    const bool valid = row < g.rows_valid;
-    const long long col0 = static_cast<long long>(t.n) * BN;
-    const long long shard = col0 / g.shard_cols;
-    const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
-                         static_cast<long long>(row) * g.ld_out + lc;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tb + c * 32, r);
-      tmem_ld_wait();
-      if (valid) store_act32<EPI>(out + c * 32, r);
-    }
-  }
-}
-
-template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    tp_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const GemmArgs g) {
-  constexpr int STAGES = Traits<BN>::STAGES;
-  constexpr uint32_t A_BYTES = BM * BK * 2;
-  constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t TMEM_COLS = tmem_cols<BN>();
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  // barriers: full[STAGES] | empty[STAGES] | tfull[kAcc] | tempty[kAcc] | drain | never
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2 * kAcc + 2);
-  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
-
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
-  const uint32_t drain = bar0 + 8u * (2 * STAGES + 2 * kAcc);
-  const uint32_t never = drain + 8u;  // nothing ever arrives here (timeout test)
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < kAcc; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);
-    }
-    mbar_init(drain, 1);
-    mbar_init(never, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&mapA);
-    prefetch_tmap(&mapB);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = g.slots * g.m_tiles * g.n_tiles;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer ----
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, last_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, w)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          const int seg = kt / g.kt_per_seg;
-          const int kk = (kt - seg * g.kt_per_seg) * BK;
-          if (g.a_seg)
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kk, t.m * BM, seg);
-          else
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kt * BK, t.m * BM, 0);
-          if (g.b_seg)
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kk, t.n * BN, seg);
-          else
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kt * BK, t.n * BN, 0);
-          issued |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        // Every copy already issued must land before the CTA may exit.
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) drain_bar(full_bar(s), (last_par >> s) & 1u, g.status);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer ----
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      // Under a test wait limit, first wait for an event that never happens,
-      // so that the timeout path runs with copies in flight.
-      bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g);
-        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // +32 B per K=16 step -> +2 in the address field
-            tc_mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kt > t.kt0 || k > 0) ? 1u : 0u);
-          tc_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(tfull_bar(acc));
-        if (++acc == kAcc) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-      }
-      // Every MMA issued must be complete before tensor memory is released.
-      tc_commit(drain);
-      drain_bar(drain, 0u, g.status);
-    }
-    __syncwarp();
-  } else {
-    // ---- epilogue (warps 2..5) ----
-    const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are this warp's
-    const int row_in_tile = q * 32 + lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit t = decode_unit(u, g);
-      const bool ok = wait_bar(tfull_bar(acc), acc_phase, w);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, EPI>(tb, t, t.m * BM, row_in_tile, g);
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
-      if (++acc == kAcc) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
-}
-
-// ---- CTA-pair variant ------------------------------------------------------
-//
-// Cluster of 2 CTAs on a 256 x 256 output tile.  CTA r loads rows
-// [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
-// tile into its own shared memory (32 KiB per stage, 7 stages); one thread of
-// CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both
-// CTAs' tiles and leaves rows [128 r, 128 r + 128) x 256 columns in CTA r's
-// tensor memory.  Each CTA's copies complete on its own barrier; in CTA 1 a
-// relay thread forwards "stage full" to CTA 0, so every CTA can always wait
-// for its own copies.  Commits are multicast to both CTAs' barriers; the
-// epilogue warps of both CTAs release an accumulator on CTA 0's barrier.
-#ifndef TP_PAIR_STAGES
-#define TP_PAIR_STAGES 7
-#endif
-constexpr int kPairStages = TP_PAIR_STAGES;
-constexpr int kPairBN = 256;
-
-__host__ __device__ constexpr size_t pair_smem_bytes() {
-  return 1024 + static_cast<size_t>(kPairStages) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) + 512;
-}
-static_assert(pair_smem_bytes() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
-
-template <int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    tp_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapB, const GemmArgs g) {
-  constexpr int STAGES = kPairStages;
-  constexpr int BN = kPairBN;
-  constexpr uint32_t A_BYTES = 128 * BK * 2;
-  constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
-  constexpr uint32_t TMEM_COLS = 512;
-  constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
-  constexpr int kReleaseArrivals = 8;  // 4 epilogue warps in each CTA
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  // barriers: full[S] | pfull[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain | never
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * kAcc + 2);
-  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
-
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto pfull_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + kAcc + a); };
-  const uint32_t drain = bar0 + 8u * (3 * STAGES + 2 * kAcc);
-  const uint32_t never = drain + 8u;  // nothing ever arrives here (timeout test)
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(pfull_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < kAcc; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kReleaseArrivals);
-    }
-    mbar_init(drain, 1);
-    mbar_init(never, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&mapA);
-    prefetch_tmap(&mapB);
-  }
-  if (warp == 1) {
-    tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish2();
-  }
-  tc_fence_before();
-  cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = g.slots * g.m_tiles * g.n_tiles;
-  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
-  const int nclusters = static_cast<int>(gridDim.x >> 1);
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer (both CTAs, own half of each tile) ----
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, last_par = 0;
-      bool ok = true;
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
-        const int arow = t.m * 256 + 128 * static_cast<int>(rank);
-        const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar_cluster(empty_bar(stage), phase ^ 1u, w)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          const int seg = kt / g.kt_per_seg;
-          const int kk = (kt - seg * g.kt_per_seg) * BK;
-          if (g.a_seg)
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kk, arow, seg);
-          else
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kt * BK, arow, 0);
-          if (g.b_seg)
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kk, brow, seg);
-          else
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kt * BK, brow, 0);
-          issued |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) drain_bar(full_bar(s), (last_par >> s) & 1u, g.status);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---- MMA issuer (CTA 0 only) ----
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
-        if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w) || !wait_bar_cluster(pfull_bar(stage), phase, w)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kt > t.kt0 || k > 0) ? 1u : 0u);
-          tc_commit2_multicast(empty_bar(stage), 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit2_multicast(tfull_bar(acc), 0x3);
-        if (++acc == kAcc) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-      }
-      tc_commit2(drain);
-      drain_bar(drain, 0u, g.status);
-    } else if (lane == 0) {
-      // ---- relay (CTA 1): this CTA's stage has landed -> tell CTA 0 ----
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(map_to_rank(pfull_bar(stage), 0));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-    __syncwarp();
-  } else {
-    // ---- epilogue (warps 2..5 of both CTAs) ----
-    const int q = warp & 3;
-    const int row_in_tile = q * 32 + lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int u = cluster_id; u < units; u += nclusters) {
-      const Unit t = decode_unit(u, g);
-      const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, EPI>(tb, t, t.m * 256 + 128 * static_cast<int>(rank), row_in_tile, g);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-      if (++acc == kAcc) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-  }
-
-  tc_fence_before();
-  cluster_sync();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc2(tmem_base, TMEM_COLS);
-  }
-}
-
-template <int EPI>
-cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
-                        cudaStream_t stream) {
-  constexpr size_t smem = pair_smem_bytes();
-  auto kern = tp_gemm_pair_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
-  if (units <= 0) return cudaSuccess;
-  // Clusters that fit on the GPU at once (pairs of SMs with room for one CTA each).
-  static int max_clusters[64][4];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int &mc = max_clusters[dev & 63][EPI & 3];
-  if (mc <= 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = num_sms / 2;
-    }
-    mc = n;
-  }
-  const int clusters = static_cast<int>(units < mc ? units : mc);
-  kern<<<2 * clusters, kThreads, smem, stream>>>(a, b, g);
-  return cudaGetLastError();
-}
-
-template <int BN, int EPI>
-cudaError_t launch_impl(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
-                        cudaStream_t stream) {
-  constexpr size_t smem = smem_bytes<BN>();
-  auto kern = tp_gemm_kernel<BN, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
-  if (units <= 0) return cudaSuccess;
-  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  kern<<<grid, kThreads, smem, stream>>>(a, b, g);
-  return cudaGetLastError();
-}
-
-}  // namespace
+using namespace gemm_impl;
 
 cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
                         const GemmArgs &args, int num_sms, cudaStream_t stream) {
+  if (epi >= EPI_GELU_SAVE_BF16) return launch_gemm_train(cfg, epi, mapA, mapB, args, num_sms, stream);
   switch (cfg) {
     case CFG_N256:
       switch (epi) {

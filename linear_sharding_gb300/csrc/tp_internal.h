@@ -20,7 +20,12 @@ enum Epi : int {
   EPI_SWIGLU_BF16 = 1,  // accumulator columns [0, BN/2) gate, [BN/2, BN) up -> bf16(SiLU(g) u)
   EPI_IDENT_BF16 = 2,   // Y = bf16(acc)
   EPI_F32 = 3,          // out[slot][row][col] = acc (float32 partials or the final Z)
-  EPI_F32_T = 4         // swapped operands: acc[feature][token] -> out[slot][token][feature]
+  EPI_F32_T = 4,        // swapped operands: acc[feature][token] -> out[slot][token][feature]
+  // training (backward) epilogues, same column-to-shard mapping as the bf16 ones:
+  EPI_GELU_SAVE_BF16 = 5,    // out = bf16(GeLU(acc)), out2 = bf16(acc) (the pre-activation)
+  EPI_SWIGLU_SAVE_BF16 = 6,  // out = bf16(SiLU(g) u), out2 = bf16(g), out3 = bf16(u)
+  EPI_DGELU_BF16 = 7,        // out = bf16(acc * GeLU'(aux)), aux = saved pre-activation
+  EPI_DSWIGLU_BF16 = 8       // out = bf16(acc u SiLU'(g)), out2 = bf16(acc SiLU(g)); aux = g, aux2 = u
 };
 
 // Packed rows of a SwiGLU shard alternate 128 gate rows and 128 up rows, so
@@ -48,6 +53,8 @@ struct GemmArgs {
   int shard_cols;          // output columns per shard (bf16 epilogues)
   unsigned int *status;
   unsigned long long wait_limit_ns;
+  void *out2, *out3;        // extra outputs of the training epilogues (same layout as out)
+  const void *aux, *aux2;   // saved activations read by the backward epilogues (same layout)
 };
 
 // Tile configurations the GEMM is instantiated for.
@@ -62,6 +69,15 @@ enum GemmCfg : int {
 // Launch the tensor-core GEMM.  Returns cudaSuccess or the launch error.
 cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
                         const GemmArgs &args, int num_sms, cudaStream_t stream);
+// The training epilogues (EPI_*_SAVE_BF16, EPI_D*_BF16); launch_gemm forwards to it.
+cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
+                              const GemmArgs &args, int num_sms, cudaStream_t stream);
+
+// dst[b][c][r] = src[b][r][c] for r < rows, c < cols (bf16); dst rows are
+// dst_ld long and zero past `rows`.
+cudaError_t launch_transpose_pad(const void *src, long long rows, long long cols, long long src_ld,
+                                 long long src_batch, void *dst, long long dst_ld, long long dst_batch,
+                                 int batch, cudaStream_t stream);
 
 // Float32 CUDA-core GEMM: D[m][n] = sum_k A[m][k] B[n][k], same work model
 // as the tensor-core path but with plain row-major pointers.  A rows have

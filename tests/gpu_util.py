@@ -40,3 +40,10 @@ def normwise_error(Z: np.ndarray, Zref: np.ndarray) -> float:
 # float32 inputs: normwise relative error <= 1e-4.
 TOL_BF16_ROW_RMS = 2e-2
 TOL_F32_NORMWISE = 1e-4
+
+# Gradients of the training path: the chain to dW1 and dX passes three bf16
+# roundings (the saved pre-activation, dP = dH * act'(P) and, for dW, the
+# transposed operands are exact copies) against the forward's one (Y); the
+# forward's measured row-RMS error is about 8e-3 per rounding, so the
+# gradients are held to 3e-2.
+TOL_BF16_GRAD_ROW_RMS = 3e-2
