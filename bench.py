@@ -415,6 +415,27 @@ def extras(args, tp, device, peaks, full: bool) -> dict:
     torch.cuda.empty_cache()
     out["decode_swiglu_h8192_f28672_t8"] = dec
 
+    # training: forward that keeps its activations + backward, prefill GeLU workload
+    w = WORKLOADS[WORKLOAD]
+    M, H, F, T = w["M"], w["H"], w["F"], w["T"]
+    W1, W2 = randn((H, F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F))
+    s = tp.tp_shard_weights(W1, W2, T, "gelu")
+    tp.tp_shards_enable_backward(s, W1, W2)
+    del W1, W2
+    X, dZ = randn((M, H), 1.0), randn((M, H), 1.0)
+    _, Hs, Ps = tp.tp_mlp_forward_train(s, X)
+    t_fwd = _time_calls(lambda: tp.tp_mlp_forward_train(s, X), 20)
+    t_bwd = _time_calls(lambda: tp.tp_mlp_backward(s, X, Hs, Ps, dZ), 20)
+    out["training_prefill_gelu_m2048_h4096_f16384_t4"] = {
+        "forward_ms": round(t_fwd * 1e3, 4), "backward_ms": round(t_bwd * 1e3, 4),
+        "forward_TFLOP/s": round(4 * M * H * F / t_fwd / 1e12, 1),
+        "backward_TFLOP/s": round(8 * M * H * F / t_bwd / 1e12, 1),
+        "step_TFLOP/s": round(12 * M * H * F / (t_fwd + t_bwd) / 1e12, 1),
+        "note": "timed through the Python binding, output buffers allocated per call"}
+    s.close()
+    del X, dZ, Hs, Ps
+    torch.cuda.empty_cache()
+
     ss = {}
     for name, T, n in (("prefill_gelu", 4, 2048 * 4096), ("attn_proj", 8, 4096 * 4096),
                        ("prefill_swiglu_large", 8, 8192 * 8192)):
