@@ -83,6 +83,9 @@ def _load():
         lib.orc_mlp_backward_dx.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp]
         lib.orc_mlp_backward_dw.restype = i32
         lib.orc_mlp_backward_dw.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp, dp]
+        lib.orc_block_forward.restype = i32
+        lib.orc_block_forward.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i64, i32, i32, i32,
+                                          i32, vp, i64, dp, dp]
         lib.orc_reduce_scatter_f32.restype = i32
         lib.orc_reduce_scatter_f32.argtypes = [vp, i32, i64, vp]
         lib.orc_all_gather.restype = i32
@@ -381,3 +384,23 @@ def mlp_backward_dw(X, W1, W2, dZ, act: str, fcols=None):
     _check(_load().orc_mlp_backward_dw(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dZ), _dt(X), M, H, F,
                                        ACTS[act], _ptr(f), n, _ptr(dW1), _ptr(dW2)), "mlp_backward_dw")
     return dW1, dW2
+
+
+def block_forward(X, Wqkv, Wo, W1, W2, n_heads: int, head_dim: int, T: int, act: str,
+                  causal: bool = True, sharded: bool = True, rows=None):
+    """One tensor-parallel transformer block on the selected token rows:
+    returns (out, h), each [rows x H] fp64, h the residual stream after the
+    attention all-reduce."""
+    X, Wqkv, Wo, W1, W2 = _c(X), _c(Wqkv), _c(Wo), _c(W1), _c(W2)
+    M, H = X.shape
+    F = W2.shape[0]
+    if Wqkv.shape != (H, 3 * H) or Wo.shape != (H, H) or W2.shape != (F, H) or \
+            W1.shape != (H, 2 * F if act == "swiglu" else F):
+        raise ValueError("block weight shapes do not match X")
+    r = _rows(rows, M)
+    out = np.empty((r.size, H), dtype=np.float64)
+    h = np.empty((r.size, H), dtype=np.float64)
+    _check(_load().orc_block_forward(_ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(W1), _ptr(W2), _dt(X), M, H,
+                                     n_heads, head_dim, F, ACTS[act], int(causal), T, int(sharded),
+                                     _ptr(r), r.size, _ptr(out), _ptr(h)), "block_forward")
+    return out, h

@@ -693,3 +693,138 @@ int orc_mlp_backward_dw(const void *X, const void *W1, const void *W2, const voi
     free(Hs);
     return ORC_OK;
 }
+
+/* ---- one tensor-parallel transformer block ---------------------------------
+ * "Slice the matrix itself", section "All-Reduce Synchronization": a block
+ * needs two all-reduces, one after the attention's row-parallel projection
+ * and one after the MLP's; the "Tensor parallelism" guide, section "Walking
+ * through a transformer block": heads are sharded across ranks, and the two
+ * all-reduces sit on the attention and MLP residual paths.  Readings: causal
+ * scaled-dot-product attention per head, softmax(q k^T / sqrt(hd)) v; a
+ * residual add after each all-reduce; no normalisation layers (the pages
+ * name none).  For token r:
+ *   q, k_j, v_j = x_r Wq, x_j Wk, x_j Wv   (per head h: columns [h hd, (h+1) hd))
+ *   o_h = sum_{j <= r} softmax_j(q_h . k_jh / sqrt(hd)) v_jh
+ *   a = sum over shards i of (o of shard i's heads) Wo_i   (all-reduce 1)
+ *   h_r = x_r + a
+ *   out_r = h_r + sum_i act(h_r W1_i) W2_i                  (all-reduce 2)
+ * When `sharded`, each shard's heads and MLP columns are computed from the
+ * oracle's own shard copies and the partial products summed in shard order;
+ * otherwise the dense matrices are used.  hout (may be NULL) receives h. */
+int orc_block_forward(const void *X, const void *Wqkv, const void *Wo, const void *W1,
+                      const void *W2, int dt, int64_t M, int64_t H, int n_heads, int head_dim,
+                      int64_t F, int act, int causal, int T, int sharded, const int64_t *rows,
+                      int64_t n_rows, double *out, double *hout)
+{
+    if (!X || !Wqkv || !Wo || !W1 || !W2 || !out || M <= 0 || H <= 0 || F <= 0 || T <= 0 ||
+        n_heads <= 0 || head_dim <= 0 || (int64_t)n_heads * head_dim != H)
+        return ORC_ERR_ARG;
+    if (n_heads % T != 0 || F % T != 0)
+        return ORC_ERR_INDIVISIBLE;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    int64_t kmax = 0; /* keys needed: rows [0, kmax) */
+    for (int64_t i = 0; i < n_rows; ++i)
+        if (rows[i] + 1 > kmax)
+            kmax = rows[i] + 1;
+    if (!causal)
+        kmax = M;
+    /* K and V of every needed key token, [kmax x H] each, fp64 */
+    double *K = (double *)malloc((size_t)(kmax * H + 1) * sizeof(double));
+    double *V = (double *)malloc((size_t)(kmax * H + 1) * sizeof(double));
+    if (!K || !V) {
+        free(K);
+        free(V);
+        return ORC_ERR_OOM;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t j = 0; j < kmax; ++j) {
+        row_times_matrix(X, j * H, dt, H, Wqkv, 3 * H, H, H, K + j * H);
+        row_times_matrix(X, j * H, dt, H, Wqkv, 3 * H, 2 * H, H, V + j * H);
+    }
+    const int hps = n_heads / T;
+    const int64_t W = (int64_t)hps * head_dim, Fs = F / T;
+    const int64_t ncols = (act == ORC_SWIGLU) ? 2 * F : F;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        const int64_t nk = causal ? r + 1 : M;
+        double *buf = (double *)malloc((size_t)(3 * H + nk + ncols + F) * sizeof(double));
+        if (!buf) {
+#pragma omp atomic write
+            err = ORC_ERR_OOM;
+            continue;
+        }
+        double *q = buf, *o = buf + H, *h = buf + 2 * H, *p = buf + 3 * H, *y = p + nk, *hh = y + ncols;
+        row_times_matrix(X, r * H, dt, H, Wqkv, 3 * H, 0, H, q);
+        for (int hd_i = 0; hd_i < n_heads; ++hd_i) {
+            const int64_t c0 = (int64_t)hd_i * head_dim;
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < nk; ++j) {
+                double sdot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    sdot += q[c0 + d] * K[j * H + c0 + d];
+                p[j] = sdot / sqrt((double)head_dim);
+                if (p[j] > mx)
+                    mx = p[j];
+            }
+            double sum = 0.0;
+            for (int64_t j = 0; j < nk; ++j) {
+                p[j] = exp(p[j] - mx);
+                sum += p[j];
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < nk; ++j)
+                    acc += p[j] * V[j * H + c0 + d];
+                o[c0 + d] = acc / sum;
+            }
+        }
+        /* all-reduce 1: a = sum over shards of o_i Wo_i (or the dense o Wo) */
+        for (int64_t c = 0; c < H; ++c)
+            h[c] = 0.0;
+        const int nsh = sharded ? T : 1;
+        const int64_t Wsh = sharded ? W : H;
+        for (int sidx = 0; sidx < nsh; ++sidx) {
+            for (int64_t c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < Wsh; ++k)
+                    acc += o[sidx * Wsh + k] * orc_value(Wo, (sidx * Wsh + k) * H + c, dt);
+                h[c] += acc;
+            }
+        }
+        for (int64_t c = 0; c < H; ++c)
+            h[c] += orc_value(X, r * H + c, dt);
+        if (hout)
+            for (int64_t c = 0; c < H; ++c)
+                hout[i * H + c] = h[c];
+        /* all-reduce 2: the MLP on h */
+        const int64_t Fb = sharded ? Fs : F;
+        for (int64_t c = 0; c < H; ++c)
+            out[i * H + c] = 0.0;
+        for (int sidx = 0; sidx < (sharded ? T : 1); ++sidx) {
+            const int nparts = (act == ORC_SWIGLU) ? 2 : 1;
+            for (int part = 0; part < nparts; ++part)
+                for (int64_t f = 0; f < Fb; ++f) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < H; ++k)
+                        acc += h[k] * orc_value(W1, k * ncols + part * F + sidx * Fb + f, dt);
+                    y[part * Fb + f] = acc;
+                }
+            activate_row(y, Fb, act, hh);
+            for (int64_t c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int64_t f = 0; f < Fb; ++f)
+                    acc += hh[f] * orc_value(W2, (sidx * Fb + f) * H + c, dt);
+                out[i * H + c] += acc;
+            }
+        }
+        for (int64_t c = 0; c < H; ++c)
+            out[i * H + c] += h[c];
+        free(buf);
+    }
+    free(K);
+    free(V);
+    return err;
+}

@@ -454,3 +454,72 @@ def test_backward_column_subset_matches_full():
     s1, s2 = oracle.mlp_backward_dw(d["X"], d["W1"], d["W2"], G, "swiglu", fcols=cols)
     assert np.array_equal(s1[:, :3], full1[:, cols]) and np.array_equal(s1[:, 3:], full1[:, 16 + cols])
     assert np.array_equal(s2, full2[cols])
+
+
+# --- one transformer block --------------------------------------------------------
+
+def _block_weights(H, F, act, seed):
+    rng = np.random.default_rng(seed)
+    ncols = 2 * F if act == "swiglu" else F
+    return (rng.standard_normal((H, 3 * H)) / np.sqrt(H), rng.standard_normal((H, H)) / np.sqrt(H),
+            rng.standard_normal((H, ncols)) / np.sqrt(H), rng.standard_normal((F, H)) / np.sqrt(F))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_block_sharded_equals_unsharded(act, causal):
+    """Both all-reduces reconstruct the dense block: per-shard heads and MLP
+    columns summed over shards equal the dense computation."""
+    rng = np.random.default_rng(0)
+    M, nh, hd, F = 6, 4, 4, 16
+    H = nh * hd
+    X = rng.standard_normal((M, H))
+    Wqkv, Wo, W1, W2 = _block_weights(H, F, act, 1)
+    dense, hd_ = oracle.block_forward(X, Wqkv, Wo, W1, W2, nh, hd, 1, act, causal, sharded=False)
+    for T in (1, 2, 4):
+        out, h = oracle.block_forward(X, Wqkv, Wo, W1, W2, nh, hd, T, act, causal, sharded=True)
+        assert _normwise(out, dense) <= 1e-12 and _normwise(h, hd_) <= 1e-12
+
+
+def test_block_attention_closed_forms():
+    """With Wq = 0 every score is 0, so causal attention at token r is the mean
+    of v_0..v_r, and the first token attends only to itself."""
+    rng = np.random.default_rng(3)
+    M, nh, hd, F = 5, 2, 4, 8
+    H = nh * hd
+    X = rng.standard_normal((M, H))
+    Wqkv, Wo, W1, W2 = _block_weights(H, F, "gelu", 2)
+    Wqkv[:, :H] = 0.0
+    Wo = np.eye(H)
+    W1 = np.zeros_like(W1)  # the MLP adds GeLU(0) W2 = 0
+    out, h = oracle.block_forward(X, Wqkv, Wo, W1, W2, nh, hd, 2, "gelu", causal=True)
+    V = X @ Wqkv[:, 2 * H:]
+    for r in range(M):
+        expect = X[r] + V[: r + 1].mean(axis=0)
+        assert np.allclose(h[r], expect, rtol=1e-13, atol=1e-13)
+        assert np.allclose(out[r], expect, rtol=1e-13, atol=1e-13)
+    noncausal, _ = oracle.block_forward(X, Wqkv, Wo, W1, W2, nh, hd, 2, "gelu", causal=False)
+    assert np.allclose(noncausal, X + V.mean(axis=0), rtol=1e-13, atol=1e-13)
+
+
+def test_block_matches_a_library_attention():
+    """Causal softmax attention written with library routines (scipy softmax,
+    numpy matmuls) on the same fp64 inputs."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(4)
+    M, nh, hd, F = 7, 2, 4, 8
+    H = nh * hd
+    X = rng.standard_normal((M, H))
+    Wqkv, Wo, W1, W2 = _block_weights(H, F, "swiglu", 5)
+    out, h = oracle.block_forward(X, Wqkv, Wo, W1, W2, nh, hd, 2, "swiglu", causal=True)
+    Q, K, V = X @ Wqkv[:, :H], X @ Wqkv[:, H:2 * H], X @ Wqkv[:, 2 * H:]
+    O = np.zeros((M, H))
+    mask = np.tril(np.ones((M, M), dtype=bool))
+    for g in range(nh):
+        sl = slice(g * hd, (g + 1) * hd)
+        S = np.where(mask, Q[:, sl] @ K[:, sl].T / np.sqrt(hd), -np.inf)
+        O[:, sl] = softmax(S, axis=1) @ V[:, sl]
+    href = X + O @ Wo
+    G, U = href @ W1[:, :F], href @ W1[:, F:]
+    ref = href + (G * special.expit(G) * U) @ W2
+    assert _normwise(h, href) <= 1e-13 and _normwise(out, ref) <= 1e-13
