@@ -321,6 +321,32 @@ TP_API tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void
                                  size_t ws_bytes, void *stream);
 
 /*
+ * tp_block_forward - one tensor-parallel transformer block on this GPU:
+ * head-sharded attention, then the MLP, each ending in its all-reduce-sum
+ * ("Slice the matrix itself", section "All-Reduce Synchronization": two
+ * all-reduces per layer, after the attention's and after the MLP's
+ * row-parallel projection; "Tensor parallelism" guide, section "Walking
+ * through a transformer block": heads sharded across ranks, the two
+ * all-reduces on the attention and MLP residual paths).
+ *   attn: a handle from tp_shard_weights_qkv (head_dim a multiple of 128);
+ *   mlp:  a bfloat16 handle from tp_shard_weights with the same H and T.
+ *   X [M x H] bfloat16.  Per token r and head h (heads in shard order):
+ *     o_h = sum_{j <= r} softmax_j(q_h . k_jh / sqrt(head_dim)) v_jh
+ *     (causal != 0; all keys j < M when causal == 0),
+ *     h = X + sum_i O_i Wo_i, out = h + sum_i act(h W1_i) W2_i.
+ *   No normalisation layers (the pages name none).  Q, K, V, the
+ *   probabilities, O and the MLP input h are rounded to bfloat16 on the way;
+ *   scores, sums and outputs are float32.
+ *   out [M x H] float32; h_out [M x H] float32 or NULL: the residual stream
+ *   after the attention all-reduce.  workspace: tp_block_workspace_bytes()
+ *   bytes (it holds the float32 scores, nh x M x M) or NULL.  Asynchronous.
+ */
+TP_API size_t tp_block_workspace_bytes(tp_shards_t attn, tp_shards_t mlp, int64_t M, tp_variant_t v);
+TP_API tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const void *X, int64_t M,
+                                    int causal, tp_variant_t v, float *out, float *h_out,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * tp_partial_sum - the all-reduce-sum arithmetic on one GPU ("Slice the
  * matrix itself", section "Mathematical formulation": Y = sum_i X_i W_i, then
  * All-Reduce-Sum).

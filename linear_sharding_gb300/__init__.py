@@ -37,6 +37,7 @@ EXPORTS = (
     "tp_rowpar_forward", "tp_mlp_forward_noalloc", "tp_reduce_scatter", "tp_all_gather",
     "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
+    "tp_block_workspace_bytes", "tp_block_forward",
 )
 
 _lock = threading.Lock()
@@ -99,12 +100,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_mlp_backward_workspace_bytes.restype = sz
         lib.tp_mlp_backward_workspace_bytes.argtypes = [vp, i64, i32]
         lib.tp_mlp_backward.argtypes = [vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, vp, sz, vp]
+        lib.tp_block_workspace_bytes.restype = sz
+        lib.tp_block_workspace_bytes.argtypes = [vp, vp, i64, i32]
+        lib.tp_block_forward.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, vp, sz, vp]
         for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
                      "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
                      "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
                      "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
                      "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16",
-                     "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward"):
+                     "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward",
+                     "tp_block_forward"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -395,6 +400,25 @@ def tp_mlp_backward(s: Shards, X, Hsave, Psave, dZ, variant: str = "auto", strea
                                M, VARIANT[variant], _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(ws), ws.numel(),
                                _stream(stream)), "tp_mlp_backward")
     return dX, dW1, dW2
+
+
+def tp_block_forward(attn: Shards, mlp: Shards, X, causal: bool = True, variant: str = "auto",
+                     out=None, h_out=None, workspace=None, stream=None):
+    """One TP transformer block: returns (out, h) float32 [M x H] (h is None
+    unless h_out=True or a tensor is given)."""
+    torch = _torch()
+    lib = load_library()
+    X = X.contiguous()
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty((M, attn.H), dtype=torch.float32, device=X.device)
+    if h_out is True:
+        h_out = torch.empty((M, attn.H), dtype=torch.float32, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_block_forward(attn.handle, mlp.handle, _ptr(X), M, int(bool(causal)), VARIANT[variant],
+                                _ptr(out), _ptr(h_out if h_out is not False else None), _ptr(workspace),
+                                ws_bytes, _stream(stream)), "tp_block_forward")
+    return out, (h_out if h_out is not False else None)
 
 
 def tp_last_device_status(stream=None) -> int:

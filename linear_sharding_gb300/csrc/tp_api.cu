@@ -707,6 +707,154 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
   return rowpar_any(s, d, p, Y, M, Z, ws_row, st);
 }
 
+// ---- one tensor-parallel transformer block ---------------------------------------
+
+struct BlockPlan {
+  int64_t Np = 0;   // score columns (keys) padded to a multiple of 256
+  int64_t Mp = 0;   // keys padded to a multiple of 64 (K of P V)
+  int slots_o = 1;  // O-projection accumulation slots
+  MlpPlan mlp;
+  size_t qkv = 0, S = 0, P = 0, vt = 0, O = 0, opart = 0, h = 0, hb = 0;
+  size_t total() const {
+    return round256(qkv) + round256(S) + round256(P) + round256(vt) + round256(O) + round256(opart) +
+           round256(h) + round256(hb) + mlp.total();
+  }
+};
+
+void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t v, int sms, BlockPlan *p) {
+  *p = BlockPlan();
+  const int64_t H = a->H;
+  const int nh = a->n_heads, hd = a->head_dim;
+  p->Np = (M + 255) / 256 * 256;
+  p->Mp = round64(M);
+  p->slots_o = v == TP_VAR_PARTIALS ? a->T : 1;
+  plan_mlp(m, M, v, sms, &p->mlp);
+  p->qkv = static_cast<size_t>(3 * H * M) * 2;
+  p->S = static_cast<size_t>(nh * M * p->Np) * 4;
+  p->P = static_cast<size_t>(nh * M * p->Mp) * 2;
+  p->vt = static_cast<size_t>(nh * hd * p->Mp) * 2;
+  p->O = static_cast<size_t>(M * H) * 2;
+  p->opart = p->slots_o > 1 ? static_cast<size_t>(p->slots_o * M * H) * 4 : 0;
+  p->h = static_cast<size_t>(M * H) * 4;
+  p->hb = static_cast<size_t>(M * H) * 2;
+}
+
+tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_t M, int causal,
+                               tp_variant_t v, float *out, float *h_out, void *workspace, size_t ws_bytes,
+                               cudaStream_t st) {
+  DevState *d = nullptr;
+  TP_TRY(check_handle(a, 1, &d));
+  TP_TRY(check_handle(m, 0, &d));
+  if (m->dt != TP_BF16) return TP_ERR_DTYPE;
+  if (m->H != a->H || m->T != a->T || M < 0 || !valid_variant(v)) return TP_ERR_ARG;
+  if (a->head_dim % 128 != 0) return TP_ERR_UNSUPPORTED;
+  if (M == 0) return TP_OK;
+  if (!X || !out || !aligned16(X) || !aligned16(out) || (h_out && !aligned16(h_out))) return TP_ERR_ARG;
+  if (M > (1LL << 24)) return TP_ERR_UNSUPPORTED;
+  BlockPlan p;
+  plan_block(a, m, M, v, d->sms, &p);
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
+  const int64_t H = a->H, nh = a->n_heads, hd = a->head_dim;
+  char *qkv = w.ptr;
+  float *S = reinterpret_cast<float *>(qkv + round256(p.qkv));
+  char *P = reinterpret_cast<char *>(S) + round256(p.S);
+  char *vt = P + round256(p.P);
+  char *O = vt + round256(p.vt);
+  float *opart = reinterpret_cast<float *>(O + round256(p.O));
+  float *h = reinterpret_cast<float *>(reinterpret_cast<char *>(opart) + round256(p.opart));
+  char *hb = reinterpret_cast<char *>(h) + round256(p.h);
+  char *mws = hb + round256(p.hb);
+  if (h_out) h = h_out;
+
+  // 1. QKV projection of every shard, written head-major [3][nh][M][hd]
+  CUtensorMap mx;
+  TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
+  {
+    GemmArgs g = base_args(d);
+    g.out = qkv;
+    g.shard_cols = static_cast<int>(a->R1);
+    g.head_dim = static_cast<int>(hd);
+    g.n_heads = static_cast<int>(nh);
+    GemmCall c;
+    c.a = &mx;
+    c.b_bn = &a->map_w1_b;
+    c.b_128 = &a->map_w1_a;
+    c.rows = M;
+    c.N = a->T * a->R1;
+    c.bn = a->bn1;
+    c.kps = static_cast<int>(H / 64);
+    c.epi = EPI_QKV_HEADS_BF16;
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2,
+             *V = qkv + static_cast<size_t>(2 * nh * M * hd) * 2;
+  // 2. scores S_h = Q_h K_h^T for all heads (tiles past the diagonal skipped when causal)
+  CUtensorMap mq, mk_bn, mk_128;
+  TP_TRY(make_map(&mq, Q, hd, M, nh, hd * 2, M * hd * 2, 128));
+  TP_TRY(make_map(&mk_bn, K, hd, M, nh, hd * 2, M * hd * 2, 256));
+  TP_TRY(make_map(&mk_128, K, hd, M, nh, hd * 2, M * hd * 2, 128));
+  {
+    GemmArgs g = base_args(d);
+    g.out = S;
+    g.ld_out = p.Np;
+    g.batch = static_cast<int>(nh);
+    g.batch_stride_out = M * p.Np;
+    g.causal = causal ? 1 : 0;
+    GemmCall c;
+    c.a = &mq;
+    c.a_seg = 2;
+    c.b_bn = &mk_bn;
+    c.b_128 = &mk_128;
+    c.b_seg = 2;
+    c.rows = M;
+    c.N = p.Np;
+    c.bn = 256;
+    c.kps = static_cast<int>(hd / 64);
+    c.epi = EPI_F32;
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  // 3. softmax over the allowed keys -> P (bf16, zero elsewhere)
+  TP_CUDA(launch_softmax_rows(S, p.Np, M * p.Np, P, p.Mp, M * p.Mp, static_cast<int>(M), static_cast<int>(nh),
+                              causal, 1.0f / sqrtf(static_cast<float>(hd)), st));
+  // 4. V^T per head, keys padded to Mp
+  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, vt, p.Mp, hd * p.Mp, static_cast<int>(nh), st));
+  // 5. O_h = P_h V_h into the heads-side-by-side layout [M x H]
+  CUtensorMap mp, mvt;
+  TP_TRY(make_map(&mp, P, p.Mp, M, nh, p.Mp * 2, M * p.Mp * 2, 128));
+  TP_TRY(make_map(&mvt, vt, p.Mp, hd, nh, p.Mp * 2, hd * p.Mp * 2, static_cast<uint32_t>(bn_for(hd))));
+  {
+    GemmArgs g = base_args(d);
+    g.out = O;
+    g.ld_out = H;
+    g.shard_cols = static_cast<int>(hd);
+    g.batch = static_cast<int>(nh);
+    g.batch_stride_out = hd;
+    g.causal = causal ? 2 : 0;
+    GemmCall c;
+    c.a = &mp;
+    c.a_seg = 2;
+    c.b_bn = &mvt;
+    c.b_128 = &mvt;
+    c.b_seg = 2;
+    c.rows = M;
+    c.N = hd;
+    c.bn = bn_for(hd);
+    c.kps = static_cast<int>(p.Mp / 64);
+    c.epi = EPI_IDENT_BF16;
+    TP_TRY(run_gemm(d, c, g, st));
+  }
+  // 6. row-parallel output projection + all-reduce-sum #1 (into out), 7. residual
+  CUtensorMap mo;
+  TP_TRY(make_map(&mo, O, H, M, 1, H * 2, M * H * 2, 128));
+  TP_TRY(rowpar_tc(a, d, mo, 0, M, p.slots_o, opart, out, st));
+  TP_CUDA(launch_residual(X, out, h, hb, M * H, d->sms, st));
+  // 8. the MLP on the residual stream + all-reduce-sum #2, 9. residual
+  TP_TRY(mlp_forward_impl(m, hb, M, m->act, v, out, mws, p.mlp.total(), st));
+  TP_CUDA(launch_add_inplace(out, h, M * H, d->sms, st));
+  return TP_OK;
+}
+
 }  // namespace
 
 bool tp::handle_ready_on_current_device(const tp_shards *s) {
@@ -1109,6 +1257,23 @@ tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void *A, in
     TP_TRY(rowpar_tc(s, d, ma, 0, M, slots, reinterpret_cast<float *>(w.ptr), Z, st));
   }
   return TP_OK;
+}
+
+size_t tp_block_workspace_bytes(tp_shards_t attn, tp_shards_t mlp, int64_t M, tp_variant_t v) {
+  DevState *d = nullptr;
+  if (!attn || !mlp || attn->kind != 1 || mlp->kind != 0 || M <= 0 || !valid_variant(v) ||
+      dev_state(&d) != TP_OK)
+    return 0;
+  BlockPlan p;
+  plan_block(attn, mlp, M, v, d->sms, &p);
+  return p.total();
+}
+
+tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const void *X, int64_t M, int causal,
+                             tp_variant_t v, float *out, float *h_out, void *workspace, size_t ws_bytes,
+                             void *stream) {
+  return block_forward_impl(attn, mlp, X, M, causal, v, out, h_out, workspace, ws_bytes,
+                            static_cast<cudaStream_t>(stream));
 }
 
 tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {

@@ -68,15 +68,19 @@ __host__ __device__ constexpr size_t smem_bytes() {
 }
 
 struct Unit {
-  int slot, m, n, kt0, kt1;
+  int b, slot, m, n, kt0, kt1;
+  bool skip;
 };
 
 // Unit u -> (slot, m-tile, n-tile, k range).  Inside a slot, tiles run in
 // groups of `group_m` m-tiles with m fastest, so the CTAs working at the
 // same time share B tiles (and A rows) through L2.
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g, int bm_rows, int bn) {
   Unit r;
   const int per_slot = g.m_tiles * g.n_tiles;
+  const int per_batch = g.slots * per_slot;
+  r.b = u / per_batch;
+  u -= r.b * per_batch;
   r.slot = u / per_slot;
   const int t = u - r.slot * per_slot;
   const int per_group = g.group_m * g.n_tiles;
@@ -88,7 +92,29 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
   r.n = in / gm;
   r.kt0 = r.slot * g.kt_per_slot;
   r.kt1 = min(g.kt_total, r.kt0 + g.kt_per_slot);
+  r.skip = false;
+  if (g.causal == 1) {
+    // output columns are keys: a tile entirely right of its last row's diagonal is masked
+    r.skip = static_cast<long long>(r.n) * bn >= static_cast<long long>(r.m + 1) * bm_rows;
+  } else if (g.causal == 2) {
+    // the K axis is keys: nothing past the tile's last row contributes
+    const int lim = ((r.m + 1) * bm_rows + BK - 1) / BK;
+    if (r.kt1 > lim) r.kt1 = lim;
+  }
   return r;
+}
+
+// Third tensor-map coordinate and K coordinate of k-tile kt for an operand
+// in mode 0 (flat K), 1 (K segments) or 2 (batch index).
+__device__ __forceinline__ void operand_coords(int mode, int kt, const GemmArgs &g, const Unit &t,
+                                               int &k, int &z) {
+  if (mode == 1) {
+    z = kt / g.kt_per_seg;
+    k = (kt - z * g.kt_per_seg) * BK;
+  } else {
+    z = mode == 2 ? t.b : 0;
+    k = kt * BK;
+  }
 }
 
 __device__ __forceinline__ float gelu_erf(float x) {
@@ -159,7 +185,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     tmem_ld_wait();
     const int feat = row0 + row_in_tile;
     if (feat < g.rows_valid) {
-      float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride + feat;
+      float *out = static_cast<float *>(g.out) + t.b * g.batch_stride_out + t.slot * g.slot_stride + feat;
 #pragma unroll
       for (int j = 0; j < BN; ++j)
         if (j < g.cols_valid) out[j * g.ld_out] = __uint_as_float(r[j]);
@@ -167,7 +193,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
   } else if constexpr (EPI == EPI_F32) {
     const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
-    float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
+    float *out = static_cast<float *>(g.out) + t.b * g.batch_stride_out + t.slot * g.slot_stride +
                  static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -189,7 +215,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const long long col0 = static_cast<long long>(t.n) * HALF;
     const long long shard = col0 / g.shard_cols;
     const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + t.b * g.batch_stride_out + shard * g.shard_stride +
                          static_cast<long long>(row) * g.ld_out + lc;
 #pragma unroll 1
     for (int c = 0; c < HALF / 32; ++c) {
@@ -211,7 +237,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * HALF;
     const long long shard = col0 / g.shard_cols;
-    const long long off = shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
+    const long long off = t.b * g.batch_stride_out + shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
                           (col0 - shard * g.shard_cols);
 #pragma unroll 1
     for (int c = 0; c < HALF / 32; ++c) {
@@ -235,7 +261,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * BN;
     const long long shard = col0 / g.shard_cols;
-    const long long off = shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
+    const long long off = t.b * g.batch_stride_out + shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
                           (col0 - shard * g.shard_cols);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -269,13 +295,33 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
         store_act32<EPI_IDENT_BF16>(static_cast<__nv_bfloat16 *>(g.out2) + off + c * 32, du);
       }
     }
+  } else if constexpr (EPI == EPI_QKV_HEADS_BF16) {
+    // global column -> (shard, Q/K/V, head, dim); 32-column chunks stay in one head
+    const int row = row0 + row_in_tile;
+    const bool valid = row < g.rows_valid;
+    const long long W = g.shard_cols / 3;
+    const long long hps = W / g.head_dim;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tb + c * 32, r);
+      tmem_ld_wait();
+      if (!valid) continue;
+      const long long gc = static_cast<long long>(t.n) * BN + c * 32;
+      const long long sh = gc / g.shard_cols, lc = gc - sh * g.shard_cols;
+      const long long part = lc / W, within = lc - part * W;
+      const long long head = sh * hps + within / g.head_dim, dim = within % g.head_dim;
+      const long long block = part * g.n_heads + head;
+      store_act32<EPI_IDENT_BF16>(static_cast<__nv_bfloat16 *>(g.out) +
+                                      (block * g.rows_valid + row) * g.head_dim + dim, r);
+    }
   } else {  // EPI_GELU_BF16, EPI_IDENT_BF16
     const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * BN;
     const long long shard = col0 / g.shard_cols;
     const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + t.b * g.batch_stride_out + shard * g.shard_stride +
                          static_cast<long long>(row) * g.ld_out + lc;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -346,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = g.slots * g.m_tiles * g.n_tiles;
+  const int units = (g.batch > 0 ? g.batch : 1) * g.slots * g.m_tiles * g.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -355,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g);
+        const Unit t = decode_unit(u, g, BM, BN);
+        if (t.skip) continue;
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, w)) {
             ok = false;
@@ -363,16 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          const int seg = kt / g.kt_per_seg;
-          const int kk = (kt - seg * g.kt_per_seg) * BK;
-          if (g.a_seg)
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kk, t.m * BM, seg);
-          else
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kt * BK, t.m * BM, 0);
-          if (g.b_seg)
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kk, t.n * BN, seg);
-          else
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kt * BK, t.n * BN, 0);
+          int ak, az, bk, bz;
+          operand_coords(g.a_seg, kt, g, t, ak, az);
+          operand_coords(g.b_seg, kt, g, t, bk, bz);
+          tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
+          tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -397,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so that the timeout path runs with copies in flight.
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g);
+        const Unit t = decode_unit(u, g, BM, BN);
+        if (t.skip) continue;
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -437,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit t = decode_unit(u, g);
+      const Unit t = decode_unit(u, g, BM, BN);
+      if (t.skip) continue;
       const bool ok = wait_bar(tfull_bar(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -547,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = g.slots * g.m_tiles * g.n_tiles;
+  const int units = (g.batch > 0 ? g.batch : 1) * g.slots * g.m_tiles * g.n_tiles;
   const int cluster_id = static_cast<int>(blockIdx.x >> 1);
   const int nclusters = static_cast<int>(gridDim.x >> 1);
 
@@ -558,7 +602,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
+        const Unit t = decode_unit(u, g, 256, BN);
+        if (t.skip) continue;
         const int arow = t.m * 256 + 128 * static_cast<int>(rank);
         const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
@@ -568,16 +613,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          const int seg = kt / g.kt_per_seg;
-          const int kk = (kt - seg * g.kt_per_seg) * BK;
-          if (g.a_seg)
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kk, arow, seg);
-          else
-            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, kt * BK, arow, 0);
-          if (g.b_seg)
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kk, brow, seg);
-          else
-            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, kt * BK, brow, 0);
+          int ak, az, bk, bz;
+          operand_coords(g.a_seg, kt, g, t, ak, az);
+          operand_coords(g.b_seg, kt, g, t, bk, bz);
+          tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
+          tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -599,7 +639,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
+        const Unit t = decode_unit(u, g, 256, BN);
+        if (t.skip) continue;
         if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -635,7 +676,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g);
+        const Unit t = decode_unit(u, g, 256, BN);
+        if (t.skip) continue;
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
           if (!wait_bar(full_bar(stage), phase, w)) {
             ok = false;
@@ -657,7 +699,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < units; u += nclusters) {
-      const Unit t = decode_unit(u, g);
+      const Unit t = decode_unit(u, g, 256, BN);
+      if (t.skip) continue;
       const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();

@@ -1,8 +1,9 @@
 // tp_gemm_train.cu - launches of the tensor-core GEMM (tp_gemm_impl.cuh) for
-// the training epilogues: the column-parallel GEMM that also keeps its
-// pre-activations for the backward pass, and the backward GEMM dH = dZ W2^T
-// with the activation's derivative fused into its epilogue, and the bf16
-// transpose used to feed the weight-gradient GEMMs K-major operands.
+// the training epilogues (the column-parallel GEMM that also keeps its
+// pre-activations for the backward pass; the backward GEMM dH = dZ W2^T with
+// the activation's derivative fused into its epilogue) and for the
+// transformer block's head-major QKV projection; plus the bf16 transpose
+// that gives the weight-gradient and attention GEMMs K-major operands.
 #include "tp_gemm_impl.cuh"
 
 namespace tp {
@@ -19,6 +20,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
           return launch_pair<EPI_SWIGLU_SAVE_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DGELU_BF16: return launch_pair<EPI_DGELU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DSWIGLU_BF16: return launch_pair<EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_QKV_HEADS_BF16: return launch_pair<EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -29,6 +31,8 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
           return launch_impl<256, EPI_SWIGLU_SAVE_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DGELU_BF16: return launch_impl<256, EPI_DGELU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DSWIGLU_BF16: return launch_impl<256, EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_QKV_HEADS_BF16:
+          return launch_impl<256, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -37,6 +41,8 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_GELU_SAVE_BF16: return launch_impl<128, EPI_GELU_SAVE_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DGELU_BF16: return launch_impl<128, EPI_DGELU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DSWIGLU_BF16: return launch_impl<128, EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_QKV_HEADS_BF16:
+          return launch_impl<128, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;

@@ -188,6 +188,56 @@ __global__ void shard_sum_bf16_scalar(const PartList L, int T, long long first, 
   }
 }
 
+// ---- attention core and residual stream ------------------------------------------
+
+// Row r of head b: P = softmax(scale * S) over the keys c <= r (causal) or
+// c < M, zero elsewhere up to ldp.  One CTA per row.
+__global__ void __launch_bounds__(256) softmax_rows_kernel(const float *S, long long lds, long long s_batch,
+                                                           __nv_bfloat16 *P, long long ldp, long long p_batch,
+                                                           int M, int causal, float scale) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, b = blockIdx.y;
+  const long long n = causal ? static_cast<long long>(r) + 1 : M;
+  const float *row = S + b * s_batch + static_cast<long long>(r) * lds;
+  __nv_bfloat16 *prow = P + b * p_batch + static_cast<long long>(r) * ldp;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float mx = -INFINITY;
+  for (long long c = threadIdx.x; c < n; c += blockDim.x) mx = fmaxf(mx, row[c] * scale);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[wid] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int i = 1; i < nw; ++i) mx = fmaxf(mx, red[i]);
+  __syncthreads();
+  float sum = 0.f;
+  for (long long c = threadIdx.x; c < n; c += blockDim.x) sum += __expf(row[c] * scale - mx);
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[wid] = sum;
+  __syncthreads();
+  sum = 0.f;
+  for (int i = 0; i < nw; ++i) sum += red[i];
+  const float inv = 1.0f / sum;
+  for (long long c = threadIdx.x; c < ldp; c += blockDim.x)
+    prow[c] = __float2bfloat16_rn(c < n ? __expf(row[c] * scale - mx) * inv : 0.0f);
+}
+
+// h = x + z (x bf16, z float32) -> h float32 and its bf16 copy hb.
+__global__ void residual_kernel(const __nv_bfloat16 *x, const float *z, float *h, __nv_bfloat16 *hb,
+                                long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float v = __bfloat162float(x[i]) + z[i];
+    h[i] = v;
+    hb[i] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void add_inplace_kernel(float *out, const float *h, long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    out[i] += h[i];
+}
+
 // ---- packing ------------------------------------------------------------
 
 template <typename E>
@@ -459,6 +509,30 @@ cudaError_t launch_shard_sum_bf16(const float *const *parts, int T, long long n,
   if (n4 * 4 < n)
     shard_sum_bf16_scalar<<<grid_for(n - n4 * 4, threads, num_sms, 8), threads, 0, stream>>>(
         L, T, n4 * 4, n, z);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_rows(const float *S, long long lds, long long s_batch, void *P, long long ldp,
+                                long long p_batch, int M, int heads, int causal, float scale,
+                                cudaStream_t stream) {
+  if (M <= 0 || heads <= 0) return cudaSuccess;
+  if (heads > 65535) return cudaErrorInvalidValue;
+  softmax_rows_kernel<<<dim3(M, heads), 256, 0, stream>>>(S, lds, s_batch, static_cast<__nv_bfloat16 *>(P),
+                                                          ldp, p_batch, M, causal, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual(const void *x, const float *z, float *h, void *hb, long long n, int num_sms,
+                            cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  residual_kernel<<<grid_for(n, 256, num_sms, 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(x), z, h, static_cast<__nv_bfloat16 *>(hb), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_inplace(float *out, const float *h, long long n, int num_sms, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  add_inplace_kernel<<<grid_for(n, 256, num_sms, 8), 256, 0, stream>>>(out, h, n);
   return cudaGetLastError();
 }
 
