@@ -471,6 +471,26 @@ def extras(args, tp, device, peaks, full: bool) -> dict:
         s.close()
         torch.cuda.empty_cache()
 
+        # one transformer block at the attention workload's shape, SwiGLU MLP with F = 4H
+        M, H, T, nh, hd = 4096, 4096, 8, 32, 128
+        F = 4 * H
+        a = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                    nh, hd, T)
+        m = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                                "swiglu")
+        X = randn((M, H), 1.0)
+        ob = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(tp.tp_block_workspace_bytes(a, m, M, "auto"), dtype=torch.uint8, device=device)
+        t = _time_calls(lambda: tp.tp_block_forward(a, m, X, True, "auto", ob, None, ws), 10)
+        # algorithmic flop: projections, causal attention (the half below the diagonal), MLP
+        fl = 2 * M * H * 3 * H + 2 * 2 * nh * hd * M * (M + 1) / 2 + 2 * M * H * H + 6 * M * H * F
+        out["block_m4096_h4096_32x128_t8_swiglu_f16384"] = {"ms": round(t * 1e3, 3),
+                                                             "TFLOP/s": round(fl / t / 1e12, 1)}
+        a.close()
+        m.close()
+        del ws, ob, X
+        torch.cuda.empty_cache()
+
         w = WORKLOADS["prefill_swiglu_m8192_h8192_f28672_t8_outliers"]
         M, H, F, T = w["M"], w["H"], w["F"], w["T"]
         s = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,

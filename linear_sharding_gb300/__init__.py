@@ -402,6 +402,10 @@ def tp_mlp_backward(s: Shards, X, Hsave, Psave, dZ, variant: str = "auto", strea
     return dX, dW1, dW2
 
 
+def tp_block_workspace_bytes(attn: Shards, mlp: Shards, M: int, variant: str = "auto") -> int:
+    return int(load_library().tp_block_workspace_bytes(attn.handle, mlp.handle, M, VARIANT[variant]))
+
+
 def tp_block_forward(attn: Shards, mlp: Shards, X, causal: bool = True, variant: str = "auto",
                      out=None, h_out=None, workspace=None, stream=None):
     """One TP transformer block: returns (out, h) float32 [M x H] (h is None

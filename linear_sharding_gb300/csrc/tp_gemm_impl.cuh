@@ -104,18 +104,33 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g, int bm_row
   return r;
 }
 
-// Third tensor-map coordinate and K coordinate of k-tile kt for an operand
-// in mode 0 (flat K), 1 (K segments) or 2 (batch index).
-__device__ __forceinline__ void operand_coords(int mode, int kt, const GemmArgs &g, const Unit &t,
-                                               int &k, int &z) {
-  if (mode == 1) {
-    z = kt / g.kt_per_seg;
-    k = (kt - z * g.kt_per_seg) * BK;
-  } else {
-    z = mode == 2 ? t.b : 0;
-    k = kt * BK;
+// K coordinate and third tensor-map coordinate of the k-tiles of one unit,
+// advanced one k-tile at a time (no division on the producer's path).  An
+// operand in mode 0 is [1][rows][K] (flat K), mode 1 [segments][rows][K per
+// segment], mode 2 [batch][rows][K] (third coordinate = batch index).
+struct KCursor {
+  int k, z;         // current K element and third coordinate (segmented operands)
+  int kflat;        // current K element of the virtual axis
+  int seg_end;      // K element at which the current segment ends
+  __device__ __forceinline__ void start(int kt0, const GemmArgs &g) {
+    z = kt0 / g.kt_per_seg;
+    k = (kt0 - z * g.kt_per_seg) * BK;
+    kflat = kt0 * BK;
+    seg_end = g.kt_per_seg * BK;
   }
-}
+  __device__ __forceinline__ void next() {
+    kflat += BK;
+    k += BK;
+    if (k == seg_end) {
+      k = 0;
+      ++z;
+    }
+  }
+  __device__ __forceinline__ void coords(int mode, int b, int &kc, int &zc) const {
+    kc = mode == 1 ? k : kflat;
+    zc = mode == 1 ? z : (mode == 2 ? b : 0);
+  }
+};
 
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
@@ -403,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, g, BM, BN);
         if (t.skip) continue;
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+        KCursor kc;
+        kc.start(t.kt0, g);
+        for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, w)) {
             ok = false;
             break;
@@ -411,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           int ak, az, bk, bz;
-          operand_coords(g.a_seg, kt, g, t, ak, az);
-          operand_coords(g.b_seg, kt, g, t, bk, bz);
+          kc.coords(g.a_seg, t.b, ak, az);
+          kc.coords(g.b_seg, t.b, bk, bz);
           tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
           tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
           issued |= 1u << stage;
@@ -606,7 +623,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (t.skip) continue;
         const int arow = t.m * 256 + 128 * static_cast<int>(rank);
         const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+        KCursor kc;
+        kc.start(t.kt0, g);
+        for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
           if (!wait_bar_cluster(empty_bar(stage), phase ^ 1u, w)) {
             ok = false;
             break;
@@ -614,8 +633,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           int ak, az, bk, bz;
-          operand_coords(g.a_seg, kt, g, t, ak, az);
-          operand_coords(g.b_seg, kt, g, t, bk, bz);
+          kc.coords(g.a_seg, t.b, ak, az);
+          kc.coords(g.b_seg, t.b, bk, bz);
           tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
           tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
           issued |= 1u << stage;
