@@ -526,17 +526,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Cluster of 2 CTAs on a 256 x 256 output tile.  CTA r loads rows
 // [128 r, 128 r + 128) of the A tile and rows [128 r, 128 r + 128) of the B
-// tile into its own shared memory (32 KiB per stage, 7 stages); one thread of
-// CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which reads both
-// CTAs' tiles and leaves rows [128 r, 128 r + 128) x 256 columns in CTA r's
-// tensor memory.  Each CTA's copies complete on its own barrier; in CTA 1 a
-// relay thread forwards "stage full" to CTA 0, so every CTA can always wait
-// for its own copies.  Commits are multicast to both CTAs' barriers; the
-// epilogue warps of both CTAs release an accumulator on CTA 0's barrier.
+// tile into its own shared memory (32 KiB per stage); both CTAs' copies
+// complete on CTA 0's stage barrier, which CTA 0 arms for both halves.  One
+// thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256), which
+// reads both CTAs' tiles and leaves rows [128 r, 128 r + 128) x 256 columns
+// in CTA r's tensor memory.  Commits are multicast to both CTAs' barriers;
+// the epilogue warps of both CTAs release an accumulator on CTA 0's barrier.
+// On an abort CTA 0 waits for the stages it armed; CTA 1, whose copies
+// complete on CTA 0's barriers, waits a bounded time for its copies in flight.
 #ifndef TP_PAIR_STAGES
 #define TP_PAIR_STAGES 7
 #endif
 constexpr int kPairStages = TP_PAIR_STAGES;
+// Time CTA 1 leaves its in-flight copies to land after an abort.
+constexpr unsigned long long kPeerDrainNs = 200000ull;
 constexpr int kPairBN = 256;
 
 __host__ __device__ constexpr size_t pair_smem_bytes() {
@@ -562,17 +565,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  // barriers: full[S] | pfull[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain | never
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * kAcc + 2);
+  // barriers: full[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain | never
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2 * kAcc + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto pfull_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + kAcc + a); };
-  const uint32_t drain = bar0 + 8u * (3 * STAGES + 2 * kAcc);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + kAcc + a); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 2 * kAcc);
   const uint32_t never = drain + 8u;  // nothing ever arrives here (timeout test)
 
   const int warp = threadIdx.x >> 5;
@@ -582,7 +584,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(pfull_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < kAcc; ++a) {
@@ -618,6 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
+      const bool leader = rank == 0;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g, 256, BN);
         if (t.skip) continue;
@@ -630,13 +632,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           int ak, az, bk, bz;
           kc.coords(g.a_seg, t.b, ak, az);
           kc.coords(g.b_seg, t.b, bk, bz);
-          tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
-          tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
+          if (leader) {
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_BYTES));
+            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
+            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
+          } else {
+            const uint32_t fb = map_to_rank(full_bar(stage), 0);
+            tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
+            tma_load_3d_pair(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -645,9 +653,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) drain_bar(full_bar(s), (last_par >> s) & 1u, g.status);
+      if (!ok && issued) {
+        if (leader) {
+          for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1u) drain_bar(full_bar(s), (last_par >> s) & 1u, g.status);
+        } else {
+          const unsigned long long t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < kPeerDrainNs) {
+          }
+        }
       }
     }
     __syncwarp();
@@ -664,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w) || !wait_bar_cluster(pfull_bar(stage), phase, w)) {
+          if (!wait_bar(full_bar(stage), phase, w)) {
             ok = false;
             break;
           }
@@ -689,26 +703,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_commit2(drain);
       drain_bar(drain, 0u, g.status);
-    } else if (lane == 0) {
-      // ---- relay (CTA 1): this CTA's stage has landed -> tell CTA 0 ----
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g, 256, BN);
-        if (t.skip) continue;
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(map_to_rank(pfull_bar(stage), 0));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
     }
     __syncwarp();
   } else {
