@@ -305,21 +305,38 @@ def run_ours(args) -> dict | None:
     col_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K
     row_ms = sum(e1[i].elapsed_time(e2[i]) for i in range(K)) / K
 
-    # end to end through the public host-buffer call: pinned X in, Z out
-    Xh = torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    Zh = torch.empty((M, H), dtype=torch.float32).pin_memory()
-    wsh = torch.empty(tp.tp_mlp_host_workspace_bytes(s, M, args.variant), dtype=torch.uint8, device=device)
-    for _ in range(args.warmup):
-        tp.tp_mlp_forward_host(s, Xh, Zh, wsh, args.variant)
+    # end to end through the public host-buffer call: pinned X in, Z out.  Two
+    # requests in flight on two streams (each with its own host and device
+    # buffers), so one step's copies run under the other's compute; every
+    # step's own copies stay inside the timed region.
+    n_inflight = 2
+    Xh = [torch.from_numpy(np.ascontiguousarray(d["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+          for _ in range(n_inflight)]
+    Zh = [torch.empty((M, H), dtype=torch.float32).pin_memory() for _ in range(n_inflight)]
+    wsh = [torch.empty(tp.tp_mlp_host_workspace_bytes(s, M, args.variant), dtype=torch.uint8, device=device)
+           for _ in range(n_inflight)]
+    streams = [torch.cuda.Stream(device=device) for _ in range(n_inflight)]
+    for k in range(args.warmup):
+        i = k % n_inflight
+        tp.tp_mlp_forward_host(s, Xh[i], Zh[i], wsh[i], args.variant, stream=streams[i])
     barrier(device)
     torch.cuda.synchronize()
     hs, he = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     hs.record(stream)
-    for _ in range(K):
-        tp.tp_mlp_forward_host(s, Xh, Zh, wsh, args.variant)
+    for st_ in streams:
+        st_.wait_event(hs)
+    for k in range(K):
+        i = k % n_inflight
+        tp.tp_mlp_forward_host(s, Xh[i], Zh[i], wsh[i], args.variant, stream=streams[i])
+    for st_ in streams:
+        ev = torch.cuda.Event()
+        ev.record(st_)
+        stream.wait_event(ev)
     he.record(stream)
     torch.cuda.synchronize()
     barrier(device)
+    if not torch.equal(Zh[0], Zh[1]) or not torch.isfinite(Zh[0]).all():
+        raise RuntimeError("end-to-end results differ between the two in-flight buffers")
     e2e_value, _ = aggregate(hs.elapsed_time(he) / 1e3, flops_step * K, device)
 
     peaks, peak_src = measured_peaks()
@@ -353,7 +370,8 @@ def run_ours(args) -> dict | None:
                      "traffic": traffic, "avg_launch_ms": round(col_ms, 5)},
         "rowpar_ms": round(row_ms, 5),
         "e2e": {"value": round(e2e_value / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 4},
+                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 4,
+                "api": "tp_mlp_forward_host", "in_flight": n_inflight},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "context": {"ring_allreduce_bytes_per_rank_if_T_gpus": tp.ring_allreduce_bytes(M * H, T, 4)},
