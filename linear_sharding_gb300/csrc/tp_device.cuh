@@ -107,10 +107,14 @@ struct WaitCtl {
 // hint so that a wait can run out before the awaited event happens.
 constexpr unsigned long long kShortLimitNs = 1000000ull;
 
+// Suspend hint of a normal probe: the thread may sleep up to 10 ms, and wakes
+// as soon as the awaited phase completes.
+constexpr uint32_t kProbeHintNs = 10000000u;
+
 __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity, const WaitCtl &w) {
   if (w.limit_ns < kShortLimitNs)
     return mbar_try_wait_hint(bar, parity, static_cast<uint32_t>(w.limit_ns) | 1u);
-  return mbar_try_wait(bar, parity);
+  return mbar_try_wait_hint(bar, parity, kProbeHintNs);
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if
