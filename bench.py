@@ -47,10 +47,13 @@ def parse_args(argv=None):
                    help="secondary measurements at N=1: decode + shard-sum (default), "
                         "plus attention projections and the large SwiGLU prefill (full)")
     p.add_argument("--cpu-rows", type=int, default=64, help="rows of the oracle CPU-baseline sample")
-    p.add_argument("--case", choices=("prefill", "decode", "shard_sum"), default="prefill",
+    p.add_argument("--case", choices=("prefill", "decode", "shard_sum", "train", "block"),
+                   default="prefill",
                    help="prefill: the headline step (default); decode / shard_sum: time only the "
                         "memory-bound decode MLP (H=8192, F=28672, T=8, SwiGLU, --decode-m tokens) "
-                        "or the standalone shard-sum (T=8, n=8192*8192), for profiling")
+                        "or the standalone shard-sum (T=8, n=8192*8192); train: the backward of the "
+                        "prefill MLP; block: one transformer block (M=4096, 32x128 heads, T=8, "
+                        "SwiGLU F=4H, causal); for profiling")
     p.add_argument("--decode-m", type=int, default=16)
     return p.parse_args(argv)
 
@@ -602,6 +605,35 @@ def run_case(args) -> dict:
         byts = 3 * H * F * 2 + M * H * (2 + 4)
         cfg = {"workload": "decode_swiglu_h8192_f28672_t8", "M": M, "H": H, "F": F, "T": T,
                "variant": args.variant}
+    elif args.case == "train":
+        w = WORKLOADS[WORKLOAD]
+        M, H, F, T = w["M"], w["H"], w["F"], w["T"]
+        W1, W2 = randn((H, F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F))
+        s = tp.tp_shard_weights(W1, W2, T, "gelu")
+        tp.tp_shards_enable_backward(s, W1, W2)
+        X, dZ = randn((M, H), 1.0), randn((M, H), 1.0)
+        _, Hs, Ps = tp.tp_mlp_forward_train(s, X)
+        fn = lambda: tp.tp_mlp_backward(s, X, Hs, Ps, dZ)  # noqa: E731
+        t = _time_calls(fn, args.steps, warm=args.warmup)
+        return {"metric": "backward TFLOP/s", "value": round(8 * M * H * F / t / 1e12, 1),
+                "unit": "TFLOP/s", "ms_per_call": round(t * 1e3, 4), "steps": args.steps,
+                "warmup": args.warmup, "config": {"workload": WORKLOAD, "M": M, "H": H, "F": F, "T": T}}
+    elif args.case == "block":
+        M, H, T, nh, hd = 4096, 4096, 8, 32, 128
+        F = 4 * H
+        a = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                    nh, hd, T)
+        m = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                                "swiglu")
+        X = randn((M, H), 1.0)
+        ob = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(tp.tp_block_workspace_bytes(a, m, M, args.variant), dtype=torch.uint8, device=device)
+        fn = lambda: tp.tp_block_forward(a, m, X, True, args.variant, ob, None, ws)  # noqa: E731
+        t = _time_calls(fn, args.steps, warm=args.warmup)
+        fl = 2 * M * H * 3 * H + 2 * 2 * nh * hd * M * (M + 1) / 2 + 2 * M * H * H + 6 * M * H * F
+        return {"metric": "transformer block TFLOP/s", "value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
+                "ms_per_call": round(t * 1e3, 4), "steps": args.steps, "warmup": args.warmup,
+                "config": {"workload": "block_m4096_h4096_32x128_t8_swiglu_f16384_causal"}}
     else:
         T, n = 8, 8192 * 8192
         P = [torch.randn(n, generator=gen, device=device) for _ in range(T)]
