@@ -86,6 +86,8 @@ def _load():
         lib.orc_block_forward.restype = i32
         lib.orc_block_forward.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i64, i32, i32, i32,
                                           i32, vp, i64, dp, dp]
+        lib.orc_attention.restype = i32
+        lib.orc_attention.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, vp, i64, dp]
         lib.orc_reduce_scatter_f32.restype = i32
         lib.orc_reduce_scatter_f32.argtypes = [vp, i32, i64, vp]
         lib.orc_all_gather.restype = i32
@@ -404,3 +406,18 @@ def block_forward(X, Wqkv, Wo, W1, W2, n_heads: int, head_dim: int, T: int, act:
                                      n_heads, head_dim, F, ACTS[act], int(causal), T, int(sharded),
                                      _ptr(r), r.size, _ptr(out), _ptr(h)), "block_forward")
     return out, h
+
+
+def attention(Q, K, V, causal: bool = True, rows=None) -> np.ndarray:
+    """Scaled dot-product attention per head on head-major Q, K, V
+    [n_heads x M x head_dim] (bfloat16 bits, float32 or float64): returns the
+    selected token rows [rows x n_heads*head_dim] fp64, heads side by side."""
+    Q, K, V = _c(Q), _c(K), _c(V)
+    if Q.ndim != 3 or K.shape != Q.shape or V.shape != Q.shape or not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K and V must share one shape [n_heads, M, head_dim] and one dtype")
+    nh, M, hd = Q.shape
+    r = _rows(rows, M)
+    out = np.empty((r.size, nh * hd), dtype=np.float64)
+    _check(_load().orc_attention(_ptr(Q), _ptr(K), _ptr(V), _dt(Q), M, nh, hd, int(causal), _ptr(r), r.size,
+                                 _ptr(out)), "attention")
+    return out

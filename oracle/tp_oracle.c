@@ -828,3 +828,60 @@ int orc_block_forward(const void *X, const void *Wqkv, const void *Wo, const voi
     free(V);
     return err;
 }
+
+/* ---- attention core per head -----------------------------------------------
+ * "Tensor parallelism" guide, section "Walking through a transformer block":
+ * heads are sharded across ranks, so each head's attention is computed on the
+ * shard that owns it.  Reading (as for the block): scaled dot-product
+ * attention, causal or over all keys.  For head h and token r:
+ *   s_j = q_r . k_j / sqrt(hd),  w_j = exp(s_j - max_j s_j),
+ *   o_r = sum_j w_j v_j / sum_j w_j
+ * over keys j <= r (causal) or j < M.  Q, K and V are head-major
+ * [n_heads][M][hd]; out is [n_rows][n_heads hd], heads side by side. */
+int orc_attention(const void *Q, const void *K, const void *V, int dt, int64_t M, int n_heads,
+                  int head_dim, int causal, const int64_t *rows, int64_t n_rows, double *out)
+{
+    if (!Q || !K || !V || !out || M <= 0 || n_heads <= 0 || head_dim <= 0)
+        return ORC_ERR_ARG;
+    if (check_rows(rows, n_rows, M))
+        return ORC_ERR_ARG;
+    const int64_t width = (int64_t)n_heads * head_dim;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        const int64_t nk = causal ? r + 1 : M;
+        double *s = (double *)malloc((size_t)nk * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            err = ORC_ERR_OOM;
+            continue;
+        }
+        for (int h = 0; h < n_heads; ++h) {
+            const int64_t base = (int64_t)h * M * head_dim;
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < nk; ++j) {
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += orc_value(Q, base + r * head_dim + d, dt) *
+                           orc_value(K, base + j * head_dim + d, dt);
+                s[j] = dot / sqrt((double)head_dim);
+                if (s[j] > mx)
+                    mx = s[j];
+            }
+            double den = 0.0;
+            for (int64_t j = 0; j < nk; ++j) {
+                s[j] = exp(s[j] - mx);
+                den += s[j];
+            }
+            for (int d = 0; d < head_dim; ++d) {
+                double num = 0.0;
+                for (int64_t j = 0; j < nk; ++j)
+                    num += s[j] * orc_value(V, base + j * head_dim + d, dt);
+                out[i * width + (int64_t)h * head_dim + d] = num / den;
+            }
+        }
+        free(s);
+    }
+    return err;
+}

@@ -20,6 +20,11 @@ test says otherwise; draws in this fixed order, float32 samples):
   ~ N(0, 1/H); Wo [H x H] ~ N(0, 1/H); A [M x H] ~ N(0, 1) (the attention
   output that feeds the output projection; heads side by side).
 * Partial sums for the standalone shard-sum: P [T x n] float32 ~ N(0, 1).
+* Attention core: Q, K, V head-major [n_heads x M x head_dim] ~ N(0, 1),
+  drawn in that order; Q is then scaled by ``q_scale`` (score spread: 1 gives
+  scores of about unit variance, larger values peakier softmax rows) and key
+  row j by 1 + ``key_ramp`` * j / M (later keys score higher, so a row's
+  running maximum keeps moving); bfloat16.
 """
 from __future__ import annotations
 
@@ -33,6 +38,7 @@ __all__ = [
     "mlp_inputs",
     "attn_inputs",
     "partials_inputs",
+    "attention_inputs",
 ]
 
 # Workload shapes.  Names say what each one is; the sizes are those of the
@@ -136,3 +142,16 @@ def partials_inputs(T: int, n: int, seed: int = 0) -> np.ndarray:
     """Draw T partial products of n float32 values each, [T x n] ~ N(0, 1)."""
     rng = np.random.default_rng(seed)
     return _normal(rng, (T, n), 1.0)
+
+
+def attention_inputs(M: int, n_heads: int, head_dim: int = 128, seed: int = 0, q_scale: float = 1.0,
+                     key_ramp: float = 0.0) -> dict:
+    """Draw head-major Q, K, V [n_heads x M x head_dim] (bfloat16 bit patterns)."""
+    rng = np.random.default_rng(seed)
+    shape = (n_heads, M, head_dim)
+    Q, K, V = _normal(rng, shape, 1.0), _normal(rng, shape, 1.0), _normal(rng, shape, 1.0)
+    if q_scale != 1.0:
+        Q *= np.float32(q_scale)
+    if key_ramp != 0.0:
+        K *= (1.0 + np.float32(key_ramp) * np.arange(M, dtype=np.float32) / np.float32(M))[None, :, None]
+    return dict(Q=f32_to_bf16_bits(Q), K=f32_to_bf16_bits(K), V=f32_to_bf16_bits(V))

@@ -523,3 +523,83 @@ def test_block_matches_a_library_attention():
     G, U = href @ W1[:, :F], href @ W1[:, F:]
     ref = href + (G * special.expit(G) * U) @ W2
     assert _normwise(h, href) <= 1e-13 and _normwise(out, ref) <= 1e-13
+
+
+# --- attention core (per head) ------------------------------------------------
+
+def _library_attention(Q, K, V, causal):
+    """Scaled dot-product attention per head from library routines (scipy
+    softmax, numpy matmuls): [nh, M, hd] -> [M, nh*hd]."""
+    from scipy.special import softmax
+    nh, M, hd = Q.shape
+    mask = np.tril(np.ones((M, M), dtype=bool)) if causal else np.ones((M, M), dtype=bool)
+    return np.concatenate([softmax(np.where(mask, Q[h] @ K[h].T / np.sqrt(hd), -np.inf), axis=1) @ V[h]
+                           for h in range(nh)], axis=1)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_matches_a_library_attention(causal):
+    """Softmax attention written with library routines on the same fp64
+    inputs; 3 heads so that a head offset slip shows."""
+    rng = np.random.default_rng(11)
+    Q, K, V = (rng.standard_normal((3, 9, 8)) for _ in range(3))
+    got = oracle.attention(Q, K, V, causal=causal)
+    assert _normwise(got, _library_attention(Q, K, V, causal)) <= 1e-13
+
+
+def test_attention_closed_forms():
+    """Q = 0 makes every score 0: causal attention at token r is the mean of
+    v_0..v_r (non-causal: of all v), and token 0 attends only to itself."""
+    rng = np.random.default_rng(12)
+    K, V = rng.standard_normal((2, 6, 4)), rng.standard_normal((2, 6, 4))
+    Q = np.zeros_like(K)
+    got = oracle.attention(Q, K, V, causal=True)
+    for r in range(6):
+        expect = np.concatenate([V[h, : r + 1].mean(axis=0) for h in range(2)])
+        assert np.allclose(got[r], expect, rtol=1e-14, atol=1e-14)
+    full = oracle.attention(Q, K, V, causal=False)
+    assert np.allclose(full, np.concatenate([V[h].mean(axis=0) for h in range(2)])[None, :].repeat(6, 0),
+                       rtol=1e-14, atol=1e-14)
+    Qr = rng.standard_normal((2, 6, 4))
+    assert np.array_equal(oracle.attention(Qr, K, V, causal=True, rows=[0]), V[:, 0].reshape(1, -1))
+
+
+def test_attention_key_shift_invariance_and_scale():
+    """Adding one vector e to every key adds q.e/sqrt(hd) to all scores of a
+    row, which the softmax removes; a score gap of d log 2 between two keys
+    weighs them 2^-d : 1 (the 1/sqrt(hd) scale, checked with hd = 4)."""
+    rng = np.random.default_rng(13)
+    Q, K, V = (rng.standard_normal((2, 7, 4)) for _ in range(3))
+    e = rng.standard_normal(4) * 3.0
+    base = oracle.attention(Q, K, V, causal=True)
+    assert _normwise(oracle.attention(Q, K + e, V, causal=True), base) <= 1e-12
+    # two keys, q . (k1 - k0) / 2 = 3 log 2: weights 1/9 and 8/9
+    q = np.array([[[1.0, 0.0, 0.0, 0.0]] * 2])
+    k = np.array([[[0.0, 0.0, 0.0, 0.0], [6 * math.log(2), 0.0, 0.0, 0.0]]])
+    v = np.array([[[1.0, 0.0, 0.0, 0.0], [0.0, 1.0, 0.0, 0.0]]])
+    got = oracle.attention(q, k, v, causal=False, rows=[0])
+    assert np.allclose(got[0], [1 / 9, 8 / 9, 0.0, 0.0], rtol=1e-14, atol=1e-15)
+
+
+def test_attention_bf16_inputs_widen_exactly():
+    """bfloat16 inputs are the same numbers as their fp64 widening."""
+    rng = np.random.default_rng(14)
+    Qf, Kf, Vf = (rng.standard_normal((2, 5, 8)).astype(np.float32) for _ in range(3))
+    Qb, Kb, Vb = (f32_to_bf16_bits(a) for a in (Qf, Kf, Vf))
+    wide = [(b.astype(np.uint32) << 16).view(np.float32).astype(np.float64) for b in (Qb, Kb, Vb)]
+    assert np.array_equal(oracle.attention(Qb, Kb, Vb), oracle.attention(*wide))
+
+
+def test_block_attention_is_the_attention_core():
+    """The block's attention contribution (Wo = I, MLP zero, T = 1) equals
+    the attention of its projections, so the GPU block and the GPU attention
+    core are checked against one definition."""
+    rng = np.random.default_rng(15)
+    M, nh, hd, F = 6, 2, 4, 8
+    H = nh * hd
+    X = rng.standard_normal((M, H))
+    Wqkv, _, W1, W2 = _block_weights(H, F, "gelu", 16)
+    _, h = oracle.block_forward(X, Wqkv, np.eye(H), np.zeros_like(W1), W2, nh, hd, 1, "gelu", causal=True)
+    heads = lambda A: A.reshape(M, nh, hd).transpose(1, 0, 2).copy()  # noqa: E731
+    Q, K, V = (heads(X @ Wqkv[:, i * H:(i + 1) * H]) for i in range(3))
+    assert _normwise(h - X, oracle.attention(Q, K, V, causal=True)) <= 1e-13
