@@ -47,13 +47,14 @@ def parse_args(argv=None):
                    help="secondary measurements at N=1: decode + shard-sum (default), "
                         "plus attention projections and the large SwiGLU prefill (full)")
     p.add_argument("--cpu-rows", type=int, default=64, help="rows of the oracle CPU-baseline sample")
-    p.add_argument("--case", choices=("prefill", "decode", "shard_sum", "train", "block"),
+    p.add_argument("--case", choices=("prefill", "decode", "shard_sum", "train", "block", "attention"),
                    default="prefill",
                    help="prefill: the headline step (default); decode / shard_sum: time only the "
                         "memory-bound decode MLP (H=8192, F=28672, T=8, SwiGLU, --decode-m tokens) "
                         "or the standalone shard-sum (T=8, n=8192*8192); train: the backward of the "
                         "prefill MLP; block: one transformer block (M=4096, 32x128 heads, T=8, "
-                        "SwiGLU F=4H, causal); for profiling")
+                        "SwiGLU F=4H, causal); attention: the block's fused causal attention core "
+                        "(M=4096, 32 heads of 128); for profiling")
     p.add_argument("--decode-m", type=int, default=16)
     return p.parse_args(argv)
 
@@ -492,6 +493,16 @@ def extras(args, tp, device, peaks, full: bool) -> dict:
         s.close()
         torch.cuda.empty_cache()
 
+        # the block's fused causal attention core alone (4096 tokens, 32 heads of 128)
+        M, nh, hd = 4096, 32, 128
+        Qa, Ka, Va = (randn((nh, M, hd), 1.0) for _ in range(3))
+        Oa = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=device)
+        wsa = torch.empty(tp.tp_attention_workspace_bytes(M, nh, hd), dtype=torch.uint8, device=device)
+        t = _time_calls(lambda: tp.tp_attention_forward(Qa, Ka, Va, True, Oa, wsa), 20)
+        fl = 2 * 2 * nh * hd * M * (M + 1) / 2
+        out["attention_m4096_32x128_causal"] = {"us": round(t * 1e6, 1), "TFLOP/s": round(fl / t / 1e12, 1)}
+        del Qa, Ka, Va, Oa, wsa
+
         # one transformer block at the attention workload's shape, SwiGLU MLP with F = 4H
         M, H, T, nh, hd = 4096, 4096, 8, 32, 128
         F = 4 * H
@@ -634,6 +645,19 @@ def run_case(args) -> dict:
         return {"metric": "transformer block TFLOP/s", "value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
                 "ms_per_call": round(t * 1e3, 4), "steps": args.steps, "warmup": args.warmup,
                 "config": {"workload": "block_m4096_h4096_32x128_t8_swiglu_f16384_causal"}}
+    elif args.case == "attention":
+        M, nh, hd = 4096, 32, 128
+        Q, K, V = (randn((nh, M, hd), 1.0) for _ in range(3))
+        O = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=device)
+        ws = torch.empty(tp.tp_attention_workspace_bytes(M, nh, hd), dtype=torch.uint8, device=device)
+        fn = lambda: tp.tp_attention_forward(Q, K, V, True, O, ws)  # noqa: E731
+        t = _time_calls(fn, args.steps, warm=args.warmup)
+        if tp.tp_last_device_status() != 0:
+            raise RuntimeError("device status error")
+        fl = 2 * 2 * nh * hd * M * (M + 1) / 2  # Q K^T and P V over the allowed (causal) pairs
+        return {"metric": "attention TFLOP/s", "value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
+                "ms_per_call": round(t * 1e3, 4), "steps": args.steps, "warmup": args.warmup,
+                "config": {"workload": "attention_m4096_32x128_causal"}}
     else:
         T, n = 8, 8192 * 8192
         P = [torch.randn(n, generator=gen, device=device) for _ in range(T)]

@@ -328,7 +328,8 @@ TP_API tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void
  * row-parallel projection; "Tensor parallelism" guide, section "Walking
  * through a transformer block": heads sharded across ranks, the two
  * all-reduces on the attention and MLP residual paths).
- *   attn: a handle from tp_shard_weights_qkv (head_dim a multiple of 128);
+ *   attn: a handle from tp_shard_weights_qkv with head_dim 128 (other head
+ *         dims -> TP_ERR_UNSUPPORTED);
  *   mlp:  a bfloat16 handle from tp_shard_weights with the same H and T.
  *   X [M x H] bfloat16.  Per token r and head h (heads in shard order):
  *     o_h = sum_{j <= r} softmax_j(q_h . k_jh / sqrt(head_dim)) v_jh
@@ -336,15 +337,42 @@ TP_API tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void
  *     h = X + sum_i O_i Wo_i, out = h + sum_i act(h W1_i) W2_i.
  *   No normalisation layers (the pages name none).  Q, K, V, the
  *   probabilities, O and the MLP input h are rounded to bfloat16 on the way;
- *   scores, sums and outputs are float32.
+ *   scores, sums and outputs are float32.  The attention core is the one of
+ *   tp_attention_forward (scores never reach memory).
  *   out [M x H] float32; h_out [M x H] float32 or NULL: the residual stream
  *   after the attention all-reduce.  workspace: tp_block_workspace_bytes()
- *   bytes (it holds the float32 scores, nh x M x M) or NULL.  Asynchronous.
+ *   bytes or NULL.  Asynchronous.
  */
 TP_API size_t tp_block_workspace_bytes(tp_shards_t attn, tp_shards_t mlp, int64_t M, tp_variant_t v);
 TP_API tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const void *X, int64_t M,
                                     int causal, tp_variant_t v, float *out, float *h_out,
                                     void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * tp_attention_forward - the attention core of the block for a set of heads
+ * ("Tensor parallelism" guide, section "Walking through a transformer
+ * block": heads are sharded across ranks, so each head's attention runs
+ * where its shard lives, with no communication).  For every head h and
+ * token r < M:
+ *   O[r][h hd + d] = sum_j softmax_j(q_rh . k_jh / sqrt(hd)) v_jh[d]
+ * over keys j <= r (causal != 0) or all j < M (causal == 0); scores and
+ * probabilities stay on chip (one fused kernel per call after a transpose of
+ * V).  The probabilities are rounded to bfloat16 for the P V product and the
+ * sums are float32.
+ *   Q, K, V: bfloat16, head-major [n_heads][M][head_dim], device, 16-byte
+ *            aligned (the layout tp_block_forward's QKV projection writes).
+ *   head_dim must be 128 (else TP_ERR_UNSUPPORTED).
+ *   O: bfloat16 [M][ldo] out, head h in columns [h hd, (h+1) hd);
+ *      ldo >= n_heads hd and a multiple of 8; 16-byte aligned; must not
+ *      overlap Q, K or V (TP_ERR_ARG).
+ *   workspace: tp_attention_workspace_bytes(M, n_heads, head_dim) bytes
+ *      (V transposed per head) or NULL to allocate on `stream`.
+ *   M == 0 is a no-op.  Asynchronous on `stream`.
+ */
+TP_API size_t tp_attention_workspace_bytes(int64_t M, int n_heads, int head_dim);
+TP_API tp_status_t tp_attention_forward(const void *Q, const void *K, const void *V, int64_t M,
+                                        int n_heads, int head_dim, int causal, void *O, int64_t ldo,
+                                        void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * tp_partial_sum - the all-reduce-sum arithmetic on one GPU ("Slice the

@@ -37,7 +37,8 @@ EXPORTS = (
     "tp_rowpar_forward", "tp_mlp_forward_noalloc", "tp_reduce_scatter", "tp_all_gather",
     "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
-    "tp_block_workspace_bytes", "tp_block_forward",
+    "tp_block_workspace_bytes", "tp_block_forward", "tp_attention_workspace_bytes",
+    "tp_attention_forward",
 )
 
 _lock = threading.Lock()
@@ -103,13 +104,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_block_workspace_bytes.restype = sz
         lib.tp_block_workspace_bytes.argtypes = [vp, vp, i64, i32]
         lib.tp_block_forward.argtypes = [vp, vp, vp, i64, i32, i32, vp, vp, vp, sz, vp]
+        lib.tp_attention_workspace_bytes.restype = sz
+        lib.tp_attention_workspace_bytes.argtypes = [i64, i32, i32]
+        lib.tp_attention_forward.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp, i64, vp, sz, vp]
         for name in ("tp_shard_weights", "tp_shard_weights_qkv", "tp_shard_get", "tp_shard_info",
                      "tp_mlp_forward", "tp_mlp_forward_host", "tp_attn_proj_forward",
                      "tp_partial_sum", "tp_last_device_status", "tp_set_wait_limit_ns",
                      "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
                      "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16",
                      "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward",
-                     "tp_block_forward"):
+                     "tp_block_forward", "tp_attention_forward"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -423,6 +427,30 @@ def tp_block_forward(attn: Shards, mlp: Shards, X, causal: bool = True, variant:
                                 _ptr(out), _ptr(h_out if h_out is not False else None), _ptr(workspace),
                                 ws_bytes, _stream(stream)), "tp_block_forward")
     return out, (h_out if h_out is not False else None)
+
+
+def tp_attention_workspace_bytes(M: int, n_heads: int, head_dim: int = 128) -> int:
+    return int(load_library().tp_attention_workspace_bytes(M, n_heads, head_dim))
+
+
+def tp_attention_forward(Q, K, V, causal: bool = True, out=None, workspace=None, stream=None):
+    """Attention per head: Q, K, V bf16 [n_heads, M, head_dim] (device) ->
+    O bf16 [M, n_heads * head_dim], heads side by side."""
+    torch = _torch()
+    lib = load_library()
+    Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
+    nh, M, hd = Q.shape
+    if K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K and V must have the same shape [n_heads, M, head_dim]")
+    if not (Q.dtype == K.dtype == V.dtype == torch.bfloat16):
+        raise TypeError("tp_attention_forward takes bfloat16 Q, K and V")
+    if out is None:
+        out = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=Q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.tp_attention_forward(_ptr(Q), _ptr(K), _ptr(V), M, nh, hd, int(bool(causal)), _ptr(out),
+                                    out.stride(0), _ptr(workspace), ws_bytes, _stream(stream)),
+           "tp_attention_forward")
+    return out
 
 
 def tp_last_device_status(stream=None) -> int:

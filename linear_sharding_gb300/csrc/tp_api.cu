@@ -127,6 +127,11 @@ tp_status_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool ranges_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
 size_t esize(tp_dtype_t dt) { return dt == TP_BF16 ? 2 : 4; }
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
@@ -709,30 +714,53 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
 
 // ---- one tensor-parallel transformer block ---------------------------------------
 
+// Attention core (the block's, and tp_attention_forward): V is transposed
+// per head into V^T [heads][128][Mp] (keys padded with zeros to Mp, a
+// multiple of 64), then the fused kernel reads Q, K and V^T through TMA.
+size_t attention_vt_bytes(int64_t M, int64_t heads) {
+  return static_cast<size_t>(heads * kAttnHeadDim * round64(M)) * 2;
+}
+
+tp_status_t attention_core(const DevState *d, const void *Q, const void *K, const void *V, int64_t M,
+                           int64_t heads, int causal, void *O, int64_t ldo, void *vt, cudaStream_t st) {
+  const int64_t hd = kAttnHeadDim, Mp = round64(M);
+  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, vt, Mp, hd * Mp, static_cast<int>(heads), st));
+  CUtensorMap mq, mk, mvt;
+  TP_TRY(make_map(&mq, Q, hd, M, heads, hd * 2, M * hd * 2, 128));
+  TP_TRY(make_map(&mk, K, hd, M, heads, hd * 2, M * hd * 2, 128));
+  TP_TRY(make_map(&mvt, vt, Mp, hd, heads, Mp * 2, hd * Mp * 2, 128));
+  AttnArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.M = static_cast<int>(M);
+  g.heads = static_cast<int>(heads);
+  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.causal = causal ? 1 : 0;
+  g.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
+  g.O = O;
+  g.ldo = ldo;
+  g.status = d->status;
+  g.wait_limit_ns = g_wait_ns.load();
+  TP_CUDA(launch_attention(mq, mk, mvt, g, d->sms, st));
+  return TP_OK;
+}
+
 struct BlockPlan {
-  int64_t Np = 0;   // score columns (keys) padded to a multiple of 256
-  int64_t Mp = 0;   // keys padded to a multiple of 64 (K of P V)
   int slots_o = 1;  // O-projection accumulation slots
   MlpPlan mlp;
-  size_t qkv = 0, S = 0, P = 0, vt = 0, O = 0, opart = 0, h = 0, hb = 0;
+  size_t qkv = 0, vt = 0, O = 0, opart = 0, h = 0, hb = 0;
   size_t total() const {
-    return round256(qkv) + round256(S) + round256(P) + round256(vt) + round256(O) + round256(opart) +
-           round256(h) + round256(hb) + mlp.total();
+    return round256(qkv) + round256(vt) + round256(O) + round256(opart) + round256(h) + round256(hb) +
+           mlp.total();
   }
 };
 
 void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t v, int sms, BlockPlan *p) {
   *p = BlockPlan();
   const int64_t H = a->H;
-  const int nh = a->n_heads, hd = a->head_dim;
-  p->Np = (M + 255) / 256 * 256;
-  p->Mp = round64(M);
   p->slots_o = v == TP_VAR_PARTIALS ? a->T : 1;
   plan_mlp(m, M, v, sms, &p->mlp);
   p->qkv = static_cast<size_t>(3 * H * M) * 2;
-  p->S = static_cast<size_t>(nh * M * p->Np) * 4;
-  p->P = static_cast<size_t>(nh * M * p->Mp) * 2;
-  p->vt = static_cast<size_t>(nh * hd * p->Mp) * 2;
+  p->vt = attention_vt_bytes(M, a->n_heads);
   p->O = static_cast<size_t>(M * H) * 2;
   p->opart = p->slots_o > 1 ? static_cast<size_t>(p->slots_o * M * H) * 4 : 0;
   p->h = static_cast<size_t>(M * H) * 4;
@@ -747,7 +775,7 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   TP_TRY(check_handle(m, 0, &d));
   if (m->dt != TP_BF16) return TP_ERR_DTYPE;
   if (m->H != a->H || m->T != a->T || M < 0 || !valid_variant(v)) return TP_ERR_ARG;
-  if (a->head_dim % 128 != 0) return TP_ERR_UNSUPPORTED;
+  if (a->head_dim != kAttnHeadDim) return TP_ERR_UNSUPPORTED;
   if (M == 0) return TP_OK;
   if (!X || !out || !aligned16(X) || !aligned16(out) || (h_out && !aligned16(h_out))) return TP_ERR_ARG;
   if (M > (1LL << 24)) return TP_ERR_UNSUPPORTED;
@@ -757,9 +785,7 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
   const int64_t H = a->H, nh = a->n_heads, hd = a->head_dim;
   char *qkv = w.ptr;
-  float *S = reinterpret_cast<float *>(qkv + round256(p.qkv));
-  char *P = reinterpret_cast<char *>(S) + round256(p.S);
-  char *vt = P + round256(p.P);
+  char *vt = qkv + round256(p.qkv);
   char *O = vt + round256(p.vt);
   float *opart = reinterpret_cast<float *>(O + round256(p.O));
   float *h = reinterpret_cast<float *>(reinterpret_cast<char *>(opart) + round256(p.opart));
@@ -789,61 +815,8 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   }
   const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2,
              *V = qkv + static_cast<size_t>(2 * nh * M * hd) * 2;
-  // 2. scores S_h = Q_h K_h^T for all heads (tiles past the diagonal skipped when causal)
-  CUtensorMap mq, mk_bn, mk_128;
-  TP_TRY(make_map(&mq, Q, hd, M, nh, hd * 2, M * hd * 2, 128));
-  TP_TRY(make_map(&mk_bn, K, hd, M, nh, hd * 2, M * hd * 2, 256));
-  TP_TRY(make_map(&mk_128, K, hd, M, nh, hd * 2, M * hd * 2, 128));
-  {
-    GemmArgs g = base_args(d);
-    g.out = S;
-    g.ld_out = p.Np;
-    g.batch = static_cast<int>(nh);
-    g.batch_stride_out = M * p.Np;
-    g.causal = causal ? 1 : 0;
-    GemmCall c;
-    c.a = &mq;
-    c.a_seg = 2;
-    c.b_bn = &mk_bn;
-    c.b_128 = &mk_128;
-    c.b_seg = 2;
-    c.rows = M;
-    c.N = p.Np;
-    c.bn = 256;
-    c.kps = static_cast<int>(hd / 64);
-    c.epi = EPI_F32;
-    TP_TRY(run_gemm(d, c, g, st));
-  }
-  // 3. softmax over the allowed keys -> P (bf16, zero elsewhere)
-  TP_CUDA(launch_softmax_rows(S, p.Np, M * p.Np, P, p.Mp, M * p.Mp, static_cast<int>(M), static_cast<int>(nh),
-                              causal, 1.0f / sqrtf(static_cast<float>(hd)), st));
-  // 4. V^T per head, keys padded to Mp
-  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, vt, p.Mp, hd * p.Mp, static_cast<int>(nh), st));
-  // 5. O_h = P_h V_h into the heads-side-by-side layout [M x H]
-  CUtensorMap mp, mvt;
-  TP_TRY(make_map(&mp, P, p.Mp, M, nh, p.Mp * 2, M * p.Mp * 2, 128));
-  TP_TRY(make_map(&mvt, vt, p.Mp, hd, nh, p.Mp * 2, hd * p.Mp * 2, static_cast<uint32_t>(bn_for(hd))));
-  {
-    GemmArgs g = base_args(d);
-    g.out = O;
-    g.ld_out = H;
-    g.shard_cols = static_cast<int>(hd);
-    g.batch = static_cast<int>(nh);
-    g.batch_stride_out = hd;
-    g.causal = causal ? 2 : 0;
-    GemmCall c;
-    c.a = &mp;
-    c.a_seg = 2;
-    c.b_bn = &mvt;
-    c.b_128 = &mvt;
-    c.b_seg = 2;
-    c.rows = M;
-    c.N = hd;
-    c.bn = bn_for(hd);
-    c.kps = static_cast<int>(p.Mp / 64);
-    c.epi = EPI_IDENT_BF16;
-    TP_TRY(run_gemm(d, c, g, st));
-  }
+  // 2.-5. causal attention per head, fused: O [M x H], heads side by side
+  TP_TRY(attention_core(d, Q, K, V, M, nh, causal, O, H, vt, st));
   // 6. row-parallel output projection + all-reduce-sum #1 (into out), 7. residual
   CUtensorMap mo;
   TP_TRY(make_map(&mo, O, H, M, 1, H * 2, M * H * 2, 128));
@@ -1276,6 +1249,35 @@ tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const void *X, i
                             static_cast<cudaStream_t>(stream));
 }
 
+size_t tp_attention_workspace_bytes(int64_t M, int n_heads, int head_dim) {
+  if (M <= 0 || n_heads <= 0 || head_dim != kAttnHeadDim) return 0;
+  return attention_vt_bytes(M, n_heads);
+}
+
+tp_status_t tp_attention_forward(const void *Q, const void *K, const void *V, int64_t M, int n_heads,
+                                 int head_dim, int causal, void *O, int64_t ldo, void *workspace,
+                                 size_t ws_bytes, void *stream) {
+  if (M < 0 || n_heads <= 0 || head_dim <= 0) return TP_ERR_ARG;
+  if (head_dim != kAttnHeadDim) return TP_ERR_UNSUPPORTED;
+  if (M == 0) return TP_OK;
+  if (M > (1LL << 24) || cdiv(M, 128) * n_heads >= (1LL << 31)) return TP_ERR_UNSUPPORTED;
+  if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return TP_ERR_ARG;
+  const int64_t width = static_cast<int64_t>(n_heads) * head_dim;
+  if (ldo < width || ldo % 8 != 0) return TP_ERR_ARG;
+  const size_t in_bytes = static_cast<size_t>(M * width) * 2;
+  const size_t out_bytes = static_cast<size_t>((M - 1) * ldo + width) * 2;
+  if (ranges_overlap(O, out_bytes, Q, in_bytes) || ranges_overlap(O, out_bytes, K, in_bytes) ||
+      ranges_overlap(O, out_bytes, V, in_bytes))
+    return TP_ERR_ARG;
+  DevState *d = nullptr;
+  TP_TRY(dev_state(&d));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Workspace w;
+  TP_TRY(get_ws(&w, workspace, ws_bytes, attention_vt_bytes(M, n_heads), st));
+  return attention_core(d, Q, K, V, M, n_heads, causal, O, ldo, w.ptr, st);
+}
+
 tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {
   if (!Zi || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;
   if (n == 0) return TP_OK;
@@ -1295,12 +1297,6 @@ tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, v
   return cuda_status(launch_shard_sum(Zi, T, n, Z, d->sms, static_cast<cudaStream_t>(stream)));
 }
 
-namespace {
-bool ranges_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-  return a0 < b0 + bbytes && b0 < a0 + abytes;
-}
-}  // namespace
 
 tp_status_t tp_reduce_scatter(const float *const *Zi, int T, int64_t n, float *const *out, void *stream) {
   if (!Zi || !out || T < 1 || T > kMaxShards || n < 0) return TP_ERR_ARG;

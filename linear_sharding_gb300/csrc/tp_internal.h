@@ -87,6 +87,27 @@ cudaError_t launch_transpose_pad(const void *src, long long rows, long long cols
                                  long long src_batch, void *dst, long long dst_ld, long long dst_batch,
                                  int batch, cudaStream_t stream);
 
+// Fused attention core over `heads` independent heads of dimension 128:
+// O_h[r] = sum over keys j (j <= r when causal, j < M) of
+// softmax_j(q_r . k_j * scale) v_j, for every token r < M.  Q and K are
+// head-major [heads][M][128] bf16 tensor maps (box 64 x 128), V^T is
+// [heads][128][Mp] bf16 (box 64 keys x 128 rows, keys past M zero); O is
+// bf16 [M][ldo] with head h in columns [128 h, 128 h + 128).
+struct AttnArgs {
+  int M;
+  int heads;
+  int m_tiles;        // query tiles of 128 rows
+  int causal;
+  float scale_log2;   // scale * log2(e)
+  void *O;
+  long long ldo;
+  unsigned int *status;
+  unsigned long long wait_limit_ns;
+};
+constexpr int kAttnHeadDim = 128;
+cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapVt,
+                             const AttnArgs &args, int num_sms, cudaStream_t stream);
+
 // Float32 CUDA-core GEMM: D[m][n] = sum_k A[m][k] B[n][k], same work model
 // as the tensor-core path but with plain row-major pointers.  A rows have
 // stride lda; segments (shards) of A and B along K are `a_seg`/`b_seg`

@@ -47,3 +47,24 @@ TOL_F32_NORMWISE = 1e-4
 # forward's measured row-RMS error is about 8e-3 per rounding, so the
 # gradients are held to 3e-2.
 TOL_BF16_GRAD_ROW_RMS = 3e-2
+
+# The attention output passes through two bf16 roundings: the probabilities P
+# (each weight relative 2^-9, rounded once before the P V product) and the
+# stored output O.  Checked elementwise like any stored bf16 tensor, as
+# |O - ref| <= 2^-8 |ref| + TOL_ATTN_ELEMENT * RMS(ref row): the first term
+# holds O's own rounding (<= 2^-9 |ref|); the second the probability rounding,
+# whose error is a weighted sum of (v_j - o) with independent relative errors
+# of at most 2^-9 (measured <= 1.03e-2 of the row RMS alone and <= 8.1e-3 on
+# top of the first term, on the parity inputs, by emulating the kernel's
+# arithmetic in numpy).  The row-RMS measure is held to the multi-rounding
+# bound TOL_BF16_GRAD_ROW_RMS.
+TOL_ATTN_ELEMENT = 1.5e-2
+
+
+def attention_elementwise_ok(got: np.ndarray, ref: np.ndarray) -> float:
+    """Largest (|got - ref| - 2^-8 |ref|) / RMS(ref row); the check passes
+    when it is <= TOL_ATTN_ELEMENT."""
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    slack = (np.abs(np.asarray(got, np.float64) - ref) - 2.0 ** -8 * np.abs(ref)) / np.maximum(rms, 1e-300)
+    return float(np.max(slack))
