@@ -714,21 +714,21 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
 
 // ---- one tensor-parallel transformer block ---------------------------------------
 
-// Attention core (the block's, and tp_attention_forward): V is transposed
-// per head into V^T [heads][128][Mp] (keys padded with zeros to Mp, a
-// multiple of 64), then the fused kernel reads Q, K and V^T through TMA.
+// Attention core (the block's, and tp_attention_forward): the fused kernel
+// reads Q, K and V^T [heads][128][round64(M)] through TMA.  The V^T map's key
+// extent is M, so the copy engine fills keys past M with zeros whatever the
+// padding columns hold.
 size_t attention_vt_bytes(int64_t M, int64_t heads) {
   return static_cast<size_t>(heads * kAttnHeadDim * round64(M)) * 2;
 }
 
-tp_status_t attention_core(const DevState *d, const void *Q, const void *K, const void *V, int64_t M,
-                           int64_t heads, int causal, void *O, int64_t ldo, void *vt, cudaStream_t st) {
+tp_status_t attention_core_vt(const DevState *d, const void *Q, const void *K, const void *Vt, int64_t M,
+                              int64_t heads, int causal, void *O, int64_t ldo, cudaStream_t st) {
   const int64_t hd = kAttnHeadDim, Mp = round64(M);
-  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, vt, Mp, hd * Mp, static_cast<int>(heads), st));
   CUtensorMap mq, mk, mvt;
   TP_TRY(make_map(&mq, Q, hd, M, heads, hd * 2, M * hd * 2, 128));
   TP_TRY(make_map(&mk, K, hd, M, heads, hd * 2, M * hd * 2, 128));
-  TP_TRY(make_map(&mvt, vt, Mp, hd, heads, Mp * 2, hd * Mp * 2, 128));
+  TP_TRY(make_map(&mvt, Vt, M, hd, heads, Mp * 2, hd * Mp * 2, 128));
   AttnArgs g;
   std::memset(&g, 0, sizeof g);
   g.M = static_cast<int>(M);
@@ -759,7 +759,7 @@ void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t 
   const int64_t H = a->H;
   p->slots_o = v == TP_VAR_PARTIALS ? a->T : 1;
   plan_mlp(m, M, v, sms, &p->mlp);
-  p->qkv = static_cast<size_t>(3 * H * M) * 2;
+  p->qkv = static_cast<size_t>(2 * H * M) * 2;  // Q and K head-major; V goes to vt transposed
   p->vt = attention_vt_bytes(M, a->n_heads);
   p->O = static_cast<size_t>(M * H) * 2;
   p->opart = p->slots_o > 1 ? static_cast<size_t>(p->slots_o * M * H) * 4 : 0;
@@ -793,12 +793,15 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   char *mws = hb + round256(p.hb);
   if (h_out) h = h_out;
 
-  // 1. QKV projection of every shard, written head-major [3][nh][M][hd]
+  // 1. QKV projection of every shard: Q and K head-major [2][nh][M][hd], V transposed per
+  //    head into vt [nh][hd][round64(M)]
   CUtensorMap mx;
   TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
   {
     GemmArgs g = base_args(d);
     g.out = qkv;
+    g.out2 = vt;
+    g.ld_out = round64(M);
     g.shard_cols = static_cast<int>(a->R1);
     g.head_dim = static_cast<int>(hd);
     g.n_heads = static_cast<int>(nh);
@@ -813,10 +816,9 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
     c.epi = EPI_QKV_HEADS_BF16;
     TP_TRY(run_gemm(d, c, g, st));
   }
-  const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2,
-             *V = qkv + static_cast<size_t>(2 * nh * M * hd) * 2;
+  const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2;
   // 2.-5. causal attention per head, fused: O [M x H], heads side by side
-  TP_TRY(attention_core(d, Q, K, V, M, nh, causal, O, H, vt, st));
+  TP_TRY(attention_core_vt(d, Q, K, vt, M, nh, causal, O, H, st));
   // 6. row-parallel output projection + all-reduce-sum #1 (into out), 7. residual
   CUtensorMap mo;
   TP_TRY(make_map(&mo, O, H, M, 1, H * 2, M * H * 2, 128));
@@ -1275,7 +1277,9 @@ tp_status_t tp_attention_forward(const void *Q, const void *K, const void *V, in
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, attention_vt_bytes(M, n_heads), st));
-  return attention_core(d, Q, K, V, M, n_heads, causal, O, ldo, w.ptr, st);
+  const int64_t hd = kAttnHeadDim, Mp = round64(M);
+  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, w.ptr, Mp, hd * Mp, n_heads, st));
+  return attention_core_vt(d, Q, K, w.ptr, M, n_heads, causal, O, ldo, st);
 }
 
 tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {

@@ -136,6 +136,38 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
+// Non-suspending probe of a phase (mbarrier.test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// wait_bar by polling: for hand-offs on a kernel's critical path, where the
+// wake-up latency of a suspended wait would idle the tensor core.  Bounded
+// the same way (abort flag and time limit, checked every 256 probes).
+__device__ __forceinline__ bool wait_bar_spin(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort = 1;
+        atomicOr(w.status, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // wait_bar for barriers that the peer CTA arrives on.
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const WaitCtl &w) {
   return wait_bar(bar, parity, w);
@@ -235,6 +267,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (tmem) [+]= A (tmem) * B (smem)^T, A M x 16 bf16 in tensor memory: lane i
+// holds row i, each 32-bit column a pair of consecutive K elements (the lower
+// K index in the low half).
+__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -346,6 +391,16 @@ __device__ __forceinline__ void tmem_reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
                  "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// 32 lanes x 2 consecutive columns of 32-bit (thread t gets its lane's two).
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
+}
+
+// 32 lanes x 1 column of 32-bit from a register (complete with tmem_st_wait).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r0) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r0) : "memory");
 }
 
 // 32 lanes x 32 consecutive columns of 32-bit from registers (the inverse of
