@@ -68,19 +68,15 @@ __host__ __device__ constexpr size_t smem_bytes() {
 }
 
 struct Unit {
-  int b, slot, m, n, kt0, kt1;
-  bool skip;
+  int slot, m, n, kt0, kt1;
 };
 
 // Unit u -> (slot, m-tile, n-tile, k range).  Inside a slot, tiles run in
 // groups of `group_m` m-tiles with m fastest, so the CTAs working at the
 // same time share B tiles (and A rows) through L2.
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g, int bm_rows, int bn) {
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
   Unit r;
   const int per_slot = g.m_tiles * g.n_tiles;
-  const int per_batch = g.slots * per_slot;
-  r.b = u / per_batch;
-  u -= r.b * per_batch;
   r.slot = u / per_slot;
   const int t = u - r.slot * per_slot;
   const int per_group = g.group_m * g.n_tiles;
@@ -92,22 +88,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g, int bm_row
   r.n = in / gm;
   r.kt0 = r.slot * g.kt_per_slot;
   r.kt1 = min(g.kt_total, r.kt0 + g.kt_per_slot);
-  r.skip = false;
-  if (g.causal == 1) {
-    // output columns are keys: a tile entirely right of its last row's diagonal is masked
-    r.skip = static_cast<long long>(r.n) * bn >= static_cast<long long>(r.m + 1) * bm_rows;
-  } else if (g.causal == 2) {
-    // the K axis is keys: nothing past the tile's last row contributes
-    const int lim = ((r.m + 1) * bm_rows + BK - 1) / BK;
-    if (r.kt1 > lim) r.kt1 = lim;
-  }
   return r;
 }
 
 // K coordinate and third tensor-map coordinate of the k-tiles of one unit,
 // advanced one k-tile at a time (no division on the producer's path).  An
 // operand in mode 0 is [1][rows][K] (flat K), mode 1 [segments][rows][K per
-// segment], mode 2 [batch][rows][K] (third coordinate = batch index).
+// segment].
 struct KCursor {
   int k, z;         // current K element and third coordinate (segmented operands)
   int kflat;        // current K element of the virtual axis
@@ -126,9 +113,9 @@ struct KCursor {
       ++z;
     }
   }
-  __device__ __forceinline__ void coords(int mode, int b, int &kc, int &zc) const {
+  __device__ __forceinline__ void coords(int mode, int &kc, int &zc) const {
     kc = mode == 1 ? k : kflat;
-    zc = mode == 1 ? z : (mode == 2 ? b : 0);
+    zc = mode == 1 ? z : 0;
   }
 };
 
@@ -200,7 +187,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     tmem_ld_wait();
     const int feat = row0 + row_in_tile;
     if (feat < g.rows_valid) {
-      float *out = static_cast<float *>(g.out) + t.b * g.batch_stride_out + t.slot * g.slot_stride + feat;
+      float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride + feat;
 #pragma unroll
       for (int j = 0; j < BN; ++j)
         if (j < g.cols_valid) out[j * g.ld_out] = __uint_as_float(r[j]);
@@ -208,7 +195,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
   } else if constexpr (EPI == EPI_F32) {
     const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
-    float *out = static_cast<float *>(g.out) + t.b * g.batch_stride_out + t.slot * g.slot_stride +
+    float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
                  static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -230,7 +217,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const long long col0 = static_cast<long long>(t.n) * HALF;
     const long long shard = col0 / g.shard_cols;
     const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + t.b * g.batch_stride_out + shard * g.shard_stride +
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
                          static_cast<long long>(row) * g.ld_out + lc;
 #pragma unroll 1
     for (int c = 0; c < HALF / 32; ++c) {
@@ -252,7 +239,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * HALF;
     const long long shard = col0 / g.shard_cols;
-    const long long off = t.b * g.batch_stride_out + shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
+    const long long off = shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
                           (col0 - shard * g.shard_cols);
 #pragma unroll 1
     for (int c = 0; c < HALF / 32; ++c) {
@@ -276,7 +263,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const bool valid = row < g.rows_valid;
     const long long col0 = static_cast<long long>(t.n) * BN;
     const long long shard = col0 / g.shard_cols;
-    const long long off = t.b * g.batch_stride_out + shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
+    const long long off = shard * g.shard_stride + static_cast<long long>(row) * g.ld_out +
                           (col0 - shard * g.shard_cols);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -344,7 +331,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const long long col0 = static_cast<long long>(t.n) * BN;
     const long long shard = col0 / g.shard_cols;
     const long long lc = col0 - shard * g.shard_cols;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + t.b * g.batch_stride_out + shard * g.shard_stride +
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(g.out) + shard * g.shard_stride +
                          static_cast<long long>(row) * g.ld_out + lc;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -415,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = (g.batch > 0 ? g.batch : 1) * g.slots * g.m_tiles * g.n_tiles;
+  const int units = g.slots * g.m_tiles * g.n_tiles;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -424,8 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g, BM, BN);
-        if (t.skip) continue;
+        const Unit t = decode_unit(u, g);
         KCursor kc;
         kc.start(t.kt0, g);
         for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
@@ -436,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           int ak, az, bk, bz;
-          kc.coords(g.a_seg, t.b, ak, az);
-          kc.coords(g.b_seg, t.b, bk, bz);
+          kc.coords(g.a_seg, ak, az);
+          kc.coords(g.b_seg, bk, bz);
           tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
           tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
           issued |= 1u << stage;
@@ -464,8 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so that the timeout path runs with copies in flight.
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, g, BM, BN);
-        if (t.skip) continue;
+        const Unit t = decode_unit(u, g);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -505,8 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit t = decode_unit(u, g, BM, BN);
-      if (t.skip) continue;
+      const Unit t = decode_unit(u, g);
       const bool ok = wait_bar(tfull_bar(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -617,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = (g.batch > 0 ? g.batch : 1) * g.slots * g.m_tiles * g.n_tiles;
+  const int units = g.slots * g.m_tiles * g.n_tiles;
   const int cluster_id = static_cast<int>(blockIdx.x >> 1);
   const int nclusters = static_cast<int>(gridDim.x >> 1);
 
@@ -629,8 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       const bool leader = rank == 0;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g, 256, BN);
-        if (t.skip) continue;
+        const Unit t = decode_unit(u, g);
         const int arow = t.m * 256 + 128 * static_cast<int>(rank);
         const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
         KCursor kc;
@@ -641,8 +624,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           int ak, az, bk, bz;
-          kc.coords(g.a_seg, t.b, ak, az);
-          kc.coords(g.b_seg, t.b, bk, bz);
+          kc.coords(g.a_seg, ak, az);
+          kc.coords(g.b_seg, bk, bz);
           if (leader) {
             const uint32_t fb = full_bar(stage);
             mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_BYTES));
@@ -680,8 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
       for (int u = cluster_id; u < units && ok; u += nclusters) {
-        const Unit t = decode_unit(u, g, 256, BN);
-        if (t.skip) continue;
+        const Unit t = decode_unit(u, g);
         if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -720,8 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < units; u += nclusters) {
-      const Unit t = decode_unit(u, g, 256, BN);
-      if (t.skip) continue;
+      const Unit t = decode_unit(u, g);
       const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();

@@ -35,13 +35,12 @@ enum Epi : int {
 constexpr int kSwigluGranule = 128;
 
 // Work description of one tensor-core GEMM launch: D[m][n] = sum_k A[m][k] B[n][k]
-// over units (batch, slot, m-tile, n-tile).  The virtual K axis is `kt_total` tiles
+// over units (slot, m-tile, n-tile).  The virtual K axis is `kt_total` tiles
 // of 64, made of segments (shards) of `kt_per_seg` tiles.  A segmented
 // operand (a_seg / b_seg = 1) is a 3-D tensor map [segments][rows][K per
 // segment] and k-tile kt reads coordinate (kt % kt_per_seg * 64, row,
 // kt / kt_per_seg); a flat operand (0) is [1][rows][K] and reads (kt * 64,
-// row, 0); a batched operand (2) is [batch][rows][K] and reads (kt * 64,
-// row, batch index).  Slot s covers k-tiles [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
+// row, 0).  Slot s covers k-tiles [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
 struct GemmArgs {
   int m_tiles, n_tiles, slots;
   int kt_total, kt_per_seg, kt_per_slot;
@@ -58,10 +57,6 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
   void *out2, *out3;        // extra outputs of the training epilogues (same layout as out)
   const void *aux, *aux2;   // saved activations read by the backward epilogues (same layout)
-  int batch;                // independent GEMMs (operand mode 2 indexes them); 0 or 1 = one
-  long long batch_stride_out;  // elements between the batches' outputs
-  int causal;               // 1: skip tiles whose columns (keys) all lie past the tile's last row;
-                            // 2: stop the K loop (keys) at the tile's last row
   int head_dim;             // EPI_QKV_HEADS_BF16: columns per head
   int n_heads;              // EPI_QKV_HEADS_BF16: heads over all shards
 };
@@ -145,11 +140,6 @@ cudaError_t launch_all_gather(const void *const *parts, int T, long long nb_byte
 cudaError_t launch_shard_sum_bf16(const float *const *parts, int T, long long n, void *Z, int num_sms,
                                   cudaStream_t stream);
 
-// P[b][r][c] = softmax over keys c of scale * S[b][r][c] (causal: c <= r),
-// bf16, zero past the allowed keys up to ldp columns.
-cudaError_t launch_softmax_rows(const float *S, long long lds, long long s_batch, void *P, long long ldp,
-                                long long p_batch, int M, int heads, int causal, float scale,
-                                cudaStream_t stream);
 // h = x + z (x bf16, z float32) -> h float32 and hb = bf16(h).
 cudaError_t launch_residual(const void *x, const float *z, float *h, void *hb, long long n, int num_sms,
                             cudaStream_t stream);

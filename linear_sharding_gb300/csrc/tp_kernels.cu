@@ -188,71 +188,7 @@ __global__ void shard_sum_bf16_scalar(const PartList L, int T, long long first, 
   }
 }
 
-// ---- attention core and residual stream ------------------------------------------
-
-// Row r of head b: P = softmax(scale * S) over the keys c <= r (causal) or
-// c < M.  P is written (zero past the allowed keys) up to `wend` columns: all
-// of ldp, or, when causal, up to the next multiple of 256 past r, which is as
-// far as the P V GEMM's K loop reads for this row.  One CTA per row, 16-byte
-// loads of S, 8-byte stores of P.
-__global__ void __launch_bounds__(256) softmax_rows_kernel(const float *S, long long lds, long long s_batch,
-                                                           __nv_bfloat16 *P, long long ldp, long long p_batch,
-                                                           int M, int causal, float scale) {
-  __shared__ float red[8];
-  const int r = blockIdx.x, b = blockIdx.y;
-  const long long n = causal ? static_cast<long long>(r) + 1 : M;
-  long long wend = ldp;
-  if (causal) {
-    const long long lim = (n + 255) / 256 * 256;
-    if (lim < wend) wend = lim;
-  }
-  const float *row = S + b * s_batch + static_cast<long long>(r) * lds;
-  __nv_bfloat16 *prow = P + b * p_batch + static_cast<long long>(r) * ldp;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const long long n4 = n / 4;
-  const float4 *row4 = reinterpret_cast<const float4 *>(row);
-  float mx = -INFINITY;
-  for (long long c = threadIdx.x; c < n4; c += blockDim.x) {
-    const float4 v = row4[c];
-    mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-  }
-  for (long long c = n4 * 4 + threadIdx.x; c < n; c += blockDim.x) mx = fmaxf(mx, row[c]);
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[wid] = mx;
-  __syncthreads();
-  mx = red[0];
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
-  mx *= scale;
-  __syncthreads();
-  float sum = 0.f;
-  for (long long c = threadIdx.x; c < n4; c += blockDim.x) {
-    const float4 v = row4[c];
-    sum += __expf(v.x * scale - mx) + __expf(v.y * scale - mx) + __expf(v.z * scale - mx) +
-           __expf(v.w * scale - mx);
-  }
-  for (long long c = n4 * 4 + threadIdx.x; c < n; c += blockDim.x) sum += __expf(row[c] * scale - mx);
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) red[wid] = sum;
-  __syncthreads();
-  sum = 0.f;
-  for (int i = 0; i < 8; ++i) sum += red[i];
-  const float inv = 1.0f / sum;
-  const long long w4 = wend / 4;  // wend and ldp are multiples of 4
-  uint2 *prow4 = reinterpret_cast<uint2 *>(prow);
-  for (long long c = threadIdx.x; c < w4; c += blockDim.x) {
-    float e[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const long long col = 4 * c + k;
-      e[k] = col < n ? __expf(row[col] * scale - mx) * inv : 0.0f;
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(e[0], e[1]), hi = __floats2bfloat162_rn(e[2], e[3]);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t *>(&lo);
-    pk.y = *reinterpret_cast<uint32_t *>(&hi);
-    prow4[c] = pk;
-  }
-}
+// ---- residual stream ----------------------------------------------------------------
 
 // h = x + z (x bf16, z float32) -> h float32 and its bf16 copy hb.
 __global__ void residual_kernel(const __nv_bfloat16 *x, const float *z, float *h, __nv_bfloat16 *hb,
@@ -542,16 +478,6 @@ cudaError_t launch_shard_sum_bf16(const float *const *parts, int T, long long n,
   if (n4 * 4 < n)
     shard_sum_bf16_scalar<<<grid_for(n - n4 * 4, threads, num_sms, 8), threads, 0, stream>>>(
         L, T, n4 * 4, n, z);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_softmax_rows(const float *S, long long lds, long long s_batch, void *P, long long ldp,
-                                long long p_batch, int M, int heads, int causal, float scale,
-                                cudaStream_t stream) {
-  if (M <= 0 || heads <= 0) return cudaSuccess;
-  if (heads > 65535) return cudaErrorInvalidValue;
-  softmax_rows_kernel<<<dim3(M, heads), 256, 0, stream>>>(S, lds, s_batch, static_cast<__nv_bfloat16 *>(P),
-                                                          ldp, p_batch, M, causal, scale);
   return cudaGetLastError();
 }
 
