@@ -3,34 +3,37 @@
 // block": heads are sharded across ranks, so each head's attention is local
 // to the shard that owns it and needs no communication).
 //
-// One CTA per SM walks units (head, 128-query tile) and computes, for each
-// query row r of the tile,
+// One CTA per SM walks units (head, pair of adjacent 128-query tiles A and B)
+// and computes, for each query row r,
 //   O[r] = sum_{j allowed} 2^(t_rj - m_r) v_j / sum_{j allowed} 2^(t_rj - m_r),
 //   t_rj = (q_r . k_j / sqrt(128)) log2(e),
 // which is the softmax-weighted sum of the values for any shift m_r.  Keys
 // are visited 128 at a time and neither scores nor probabilities leave the
 // SM, or even reach shared memory:
-//   warp 0      TMA producer: the Q tile once per unit; K and V^T tiles of
-//               128 keys through two 3-deep rings, keys one tile ahead of
-//               values (S needs only K, P V only V);
-//   warp 1      TMEM allocation; one thread issues S_j = Q K_j^T (128 x 128,
-//               K = 128, both operands in shared memory) into one of three
-//               TMEM buffers and, once the softmax threads have overwritten
-//               that buffer's first 64 columns with P_j (bf16 pairs),
-//               O += P_j V_j with P_j read from TMEM (128 x 128, K = 128 keys)
-//               into the output accumulator, also in TMEM;
-//   warps 2..5  one thread per query row (TMEM lane = row): the row of S_j
-//               into registers, its maximum, P_j = 2^(t - m_r) rounded to
-//               bf16 back into TMEM, and the row sum of those rounded weights.
-// The shift m_r is raised only when a tile's maximum exceeds it by more than
-// 8 (so P <= 2^8): then the row's sum and its accumulator are scaled by
-// 2^(m_old - m_new) once the previous P V has completed.  After the first
-// tiles this is rare, so the accumulator normally stays with the tensor core.
+//   warp 0      TMA producer: both Q tiles once per unit; K and V^T tiles of
+//               128 keys (shared by the two query tiles) through a 3-deep and
+//               a 2-deep ring, keys one tile ahead of values;
+//   warp 1      TMEM allocation; one thread issues, per key tile j,
+//               O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
+//               S_B = Q_B K_{j+1}^T (tcgen05, 128 x 128, K = 128; P read from
+//               TMEM, the rest from shared memory), so the tensor core works
+//               on one tile while the other tile's probabilities are made;
+//   warps 2..5  softmax of tile A, warps 6..9 of tile B: one thread per query
+//               row (TMEM lane = row) reads the row of S into registers, takes
+//               its maximum, writes P = 2^(t - m_r) as bf16 over the upper 64
+//               columns of the same TMEM buffer, and adds the rounded weights
+//               to the row sum.
+// Each query tile has one S/P buffer: the next S into it is issued after the
+// P V that reads it, and tcgen05 MMAs of one thread run in issue order.  The
+// shift m_r is raised only when a tile's maximum exceeds it by more than 8 (so
+// P <= 2^8): then the row's sum and its accumulator are scaled by
+// 2^(m_old - m_new).  The previous P V is complete at that point, because the
+// commit that signalled this S covers every MMA issued before it.
 // Units run heaviest first (causal: the last query tiles) and are dealt to
 // the CTAs in snake order, so CTA loads stay even.  Waits poll (the S ->
-// softmax -> P V round trip is on the critical path, and a suspended wait
-// wakes too late) and are bounded like the GEMM's; on a timeout the CTA
-// drains what it issued and reports through the status word.
+// softmax -> P V hand-off is on the critical path, and a suspended wait wakes
+// too late) and are bounded like the GEMM's; on a timeout the CTA drains what
+// it issued and reports through the status word.
 #include <cuda_bf16.h>
 
 #include "tp_device.cuh"
@@ -39,35 +42,42 @@
 namespace tp {
 namespace {
 
-constexpr int kTile = 128;                // queries per unit, keys per step
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kTile = 128;                // queries per tile, keys per step
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 128;      // per query tile
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
 constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
-constexpr int kSbuf = 3;                  // S / P buffers in TMEM
-constexpr int kKst = 3, kVst = 3;         // K and V^T tiles in shared memory
+constexpr int kKst = 3, kVst = 2;         // K and V^T tiles in shared memory
 constexpr int kBars = 28;
 constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
-// Q | K[kKst] | Vt[kVst] | barriers
-constexpr size_t kSmemBytes = 1024 + (1 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
+// Q[2] | K[kKst] | Vt[kVst] | barriers
+constexpr size_t kSmemBytes = 1024 + (2 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "attention tiles exceed the shared memory of one CTA");
 
-// TMEM columns: S/P buffers 0..383 (128 each), O 384..511
-constexpr uint32_t kOcol = kSbuf * 128;
+// TMEM columns: S/P of tile A 0..127, of tile B 128..255, O_A 256..383, O_B 384..511
+constexpr uint32_t kOcol = 256;
 
 struct AttnUnit {
-  int head, mt, nkt;  // head, query tile, key tiles to visit
+  int head;
+  int mt[2];   // query tiles A and B (B = -1 when the last pair has one tile)
+  int nkt[2];  // key tiles each one visits (0 for an absent tile)
+  int nk;      // key tiles the unit visits: max(nkt)
 };
 
 // k-th unit of CTA b among G CTAs: snake order over the heaviest-first list.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? G - 1 - b : b); }
 
 __device__ __forceinline__ AttnUnit decode(int u, const AttnArgs &a) {
+  const int pairs = (a.m_tiles + 1) / 2;
   AttnUnit t;
-  t.mt = a.m_tiles - 1 - u / a.heads;
+  const int p = pairs - 1 - u / a.heads;
   t.head = u % a.heads;
-  t.nkt = a.causal ? t.mt + 1 : a.m_tiles;
+  t.mt[0] = 2 * p;
+  t.mt[1] = 2 * p + 1 < a.m_tiles ? 2 * p + 1 : -1;
+  for (int w = 0; w < 2; ++w)
+    t.nkt[w] = t.mt[w] < 0 ? 0 : (a.causal ? t.mt[w] + 1 : a.m_tiles);
+  t.nk = t.nkt[0] > t.nkt[1] ? t.nkt[0] : t.nkt[1];
   return t;
 }
 
@@ -88,6 +98,8 @@ struct Ring {
   }
 };
 
+// 320 threads: the 10 warps leave 3 on two of the 4 SM sub-partitions, whose 16K registers
+// each then cap a thread at 168
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                     const __grid_constant__ CUtensorMap mapVt, const AttnArgs a) {
@@ -95,8 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem;
-  uint8_t *sK = sQ + kTileBytes;
+  uint8_t *sQ = smem;                  // 2 tiles
+  uint8_t *sK = sQ + 2 * kTileBytes;
   uint8_t *sV = sK + kKst * kTileBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sV + kVst * kTileBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
@@ -107,15 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto k_full = [&](int s) { return b0 + 16 + 8u * s; };    // kKst
   auto k_empty = [&](int s) { return b0 + 40 + 8u * s; };   // kKst
   auto v_full = [&](int s) { return b0 + 64 + 8u * s; };    // kVst
-  auto v_empty = [&](int s) { return b0 + 88 + 8u * s; };   // kVst
-  auto s_full = [&](int s) { return b0 + 112 + 8u * s; };   // S_j computed (kSbuf)
-  // the P V that read P from it is done; as each commit covers every earlier MMA, also
-  // "all P V products up to that one are in O" (kSbuf)
-  auto s_empty = [&](int s) { return b0 + 136 + 8u * s; };
-  auto p_full = [&](int s) { return b0 + 160 + 8u * s; };   // P_j written over S_j (kSbuf)
-  const uint32_t o_free = b0 + 184;   // one phase per unit: the accumulator has been read out
-  const uint32_t drain = b0 + 192, never = b0 + 200;
-  static_assert(kKst <= 3 && kVst <= 3 && kSbuf <= 3 && 26 <= kBars, "barrier layout");
+  auto v_empty = [&](int s) { return b0 + 80 + 8u * s; };   // kVst
+  auto s_full = [&](int w) { return b0 + 96 + 8u * w; };    // S of tile w computed
+  auto p_full = [&](int w) { return b0 + 112 + 8u * w; };   // P of tile w written over its S
+  auto o_full = [&](int w) { return b0 + 128 + 8u * w; };   // tile w's last P V of the unit done
+  auto o_free = [&](int w) { return b0 + 144 + 8u * w; };   // tile w's O read out
+  const uint32_t drain = b0 + 160, never = b0 + 168;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -129,12 +138,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int s = 0; s < kSbuf; ++s) {
-      mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 1);
-      mbar_init(p_full(s), kSoftmaxThreads);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(s_full(w), 1);
+      mbar_init(p_full(w), kSoftmaxThreads);
+      mbar_init(o_full(w), 1);
+      mbar_init(o_free(w), kSoftmaxThreads);
     }
-    mbar_init(o_free, kSoftmaxThreads);
     mbar_init(drain, 1);
     mbar_init(never, 1);
     *abort_flag = 0;
@@ -154,14 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{abort_flag, a.status, a.wait_limit_ns};
-  const int units = a.heads * a.m_tiles;
+  const int units = a.heads * ((a.m_tiles + 1) / 2);
   const int G = gridDim.x, b = blockIdx.x;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer ----
-      // Loads per unit, in order: Q, K_0, then for each j: K_{j+1} (if any), V_j.
-      int kc = 0, vc = 0, qc = 0;  // K, V tiles and Q tiles issued so far
+      // Loads per unit, in order: Q_A and Q_B, K_0, then for each j: K_{j+1} (if any), V_j.
+      int kc = 0, vc = 0, qc = 0;  // K, V tiles and Q pairs issued so far
       Ring kr, vr;
       bool ok = true;
       auto load_k = [&](const AttnUnit &t, int j) -> bool {
@@ -189,13 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
         if (!wait_bar_spin(q_empty, (qc & 1u) ^ 1u, w)) break;
-        mbar_arrive_expect_tx(q_full, kTileBytes);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
+        mbar_arrive_expect_tx(q_full, (t.mt[1] >= 0 ? 2 : 1) * kTileBytes);
+        for (int q = 0; q < 2; ++q) {
+          if (t.mt[q] < 0) continue;
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_3d(smem_u32(sQ + q * kTileBytes + kb * kSub), &mapQ, q_full, kb * 64, t.mt[q] * kTile,
+                        t.head);
+        }
         ++qc;
         if (!load_k(t, 0)) break;
-        for (int j = 0; j < t.nkt; ++j) {
-          if (j + 1 < t.nkt && !load_k(t, j + 1)) {
+        for (int j = 0; j < t.nk; ++j) {
+          if (j + 1 < t.nk && !load_k(t, j + 1)) {
             ok = false;
             break;
           }
@@ -221,26 +234,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer ----
-      int uc = 0;           // units started
-      Ring kr, vr, sr, pr;  // K tile and S buffer of the next S; V tile and S buffer of the next P V
+      int uc = 0;                            // units started
+      Ring kr, vr;                           // K tile of the next S, V tile of the next P V
+      uint32_t sph[2] = {0u, 0u};            // phase of tile q's next p_full wait
+      uint32_t ofp[2] = {0u, 0u};            // units tile q took part in (o_free phases)
       bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_spin(never, 0u, w);
-      auto issue_s = [&]() -> bool {
-        // S = Q K^T over head_dim 128: two 64-wide sub-tiles x four K = 16 steps
-        if (!wait_bar_spin(k_full(kr.buf), kr.phase, w) || !wait_bar_spin(s_empty(sr.buf), sr.phase ^ 1u, w))
-          return false;
-        tc_fence_after();
-        const uint32_t d = tmem + sr.buf * 128;
+      auto issue_s = [&](int q, const uint32_t kbase) {
+        // S_q = Q_q K^T over head_dim 128: two 64-wide sub-tiles x four K = 16 steps
+        const uint32_t d = tmem + q * 128;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + kb * kSub));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sK + kr.buf * kTileBytes + kb * kSub));
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + q * kTileBytes + kb * kSub));
+          const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
 #pragma unroll
           for (int k = 0; k < 4; ++k) tc_mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) ? 1u : 0u);
         }
-        tc_commit(s_full(sr.buf));
+        tc_commit(s_full(q));
+      };
+      // S of both tiles for key tile j (tiles that visit it), then release K_j
+      auto issue_s_pair = [&](const AttnUnit &t, int j) -> bool {
+        if (!wait_bar_spin(k_full(kr.buf), kr.phase, w)) return false;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
+        for (int q = 0; q < 2; ++q)
+          if (j < t.nkt[q]) issue_s(q, kbase);
         tc_commit(k_empty(kr.buf));
         kr.next(kKst);
-        sr.next(kSbuf);
         return true;
       };
       for (int k = 0; ok; ++k) {
@@ -249,48 +268,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         const AttnUnit t = decode(u, a);
         if (!wait_bar_spin(q_full, uc & 1u, w)) break;
         tc_fence_after();
-        if (!issue_s()) break;
-        for (int j = 0; j < t.nkt; ++j) {
-          if (j + 1 < t.nkt) {
-            if (!issue_s()) {
-              ok = false;
-              break;
-            }
-          } else {
-            tc_commit(q_empty);  // every S of this unit is issued: Q may be replaced
-          }
-          // O += P_j V_j once the softmax threads have written P_j over S_j (and, for the
-          // first key tile, read out the previous unit's O)
-          if (!wait_bar_spin(p_full(pr.buf), pr.phase, w) || !wait_bar_spin(v_full(vr.buf), vr.phase, w) ||
-              (j == 0 && !wait_bar_spin(o_free, (uc & 1u) ^ 1u, w))) {
+        if (!issue_s_pair(t, 0)) break;
+        if (t.nk == 1) tc_commit(q_empty);
+        for (int j = 0; j < t.nk && ok; ++j) {
+          if (!wait_bar_spin(v_full(vr.buf), vr.phase, w)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t pa = tmem + pr.buf * 128;  // P: 64 columns of bf16 pairs
+          const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
+          bool k_next_ready = false;
+          for (int q = 0; q < 2 && ok; ++q) {
+            if (j >= t.nkt[q]) continue;
+            // O_q += P_q V_j once the softmax threads have written P_q (and, for the unit's
+            // first key tile, read out the previous unit's O_q)
+            if (!wait_bar_spin(p_full(q), sph[q], w) || (j == 0 && !wait_bar_spin(o_free(q), ofp[q] ^ 1u, w))) {
+              ok = false;
+              break;
+            }
+            sph[q] ^= 1u;
+            tc_fence_after();
+            const uint32_t pa = tmem + q * 128 + 64;  // P: the upper 64 columns, bf16 pairs
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = sw128_kmajor_desc(smem_u32(sV + vr.buf * kTileBytes + (kk >> 2) * kSub));
-            tc_mma_bf16_tmem_a(tmem + kOcol, pa + 8u * kk, bd + 2u * (kk & 3), IDESC, (j | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bd = sw128_kmajor_desc(vbase + (kk >> 2) * kSub);
+              tc_mma_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, bd + 2u * (kk & 3), IDESC, (j | kk) ? 1u : 0u);
+            }
+            if (j + 1 == t.nkt[q]) tc_commit(o_full(q));
+            // then this tile's S for key tile j + 1, so the other tile's P V overlaps its softmax
+            if (j + 1 < t.nkt[q]) {
+              if (!k_next_ready) {
+                if (!wait_bar_spin(k_full(kr.buf), kr.phase, w)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              issue_s(q, smem_u32(sK + kr.buf * kTileBytes));
+            }
           }
-          tc_commit(s_empty(pr.buf));
+          if (!ok) break;
           tc_commit(v_empty(vr.buf));
           vr.next(kVst);
-          pr.next(kSbuf);
+          if (k_next_ready) {
+            tc_commit(k_empty(kr.buf));
+            kr.next(kKst);
+          }
+          if (j + 2 == t.nk) tc_commit(q_empty);  // every S of this unit is issued
         }
         ++uc;
+        for (int q = 0; q < 2; ++q)
+          if (t.nkt[q] > 0) ofp[q] ^= 1u;
       }
       tc_commit(drain);
       drain_bar(drain, 0u, a.status);
     }
     __syncwarp();
   } else {
-    // ---- softmax and output (warp w reads TMEM lanes 32 (w % 4) .. + 31) ----
+    // ---- softmax and output: warps 2..5 tile A, 6..9 tile B (warp v reads TMEM lanes
+    // 32 (v % 4) .. + 31) ----
+    const int q = (warp - 2) >> 2;
     const int row_in_tile = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ob = tmem + lane_base + kOcol;
+    const uint32_t sb = tmem + lane_base + q * 128;
+    const uint32_t ob = tmem + lane_base + kOcol + q * 128;
     const float c = a.scale_log2;
-    Ring sr, prv;  // S / P buffer of the current key tile, of the previous one
+    uint32_t sph = 0, uc = 0;  // phase of the next s_full wait; units this tile took part in
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool got = wait_bar_spin(bar, parity, w);
@@ -300,79 +343,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_of(k, b, G);
       if (u >= units) break;
       const AttnUnit t = decode(u, a);
-      const int row = t.mt * kTile + row_in_tile;
+      if (t.nkt[q] == 0) continue;  // the last pair's missing tile B
+      const int row = t.mt[q] * kTile + row_in_tile;
       float m_used = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < t.nkt; prv = sr, ++j, sr.next(kSbuf)) {
-        if (!wait_all(s_full(sr.buf), sr.phase)) {
+      for (int j = 0; j < t.nkt[q]; ++j) {
+        if (!wait_all(s_full(q), sph)) {
           ok = false;
           break;
         }
+        sph ^= 1u;
         tc_fence_after();
-        // the row of S_j: 128 scores in registers
-        uint32_t s[4][32];
-        const uint32_t sb = tmem + lane_base + sr.buf * 128;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(sb + cc * 32, s[cc]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_reg_fence(s[cc]);
         // allowed keys of this tile: key0 + i for i <= kmax (causal: key <= row; always key < M)
         const int key0 = j * kTile;
         int kmax = a.M - 1 - key0;
         if (a.causal && row - key0 < kmax) kmax = row - key0;
-        if (kmax < kTile - 1) {
+        const bool masked = kmax < kTile - 1;
+        // the row of S_j in two halves of 64 scores (registers for one half at a time):
+        // first its maximum, then the weights
+        uint32_t s[2][32];
+        auto load_half = [&](int hh) {
+          tmem_ld32(sb + hh * 64, s[0]);
+          tmem_ld32(sb + hh * 64 + 32, s[1]);
+          tmem_ld_wait();
+          tmem_reg_fence(s[0]);
+          tmem_reg_fence(s[1]);
+          if (masked) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
-        }
+              for (int i = 0; i < 32; ++i)
+                if (hh * 64 + cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
+          }
+        };
         // row maximum: eight independent chains
         float mx8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float m = __uint_as_float(s[q >> 1][(q & 1) * 16]);
+        for (int hh = 0; hh < 2; ++hh) {
+          load_half(hh);
 #pragma unroll
-          for (int i = 1; i < 16; ++i) m = fmaxf(m, __uint_as_float(s[q >> 1][(q & 1) * 16 + i]));
-          mx8[q] = m;
+          for (int g4 = 0; g4 < 4; ++g4) {
+            float m = hh ? mx8[g4] : __uint_as_float(s[g4 >> 1][(g4 & 1) * 16]);
+#pragma unroll
+            for (int i = hh ? 0 : 1; i < 16; ++i) m = fmaxf(m, __uint_as_float(s[g4 >> 1][(g4 & 1) * 16 + i]));
+            mx8[g4] = m;
+          }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
         const float m_tile = mx * c;
         const bool raise = m_tile > m_used + kRescaleGap;
         const float m_new = raise ? m_tile : m_used;
         const float alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
         m_used = m_new;
-        // P = 2^(t - m) as bf16 pairs over the first 64 columns of the S buffer.  The row
-        // sum adds the rounded weights the P V product uses, so each output is a convex
-        // combination of the values (the rounding of P cancels in it).
+        // P = 2^(t - m) as bf16 pairs over the upper 64 columns of the S buffer: keys 64 hh ..
+        // 64 hh + 63 into columns 64 + 32 hh ..  The upper half of S is still in registers, so
+        // it goes first (into columns 96..127), then the lower half is read again (into
+        // 64..95, whose scores are used by then).  The row sum adds the rounded weights the
+        // P V product uses, so each output is a convex combination of the values (the
+        // rounding of P cancels in it).
         float sum8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sum8[q] = 0.f;
+        for (int g8 = 0; g8 < 8; ++g8) sum8[g8] = 0.f;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];  // keys 64 hh .. 64 hh + 63
+        for (int hh = 1; hh >= 0; --hh) {
+          if (hh == 0) load_half(0);
+          uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = 64 * hh + 2 * i;
-            pk[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(s[key >> 5][key & 31]), c, -m_new)),
-                                ex2_approx(fmaf(__uint_as_float(s[key >> 5][(key & 31) + 1]), c, -m_new)));
+            pk[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(s[i >> 4][(2 * i) & 31]), c, -m_new)),
+                                ex2_approx(fmaf(__uint_as_float(s[i >> 4][(2 * i + 1) & 31]), c, -m_new)));
             sum8[(2 * i) & 7] += __uint_as_float(pk[i] << 16);
             sum8[(2 * i + 1) & 7] += __uint_as_float(pk[i] & 0xFFFF0000u);
           }
-          tmem_st32(sb + hh * 32, pk);
+          tmem_st32(sb + 64 + hh * 32, pk);
         }
         const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         l_run = fmaf(l_run, alpha, sum);
-        // a raised shift also scales the accumulated O, once the previous P V is in it.  The
-        // P V before that in the same buffer is done (S_{j-1} was computed into the buffer
-        // after it), so the parity wait below names the current or the preceding phase.
+        // a raised shift also scales the accumulated O; the previous P V is already in it
+        // (the commit that signalled this S covered it)
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          if (!wait_all(s_empty(prv.buf), prv.phase)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t r[32];
@@ -386,11 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(sr.buf));
+        mbar_arrive(p_full(q));
       }
       if (!ok) break;
-      // read out O / l once the unit's last P V (and so every earlier one) is done
-      if (!wait_all(s_empty(prv.buf), prv.phase)) break;
+      // read out O / l once this tile's last P V of the unit is done
+      if (!wait_all(o_full(q), uc & 1u)) break;
+      ++uc;
       tc_fence_after();
       const float inv = 1.0f / l_run;
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.O) + static_cast<long long>(row) * a.ldo +
@@ -403,16 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_reg_fence(r);
         if (row < a.M) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[cc * 4 + q] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
+          for (int g4 = 0; g4 < 4; ++g4)
+            dst[cc * 4 + g4] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * g4]) * inv, __uint_as_float(r[8 * g4 + 1]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * inv, __uint_as_float(r[8 * g4 + 3]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * inv, __uint_as_float(r[8 * g4 + 5]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * inv, __uint_as_float(r[8 * g4 + 7]) * inv));
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free);
+      mbar_arrive(o_free(q));
     }
   }
 
@@ -431,7 +480,7 @@ cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, c
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(args.heads) * args.m_tiles;
+  const long long units = static_cast<long long>(args.heads) * ((args.m_tiles + 1) / 2);
   if (units <= 0) return cudaSuccess;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapQ, mapK, mapVt, args);
