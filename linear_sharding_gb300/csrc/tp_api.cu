@@ -243,10 +243,30 @@ GemmCfg cfg_for(int bn) { return bn == 256 ? CFG_N256 : CFG_N128; }
 // (cta_group::2): half the B-tile traffic per SM and a deeper stage ring.
 bool use_pair(int bn, int64_t M) { return bn == 256 && M > 128; }
 
+// A residual added to a row-parallel layer's output Z [M x H]: Z += add_f32 (float32)
+// and/or Z += add_bf16 (bf16), then, with out_bf16, out_bf16 = bf16(Z).  All null: none.
+struct Residual {
+  const float *add_f32 = nullptr;
+  const void *add_bf16 = nullptr;
+  void *out_bf16 = nullptr;
+  bool any() const { return add_f32 || add_bf16 || out_bf16; }
+};
+
+// The residual as separate elementwise kernels over Z (when it is not fused).
+tp_status_t apply_residual(const DevState *d, float *Z, int64_t n, const Residual &r, cudaStream_t st) {
+  if (r.add_bf16 || r.out_bf16) {
+    if (!r.add_bf16 || !r.out_bf16) return TP_ERR_ARG;
+    TP_CUDA(launch_residual(r.add_bf16, Z, Z, r.out_bf16, n, d->sms, st));
+  }
+  if (r.add_f32) TP_CUDA(launch_add_inplace(Z, r.add_f32, n, d->sms, st));
+  return TP_OK;
+}
+
 // Row-parallel GEMM over T shards into Z, with `slots` accumulation slots
-// (slots > 1: float32 partials in P, then the shard-sum).
+// (slots > 1: float32 partials in P, then the shard-sum).  A residual is fused
+// into the GEMM's epilogue with one slot, and applied after the shard-sum otherwise.
 tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &mapA, int a_seg,
-                      int64_t M, int slots, float *P, float *Z, cudaStream_t st) {
+                      int64_t M, int slots, float *P, float *Z, cudaStream_t st, const Residual &res = Residual()) {
   const int64_t H = s->H;
   const bool pair = use_pair(s->bn2, M);
   GemmArgs g = base_args(d);
@@ -263,11 +283,21 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
   g.out = slots > 1 ? static_cast<void *>(P) : static_cast<void *>(Z);
   g.ld_out = H;
   g.slot_stride = M * H;
+  Epi epi = EPI_F32;
+  if (slots == 1 && res.any()) {
+    epi = EPI_F32_RESID;
+    g.aux = res.add_f32;
+    g.aux2 = res.add_bf16;
+    g.out2 = res.out_bf16;
+  }
   if (pair)
-    TP_CUDA(launch_gemm(CFG_PAIR_N256, EPI_F32, mapA, s->map_w2_a, g, d->sms, st));
+    TP_CUDA(launch_gemm(CFG_PAIR_N256, epi, mapA, s->map_w2_a, g, d->sms, st));
   else
-    TP_CUDA(launch_gemm(cfg_for(s->bn2), EPI_F32, mapA, s->map_w2_b, g, d->sms, st));
-  if (slots > 1) TP_CUDA(launch_shard_sum_strided(P, slots, M * H, M * H, Z, d->sms, st));
+    TP_CUDA(launch_gemm(cfg_for(s->bn2), epi, mapA, s->map_w2_b, g, d->sms, st));
+  if (slots > 1) {
+    TP_CUDA(launch_shard_sum_strided(P, slots, M * H, M * H, Z, d->sms, st));
+    TP_TRY(apply_residual(d, Z, M * H, res, st));
+  }
   return TP_OK;
 }
 
@@ -407,13 +437,15 @@ tp_status_t colpar_any(const tp_shards *s, const DevState *d, const MlpPlan &p, 
 }
 
 tp_status_t rowpar_any(const tp_shards *s, const DevState *d, const MlpPlan &p, const void *Y,
-                       int64_t M, float *Z, char *ws_row, cudaStream_t st) {
+                       int64_t M, float *Z, char *ws_row, cudaStream_t st, const Residual &res = Residual()) {
   float *P = reinterpret_cast<float *>(ws_row);
-  if (p.simt) return rowpar_simt(s, d, p, Y, M, Z, P, st);
-  if (p.decode) return rowpar_decode(s, d, p, Y, M, Z, P, st);
+  if (p.simt || p.decode) {
+    TP_TRY(p.simt ? rowpar_simt(s, d, p, Y, M, Z, P, st) : rowpar_decode(s, d, p, Y, M, Z, P, st));
+    return apply_residual(d, Z, M * s->H, res, st);
+  }
   CUtensorMap my;
   TP_TRY(make_map(&my, Y, s->Fs, M, s->T, s->Fs * 2, M * s->Fs * 2, 128));
-  return rowpar_tc(s, d, my, 1, M, p.slots2, P, Z, st);
+  return rowpar_tc(s, d, my, 1, M, p.slots2, P, Z, st, res);
 }
 
 tp_status_t check_handle(const tp_shards *s, int kind, DevState **d) {
@@ -694,7 +726,8 @@ bool act_ok(const tp_shards *s, tp_act_t act) {
 }
 
 tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
-                             float *Z, void *workspace, size_t ws_bytes, cudaStream_t st) {
+                             float *Z, void *workspace, size_t ws_bytes, cudaStream_t st,
+                             const Residual &res = Residual()) {
   DevState *d = nullptr;
   TP_TRY(check_handle(s, 0, &d));
   if (M < 0 || !valid_variant(v) || !act_ok(s, act)) return TP_ERR_ARG;
@@ -709,7 +742,7 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
   char *ws_col = Y + round256(p.y_bytes);
   char *ws_row = ws_col + round256(p.col_bytes);
   TP_TRY(colpar_any(s, d, p, X, M, act, Y, ws_col, st));
-  return rowpar_any(s, d, p, Y, M, Z, ws_row, st);
+  return rowpar_any(s, d, p, Y, M, Z, ws_row, st, res);
 }
 
 // ---- one tensor-parallel transformer block ---------------------------------------
@@ -819,14 +852,18 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2;
   // 2.-5. causal attention per head, fused: O [M x H], heads side by side
   TP_TRY(attention_core_vt(d, Q, K, vt, M, nh, causal, O, H, st));
-  // 6. row-parallel output projection + all-reduce-sum #1 (into out), 7. residual
+  // 6. row-parallel output projection + all-reduce-sum #1, 7. residual: h = X + the sum,
+  //    hb = bf16(h) (fused into the GEMM's epilogue when it accumulates all shards in TMEM)
   CUtensorMap mo;
   TP_TRY(make_map(&mo, O, H, M, 1, H * 2, M * H * 2, 128));
-  TP_TRY(rowpar_tc(a, d, mo, 0, M, p.slots_o, opart, out, st));
-  TP_CUDA(launch_residual(X, out, h, hb, M * H, d->sms, st));
-  // 8. the MLP on the residual stream + all-reduce-sum #2, 9. residual
-  TP_TRY(mlp_forward_impl(m, hb, M, m->act, v, out, mws, p.mlp.total(), st));
-  TP_CUDA(launch_add_inplace(out, h, M * H, d->sms, st));
+  Residual r1;
+  r1.add_bf16 = X;
+  r1.out_bf16 = hb;
+  TP_TRY(rowpar_tc(a, d, mo, 0, M, p.slots_o, opart, h, st, r1));
+  // 8. the MLP on the residual stream + all-reduce-sum #2, 9. residual: out = h + the sum
+  Residual r2;
+  r2.add_f32 = h;
+  TP_TRY(mlp_forward_impl(m, hb, M, m->act, v, out, mws, p.mlp.total(), st, r2));
   return TP_OK;
 }
 

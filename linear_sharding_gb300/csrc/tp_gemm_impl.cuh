@@ -210,6 +210,57 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
     }
+  } else if constexpr (EPI == EPI_F32_RESID) {
+    const int row = row0 + row_in_tile;
+    const bool valid = row < g.rows_valid;
+    const long long off = static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
+    float *out = static_cast<float *>(g.out) + off;
+    const float *addf = static_cast<const float *>(g.aux);
+    const __nv_bfloat16 *addb = static_cast<const __nv_bfloat16 *>(g.aux2);
+    __nv_bfloat16 *outb = static_cast<__nv_bfloat16 *>(g.out2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tb + c * 32, r);
+      tmem_ld_wait();
+      if (!valid) continue;
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      if (addf) {
+        const float4 *a = reinterpret_cast<const float4 *>(addf + off + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 x = a[j];
+          v[4 * j] += x.x;
+          v[4 * j + 1] += x.y;
+          v[4 * j + 2] += x.z;
+          v[4 * j + 3] += x.w;
+        }
+      }
+      if (addb) {
+        const uint4 *a = reinterpret_cast<const uint4 *>(addb + off + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 x = a[j];
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * j + 2 * k] += __uint_as_float(w[k] << 16);
+            v[8 * j + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      }
+      float4 *d = reinterpret_cast<float4 *>(out + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if (outb) {
+        uint32_t vb[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vb[j] = __float_as_uint(v[j]);
+        store_act32<EPI_IDENT_BF16>(outb + off + c * 32, vb);
+      }
+    }
   } else if constexpr (EPI == EPI_SWIGLU_BF16) {
     constexpr int HALF = BN / 2;
     const int row = row0 + row_in_tile;

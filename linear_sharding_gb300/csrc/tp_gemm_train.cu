@@ -2,7 +2,8 @@
 // the training epilogues (the column-parallel GEMM that also keeps its
 // pre-activations for the backward pass; the backward GEMM dH = dZ W2^T with
 // the activation's derivative fused into its epilogue) and for the
-// transformer block's head-major QKV projection; plus the bf16 transpose
+// transformer block (the head-major QKV projection, and the row-parallel
+// projections with their residual adds fused); plus the bf16 transpose
 // that gives the weight-gradient and attention GEMMs K-major operands.
 #include "tp_gemm_impl.cuh"
 
@@ -21,6 +22,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_DGELU_BF16: return launch_pair<EPI_DGELU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_DSWIGLU_BF16: return launch_pair<EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_QKV_HEADS_BF16: return launch_pair<EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_RESID: return launch_pair<EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -33,6 +35,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_DSWIGLU_BF16: return launch_impl<256, EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_QKV_HEADS_BF16:
           return launch_impl<256, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_RESID: return launch_impl<256, EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -43,6 +46,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_DSWIGLU_BF16: return launch_impl<128, EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_QKV_HEADS_BF16:
           return launch_impl<128, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_RESID: return launch_impl<128, EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;

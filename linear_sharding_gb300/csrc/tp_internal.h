@@ -26,8 +26,10 @@ enum Epi : int {
   EPI_SWIGLU_SAVE_BF16 = 6,  // out = bf16(SiLU(g) u), out2 = bf16(g), out3 = bf16(u)
   EPI_DGELU_BF16 = 7,        // out = bf16(acc * GeLU'(aux)), aux = saved pre-activation
   EPI_DSWIGLU_BF16 = 8,      // out = bf16(acc u SiLU'(g)), out2 = bf16(acc SiLU(g)); aux = g, aux2 = u
-  EPI_QKV_HEADS_BF16 = 9     // out = bf16(acc) head-major: [3][n_heads][M][head_dim] (Q, K, V);
+  EPI_QKV_HEADS_BF16 = 9,    // out = bf16(acc) head-major: [3][n_heads][M][head_dim] (Q, K, V);
                              // with out2, V goes there transposed instead: [n_heads][head_dim][ld_out]
+  EPI_F32_RESID = 10         // one slot: out = acc (+ aux, float32) (+ aux2, bf16), same layout as out;
+                             // with out2, also out2 = bf16(out) (a residual add fused into the GEMM)
 };
 
 // Packed rows of a SwiGLU shard alternate 128 gate rows and 128 up rows, so
