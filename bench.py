@@ -433,6 +433,13 @@ def extras(args, tp, device, peaks, full: bool) -> dict:
         byts = 3 * H * F * 2 + M * H * (2 + 4)
         dec[f"M{M}"] = {"us": round(t * 1e6, 1), "GB/s": round(byts / t / 1e9, 1),
                         "frac_hbm": round(byts / t / 1e9 / hbm, 3)}
+        # the same step captured once into a CUDA graph and replayed (a decode loop's form)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            tp.tp_mlp_forward(s, X, "auto", Z, ws)
+        tg = _time_calls(graph.replay, 50)
+        dec[f"M{M}"].update({"graph_us": round(tg * 1e6, 1), "graph_frac_hbm": round(byts / tg / 1e9 / hbm, 3)})
+        del graph
     s.close()
     torch.cuda.empty_cache()
     out["decode_swiglu_h8192_f28672_t8"] = dec

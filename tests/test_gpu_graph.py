@@ -1,0 +1,50 @@
+"""The forward pass can be captured into a CUDA graph and replayed: with a
+caller-provided workspace, tp_mlp_forward only enqueues kernels on the
+current stream (no allocation, no synchronisation), so a decode loop can
+replay one captured step.  The replay must give the same bits as the eager
+call, also after the input buffer is refilled in place."""
+import numpy as np
+import pytest
+
+from synth import mlp_inputs
+from tests.gpu_util import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import linear_sharding_gb300 as tp
+    tp.load_library()
+    return tp
+
+
+@pytest.mark.parametrize("M,H,F,T,act,variant", [
+    (16, 1024, 4096, 4, "swiglu", "auto"),      # decode kernels (split-K, weights as the MMA's A)
+    (256, 1024, 4096, 4, "gelu", "tmem_acc"),   # CTA-pair prefill tiles
+    (256, 1024, 4096, 4, "gelu", "partials"),   # partials + shard-sum
+])
+def test_forward_replays_from_a_cuda_graph(tp, M, H, F, T, act, variant):
+    import torch
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=31, x_rows=max(M, 16))
+    d2 = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=32, x_rows=max(M, 16))
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    X, X2 = to_device(d["X"]), to_device(d2["X"])
+    ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, variant), 16), dtype=torch.uint8, device="cuda")
+    eager1 = tp.tp_mlp_forward(s, X, variant, None, ws).clone()
+    eager2 = tp.tp_mlp_forward(s, X2, variant, None, ws).clone()
+    torch.cuda.synchronize()
+    Xin = X.clone()
+    Z = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tp.tp_mlp_forward(s, Xin, variant, Z, ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Z, eager1)
+    Xin.copy_(X2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Z, eager2)
+    assert tp.tp_last_device_status() == 0
+    s.close()
