@@ -436,6 +436,17 @@ TP_API tp_status_t tp_last_device_status(void *stream);
  */
 TP_API tp_status_t tp_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * tp_inject_alloc_failures - failure injection for tests (the pages have no
+ * counterpart): the next `count` device allocations this library makes
+ * (workspaces it allocates itself, shard buffers, scratch of tp_shard_get)
+ * fail as if the device were out of memory.  The calls that needed them
+ * return TP_ERR_OOM and leave nothing allocated behind; later calls work
+ * again.  0 cancels pending failures; count < 0 -> TP_ERR_ARG.  Process-wide;
+ * no CUDA call is made.
+ */
+TP_API tp_status_t tp_inject_alloc_failures(int count);
+
 #ifdef __cplusplus
 }
 #endif

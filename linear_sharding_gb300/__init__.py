@@ -38,7 +38,7 @@ EXPORTS = (
     "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
     "tp_block_workspace_bytes", "tp_block_forward", "tp_attention_workspace_bytes",
-    "tp_attention_forward",
+    "tp_attention_forward", "tp_inject_alloc_failures",
 )
 
 _lock = threading.Lock()
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_partial_sum.argtypes = [ctypes.POINTER(vp), i32, i64, vp, vp]
         lib.tp_last_device_status.argtypes = [vp]
         lib.tp_set_wait_limit_ns.argtypes = [u64]
+        lib.tp_inject_alloc_failures.argtypes = [i32]
         lib.tp_colpar_workspace_bytes.restype = sz
         lib.tp_colpar_workspace_bytes.argtypes = [vp, i64]
         lib.tp_colpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
@@ -113,7 +114,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                      "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
                      "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16",
                      "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward",
-                     "tp_block_forward", "tp_attention_forward"):
+                     "tp_block_forward", "tp_attention_forward", "tp_inject_alloc_failures"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -460,3 +461,8 @@ def tp_last_device_status(stream=None) -> int:
 
 def tp_set_wait_limit_ns(ns: int) -> None:
     _check(load_library().tp_set_wait_limit_ns(int(ns)), "tp_set_wait_limit_ns")
+
+
+def tp_inject_alloc_failures(count: int) -> None:
+    """Make the library's next `count` device allocations fail (tests); 0 cancels."""
+    _check(load_library().tp_inject_alloc_failures(int(count)), "tp_inject_alloc_failures")

@@ -48,6 +48,27 @@ std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
+// Failure injection (tp_inject_alloc_failures): device allocations still to fail.
+std::atomic<int> g_fail_allocs{0};
+
+bool take_injected_failure() {
+  int n = g_fail_allocs.load();
+  while (n > 0)
+    if (g_fail_allocs.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
+
+// Every device allocation of the library goes through these two.
+cudaError_t lib_malloc(void **p, size_t bytes) {
+  if (take_injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, bytes);
+}
+
+cudaError_t lib_malloc_async(void **p, size_t bytes, cudaStream_t st) {
+  if (take_injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaMallocAsync(p, bytes, st);
+}
+
 tp_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return TP_OK;
   if (e == cudaErrorMemoryAllocation) return TP_ERR_OOM;
@@ -76,7 +97,7 @@ tp_status_t dev_state(DevState **out, int *dev_out = nullptr) {
       return TP_ERR_CUDA;
     if (major != 10 || minor != 3) return TP_ERR_ARCH;
     unsigned int *st = nullptr;
-    if (cudaMalloc(&st, 256) != cudaSuccess) return TP_ERR_OOM;
+    if (lib_malloc(reinterpret_cast<void **>(&st), 256) != cudaSuccess) return TP_ERR_OOM;
     if (cudaMemset(st, 0, 256) != cudaSuccess) {
       cudaFree(st);
       return TP_ERR_CUDA;
@@ -480,7 +501,7 @@ tp_status_t get_ws(Workspace *w, void *given, size_t given_bytes, size_t need, c
   }
   if (need == 0) return TP_OK;
   void *p = nullptr;
-  if (cudaMallocAsync(&p, need, st) != cudaSuccess) return TP_ERR_OOM;
+  if (lib_malloc_async(&p, need, st) != cudaSuccess) return TP_ERR_OOM;
   w->ptr = static_cast<char *>(p);
   w->owned = true;
   return TP_OK;
@@ -902,6 +923,12 @@ const char *tp_status_str(tp_status_t s) {
 
 int tp_abi_version(void) { return TP_ABI_VERSION; }
 
+tp_status_t tp_inject_alloc_failures(int count) {
+  if (count < 0) return TP_ERR_ARG;
+  g_fail_allocs.store(count);
+  return TP_OK;
+}
+
 tp_status_t tp_set_wait_limit_ns(uint64_t ns) {
   g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
   return TP_OK;
@@ -938,7 +965,7 @@ tp_status_t tp_shard_weights(const void *W1, const void *W2, int64_t H, int64_t 
   s->dt = dt;
   s->R1 = act == TP_ACT_SWIGLU ? 2 * Fs : Fs;
   const size_t b1 = static_cast<size_t>(T * s->R1 * H) * eb, b2 = static_cast<size_t>(T * H * Fs) * eb;
-  if (cudaMalloc(&s->w1p, b1) != cudaSuccess || cudaMalloc(&s->w2p, b2) != cudaSuccess) {
+  if (lib_malloc(&s->w1p, b1) != cudaSuccess || lib_malloc(&s->w2p, b2) != cudaSuccess) {
     tp_shards_destroy(s);
     return TP_ERR_OOM;
   }
@@ -993,7 +1020,7 @@ tp_status_t tp_shard_weights_qkv(const void *Wqkv, const void *Wo, int64_t H, in
   s->head_dim = head_dim;
   s->R1 = 3 * W;
   const size_t b1 = static_cast<size_t>(T * s->R1 * H) * 2, b2 = static_cast<size_t>(T * H * W) * 2;
-  if (cudaMalloc(&s->w1p, b1) != cudaSuccess || cudaMalloc(&s->w2p, b2) != cudaSuccess) {
+  if (lib_malloc(&s->w1p, b1) != cudaSuccess || lib_malloc(&s->w2p, b2) != cudaSuccess) {
     tp_shards_destroy(s);
     return TP_ERR_OOM;
   }
@@ -1052,7 +1079,7 @@ tp_status_t tp_shard_get(tp_shards_t s, int i, int which, void *host_dst) {
     return TP_ERR_ARG;
   }
   void *tmp = nullptr;
-  if (cudaMalloc(&tmp, static_cast<size_t>(elems) * eb) != cudaSuccess) return TP_ERR_OOM;
+  if (lib_malloc(&tmp, static_cast<size_t>(elems) * eb) != cudaSuccess) return TP_ERR_OOM;
   tp_status_t r = cuda_status(launch_unpack(mode, packed, tmp, i, wh, R, K, static_cast<int>(eb), W, 0));
   if (r == TP_OK) r = cuda_status(cudaMemcpy(host_dst, tmp, static_cast<size_t>(elems) * eb,
                                              cudaMemcpyDeviceToHost));
@@ -1095,8 +1122,8 @@ tp_status_t tp_shards_enable_backward(tp_shards_t s, const void *W1, const void 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t H = s->H, F = s->F, ncols = s->act == TP_ACT_SWIGLU ? 2 * F : F;
   const size_t b1 = static_cast<size_t>(H * ncols) * 2, b2 = static_cast<size_t>(F * H) * 2;
-  if (!s->w1o && cudaMalloc(&s->w1o, b1) != cudaSuccess) return TP_ERR_OOM;
-  if (!s->w2o && cudaMalloc(&s->w2o, b2) != cudaSuccess) return TP_ERR_OOM;
+  if (!s->w1o && lib_malloc(&s->w1o, b1) != cudaSuccess) return TP_ERR_OOM;
+  if (!s->w2o && lib_malloc(&s->w2o, b2) != cudaSuccess) return TP_ERR_OOM;
   TP_CUDA(cudaMemcpyAsync(s->w1o, W1, b1, cudaMemcpyDeviceToDevice, st));
   TP_CUDA(cudaMemcpyAsync(s->w2o, W2, b2, cudaMemcpyDeviceToDevice, st));
   s->bn_dh = s->Fs % 256 == 0 ? 256 : 128;

@@ -351,3 +351,43 @@ def test_partial_sum_bf16_bit_exact(tp, T, n):
     Z = tp.tp_partial_sum_bf16([to_device(P[t]) for t in range(T)])
     _sync()
     assert np.array_equal(bf16_bits(Z), oracle.partial_sum_bf16(P))
+
+
+# ---- failure injection: device allocation failures ---------------------------------
+
+def test_injected_allocation_failures_report_oom_and_recover(tp):
+    """With tp_inject_alloc_failures the library's next allocations fail as if
+    the device were full: making shards, a self-allocated workspace and
+    enabling the backward each return TP_ERR_OOM, nothing stays allocated,
+    and the same calls work right after."""
+    import torch
+    M, H, F, T = 64, 512, 2048, 4
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=41, x_rows=M)
+    W1, W2, X = to_device(d["W1"]), to_device(d["W2"]), to_device(d["X"])
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    try:
+        tp.tp_inject_alloc_failures(1)
+        with pytest.raises(tp.TPError) as e:
+            tp.tp_shard_weights(W1, W2, T, "gelu")
+        assert e.value.code == 5
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] >= free0 - (8 << 20)  # the failed calls freed what they took
+        s = tp.tp_shard_weights(W1, W2, T, "gelu")
+        tp.tp_inject_alloc_failures(1)
+        with pytest.raises(tp.TPError) as e:
+            tp.tp_mlp_forward(s, X)  # no workspace given: the library allocates one
+        assert e.value.code == 5
+        tp.tp_inject_alloc_failures(1)
+        with pytest.raises(tp.TPError) as e:
+            tp.tp_shards_enable_backward(s, W1, W2)
+        assert e.value.code == 5
+        Z = tp.tp_mlp_forward(s, X)
+        _sync()
+        assert tp.tp_last_device_status() == 0
+        assert rowwise_rms_error(Z.cpu().numpy(),
+                                 oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")) <= TOL_BF16_ROW_RMS
+        tp.tp_shards_enable_backward(s, W1, W2)
+        s.close()
+    finally:
+        tp.tp_inject_alloc_failures(0)

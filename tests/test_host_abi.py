@@ -71,6 +71,11 @@ def test_argument_errors_are_status_codes(lib):
     assert lib.tp_partial_sum(arr, 2, -1, dummy, None) == 1
     overlap = (ctypes.c_void_p * 2)(256, 4096)
     assert lib.tp_partial_sum(overlap, 2, 16, ctypes.c_void_p(4096 + 32), None) == 1
+    assert lib.tp_attention_forward(dummy, dummy, dummy, 16, 2, 64, 1, dummy, 256, None, 0, None) == 9
+    assert lib.tp_attention_forward(dummy, dummy, dummy, -1, 2, 128, 1, dummy, 256, None, 0, None) == 1
+    assert lib.tp_attention_workspace_bytes(100, 2, 64) == 0
+    assert lib.tp_inject_alloc_failures(-1) == 1
+    assert lib.tp_inject_alloc_failures(3) == 0 and lib.tp_inject_alloc_failures(0) == 0
     lib.tp_shards_destroy(None)
 
 
