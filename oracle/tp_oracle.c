@@ -24,7 +24,17 @@
  *     "Output Combination").
  *   - Attention: heads are sharded across ranks ("Tensor parallelism" guide,
  *     section "Walking through a transformer block"), so the QKV projection
- *     is column-parallel by head and the output projection row-parallel.
+ *     is column-parallel by head and the output projection row-parallel; the
+ *     attention core of each head is local (orc_attention), and one whole
+ *     block adds the two all-reduces and residuals (orc_block_forward).
+ *   - The collectives around the all-reduce: reduce-scatter, all-gather and
+ *     the sum rounded once to bfloat16 ("Slice the matrix itself", section
+ *     "Column-Parallel & Row-Parallel GEMMs", the NCCL primitives named
+ *     there).
+ *   - The backward pass of the MLP: the input gradient is again a sum over
+ *     shards (the all-reduce of the backward pass), the weight gradients are
+ *     per shard ("Tensor Parallelism in Action", section 1: all-reduces in
+ *     the forward and the backward pass).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - GeLU is the exact form 0.5 y (1 + erf(y / sqrt 2)).
