@@ -28,13 +28,12 @@
  *     attention core of each head is local (orc_attention), and one whole
  *     block adds the two all-reduces and residuals (orc_block_forward).
  *   - The collectives around the all-reduce: reduce-scatter, all-gather and
- *     the sum rounded once to bfloat16 ("Slice the matrix itself", section
- *     "Column-Parallel & Row-Parallel GEMMs", the NCCL primitives named
- *     there).
+ *     the sum rounded once to bfloat16 ("Tensor Parallelism in Action",
+ *     section 2, question 3 names AllReduce, AllGather and ReduceScatter).
  *   - The backward pass of the MLP: the input gradient is again a sum over
  *     shards (the all-reduce of the backward pass), the weight gradients are
- *     per shard ("Tensor Parallelism in Action", section 1: all-reduces in
- *     the forward and the backward pass).
+ *     per shard ("Slice the matrix itself", section "Strict NVLink Domain
+ *     Constraint": all-reduces in every layer's forward and backward pass).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - GeLU is the exact form 0.5 y (1 + erf(y / sqrt 2)).
