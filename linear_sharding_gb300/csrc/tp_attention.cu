@@ -78,6 +78,12 @@ __device__ __forceinline__ AttnUnit decode(int u, const AttnArgs &a) {
   for (int w = 0; w < 2; ++w)
     t.nkt[w] = t.mt[w] < 0 ? 0 : (a.causal ? t.mt[w] + 1 : a.m_tiles);
   t.nk = t.nkt[0] > t.nkt[1] ? t.nkt[0] : t.nkt[1];
+  if (!TP_CHECK(t.head < a.heads && t.mt[0] >= 0 && t.mt[1] < a.m_tiles && t.nk >= 1 && t.nk <= a.m_tiles,
+                a.status)) {
+    t.mt[1] = -1;  // keep the unit's shape sane: tile A alone over one key tile
+    t.nkt[0] = t.nk = 1;
+    t.nkt[1] = 0;
+  }
   return t;
 }
 
@@ -358,6 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kmax = a.M - 1 - key0;
         if (a.causal && row - key0 < kmax) kmax = row - key0;
         const bool masked = kmax < kTile - 1;
+        // every key tile a row visits holds at least one allowed key (its own, or key < M)
+        if (!TP_CHECK(kmax >= 0, a.status)) kmax = 0;
         // the row of S_j in two halves of 64 scores (registers for one half at a time):
         // first its maximum, then the weights
         uint32_t s[2][32];
@@ -442,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++uc;
       tc_fence_after();
       const float inv = 1.0f / l_run;
+      const bool in_row = TP_CHECK((t.head + 1) * static_cast<long long>(kAttnHeadDim) <= a.ldo, a.status);
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.O) + static_cast<long long>(row) * a.ldo +
                                              static_cast<long long>(t.head) * kAttnHeadDim);
 #pragma unroll
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ob + cc * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
-        if (row < a.M) {
+        if (row < a.M && in_row) {
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4)
             dst[cc * 4 + g4] = make_uint4(

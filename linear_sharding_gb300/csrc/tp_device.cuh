@@ -11,6 +11,17 @@
 
 namespace tp {
 
+// Device-side checks of the kernels' index arithmetic, compiled in with
+// -DTP_DEVICE_CHECKS=1 (the debug library): TP_CHECK(cond, status) records a
+// failure in the status word (kDevCheck, reported as TP_ERR_DEVICE_CHECK) and
+// yields false, so the caller skips the guarded work.  In the normal build it
+// is `true` and `cond` is not evaluated.  Nothing traps.
+#if defined(TP_DEVICE_CHECKS) && TP_DEVICE_CHECKS
+#define TP_CHECK(cond, status) ((cond) ? true : (atomicOr((status), ::tp::kDevCheck), false))
+#else
+#define TP_CHECK(cond, status) true
+#endif
+
 // Fixed limit for the clean-up waits after an abort (copies and MMAs that
 // were already issued always finish; this only bounds the wait).
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;

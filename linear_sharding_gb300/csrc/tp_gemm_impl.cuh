@@ -88,6 +88,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
   r.n = in / gm;
   r.kt0 = r.slot * g.kt_per_slot;
   r.kt1 = min(g.kt_total, r.kt0 + g.kt_per_slot);
+  // a unit outside the tile grid or an empty K range is a bug in the work split: report it and
+  // turn the unit into an empty one on tile (0, 0)
+  if (!TP_CHECK(r.slot < g.slots && r.m < g.m_tiles && r.n < g.n_tiles && r.kt0 < r.kt1, g.status)) {
+    r.m = r.n = 0;
+    r.kt1 = r.kt0;
+  }
   return r;
 }
 
