@@ -20,8 +20,12 @@ struct tp_shards {
   tp_dtype_t dt = TP_BF16;
   int n_heads = 0, head_dim = 0;
   int64_t R1 = 0;  // packed first-layer rows per shard (Fs, 2 Fs for SwiGLU, 3 W for QKV)
-  void *w1p = nullptr;  // [T][R1][H]
-  void *w2p = nullptr;  // [T][H][Fs]
+  // Packed shards: logically W1_i^T [T][R1][H] and W2_i^T [T][H][Fs] (K-major).
+  // Float32: stored so.  Bfloat16: in k-tiles of 64, [H/64][T R1][64] and
+  // [T][Fs/64][H][64], so that every 128-row x 64 copy the GEMMs make of a
+  // weight is one contiguous 16 KiB block.
+  void *w1p = nullptr;
+  void *w2p = nullptr;
   int bn1 = 256, bn2 = 256;
   CUtensorMap map_w1_b, map_w1_a, map_w2_b, map_w2_a;
   // backward operands: W1 [H x ncols] and W2 [F x H] in the caller's layout
@@ -144,6 +148,18 @@ tp_status_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TP_OK : TP_ERR_CUDA;
+}
+
+// Tensor maps of the k-tile-blocked bf16 weights (operand mode kKtileBlocked:
+// coordinate (0, row, k-tile)).  W1: k-tile kt of all T R1 rows; W2: k-tile
+// kt of shard i is plane i (Ks/64) + kt of H rows.  Ks is the per-shard K of W2.
+tp_status_t make_weight_maps(tp_shards *s, int64_t Ks) {
+  const int64_t rows1 = s->T * s->R1, kt1 = s->H / 64, kt2 = s->T * (Ks / 64);
+  tp_status_t r = make_map(&s->map_w1_b, s->w1p, 64, rows1, kt1, 128, rows1 * 128, s->bn1);
+  if (r == TP_OK) r = make_map(&s->map_w1_a, s->w1p, 64, rows1, kt1, 128, rows1 * 128, 128);
+  if (r == TP_OK) r = make_map(&s->map_w2_b, s->w2p, 64, s->H, kt2, 128, s->H * 128, s->bn2);
+  if (r == TP_OK) r = make_map(&s->map_w2_a, s->w2p, 64, s->H, kt2, 128, s->H * 128, 128);
+  return r;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -298,7 +314,7 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
   g.kt_total = s->T * g.kt_per_seg;
   g.kt_per_slot = g.kt_total / slots;
   g.a_seg = a_seg;
-  g.b_seg = 1;
+  g.b_seg = kKtileBlocked;
   g.rows_valid = static_cast<int>(M);
   g.cols_valid = static_cast<int>(H);
   g.out = slots > 1 ? static_cast<void *>(P) : static_cast<void *>(Z);
@@ -333,6 +349,7 @@ tp_status_t colpar_tc(const tp_shards *s, const DevState *d, const void *X, int6
   g.m_tiles = static_cast<int>(cdiv(M, pair ? 256 : 128));
   g.n_tiles = static_cast<int>(s->T * s->R1 / s->bn1);
   g.slots = 1;
+  g.b_seg = kKtileBlocked;
   g.kt_total = static_cast<int>(H / 64);
   g.kt_per_seg = g.kt_total;
   g.kt_per_slot = g.kt_total;
@@ -360,6 +377,7 @@ tp_status_t colpar_decode(const tp_shards *s, const DevState *d, const MlpPlan &
   g.m_tiles = static_cast<int>(rows1 / 128);
   g.n_tiles = 1;
   g.slots = p.slots1;
+  g.a_seg = kKtileBlocked;
   g.kt_total = static_cast<int>(H / 64);
   g.kt_per_seg = g.kt_total;
   g.kt_per_slot = g.kt_total / p.slots1;
@@ -389,7 +407,7 @@ tp_status_t rowpar_decode(const tp_shards *s, const DevState *d, const MlpPlan &
   g.kt_per_seg = static_cast<int>(Fs / 64);
   g.kt_total = static_cast<int>(T) * g.kt_per_seg;
   g.kt_per_slot = g.kt_total / p.slots2;
-  g.a_seg = 1;
+  g.a_seg = kKtileBlocked;
   g.b_seg = 1;
   g.group_m = 1;
   g.rows_valid = static_cast<int>(H);
@@ -598,6 +616,7 @@ tp_status_t mlp_forward_train_impl(tp_shards *s, const void *X, int64_t M, tp_ac
   c.a = &mx;
   c.b_bn = &s->map_w1_b;
   c.b_128 = &s->map_w1_a;
+  c.b_seg = kKtileBlocked;
   c.rows = M;
   c.N = T * s->R1;
   c.bn = s->bn1;
@@ -863,6 +882,7 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
     c.a = &mx;
     c.b_bn = &a->map_w1_b;
     c.b_128 = &a->map_w1_a;
+    c.b_seg = kKtileBlocked;
     c.rows = M;
     c.N = a->T * a->R1;
     c.bn = a->bn1;
@@ -977,11 +997,7 @@ tp_status_t tp_shard_weights(const void *W1, const void *W2, int64_t H, int64_t 
   if (r == TP_OK && dt == TP_BF16) {
     s->bn1 = (act == TP_ACT_SWIGLU || Fs % 256 == 0) ? 256 : 128;
     s->bn2 = (H % 256 == 0) ? 256 : 128;
-    const int64_t rows1 = T * s->R1;
-    r = make_map(&s->map_w1_b, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, s->bn1);
-    if (r == TP_OK) r = make_map(&s->map_w1_a, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, 128);
-    if (r == TP_OK) r = make_map(&s->map_w2_b, s->w2p, Fs, H, T, Fs * 2, H * Fs * 2, s->bn2);
-    if (r == TP_OK) r = make_map(&s->map_w2_a, s->w2p, Fs, H, T, Fs * 2, H * Fs * 2, 128);
+    r = make_weight_maps(s, Fs);
   }
   if (r != TP_OK) {
     tp_shards_destroy(s);
@@ -1029,11 +1045,7 @@ tp_status_t tp_shard_weights_qkv(const void *Wqkv, const void *Wo, int64_t H, in
   if (r == TP_OK) {
     s->bn1 = ((3 * W) % 256 == 0) ? 256 : 128;
     s->bn2 = (H % 256 == 0) ? 256 : 128;
-    const int64_t rows1 = T * s->R1;
-    r = make_map(&s->map_w1_b, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, s->bn1);
-    if (r == TP_OK) r = make_map(&s->map_w1_a, s->w1p, H, rows1, 1, H * 2, rows1 * H * 2, 128);
-    if (r == TP_OK) r = make_map(&s->map_w2_b, s->w2p, W, H, T, W * 2, H * W * 2, s->bn2);
-    if (r == TP_OK) r = make_map(&s->map_w2_a, s->w2p, W, H, T, W * 2, H * W * 2, 128);
+    r = make_weight_maps(s, W);
   }
   if (r != TP_OK) {
     tp_shards_destroy(s);
@@ -1080,7 +1092,7 @@ tp_status_t tp_shard_get(tp_shards_t s, int i, int which, void *host_dst) {
   }
   void *tmp = nullptr;
   if (lib_malloc(&tmp, static_cast<size_t>(elems) * eb) != cudaSuccess) return TP_ERR_OOM;
-  tp_status_t r = cuda_status(launch_unpack(mode, packed, tmp, i, wh, R, K, static_cast<int>(eb), W, 0));
+  tp_status_t r = cuda_status(launch_unpack(mode, packed, tmp, i, s->T, wh, R, K, static_cast<int>(eb), W, 0));
   if (r == TP_OK) r = cuda_status(cudaMemcpy(host_dst, tmp, static_cast<size_t>(elems) * eb,
                                              cudaMemcpyDeviceToHost));
   cudaFree(tmp);

@@ -120,8 +120,8 @@ struct KCursor {
     }
   }
   __device__ __forceinline__ void coords(int mode, int &kc, int &zc) const {
-    kc = mode == 1 ? k : kflat;
-    zc = mode == 1 ? z : 0;
+    kc = mode == 1 ? k : mode == kKtileBlocked ? 0 : kflat;
+    zc = mode == 1 ? z : mode == kKtileBlocked ? kflat / BK : 0;
   }
 };
 

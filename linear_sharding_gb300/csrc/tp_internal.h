@@ -42,7 +42,11 @@ constexpr int kSwigluGranule = 128;
 // operand (a_seg / b_seg = 1) is a 3-D tensor map [segments][rows][K per
 // segment] and k-tile kt reads coordinate (kt % kt_per_seg * 64, row,
 // kt / kt_per_seg); a flat operand (0) is [1][rows][K] and reads (kt * 64,
-// row, 0).  Slot s covers k-tiles [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
+// row, 0); a k-tile-blocked operand (kKtileBlocked, the packed bf16 weights)
+// is [k-tiles][rows][64] and reads (0, row, kt).  Slot s covers k-tiles
+// [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
+constexpr int kKtileBlocked = 2;
+
 struct GemmArgs {
   int m_tiles, n_tiles, slots;
   int kt_total, kt_per_seg, kt_per_slot;
@@ -155,16 +159,20 @@ enum PackMode : int {
   PACK_QKV = 2,        // dst[s][r][k] = Wqkv[k][(r / W) * H + s*W + r % W]
   PACK_ROWS = 3        // dst[s][n][k] = W2[s*Ks + k][n]
 };
-// dst is [S][R][K]; src is row-major with leading dimension src_ld; esize is
-// 2 or 4 bytes; `F` is the width of one half of [Wg | Wu], `H` the QKV
-// hidden size, `W` the per-shard width (Fs or head columns).
+// Logical dst is [S][R][K]; src is row-major with leading dimension src_ld;
+// esize is 2 or 4 bytes; `F` is the width of one half of [Wg | Wu], `H` the
+// QKV hidden size, `W` the per-shard width (Fs or head columns).  Float32
+// weights (CUDA-core path) are stored as [S][R][K].  Bfloat16 weights (TMA
+// path, K a multiple of 64) are stored in k-tiles of 64, each tile holding
+// the 64 K values of every row contiguously (see packed_index), so that one
+// 128-row x 64 copy is one contiguous 16 KiB block of memory.
 cudaError_t launch_pack(PackMode mode, const void *src, long long src_ld, void *dst, int S,
                         long long R, long long K, int esize, long long F, long long H, long long W,
                         cudaStream_t stream);
-// Inverse: the logical shard s (row-major [H x W] for W1-like modes and
+// Inverse: the logical shard s of S (row-major [H x W] for W1-like modes and
 // `which` = 0/1 gate/up; [W x N] for PACK_ROWS) from the packed buffer.
-cudaError_t launch_unpack(PackMode mode, const void *packed, void *dst, int s, int which, long long R,
-                          long long K, int esize, long long W, cudaStream_t stream);
+cudaError_t launch_unpack(PackMode mode, const void *packed, void *dst, int s, int S, int which,
+                          long long R, long long K, int esize, long long W, cudaStream_t stream);
 
 // Decode finalize: h[s][t][j] = bf16(act(sum over slots of P[slot][t][row(s, j)])) for
 // SwiGLU (gate and up rows) or GeLU/identity.

@@ -6,7 +6,7 @@
 //     loads and stores, grid sized to the SM count;
 //   - the weight packing into per-shard K-major buffers (the column blocks
 //     of W1 and row blocks of W2 of "Tensor Parallelism in Action", section
-//     1) and its inverse for layout checks;
+//     1; bfloat16 in k-tiles of 64) and its inverse for layout checks;
 //   - the float32 CUDA-core GEMM used for float32 inputs;
 //   - the decode activation, which finishes split-K first-layer partials.
 #include <cuda_bf16.h>
@@ -235,11 +235,26 @@ __device__ __forceinline__ void pack_src(int mode, int s, long long r, long long
   }
 }
 
+// Offset of logical element [s][r][k] (S segments of R rows and K columns)
+// in a packed buffer.  Row-major: (s R + r) K + k.  K-tile blocked: 64-wide
+// k-tiles, each holding its 64 values of every row of the tensor map's view
+// contiguously.  The first-layer modes view the buffer as S R rows of K
+// (shards side by side along the rows), so tile kt is [S R][64] at
+// kt S R 64; PACK_ROWS views it as R rows of K per shard (shards along K), so
+// tile kt of shard s is [R][64] at (s K/64 + kt) R 64.
+__device__ __forceinline__ long long packed_index(int mode, bool blocked, int s, int S, long long r,
+                                                  long long R, long long k, long long K) {
+  if (!blocked) return (static_cast<long long>(s) * R + r) * K + k;
+  const long long kt = k >> 6, kk = k & 63;
+  if (mode == PACK_ROWS) return ((static_cast<long long>(s) * (K >> 6) + kt) * R + r) * 64 + kk;
+  return (kt * S * R + static_cast<long long>(s) * R + r) * 64 + kk;
+}
+
 // dst[s][r][k] = src[srow][scol] through a 32 x 32 shared-memory tile so that
 // both the reads (along source columns) and the writes (along k) coalesce.
 template <typename E>
-__global__ void pack_kernel(int mode, const E *src, long long src_ld, E *dst, long long R, long long K,
-                            long long F, long long H, long long W) {
+__global__ void pack_kernel(int mode, bool blocked, const E *src, long long src_ld, E *dst, long long R,
+                            long long K, long long F, long long H, long long W) {
   __shared__ E tile[32][33];
   const int s = blockIdx.z;
   const long long r0 = static_cast<long long>(blockIdx.y) * 32;
@@ -255,7 +270,7 @@ __global__ void pack_kernel(int mode, const E *src, long long src_ld, E *dst, lo
   __syncthreads();
   for (int rr = threadIdx.y; rr < 32; rr += blockDim.y) {
     const long long r = r0 + rr, k = k0 + threadIdx.x;
-    if (k < K && r < R) dst[(static_cast<long long>(s) * R + r) * K + k] = tile[threadIdx.x][rr];
+    if (k < K && r < R) dst[packed_index(mode, blocked, s, gridDim.z, r, R, k, K)] = tile[threadIdx.x][rr];
   }
 }
 
@@ -263,8 +278,8 @@ __global__ void pack_kernel(int mode, const E *src, long long src_ld, E *dst, lo
 // per thread).  W1-like modes: out [K x Wl] with Wl = W (3W for QKV);
 // PACK_ROWS: out [K x R].
 template <typename E>
-__global__ void unpack_kernel(int mode, const E *packed, E *out, int s, int which, long long R,
-                              long long K, long long W) {
+__global__ void unpack_kernel(int mode, bool blocked, const E *packed, E *out, int s, int S, int which,
+                              long long R, long long K, long long W) {
   const long long cols = (mode == PACK_ROWS) ? R : (mode == PACK_QKV ? 3 * W : W);
   const long long total = K * cols;
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -276,7 +291,7 @@ __global__ void unpack_kernel(int mode, const E *packed, E *out, int s, int whic
           c % kSwigluGranule;
     else
       r = c;
-    out[e] = packed[(static_cast<long long>(s) * R + r) * K + k];
+    out[e] = packed[packed_index(mode, blocked, s, S, r, R, k, K)];
   }
 }
 
@@ -499,30 +514,31 @@ cudaError_t launch_pack(PackMode mode, const void *src, long long src_ld, void *
                         long long K, int esize, long long F, long long H, long long W,
                         cudaStream_t stream) {
   if (S < 1 || R < 1 || K < 1) return cudaErrorInvalidValue;
+  if (esize == 2 && K % 64 != 0) return cudaErrorInvalidValue;  // whole k-tiles only
   const long long gy = (R + 31) / 32, gx = (K + 31) / 32;
   if (gy > 65535 || gx > 2147483647LL || S > 65535) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(S));
   dim3 block(32, 8);
   if (esize == 2)
-    pack_kernel<uint16_t><<<grid, block, 0, stream>>>(mode, static_cast<const uint16_t *>(src), src_ld,
+    pack_kernel<uint16_t><<<grid, block, 0, stream>>>(mode, true, static_cast<const uint16_t *>(src), src_ld,
                                                       static_cast<uint16_t *>(dst), R, K, F, H, W);
   else if (esize == 4)
-    pack_kernel<uint32_t><<<grid, block, 0, stream>>>(mode, static_cast<const uint32_t *>(src), src_ld,
+    pack_kernel<uint32_t><<<grid, block, 0, stream>>>(mode, false, static_cast<const uint32_t *>(src), src_ld,
                                                       static_cast<uint32_t *>(dst), R, K, F, H, W);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(PackMode mode, const void *packed, void *dst, int s, int which, long long R,
-                          long long K, int esize, long long W, cudaStream_t stream) {
+cudaError_t launch_unpack(PackMode mode, const void *packed, void *dst, int s, int S, int which,
+                          long long R, long long K, int esize, long long W, cudaStream_t stream) {
   const int grid = 1024, threads = 256;
   if (esize == 2)
     unpack_kernel<uint16_t><<<grid, threads, 0, stream>>>(
-        mode, static_cast<const uint16_t *>(packed), static_cast<uint16_t *>(dst), s, which, R, K, W);
+        mode, true, static_cast<const uint16_t *>(packed), static_cast<uint16_t *>(dst), s, S, which, R, K, W);
   else if (esize == 4)
     unpack_kernel<uint32_t><<<grid, threads, 0, stream>>>(
-        mode, static_cast<const uint32_t *>(packed), static_cast<uint32_t *>(dst), s, which, R, K, W);
+        mode, false, static_cast<const uint32_t *>(packed), static_cast<uint32_t *>(dst), s, S, which, R, K, W);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
