@@ -532,6 +532,7 @@ struct GemmCall {
   int a_seg = 0;
   const CUtensorMap *b_bn = nullptr, *b_128 = nullptr;  // B maps with box bn rows / 128 rows
   int b_seg = 0;
+  int a_mn_seg = 0, b_mn_seg = 0;  // EPI_F32_MN: MN rows per segment of A / B
   int64_t rows = 0, N = 0;
   int bn = 256, kps = 0, nseg = 1, slots = 1;
   Epi epi = EPI_F32;
@@ -547,6 +548,8 @@ tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStrea
   g.kt_per_slot = g.kt_total / c.slots;
   g.a_seg = c.a_seg;
   g.b_seg = c.b_seg;
+  g.a_mn_seg = c.a_mn_seg;
+  g.b_mn_seg = c.b_mn_seg;
   g.rows_valid = static_cast<int>(c.rows);
   g.cols_valid = static_cast<int>(c.N);
   if (pair) TP_CUDA(launch_gemm(CFG_PAIR_N256, c.epi, *c.a, *c.b_128, g, d->sms, st));
@@ -562,30 +565,22 @@ struct TrainPlan {
   int slots2 = 1;       // forward row-parallel slots
   int slots_dx = 1;     // backward dX slots
   int nseg = 1;         // segments of dP (T, or 2T for SwiGLU: dG shards then dU shards)
-  int64_t Mp = 0;       // tokens padded to a multiple of 64 (K of the weight gradients)
   size_t fwd_row = 0;   // forward: row-parallel partials
-  size_t dP = 0, xt = 0, dzt = 0, ht = 0, dpt = 0, dx_part = 0;
+  size_t dP = 0, dx_part = 0;
   size_t fwd_total() const { return round256(fwd_row); }
-  size_t bwd_total() const {
-    return round256(dP) + round256(xt) + round256(dzt) + round256(ht) + round256(dpt) + round256(dx_part);
-  }
+  size_t bwd_total() const { return round256(dP) + round256(dx_part); }
 };
 
 void plan_train(const tp_shards *s, int64_t M, tp_variant_t v, int sms, TrainPlan *p) {
   *p = TrainPlan();
-  const int64_t H = s->H, Fs = s->Fs, T = s->T, F = s->F;
+  const int64_t H = s->H, Fs = s->Fs, T = s->T;
   MlpPlan fp;
   plan_mlp(s, M > kDecodeMaxM ? M : kDecodeMaxM + 1, v, sms, &fp);
   p->slots2 = fp.slots2;
   p->fwd_row = p->slots2 > 1 ? static_cast<size_t>(p->slots2 * M * H) * 4 : 0;
   p->nseg = static_cast<int>(s->act == TP_ACT_SWIGLU ? 2 * T : T);
   p->slots_dx = (v == TP_VAR_PARTIALS) ? p->nseg : 1;
-  p->Mp = round64(M);
   p->dP = static_cast<size_t>(p->nseg * M * Fs) * 2;
-  p->xt = static_cast<size_t>(H * p->Mp) * 2;
-  p->dzt = p->xt;
-  p->ht = static_cast<size_t>(F * p->Mp) * 2;
-  p->dpt = static_cast<size_t>(p->nseg * Fs * p->Mp) * 2;
   p->dx_part = p->slots_dx > 1 ? static_cast<size_t>(p->slots_dx * M * H) * 4 : 0;
 }
 
@@ -654,14 +649,10 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   plan_train(s, M, v, d->sms, &p);
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.bwd_total(), st));
-  const int64_t H = s->H, T = s->T, Fs = s->Fs, F = s->F, Mp = p.Mp;
+  const int64_t H = s->H, T = s->T, Fs = s->Fs, F = s->F;
   const int64_t ncols = p.nseg * Fs;
   char *dP = w.ptr;
-  char *xt = dP + round256(p.dP);
-  char *dzt = xt + round256(p.xt);
-  char *ht = dzt + round256(p.dzt);
-  char *dpt = ht + round256(p.ht);
-  float *dxp = reinterpret_cast<float *>(dpt + round256(p.dpt));
+  float *dxp = reinterpret_cast<float *>(dP + round256(p.dP));
 
   // 1. dH = dZ W2^T for every shard, times the activation's derivative -> dP
   CUtensorMap mdz;
@@ -715,32 +706,28 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
     TP_TRY(run_gemm(d, c, g, st));
     if (p.slots_dx > 1) TP_CUDA(launch_shard_sum_strided(dxp, p.slots_dx, M * H, M * H, dX, d->sms, st));
   }
-  // 3. K-major operands for the weight gradients (K = tokens, padded to Mp)
-  TP_CUDA(launch_transpose_pad(X, M, H, H, 0, xt, Mp, 0, 1, st));
-  TP_CUDA(launch_transpose_pad(dZ, M, H, H, 0, dzt, Mp, 0, 1, st));
-  TP_CUDA(launch_transpose_pad(Hsave, M, Fs, Fs, M * Fs, ht, Mp, Fs * Mp, static_cast<int>(T), st));
-  TP_CUDA(launch_transpose_pad(dP, M, Fs, Fs, M * Fs, dpt, Mp, Fs * Mp, p.nseg, st));
-  // 4. dW2 = H^T dZ  [F x H];  5. dW1 = X^T dP  [H x ncols]
-  const int bnh = bn_for(H), bnc = bn_for(ncols);
-  CUtensorMap m_ht, m_xt, m_dzt_bn, m_dzt_128, m_dpt_bn, m_dpt_128;
-  TP_TRY(make_map(&m_ht, ht, Mp, F, 1, Mp * 2, F * Mp * 2, 128));
-  TP_TRY(make_map(&m_xt, xt, Mp, H, 1, Mp * 2, H * Mp * 2, 128));
-  TP_TRY(make_map(&m_dzt_bn, dzt, Mp, H, 1, Mp * 2, H * Mp * 2, bnh));
-  TP_TRY(make_map(&m_dzt_128, dzt, Mp, H, 1, Mp * 2, H * Mp * 2, 128));
-  TP_TRY(make_map(&m_dpt_bn, dpt, Mp, ncols, 1, Mp * 2, ncols * Mp * 2, bnc));
-  TP_TRY(make_map(&m_dpt_128, dpt, Mp, ncols, 1, Mp * 2, ncols * Mp * 2, 128));
+  // 3. dW2 = H^T dZ  [F x H];  4. dW1 = X^T dP  [H x ncols].  K is the token axis, so every
+  // operand is read MN-major straight from its [tokens][features] layout (64 x 64 boxes; the
+  // copies fill tokens past M with zeros): per-shard H and dP as [segments][M][Fs].
+  CUtensorMap m_h, m_x, m_dz, m_dp;
+  TP_TRY(make_map(&m_h, Hsave, Fs, M, T, Fs * 2, M * Fs * 2, 64));
+  TP_TRY(make_map(&m_x, X, H, M, 1, H * 2, M * H * 2, 64));
+  TP_TRY(make_map(&m_dz, dZ, H, M, 1, H * 2, M * H * 2, 64));
+  TP_TRY(make_map(&m_dp, dP, Fs, M, p.nseg, Fs * 2, M * Fs * 2, 64));
+  const int ktok = static_cast<int>(cdiv(M, 64));
   {
     GemmArgs g = base_args(d);
     g.out = dW2;
     g.ld_out = H;
     GemmCall c;
-    c.a = &m_ht;
-    c.b_bn = &m_dzt_bn;
-    c.b_128 = &m_dzt_128;
+    c.a = &m_h;
+    c.a_mn_seg = static_cast<int>(Fs);
+    c.b_bn = c.b_128 = &m_dz;
     c.rows = F;
     c.N = H;
-    c.bn = bnh;
-    c.kps = static_cast<int>(Mp / 64);
+    c.bn = bn_for(H);
+    c.kps = ktok;
+    c.epi = EPI_F32_MN;
     TP_TRY(run_gemm(d, c, g, st));
   }
   {
@@ -748,13 +735,14 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
     g.out = dW1;
     g.ld_out = ncols;
     GemmCall c;
-    c.a = &m_xt;
-    c.b_bn = &m_dpt_bn;
-    c.b_128 = &m_dpt_128;
+    c.a = &m_x;
+    c.b_bn = c.b_128 = &m_dp;
+    c.b_mn_seg = static_cast<int>(Fs);
     c.rows = H;
     c.N = ncols;
-    c.bn = bnc;
-    c.kps = static_cast<int>(Mp / 64);
+    c.bn = bn_for(ncols);
+    c.kps = ktok;
+    c.epi = EPI_F32_MN;
     TP_TRY(run_gemm(d, c, g, st));
   }
   return TP_OK;

@@ -444,8 +444,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
          | (static_cast<uint64_t>(2) << 61);               // swizzle mode: 128 B
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile in the 128-byte
+// swizzle, as TMA writes it from a [K][MN] tensor with 64 x 64 boxes: each box
+// is 64 K rows of 64 MN elements (128 B a row), and box i of the tile holds MN
+// elements [64 i, 64 i + 64) at 8 KiB i.  Leading byte offset: 8 KiB between
+// those 64-element MN blocks; stride byte offset: 1 KiB between groups of 8 K
+// rows.  One K = 16 step advances the start by 2 KiB.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)  // start address / 16
+         | (static_cast<uint64_t>(8192 >> 4) << 16)        // leading byte offset: next 64 MN
+         | (static_cast<uint64_t>(1024 >> 4) << 32)        // stride byte offset: next 8 K rows
+         | (static_cast<uint64_t>(1) << 46)                // descriptor version (tcgen05)
+         | (static_cast<uint64_t>(2) << 61);               // swizzle mode: 128 B
+}
+
 // Instruction descriptor: bf16 A and B (both K-major), fp32 accumulator,
-// shape M x N.
+// shape M x N.  Bits 15 and 16 (kIdescMnA, kIdescMnB) mark A or B MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                  // D format: f32
          | (1u << 7)                                // A format: bf16
@@ -453,5 +467,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
+constexpr uint32_t kIdescMnA = 1u << 15;
+constexpr uint32_t kIdescMnB = 1u << 16;
 
 }  // namespace tp

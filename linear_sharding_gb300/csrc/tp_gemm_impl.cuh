@@ -125,6 +125,23 @@ struct KCursor {
   }
 };
 
+// Tensor-map coordinates (x, z) of the 64-row blocks [row0 + 64 i, row0 + 64 i + 64) of an
+// MN-major operand tile (EPI_F32_MN): x is the row within its MN segment of `seg` rows, z the
+// segment (seg = 0: one segment).  Set once per unit; a block never straddles segments.
+template <int N>
+struct MnBlocks {
+  int x[N], z[N];
+  __device__ __forceinline__ void set(int row0, int seg) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const int r = row0 + 64 * i;
+      z[i] = seg > 0 ? r / seg : 0;
+      x[i] = r - z[i] * seg;
+    }
+  }
+};
+constexpr uint32_t kMnBlockBytes = 64 * BK * 2;  // one 64 x 64 box
+
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
@@ -198,7 +215,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
       for (int j = 0; j < BN; ++j)
         if (j < g.cols_valid) out[j * g.ld_out] = __uint_as_float(r[j]);
     }
-  } else if constexpr (EPI == EPI_F32) {
+  } else if constexpr (EPI == EPI_F32 || EPI == EPI_F32_MN) {
     const int row = row0 + row_in_tile;
     const bool valid = row < g.rows_valid;
     float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
@@ -467,8 +484,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
+      constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
+      constexpr int kBBlocks = BN >= 64 ? BN / 64 : 1;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, g);
+        MnBlocks<BM / 64> ablk;
+        MnBlocks<kBBlocks> bblk;
+        if constexpr (amn) ablk.set(t.m * BM, g.a_mn_seg);
+        if constexpr (bmn) bblk.set(t.n * BN, g.b_mn_seg);
         KCursor kc;
         kc.start(t.kt0, g);
         for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
@@ -481,8 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           int ak, az, bk, bz;
           kc.coords(g.a_seg, ak, az);
           kc.coords(g.b_seg, bk, bz);
-          tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
-          tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
+          if constexpr (amn) {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_3d(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, fb, ablk.x[i], kc.kflat,
+                          ablk.z[i]);
+          } else {
+            tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
+          }
+          if constexpr (bmn && BN >= 64) {
+#pragma unroll
+            for (int i = 0; i < kBBlocks; ++i)
+              tma_load_3d(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, fb, bblk.x[i], kc.kflat,
+                          bblk.z[i]);
+          } else {
+            tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
+          }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -506,6 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Under a test wait limit, first wait for an event that never happens,
       // so that the timeout path runs with copies in flight.
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
+      constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
+      constexpr uint32_t idesc = IDESC | (amn ? kIdescMnA : 0u) | (bmn ? kIdescMnB : 0u);
+      // one K = 16 step: +32 B (K-major) or +2 KiB (MN-major), in 16-byte units
+      constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, g);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
@@ -517,11 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
+          const uint32_t sa = smem_u32(sA + stage * A_BYTES), sb = smem_u32(sB + stage * B_BYTES);
+          const uint64_t ad = amn ? sw128_mnmajor_desc(sa) : sw128_kmajor_desc(sa);
+          const uint64_t bd = bmn ? sw128_mnmajor_desc(sb) : sw128_kmajor_desc(sb);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // +32 B per K=16 step -> +2 in the address field
-            tc_mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kt > t.kt0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_bf16(d, ad + astep * k, bd + bstep * k, idesc, (kt > t.kt0 || k > 0) ? 1u : 0u);
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -669,10 +711,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
       const bool leader = rank == 0;
+      constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
         const int arow = t.m * 256 + 128 * static_cast<int>(rank);
         const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
+        MnBlocks<2> ablk, bblk;  // 128 rows of A and of B in each CTA
+        if constexpr (amn) ablk.set(arow, g.a_mn_seg);
+        if constexpr (bmn) bblk.set(brow, g.b_mn_seg);
         KCursor kc;
         kc.start(t.kt0, g);
         for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
@@ -683,7 +729,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           int ak, az, bk, bz;
           kc.coords(g.a_seg, ak, az);
           kc.coords(g.b_seg, bk, bz);
-          if (leader) {
+          if constexpr (amn) {
+            // this CTA's copies complete on CTA 0's stage barrier, which CTA 0 arms for both
+            const uint32_t fb = leader ? full_bar(stage) : map_to_rank(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_BYTES));
+            auto load = [&](uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2) {
+              if (leader)
+                tma_load_3d(dst, map, fb, c0, c1, c2);
+              else
+                tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+            };
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              load(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, ablk.x[i], kc.kflat, ablk.z[i]);
+              load(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, bblk.x[i], kc.kflat, bblk.z[i]);
+            }
+          } else if (leader) {
             const uint32_t fb = full_bar(stage);
             mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_BYTES));
             tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
@@ -719,6 +780,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = !(g.wait_limit_ns < kShortLimitNs) || wait_bar(never, 0u, w);
+      constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
+      constexpr uint32_t idesc = IDESC | (amn ? kIdescMnA : 0u) | (bmn ? kIdescMnB : 0u);
+      constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
         if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
@@ -730,11 +794,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * B_BYTES));
+          const uint32_t sa = smem_u32(sA + stage * A_BYTES), sb = smem_u32(sB + stage * B_BYTES);
+          const uint64_t ad = amn ? sw128_mnmajor_desc(sa) : sw128_kmajor_desc(sa);
+          const uint64_t bd = bmn ? sw128_mnmajor_desc(sb) : sw128_kmajor_desc(sb);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kt > t.kt0 || k > 0) ? 1u : 0u);
+            tc_mma2_bf16(d, ad + astep * k, bd + bstep * k, idesc, (kt > t.kt0 || k > 0) ? 1u : 0u);
           tc_commit2_multicast(empty_bar(stage), 0x3);
           if (++stage == STAGES) {
             stage = 0;

@@ -23,6 +23,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_DSWIGLU_BF16: return launch_pair<EPI_DSWIGLU_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_QKV_HEADS_BF16: return launch_pair<EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_F32_RESID: return launch_pair<EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_MN: return launch_pair<EPI_F32_MN>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -36,6 +37,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_QKV_HEADS_BF16:
           return launch_impl<256, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_F32_RESID: return launch_impl<256, EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_MN: return launch_impl<256, EPI_F32_MN>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;
@@ -47,6 +49,7 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
         case EPI_QKV_HEADS_BF16:
           return launch_impl<128, EPI_QKV_HEADS_BF16>(mapA, mapB, args, num_sms, stream);
         case EPI_F32_RESID: return launch_impl<128, EPI_F32_RESID>(mapA, mapB, args, num_sms, stream);
+        case EPI_F32_MN: return launch_impl<128, EPI_F32_MN>(mapA, mapB, args, num_sms, stream);
         default: break;
       }
       break;

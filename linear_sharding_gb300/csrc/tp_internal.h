@@ -28,8 +28,12 @@ enum Epi : int {
   EPI_DSWIGLU_BF16 = 8,      // out = bf16(acc u SiLU'(g)), out2 = bf16(acc SiLU(g)); aux = g, aux2 = u
   EPI_QKV_HEADS_BF16 = 9,    // out = bf16(acc) head-major: [3][n_heads][M][head_dim] (Q, K, V);
                              // with out2, V goes there transposed instead: [n_heads][head_dim][ld_out]
-  EPI_F32_RESID = 10         // one slot: out = acc (+ aux, float32) (+ aux2, bf16), same layout as out;
+  EPI_F32_RESID = 10,        // one slot: out = acc (+ aux, float32) (+ aux2, bf16), same layout as out;
                              // with out2, also out2 = bf16(out) (a residual add fused into the GEMM)
+  EPI_F32_MN = 11            // as EPI_F32, with both operands MN-major (the weight gradients, whose K
+                             // is the token axis): A and B tensor maps are [segments][K][MN per
+                             // segment] with 64 x 64 boxes; a_mn_seg / b_mn_seg are the MN rows per
+                             // segment (0: one segment)
 };
 
 // Packed rows of a SwiGLU shard alternate 128 gate rows and 128 up rows, so
@@ -43,14 +47,17 @@ constexpr int kSwigluGranule = 128;
 // segment] and k-tile kt reads coordinate (kt % kt_per_seg * 64, row,
 // kt / kt_per_seg); a flat operand (0) is [1][rows][K] and reads (kt * 64,
 // row, 0); a k-tile-blocked operand (kKtileBlocked, the packed bf16 weights)
-// is [k-tiles][rows][64] and reads (0, row, kt).  Slot s covers k-tiles
-// [s*kt_per_slot, min(kt_total, (s+1)*kt_per_slot)).
+// is [k-tiles][rows][64] and reads (0, row, kt).  With EPI_F32_MN both operands
+// are MN-major and k-tile kt reads, for each 64 rows of the tile, (row %
+// mn_seg, kt * 64, row / mn_seg).  Slot s covers k-tiles [s*kt_per_slot,
+// min(kt_total, (s+1)*kt_per_slot)).
 constexpr int kKtileBlocked = 2;
 
 struct GemmArgs {
   int m_tiles, n_tiles, slots;
   int kt_total, kt_per_seg, kt_per_slot;
   int a_seg, b_seg;
+  int a_mn_seg, b_mn_seg;  // EPI_F32_MN: MN rows per segment of A / B (0: one segment)
   int group_m;          // raster: m-tiles per group (L2 reuse of B tiles)
   int rows_valid;       // valid output rows along A (M, or features when swapped)
   int cols_valid;       // valid output columns along B (N, or tokens when swapped)
