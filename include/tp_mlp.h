@@ -111,7 +111,9 @@ TP_API int tp_abi_version(void);
  *   Shard i holds columns [i F/T, (i+1) F/T) of W1 (for SWIGLU the SAME
  *   columns of Wg and of Wu) and rows [i F/T, (i+1) F/T) of W2.  The copies
  *   are bit-exact; the device layout is K-major (each shard's W1_i and W2_i
- *   stored transposed, [out x in]) for the tensor-core GEMMs.
+ *   stored transposed, [out x in]) for the tensor-core GEMMs, and for TP_BF16
+ *   cut into k-tiles of 64 columns (each tile holding the 64 K values of every
+ *   row contiguously).  tp_shard_get returns the logical shard.
  *   W1 and W2 are only read; the caller may free them once `stream` has
  *   reached the end of this call's work.
  *   Errors: F % T != 0 -> TP_ERR_INDIVISIBLE; for TP_BF16, H % 128 != 0 or
@@ -356,17 +358,16 @@ TP_API tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const voi
  * token r < M:
  *   O[r][h hd + d] = sum_j softmax_j(q_rh . k_jh / sqrt(hd)) v_jh[d]
  * over keys j <= r (causal != 0) or all j < M (causal == 0); scores and
- * probabilities stay on chip (one fused kernel per call after a transpose of
- * V).  The probabilities are rounded to bfloat16 for the P V product and the
- * sums are float32.
+ * probabilities stay on chip (one fused kernel per call).  The probabilities
+ * are rounded to bfloat16 for the P V product and the sums are float32.
  *   Q, K, V: bfloat16, head-major [n_heads][M][head_dim], device, 16-byte
  *            aligned (the layout tp_block_forward's QKV projection writes).
  *   head_dim must be 128 (else TP_ERR_UNSUPPORTED).
  *   O: bfloat16 [M][ldo] out, head h in columns [h hd, (h+1) hd);
  *      ldo >= n_heads hd and a multiple of 8; 16-byte aligned; must not
  *      overlap Q, K or V (TP_ERR_ARG).
- *   workspace: tp_attention_workspace_bytes(M, n_heads, head_dim) bytes
- *      (V transposed per head) or NULL to allocate on `stream`.
+ *   workspace, ws_bytes: unused (the call needs no scratch);
+ *      tp_attention_workspace_bytes returns 0.
  *   M == 0 is a no-op.  Asynchronous on `stream`.
  */
 TP_API size_t tp_attention_workspace_bytes(int64_t M, int n_heads, int head_dim);

@@ -559,8 +559,6 @@ tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStrea
 
 int bn_for(int64_t n) { return n % 256 == 0 ? 256 : 128; }
 
-int64_t round64(int64_t m) { return (m + 63) / 64 * 64; }
-
 struct TrainPlan {
   int slots2 = 1;       // forward row-parallel slots
   int slots_dx = 1;     // backward dX slots
@@ -776,20 +774,16 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
 // ---- one tensor-parallel transformer block ---------------------------------------
 
 // Attention core (the block's, and tp_attention_forward): the fused kernel
-// reads Q, K and V^T [heads][128][round64(M)] through TMA.  The V^T map's key
-// extent is M, so the copy engine fills keys past M with zeros whatever the
-// padding columns hold.
-size_t attention_vt_bytes(int64_t M, int64_t heads) {
-  return static_cast<size_t>(heads * kAttnHeadDim * round64(M)) * 2;
-}
-
-tp_status_t attention_core_vt(const DevState *d, const void *Q, const void *K, const void *Vt, int64_t M,
-                              int64_t heads, int causal, void *O, int64_t ldo, cudaStream_t st) {
-  const int64_t hd = kAttnHeadDim, Mp = round64(M);
-  CUtensorMap mq, mk, mvt;
+// reads head-major Q, K and V [heads][M][128] through TMA (V in 64 x 64 boxes,
+// as the P V product's MN-major operand).  The maps' key extent is M, so the
+// copy engine fills keys past M with zeros.
+tp_status_t attention_core(const DevState *d, const void *Q, const void *K, const void *V, int64_t M,
+                           int64_t heads, int causal, void *O, int64_t ldo, cudaStream_t st) {
+  const int64_t hd = kAttnHeadDim;
+  CUtensorMap mq, mk, mv;
   TP_TRY(make_map(&mq, Q, hd, M, heads, hd * 2, M * hd * 2, 128));
   TP_TRY(make_map(&mk, K, hd, M, heads, hd * 2, M * hd * 2, 128));
-  TP_TRY(make_map(&mvt, Vt, M, hd, heads, Mp * 2, hd * Mp * 2, 128));
+  TP_TRY(make_map(&mv, V, hd, M, heads, hd * 2, M * hd * 2, 64));
   AttnArgs g;
   std::memset(&g, 0, sizeof g);
   g.M = static_cast<int>(M);
@@ -801,17 +795,16 @@ tp_status_t attention_core_vt(const DevState *d, const void *Q, const void *K, c
   g.ldo = ldo;
   g.status = d->status;
   g.wait_limit_ns = g_wait_ns.load();
-  TP_CUDA(launch_attention(mq, mk, mvt, g, d->sms, st));
+  TP_CUDA(launch_attention(mq, mk, mv, g, d->sms, st));
   return TP_OK;
 }
 
 struct BlockPlan {
   int slots_o = 1;  // O-projection accumulation slots
   MlpPlan mlp;
-  size_t qkv = 0, vt = 0, O = 0, opart = 0, h = 0, hb = 0;
+  size_t qkv = 0, O = 0, opart = 0, h = 0, hb = 0;
   size_t total() const {
-    return round256(qkv) + round256(vt) + round256(O) + round256(opart) + round256(h) + round256(hb) +
-           mlp.total();
+    return round256(qkv) + round256(O) + round256(opart) + round256(h) + round256(hb) + mlp.total();
   }
 };
 
@@ -820,8 +813,7 @@ void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t 
   const int64_t H = a->H;
   p->slots_o = v == TP_VAR_PARTIALS ? a->T : 1;
   plan_mlp(m, M, v, sms, &p->mlp);
-  p->qkv = static_cast<size_t>(2 * H * M) * 2;  // Q and K head-major; V goes to vt transposed
-  p->vt = attention_vt_bytes(M, a->n_heads);
+  p->qkv = static_cast<size_t>(3 * H * M) * 2;  // Q, K and V head-major
   p->O = static_cast<size_t>(M * H) * 2;
   p->opart = p->slots_o > 1 ? static_cast<size_t>(p->slots_o * M * H) * 4 : 0;
   p->h = static_cast<size_t>(M * H) * 4;
@@ -846,23 +838,19 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
   const int64_t H = a->H, nh = a->n_heads, hd = a->head_dim;
   char *qkv = w.ptr;
-  char *vt = qkv + round256(p.qkv);
-  char *O = vt + round256(p.vt);
+  char *O = qkv + round256(p.qkv);
   float *opart = reinterpret_cast<float *>(O + round256(p.O));
   float *h = reinterpret_cast<float *>(reinterpret_cast<char *>(opart) + round256(p.opart));
   char *hb = reinterpret_cast<char *>(h) + round256(p.h);
   char *mws = hb + round256(p.hb);
   if (h_out) h = h_out;
 
-  // 1. QKV projection of every shard: Q and K head-major [2][nh][M][hd], V transposed per
-  //    head into vt [nh][hd][round64(M)]
+  // 1. QKV projection of every shard: Q, K and V head-major [3][nh][M][hd]
   CUtensorMap mx;
   TP_TRY(make_map(&mx, X, H, M, 1, H * 2, M * H * 2, 128));
   {
     GemmArgs g = base_args(d);
     g.out = qkv;
-    g.out2 = vt;
-    g.ld_out = round64(M);
     g.shard_cols = static_cast<int>(a->R1);
     g.head_dim = static_cast<int>(hd);
     g.n_heads = static_cast<int>(nh);
@@ -878,9 +866,10 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
     c.epi = EPI_QKV_HEADS_BF16;
     TP_TRY(run_gemm(d, c, g, st));
   }
-  const char *Q = qkv, *K = qkv + static_cast<size_t>(nh * M * hd) * 2;
+  const size_t head_block = static_cast<size_t>(nh * M * hd) * 2;
+  const char *Q = qkv, *K = qkv + head_block, *V = qkv + 2 * head_block;
   // 2.-5. causal attention per head, fused: O [M x H], heads side by side
-  TP_TRY(attention_core_vt(d, Q, K, vt, M, nh, causal, O, H, st));
+  TP_TRY(attention_core(d, Q, K, V, M, nh, causal, O, H, st));
   // 6. row-parallel output projection + all-reduce-sum #1, 7. residual: h = X + the sum,
   //    hb = bf16(h) (fused into the GEMM's epilogue when it accumulates all shards in TMEM)
   CUtensorMap mo;
@@ -1316,8 +1305,10 @@ tp_status_t tp_block_forward(tp_shards_t attn, tp_shards_t mlp, const void *X, i
 }
 
 size_t tp_attention_workspace_bytes(int64_t M, int n_heads, int head_dim) {
-  if (M <= 0 || n_heads <= 0 || head_dim != kAttnHeadDim) return 0;
-  return attention_vt_bytes(M, n_heads);
+  (void)M;
+  (void)n_heads;
+  (void)head_dim;
+  return 0;  // the kernel reads Q, K and V as they are
 }
 
 tp_status_t tp_attention_forward(const void *Q, const void *K, const void *V, int64_t M, int n_heads,
@@ -1336,14 +1327,11 @@ tp_status_t tp_attention_forward(const void *Q, const void *K, const void *V, in
   if (ranges_overlap(O, out_bytes, Q, in_bytes) || ranges_overlap(O, out_bytes, K, in_bytes) ||
       ranges_overlap(O, out_bytes, V, in_bytes))
     return TP_ERR_ARG;
+  (void)workspace;
+  (void)ws_bytes;
   DevState *d = nullptr;
   TP_TRY(dev_state(&d));
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  Workspace w;
-  TP_TRY(get_ws(&w, workspace, ws_bytes, attention_vt_bytes(M, n_heads), st));
-  const int64_t hd = kAttnHeadDim, Mp = round64(M);
-  TP_CUDA(launch_transpose_pad(V, M, hd, hd, M * hd, w.ptr, Mp, hd * Mp, n_heads, st));
-  return attention_core_vt(d, Q, K, w.ptr, M, n_heads, causal, O, ldo, st);
+  return attention_core(d, Q, K, V, M, n_heads, causal, O, ldo, static_cast<cudaStream_t>(stream));
 }
 
 tp_status_t tp_partial_sum(const float *const *Zi, int T, int64_t n, float *Z, void *stream) {

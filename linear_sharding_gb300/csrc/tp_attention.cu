@@ -10,9 +10,11 @@
 // which is the softmax-weighted sum of the values for any shift m_r.  Keys
 // are visited 128 at a time and neither scores nor probabilities leave the
 // SM, or even reach shared memory:
-//   warp 0      TMA producer: both Q tiles once per unit; K and V^T tiles of
+//   warp 0      TMA producer: both Q tiles once per unit; K and V tiles of
 //               128 keys (shared by the two query tiles) through a 3-deep and
-//               a 2-deep ring, keys one tile ahead of values;
+//               a 2-deep ring, keys one tile ahead of values.  Q, K and V are
+//               all head-major [heads][M][128]; V is the P V product's B
+//               operand read MN-major (its K, the key axis, is the outer one);
 //   warp 1      TMEM allocation; one thread issues, per key tile j,
 //               O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
 //               S_B = Q_B K_{j+1}^T (tcgen05, 128 x 128, K = 128; P read from
@@ -47,11 +49,11 @@ constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 128;      // per query tile
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
 constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
-constexpr int kKst = 3, kVst = 2;         // K and V^T tiles in shared memory
+constexpr int kKst = 3, kVst = 2;         // K and V tiles in shared memory
 constexpr int kBars = 28;
 constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
-// Q[2] | K[kKst] | Vt[kVst] | barriers
+// Q[2] | K[kKst] | V[kVst] | barriers
 constexpr size_t kSmemBytes = 1024 + (2 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "attention tiles exceed the shared memory of one CTA");
 
@@ -108,8 +110,9 @@ struct Ring {
 // each then cap a thread at 168
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                    const __grid_constant__ CUtensorMap mapVt, const AttnArgs a) {
+                    const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
   constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+  constexpr uint32_t IDESC_PV = IDESC | kIdescMnB;  // V is read MN-major: [keys][head_dim]
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapQ);
     prefetch_tmap(&mapK);
-    prefetch_tmap(&mapVt);
+    prefetch_tmap(&mapV);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -192,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_v = [&](const AttnUnit &t, int j) -> bool {
         if (!wait_bar_spin(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
         mbar_arrive_expect_tx(v_full(vr.buf), kTileBytes);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + kb * kSub), &mapVt, v_full(vr.buf), j * kTile + kb * 64,
-                      0, t.head);
+        // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
+        for (int h = 0; h < 2; ++h)
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf), c * 64,
+                        j * kTile + h * 64, t.head);
         ++vc;
         vr.next(kVst);
         return true;
@@ -296,8 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t pa = tmem + q * 128 + 64;  // P: the upper 64 columns, bf16 pairs
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = sw128_kmajor_desc(vbase + (kk >> 2) * kSub);
-              tc_mma_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, bd + 2u * (kk & 3), IDESC, (j | kk) ? 1u : 0u);
+              // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
+              const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
+              tc_mma_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV,
+                                 (j | kk) ? 1u : 0u);
             }
             if (j + 1 == t.nkt[q]) tc_commit(o_full(q));
             // then this tile's S for key tile j + 1, so the other tile's P V overlaps its softmax
@@ -484,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapVt,
+cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapV,
                              const AttnArgs &args, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
@@ -492,7 +499,7 @@ cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, c
   const long long units = static_cast<long long>(args.heads) * ((args.m_tiles + 1) / 2);
   if (units <= 0) return cudaSuccess;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapQ, mapK, mapVt, args);
+  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapQ, mapK, mapV, args);
   return cudaGetLastError();
 }
 

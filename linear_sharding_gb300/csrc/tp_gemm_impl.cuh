@@ -387,14 +387,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
       const long long sh = gc / g.shard_cols, lc = gc - sh * g.shard_cols;
       const long long part = lc / W, within = lc - part * W;
       const long long head = sh * hps + within / g.head_dim, dim = within % g.head_dim;
-      if (part == 2 && g.out2 != nullptr) {
-        // V transposed per head, [n_heads][head_dim][ld_out]: for each of the 32 dims the
-        // warp's 32 rows (tokens) are 64 contiguous bytes
-        __nv_bfloat16 *vt = static_cast<__nv_bfloat16 *>(g.out2) + (head * g.head_dim + dim) * g.ld_out + row;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) vt[i * g.ld_out] = __float2bfloat16_rn(__uint_as_float(r[i]));
-        continue;
-      }
       const long long block = part * g.n_heads + head;
       store_act32<EPI_IDENT_BF16>(static_cast<__nv_bfloat16 *>(g.out) +
                                       (block * g.rows_valid + row) * g.head_dim + dim, r);

@@ -26,8 +26,7 @@ enum Epi : int {
   EPI_SWIGLU_SAVE_BF16 = 6,  // out = bf16(SiLU(g) u), out2 = bf16(g), out3 = bf16(u)
   EPI_DGELU_BF16 = 7,        // out = bf16(acc * GeLU'(aux)), aux = saved pre-activation
   EPI_DSWIGLU_BF16 = 8,      // out = bf16(acc u SiLU'(g)), out2 = bf16(acc SiLU(g)); aux = g, aux2 = u
-  EPI_QKV_HEADS_BF16 = 9,    // out = bf16(acc) head-major: [3][n_heads][M][head_dim] (Q, K, V);
-                             // with out2, V goes there transposed instead: [n_heads][head_dim][ld_out]
+  EPI_QKV_HEADS_BF16 = 9,    // out = bf16(acc) head-major: [3][n_heads][M][head_dim] (Q, K, V)
   EPI_F32_RESID = 10,        // one slot: out = acc (+ aux, float32) (+ aux2, bf16), same layout as out;
                              // with out2, also out2 = bf16(out) (a residual add fused into the GEMM)
   EPI_F32_MN = 11            // as EPI_F32, with both operands MN-major (the weight gradients, whose K
@@ -90,18 +89,13 @@ cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUt
 cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
                               const GemmArgs &args, int num_sms, cudaStream_t stream);
 
-// dst[b][c][r] = src[b][r][c] for r < rows, c < cols (bf16); dst rows are
-// dst_ld long and zero past `rows`.
-cudaError_t launch_transpose_pad(const void *src, long long rows, long long cols, long long src_ld,
-                                 long long src_batch, void *dst, long long dst_ld, long long dst_batch,
-                                 int batch, cudaStream_t stream);
 
 // Fused attention core over `heads` independent heads of dimension 128:
 // O_h[r] = sum over keys j (j <= r when causal, j < M) of
-// softmax_j(q_r . k_j * scale) v_j, for every token r < M.  Q and K are
-// head-major [heads][M][128] bf16 tensor maps (box 64 x 128), V^T is
-// [heads][128][Mp] bf16 (box 64 keys x 128 rows, keys past M zero); O is
-// bf16 [M][ldo] with head h in columns [128 h, 128 h + 128).
+// softmax_j(q_r . k_j * scale) v_j, for every token r < M.  Q, K and V are
+// head-major [heads][M][128] bf16 tensor maps (Q and K box 64 x 128 rows, V
+// box 64 x 64 rows; keys past M read as zeros); O is bf16 [M][ldo] with head h
+// in columns [128 h, 128 h + 128).
 struct AttnArgs {
   int M;
   int heads;
@@ -114,7 +108,7 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
 };
 constexpr int kAttnHeadDim = 128;
-cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapVt,
+cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapV,
                              const AttnArgs &args, int num_sms, cudaStream_t stream);
 
 // Float32 CUDA-core GEMM: D[m][n] = sum_k A[m][k] B[n][k], same work model
