@@ -887,6 +887,20 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
 
 }  // namespace
 
+bool tp::encode_store_map(CUtensorMap *m, const void *base, int elem_bytes, uint64_t d0, uint64_t d1, uint64_t d2,
+                          uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || (elem_bytes != 2 && elem_bytes != 4)) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return f(m, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+           const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tp::handle_ready_on_current_device(const tp_shards *s) {
   int dev = 0;
   if (!s || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;

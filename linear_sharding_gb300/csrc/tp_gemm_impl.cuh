@@ -27,6 +27,8 @@
 // MMAs finish and releasing its tensor memory.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "tp_device.cuh"
 #include "tp_internal.h"
 
@@ -142,8 +144,55 @@ struct MnBlocks {
 };
 constexpr uint32_t kMnBlockBytes = 64 * BK * 2;  // one 64 x 64 box
 
+// GeLU(x) = x/2 (1 + erf(x / sqrt 2)), erf by Abramowitz and Stegun, "Handbook of
+// Mathematical Functions", formula 7.1.26: for u >= 0, erf(u) = 1 - (a1 t + a2 t^2 + a3 t^3 +
+// a4 t^4 + a5 t^5) e^(-u^2), t = 1 / (1 + p u), |error| <= 1.5e-7 (the tensor-core path rounds
+// the result to bfloat16, 2^-9 relative); erf(-u) = -erf(u).  Two MUFU operations and a few
+// FMA-pipe ones per value, about half the library erff: the epilogue warps share their SM
+// sub-partitions with the copy-issuing and MMA-issuing threads, so their arithmetic slows the
+// main loop.  gelu_erf and gelu_erf2 (two values with paired float32 operations) round alike.
+namespace as7126 {
+constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                kA4 = -1.453152027f, kA5 = 1.061405429f;
+constexpr float kRsqrt2 = 0.70710678118654752f, kNegLog2e = -1.4426950408889634f;
+__device__ __forceinline__ float rcp(float d) {
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(d));
+  return t;
+}
+}  // namespace as7126
+
 __device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  using namespace as7126;
+  const float u = x * kRsqrt2, au = fabsf(u);
+  const float t = rcp(fmaf(kP, au, 1.0f));
+  float p = fmaf(t, kA5, kA4);
+  p = fmaf(t, p, kA3);
+  p = fmaf(t, p, kA2);
+  p = fmaf(t, p, kA1);
+  p = p * t;
+  const float e = ex2_approx((au * au) * kNegLog2e);  // e^(-u^2)
+  const float q = fmaf(p, e, -1.0f);                  // -erf(|u|)
+  const float h = x * 0.5f;
+  return fmaf(h, copysignf(fabsf(q), u), h);
+}
+
+__device__ __forceinline__ float2 gelu_erf2(float2 x) {
+  using namespace as7126;
+  const float2 u = __fmul2_rn(x, make_float2(kRsqrt2, kRsqrt2));
+  const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
+  const float2 d = __ffma2_rn(make_float2(kP, kP), au, make_float2(1.0f, 1.0f));
+  const float2 t = make_float2(rcp(d.x), rcp(d.y));
+  float2 p = __ffma2_rn(t, make_float2(kA5, kA5), make_float2(kA4, kA4));
+  p = __ffma2_rn(t, p, make_float2(kA3, kA3));
+  p = __ffma2_rn(t, p, make_float2(kA2, kA2));
+  p = __ffma2_rn(t, p, make_float2(kA1, kA1));
+  p = __fmul2_rn(p, t);
+  const float2 a = __fmul2_rn(__fmul2_rn(au, au), make_float2(kNegLog2e, kNegLog2e));
+  const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+  const float2 q = __ffma2_rn(p, e, make_float2(-1.0f, -1.0f));
+  const float2 h = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+  return __ffma2_rn(h, make_float2(copysignf(fabsf(q.x), u.x), copysignf(fabsf(q.y), u.y)), h);
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
@@ -487,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         KCursor kc;
         kc.start(t.kt0, g);
         for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
-          if (!wait_bar(empty_bar(stage), phase ^ 1u, w)) {
+          if (!wait_bar_spin(empty_bar(stage), phase ^ 1u, w)) {
             ok = false;
             break;
           }
@@ -541,11 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, g);
-        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, w)) break;
+        if (!wait_bar_spin(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w)) {
+          if (!wait_bar_spin(full_bar(stage), phase, w)) {
             ok = false;
             break;
           }
@@ -625,16 +674,98 @@ constexpr int kPairStages = TP_PAIR_STAGES;
 constexpr unsigned long long kPeerDrainNs = 200000ull;
 constexpr int kPairBN = 256;
 
-__host__ __device__ constexpr size_t pair_smem_bytes() {
-  return 1024 + static_cast<size_t>(kPairStages) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) + 512;
+// Epilogues that leave through TMA stores: each epilogue warp stages 32 rows x 128 bytes of its
+// output in shared memory (two buffers) and one lane stores them as a box, instead of 32
+// scattered 16-byte stores per instruction, which slowed the copies feeding the next tile.
+// The staging space (32 KiB) takes one stage of the ring.
+template <int EPI>
+__host__ __device__ constexpr bool tma_store_epi() {
+  return EPI == EPI_GELU_BF16 || EPI == EPI_IDENT_BF16 || EPI == EPI_F32;
 }
-static_assert(pair_smem_bytes() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
+constexpr uint32_t kStoreBufBytes = 32 * 128;  // 32 rows x 128 B, 128-byte swizzle
+template <int EPI>
+__host__ __device__ constexpr int pair_stages() {
+  return tma_store_epi<EPI>() ? kPairStages - 1 : kPairStages;
+}
+template <int EPI>
+__host__ __device__ constexpr size_t pair_smem_bytes() {
+  return 1024 + static_cast<size_t>(pair_stages<EPI>()) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) +
+         (tma_store_epi<EPI>() ? 8 * kStoreBufBytes : 0) + 512;
+}
+static_assert(pair_smem_bytes<EPI_F32_RESID>() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
+static_assert(pair_smem_bytes<EPI_F32>() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
+
+// Epilogue of one 256-column accumulator by one warp through TMA stores: TMEM lanes
+// [32 q, 32 q + 32) are output rows wrow .. wrow + 31; 128-byte column chunks (64 bf16 or 32
+// float32) go through the warp's two staging buffers, row `lane` with its 16-byte pieces in
+// the 128-byte swizzle.  mapO is [segments][rows][columns]: shards of the bf16 Y, or slots of
+// the float32 output; rows past the map's row count are not stored.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile_tma(uint32_t tb, const Unit &t, int wrow, int lane, const GemmArgs &g,
+                                                  const CUtensorMap *mapO, uint8_t *bufs, uint32_t &nstore) {
+  constexpr bool f32 = EPI == EPI_F32;
+  constexpr int CW = f32 ? 32 : 64;  // columns per 128-byte row chunk
+  int x0, z;
+  if constexpr (f32) {
+    x0 = t.n * BN;
+    z = t.slot;
+  } else {
+    const int col0 = t.n * BN;
+    z = col0 / g.shard_cols;
+    x0 = col0 - z * g.shard_cols;
+  }
+  const bool rows_in = wrow < g.rows_valid;
+#pragma unroll 1
+  for (int c = 0; c < BN / CW; ++c) {
+    uint8_t *buf = bufs + (nstore & 1u) * kStoreBufBytes;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done with it
+    __syncwarp();
+    uint32_t w[32];
+    if constexpr (f32) {
+      tmem_ld32(tb + c * 32, w);
+      tmem_ld_wait();
+      tmem_reg_fence(w);
+    } else {
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tb + c * 64, r0);
+      tmem_ld32(tb + c * 64 + 32, r1);
+      tmem_ld_wait();
+      tmem_reg_fence(r0);
+      tmem_reg_fence(r1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
+        float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
+        if constexpr (EPI == EPI_GELU_BF16) {
+          const float2 ga = gelu_erf2(make_float2(a0, a1)), gb = gelu_erf2(make_float2(b0, b1));
+          a0 = ga.x;
+          a1 = ga.y;
+          b0 = gb.x;
+          b1 = gb.y;
+        }
+        w[j] = pack_bf16x2(a0, a1);
+        w[16 + j] = pack_bf16x2(b0, b1);
+      }
+    }
+    uint4 *row = reinterpret_cast<uint4 *>(buf + lane * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) row[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (rows_in) tma_store_3d(mapO, smem_u32(buf), x0 + c * CW, wrow, z);
+      bulk_commit();
+    }
+    ++nstore;
+  }
+}
 
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tp_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapB, const GemmArgs g) {
-  constexpr int STAGES = kPairStages;
+                        const __grid_constant__ CUtensorMap mapB,
+                        const __grid_constant__ CUtensorMap mapO, const GemmArgs g) {
+  constexpr int STAGES = pair_stages<EPI>();
   constexpr int BN = kPairBN;
   constexpr uint32_t A_BYTES = 128 * BK * 2;
   constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
@@ -647,7 +778,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint8_t *sO = sB + STAGES * B_BYTES;  // TMA-store staging: 2 buffers per epilogue warp
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sO + (tma_store_epi<EPI>() ? 8 * kStoreBufBytes : 0));
   // barriers: full[S] | empty[S] | tfull[kAcc] | tempty[kAcc] | drain | never
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 2 * kAcc + 2);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -681,6 +813,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapA);
     prefetch_tmap(&mapB);
+    if constexpr (tma_store_epi<EPI>()) prefetch_tmap(&mapO);
   }
   if (warp == 1) {
     tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
@@ -714,7 +847,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         KCursor kc;
         kc.start(t.kt0, g);
         for (int kt = t.kt0; kt < t.kt1; ++kt, kc.next()) {
-          if (!wait_bar_cluster(empty_bar(stage), phase ^ 1u, w)) {
+          if (!wait_bar_spin(empty_bar(stage), phase ^ 1u, w)) {
             ok = false;
             break;
           }
@@ -777,11 +910,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
       for (int u = cluster_id; u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
-        if (!wait_bar_cluster(tempty_bar(acc), acc_phase ^ 1u, w)) break;
+        if (!wait_bar_spin(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!wait_bar(full_bar(stage), phase, w)) {
+          if (!wait_bar_spin(full_bar(stage), phase, w)) {
             ok = false;
             break;
           }
@@ -815,6 +948,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t nstore = 0;  // TMA-store chunks this warp issued
     for (int u = cluster_id; u < units; u += nclusters) {
       const Unit t = decode_unit(u, g);
       const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
@@ -822,7 +956,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, EPI>(tb, t, t.m * 256 + 128 * static_cast<int>(rank), row_in_tile, g);
+      if constexpr (tma_store_epi<EPI>())
+        epilogue_tile_tma<BN, EPI>(tb, t, t.m * 256 + 128 * static_cast<int>(rank) + q * 32, lane, g, &mapO,
+                                   sO + q * 2 * kStoreBufBytes, nstore);
+      else
+        epilogue_tile<BN, EPI>(tb, t, t.m * 256 + 128 * static_cast<int>(rank), row_in_tile, g);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
@@ -831,6 +969,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    // the staging buffers must outlive the stores that read them
+    if (tma_store_epi<EPI>() && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -844,8 +985,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <int EPI>
 cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
                         cudaStream_t stream) {
-  constexpr size_t smem = pair_smem_bytes();
+  constexpr size_t smem = pair_smem_bytes<EPI>();
   auto kern = tp_gemm_pair_kernel<EPI>;
+  CUtensorMap o;
+  std::memset(&o, 0, sizeof o);
+  if constexpr (tma_store_epi<EPI>()) {
+    // the output as [segments][rows][columns]: float32 slots, or the bf16 per-shard Y buffers
+    bool ok;
+    const uint64_t rows = static_cast<uint64_t>(g.rows_valid);
+    if constexpr (EPI == EPI_F32) {
+      const uint64_t ld = static_cast<uint64_t>(g.ld_out) * 4;
+      const uint64_t ss = g.slots > 1 ? static_cast<uint64_t>(g.slot_stride) * 4 : rows * ld;
+      ok = encode_store_map(&o, g.out, 4, static_cast<uint64_t>(g.ld_out), rows, static_cast<uint64_t>(g.slots), ld,
+                            ss, 32, 32);
+    } else {
+      const uint64_t shards = static_cast<uint64_t>(g.cols_valid / g.shard_cols);
+      ok = encode_store_map(&o, g.out, 2, static_cast<uint64_t>(g.shard_cols), rows, shards,
+                            static_cast<uint64_t>(g.ld_out) * 2, static_cast<uint64_t>(g.shard_stride) * 2, 64, 32);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -869,7 +1028,7 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
     mc = n;
   }
   const int clusters = static_cast<int>(units < mc ? units : mc);
-  kern<<<2 * clusters, kThreads, smem, stream>>>(a, b, g);
+  kern<<<2 * clusters, kThreads, smem, stream>>>(a, b, o, g);
   return cudaGetLastError();
 }
 

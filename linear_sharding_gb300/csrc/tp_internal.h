@@ -82,6 +82,13 @@ enum GemmCfg : int {
                      // B tensor map box 128 rows (each CTA loads half of the B tile)
 };
 
+// Tensor map for the TMA stores of a GEMM epilogue: elements of 2 (bf16) or 4
+// (float32) bytes, dims {d0 (contiguous), d1, d2}, byte strides {s1, s2}, box
+// {box0, box1, 1} (box0 x elem_bytes = 128), 128-byte swizzle.  False if the
+// driver rejects it.
+bool encode_store_map(CUtensorMap *m, const void *base, int elem_bytes, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1);
+
 // Launch the tensor-core GEMM.  Returns cudaSuccess or the launch error.
 cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
                         const GemmArgs &args, int num_sms, cudaStream_t stream);

@@ -116,6 +116,33 @@ def test_mlp_bf16_small(tp, variant, act, M, H, F, T):
     assert rowwise_rms_error(Z, Zref) <= TOL_BF16_ROW_RMS
 
 
+def _bf16_round_bits(x: np.ndarray) -> np.ndarray:
+    """float64 -> bfloat16 bit patterns, rounding the float32 value to nearest even."""
+    b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_gelu_epilogue_is_exact_erf_gelu_to_bf16(tp):
+    """With W1 = I the column-parallel GEMM's output is bf16(GeLU(x)) of each input x (x * 1
+    accumulates exactly), so this checks the epilogue's erf ("Tensor Parallelism in Action",
+    section 1: Y_i = GeLU(X A_i), erf form) against the fp64 oracle's GeLU over [-8, 8]: each
+    output within one bfloat16 step of the exact value, or 1e-6 in the far negative tail.
+    M = 384 is one and a half 256-row CTA-pair tiles, so the tile stores clip a tail."""
+    M, H = 384, 256
+    xb = _bf16_round_bits(np.linspace(-8.0, 8.0, M * H)).reshape(M, H)
+    eye = np.zeros((H, H), dtype=np.uint16)
+    eye[np.arange(H), np.arange(H)] = 0x3F80  # bfloat16 1.0
+    s = tp.tp_shard_weights(to_device(eye), to_device(eye), 1, "gelu")
+    Y = tp.tp_colpar_forward(s, to_device(xb))
+    _sync()
+    got = (bf16_bits(Y[0]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    x = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = np.array([oracle.gelu(v) for v in x.ravel()]).reshape(M, H)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    err = np.abs(got - ref)
+    assert np.all(err <= step + 1e-6), float(np.max(err - step))
+
+
 @pytest.mark.parametrize("variant", ["partials", "tmem_acc", "auto"])
 @pytest.mark.parametrize("act", ["gelu", "swiglu", "identity"])
 @pytest.mark.parametrize("M", [1, 4, 16])
