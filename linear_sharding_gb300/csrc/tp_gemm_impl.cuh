@@ -195,7 +195,17 @@ __device__ __forceinline__ float2 gelu_erf2(float2 x) {
   return __ffma2_rn(h, make_float2(copysignf(fabsf(q.x), u.x), copysignf(fabsf(q.y), u.y)), h);
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU(g) = g / (1 + e^-g) with the ex2 and rcp approximations (relative error about 1e-7,
+// far below bfloat16's); silu2 pairs the multiplications and rounds alike.
+__device__ __forceinline__ float silu(float g) {
+  return g * as7126::rcp(1.0f + ex2_approx(g * as7126::kNegLog2e));
+}
+
+__device__ __forceinline__ float2 silu2(float2 g) {
+  const float2 a = __fmul2_rn(g, make_float2(as7126::kNegLog2e, as7126::kNegLog2e));
+  const float2 r = make_float2(as7126::rcp(1.0f + ex2_approx(a.x)), as7126::rcp(1.0f + ex2_approx(a.y)));
+  return __fmul2_rn(g, r);
+}
 
 // GeLU'(y) = Phi(y) + y phi(y);  SiLU'(g) = s (1 + g (1 - s)), s = sigmoid(g).
 __device__ __forceinline__ float gelu_grad(float y) {
@@ -680,7 +690,7 @@ constexpr int kPairBN = 256;
 // The staging space (32 KiB) takes one stage of the ring.
 template <int EPI>
 __host__ __device__ constexpr bool tma_store_epi() {
-  return EPI == EPI_GELU_BF16 || EPI == EPI_IDENT_BF16 || EPI == EPI_F32;
+  return EPI == EPI_GELU_BF16 || EPI == EPI_IDENT_BF16 || EPI == EPI_F32 || EPI == EPI_SWIGLU_BF16;
 }
 constexpr uint32_t kStoreBufBytes = 32 * 128;  // 32 rows x 128 B, 128-byte swizzle
 template <int EPI>
@@ -704,19 +714,21 @@ template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile_tma(uint32_t tb, const Unit &t, int wrow, int lane, const GemmArgs &g,
                                                   const CUtensorMap *mapO, uint8_t *bufs, uint32_t &nstore) {
   constexpr bool f32 = EPI == EPI_F32;
-  constexpr int CW = f32 ? 32 : 64;  // columns per 128-byte row chunk
+  constexpr bool swiglu = EPI == EPI_SWIGLU_BF16;  // 128 gate then 128 up columns -> 128 outputs
+  constexpr int CW = f32 ? 32 : 64;                 // output columns per 128-byte row chunk
+  constexpr int OUT_COLS = swiglu ? BN / 2 : BN;
   int x0, z;
   if constexpr (f32) {
     x0 = t.n * BN;
     z = t.slot;
   } else {
-    const int col0 = t.n * BN;
+    const int col0 = t.n * OUT_COLS;
     z = col0 / g.shard_cols;
     x0 = col0 - z * g.shard_cols;
   }
   const bool rows_in = wrow < g.rows_valid;
 #pragma unroll 1
-  for (int c = 0; c < BN / CW; ++c) {
+  for (int c = 0; c < OUT_COLS / CW; ++c) {
     uint8_t *buf = bufs + (nstore & 1u) * kStoreBufBytes;
     if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done with it
     __syncwarp();
@@ -725,6 +737,26 @@ __device__ __forceinline__ void epilogue_tile_tma(uint32_t tb, const Unit &t, in
       tmem_ld32(tb + c * 32, w);
       tmem_ld_wait();
       tmem_reg_fence(w);
+    } else if constexpr (swiglu) {
+      uint32_t g0[32], g1[32], u0[32], u1[32];
+      tmem_ld32(tb + c * 64, g0);
+      tmem_ld32(tb + c * 64 + 32, g1);
+      tmem_ld32(tb + BN / 2 + c * 64, u0);
+      tmem_ld32(tb + BN / 2 + c * 64 + 32, u1);
+      tmem_ld_wait();
+      tmem_reg_fence(g0);
+      tmem_reg_fence(g1);
+      tmem_reg_fence(u0);
+      tmem_reg_fence(u1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 ha = __fmul2_rn(silu2(make_float2(__uint_as_float(g0[2 * j]), __uint_as_float(g0[2 * j + 1]))),
+                                     make_float2(__uint_as_float(u0[2 * j]), __uint_as_float(u0[2 * j + 1])));
+        const float2 hb = __fmul2_rn(silu2(make_float2(__uint_as_float(g1[2 * j]), __uint_as_float(g1[2 * j + 1]))),
+                                     make_float2(__uint_as_float(u1[2 * j]), __uint_as_float(u1[2 * j + 1])));
+        w[j] = pack_bf16x2(ha.x, ha.y);
+        w[16 + j] = pack_bf16x2(hb.x, hb.y);
+      }
     } else {
       uint32_t r0[32], r1[32];
       tmem_ld32(tb + c * 64, r0);
