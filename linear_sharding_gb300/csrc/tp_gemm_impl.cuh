@@ -208,13 +208,29 @@ __device__ __forceinline__ float2 silu2(float2 g) {
 }
 
 // GeLU'(y) = Phi(y) + y phi(y);  SiLU'(g) = s (1 + g (1 - s)), s = sigmoid(g).
-__device__ __forceinline__ float gelu_grad(float y) {
-  return 0.5f * (1.0f + erff(y * 0.70710678118654752f)) +
-         y * 0.39894228040143268f * __expf(-0.5f * y * y);
+// erf(u) by the same formula 7.1.26 as gelu_erf.
+__device__ __forceinline__ float erf_as7126(float u) {
+  using namespace as7126;
+  const float au = fabsf(u);
+  const float t = rcp(fmaf(kP, au, 1.0f));
+  float p = fmaf(t, kA5, kA4);
+  p = fmaf(t, p, kA3);
+  p = fmaf(t, p, kA2);
+  p = fmaf(t, p, kA1);
+  p = p * t;
+  const float q = fmaf(p, ex2_approx((au * au) * kNegLog2e), -1.0f);  // -erf(|u|)
+  return copysignf(fabsf(q), u);
 }
 
+// GeLU'(y) = Phi(y) + y phi(y), with erf and the exponential as in the forward epilogue.
+__device__ __forceinline__ float gelu_grad(float y) {
+  return 0.5f * (1.0f + erf_as7126(y * as7126::kRsqrt2)) +
+         y * 0.39894228040143268f * ex2_approx((y * y) * (0.5f * as7126::kNegLog2e));
+}
+
+// SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g) by the ex2 and rcp approximations.
 __device__ __forceinline__ float silu_grad(float g) {
-  const float s = 1.0f / (1.0f + __expf(-g));
+  const float s = as7126::rcp(1.0f + ex2_approx(g * as7126::kNegLog2e));
   return s * (1.0f + g * (1.0f - s));
 }
 
