@@ -386,6 +386,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  pdl_trigger: the next kernel on the stream, if it was
+// launched as a programmatic dependent, may be scheduled once every CTA of this grid has
+// triggered or exited.  pdl_wait: blocks until the grid this kernel depends on (if any) has
+// completed and its memory is visible; a no-op for an ordinary launch.  A kernel launched as a
+// dependent touches no global data before pdl_wait.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // TMA tensor store of a box from this CTA's shared memory, tracked in the
 // issuing thread's bulk group (no mbarrier).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2) {

@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include <cstring>
+#include <utility>
 
 #include "tp_device.cuh"
 #include "tp_internal.h"
@@ -541,6 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above overlaps the previous kernel's tail; its outputs are read only from here on
+  pdl_trigger();
+  pdl_wait();
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
   const int units = g.slots * g.m_tiles * g.n_tiles;
@@ -871,6 +875,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above overlaps the previous kernel's tail; its outputs are read only from here on
+  pdl_trigger();
+  pdl_wait();
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
   const int units = g.slots * g.m_tiles * g.n_tiles;
@@ -1030,6 +1037,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// Launch as a programmatic dependent of the previous kernel on the stream: the kernel's
+// set-up (barriers, TMEM, tensor-map prefetch) runs while that kernel finishes, and
+// pdl_wait in the kernel orders everything after it behind that kernel's completion.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, size_t smem, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int EPI>
 cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
                         cudaStream_t stream) {
@@ -1076,8 +1101,7 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
     mc = n;
   }
   const int clusters = static_cast<int>(units < mc ? units : mc);
-  kern<<<2 * clusters, kThreads, smem, stream>>>(a, b, o, g);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(2 * clusters), smem, stream, a, b, o, g);
 }
 
 template <int BN, int EPI>
@@ -1091,8 +1115,7 @@ cudaError_t launch_impl(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
   const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  kern<<<grid, kThreads, smem, stream>>>(a, b, g);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), smem, stream, a, b, g);
 }
 
 }  // namespace
