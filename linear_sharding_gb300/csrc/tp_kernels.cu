@@ -11,6 +11,9 @@
 //   - the decode activation, which finishes split-K first-layer partials.
 #include <cuda_bf16.h>
 
+#include <utility>
+
+#include "tp_device.cuh"
 #include "tp_internal.h"
 
 namespace tp {
@@ -41,6 +44,8 @@ __device__ __forceinline__ void add4(float4 &s, const float4 &v) {
 // flight before the first add.
 template <int T>
 __global__ void __launch_bounds__(256) shard_sum_fixed(const PartList L, long long n4, float *Z) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the kernel before
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += stride) {
@@ -56,6 +61,8 @@ __global__ void __launch_bounds__(256) shard_sum_fixed(const PartList L, long lo
 
 // Any T: groups of 8 loads in flight, added in ascending order.
 __global__ void __launch_bounds__(256) shard_sum_any(const PartList L, int T, long long n4, float *Z) {
+  pdl_trigger();
+  pdl_wait();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += stride) {
@@ -76,6 +83,8 @@ __global__ void __launch_bounds__(256) shard_sum_any(const PartList L, int T, lo
 // Scalar path for elements [first, n) (the tail after the vector part, or
 // everything when a pointer is not 16-byte aligned).
 __global__ void shard_sum_scalar(const PartList L, int T, long long first, long long n, float *Z) {
+  pdl_trigger();
+  pdl_wait();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = first + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
@@ -356,6 +365,8 @@ __global__ void simt_gemm_kernel(const SimtArgs a) {
 __global__ void decode_act_kernel(const float *P, int slots, long long slot_stride, long long ldp,
                                   int M, int T, int Fs, int act, int swiglu_rows,
                                   __nv_bfloat16 *h) {
+  pdl_trigger();
+  pdl_wait();  // the partials come from the GEMM before
   const long long total = static_cast<long long>(M) * T * Fs;
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
        e += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -383,6 +394,22 @@ __global__ void decode_act_kernel(const float *P, int slots, long long slot_stri
   }
 }
 
+// Launch as a programmatic dependent of the previous kernel on the stream (the kernel calls
+// pdl_wait before reading anything).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), int grid, int threads, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 int grid_for(long long items, int threads, int num_sms, int per_sm) {
   long long g = (items + threads - 1) / threads;
   const long long cap = static_cast<long long>(num_sms) * per_sm;
@@ -407,21 +434,23 @@ cudaError_t launch_shard_sum(const float *const *parts, int T, long long n, floa
   long long n4 = aligned ? n / 4 : 0;
   if (n4 > 0) {
     const int grid = grid_for(n4, threads, num_sms, 8);
+    cudaError_t e;
     switch (T) {
-      case 1: shard_sum_fixed<1><<<grid, threads, 0, stream>>>(L, n4, Z); break;
-      case 2: shard_sum_fixed<2><<<grid, threads, 0, stream>>>(L, n4, Z); break;
-      case 4: shard_sum_fixed<4><<<grid, threads, 0, stream>>>(L, n4, Z); break;
-      case 8: shard_sum_fixed<8><<<grid, threads, 0, stream>>>(L, n4, Z); break;
-      case 16: shard_sum_fixed<16><<<grid, threads, 0, stream>>>(L, n4, Z); break;
-      default: shard_sum_any<<<grid, threads, 0, stream>>>(L, T, n4, Z); break;
+      case 1: e = launch_dependent(shard_sum_fixed<1>, grid, threads, stream, L, n4, Z); break;
+      case 2: e = launch_dependent(shard_sum_fixed<2>, grid, threads, stream, L, n4, Z); break;
+      case 4: e = launch_dependent(shard_sum_fixed<4>, grid, threads, stream, L, n4, Z); break;
+      case 8: e = launch_dependent(shard_sum_fixed<8>, grid, threads, stream, L, n4, Z); break;
+      case 16: e = launch_dependent(shard_sum_fixed<16>, grid, threads, stream, L, n4, Z); break;
+      default: e = launch_dependent(shard_sum_any, grid, threads, stream, L, T, n4, Z); break;
     }
+    if (e != cudaSuccess) return e;
   }
   const long long first = n4 * 4;
   if (first < n) {
     const int grid = grid_for(n - first, threads, num_sms, 8);
-    shard_sum_scalar<<<grid, threads, 0, stream>>>(L, T, first, n, Z);
+    return launch_dependent(shard_sum_scalar, grid, threads, stream, L, T, first, n, Z);
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_shard_sum_strided(const float *P, int slots, long long slot_stride, long long n,
@@ -562,10 +591,8 @@ cudaError_t launch_decode_act(const float *P, int slots, long long slot_stride, 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = grid_for(total, 256, sms, 8);
-  decode_act_kernel<<<grid, 256, 0, stream>>>(P, slots, slot_stride, ldp, M, T, Fs, act,
-                                              swiglu_rows ? 1 : 0,
-                                              static_cast<__nv_bfloat16 *>(h));
-  return cudaGetLastError();
+  return launch_dependent(decode_act_kernel, grid, 256, stream, P, slots, slot_stride, ldp, M, T, Fs, act,
+                          swiglu_rows ? 1 : 0, static_cast<__nv_bfloat16 *>(h));
 }
 
 }  // namespace tp
