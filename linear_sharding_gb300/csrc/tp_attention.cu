@@ -171,6 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above overlaps the previous kernel's tail; Q, K and V are read only from here on
+  pdl_trigger();
+  pdl_wait();
   const WaitCtl w{abort_flag, a.status, a.wait_limit_ns};
   const int units = a.heads * ((a.m_tiles + 1) / 2);
   const int G = gridDim.x, b = blockIdx.x;
@@ -499,8 +502,18 @@ cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, c
   const long long units = static_cast<long long>(args.heads) * ((args.m_tiles + 1) / 2);
   if (units <= 0) return cudaSuccess;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mapQ, mapK, mapV, args);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the previous kernel (the QKV projection)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel, mapQ, mapK, mapV, args);
 }
 
 }  // namespace tp
