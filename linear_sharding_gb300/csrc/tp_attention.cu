@@ -418,23 +418,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 64..95, whose scores are used by then).  The row sum adds the rounded weights the
         // P V product uses, so each output is a convex combination of the values (the
         // rounding of P cancels in it).
-        float sum8[8];
+        // (paired float32 operations: two scores per FFMA2 and FADD2)
+        float2 sum4[4];
 #pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) sum8[g8] = 0.f;
+        for (int g4 = 0; g4 < 4; ++g4) sum4[g4] = make_float2(0.f, 0.f);
+        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
 #pragma unroll
         for (int hh = 1; hh >= 0; --hh) {
           if (hh == 0) load_half(0);
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            pk[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(s[i >> 4][(2 * i) & 31]), c, -m_new)),
-                                ex2_approx(fmaf(__uint_as_float(s[i >> 4][(2 * i + 1) & 31]), c, -m_new)));
-            sum8[(2 * i) & 7] += __uint_as_float(pk[i] << 16);
-            sum8[(2 * i + 1) & 7] += __uint_as_float(pk[i] & 0xFFFF0000u);
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[i >> 4][(2 * i) & 31]),
+                                                    __uint_as_float(s[i >> 4][(2 * i + 1) & 31])),
+                                        c2, nm2);
+            pk[i] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
+            sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(__uint_as_float(pk[i] << 16),
+                                                               __uint_as_float(pk[i] & 0xFFFF0000u)));
           }
           tmem_st32(sb + 64 + hh * 32, pk);
         }
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        const float sum = ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
+                          ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
         l_run = fmaf(l_run, alpha, sum);
         // a raised shift also scales the accumulated O; the previous P V is already in it
         // (the commit that signalled this S covered it)
