@@ -89,6 +89,12 @@ __device__ __forceinline__ AttnUnit decode(int u, const AttnArgs &a) {
   return t;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -393,16 +399,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (hh * 64 + cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
           }
         };
-        // row maximum: eight independent chains
+        // row maximum: four independent chains of three-input maxima
         float mx8[8];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           load_half(hh);
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4) {
-            float m = hh ? mx8[g4] : __uint_as_float(s[g4 >> 1][(g4 & 1) * 16]);
+            const uint32_t *v = &s[g4 >> 1][(g4 & 1) * 16];
+            float m = hh ? mx8[g4] : fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
 #pragma unroll
-            for (int i = hh ? 0 : 1; i < 16; ++i) m = fmaxf(m, __uint_as_float(s[g4 >> 1][(g4 & 1) * 16 + i]));
+            for (int i = hh ? 0 : 2; i < 16; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
             mx8[g4] = m;
           }
         }
