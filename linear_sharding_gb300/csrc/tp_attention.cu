@@ -382,62 +382,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool masked = kmax < kTile - 1;
         // every key tile a row visits holds at least one allowed key (its own, or key < M)
         if (!TP_CHECK(kmax >= 0, a.status)) kmax = 0;
-        // the row of S_j in two halves of 64 scores (registers for one half at a time):
-        // first its maximum, then the weights
-        uint32_t s[2][32];
-        auto load_half = [&](int hh) {
-          tmem_ld32(sb + hh * 64, s[0]);
-          tmem_ld32(sb + hh * 64 + 32, s[1]);
-          tmem_ld_wait();
-          tmem_reg_fence(s[0]);
-          tmem_reg_fence(s[1]);
-          if (masked) {
+        // the whole row of S_j (128 scores) in registers: its maximum, then the weights
+        uint32_t s[4][32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(sb + cc * 32, s[cc]);
+        tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (hh * 64 + cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
-          }
-        };
-        // row maximum: four independent chains of three-input maxima
-        float mx8[8];
+        for (int cc = 0; cc < 4; ++cc) tmem_reg_fence(s[cc]);
+        if (masked) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          load_half(hh);
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const uint32_t *v = &s[g4 >> 1][(g4 & 1) * 16];
-            float m = hh ? mx8[g4] : fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
-#pragma unroll
-            for (int i = hh ? 0 : 2; i < 16; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-            mx8[g4] = m;
-          }
+            for (int i = 0; i < 32; ++i)
+              if (cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
         }
-        const float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+        // row maximum: four independent chains of three-input maxima
+        float mx4[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float m = fmaxf(__uint_as_float(s[cc][0]), __uint_as_float(s[cc][1]));
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) m = fmax3(m, __uint_as_float(s[cc][i]), __uint_as_float(s[cc][i + 1]));
+          mx4[cc] = m;
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_tile = mx * c;
         const bool raise = m_tile > m_used + kRescaleGap;
         const float m_new = raise ? m_tile : m_used;
         const float alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
         m_used = m_new;
         // P = 2^(t - m) as bf16 pairs over the upper 64 columns of the S buffer: keys 64 hh ..
-        // 64 hh + 63 into columns 64 + 32 hh ..  The upper half of S is still in registers, so
-        // it goes first (into columns 96..127), then the lower half is read again (into
-        // 64..95, whose scores are used by then).  The row sum adds the rounded weights the
-        // P V product uses, so each output is a convex combination of the values (the
-        // rounding of P cancels in it).
-        // (paired float32 operations: two scores per FFMA2 and FADD2)
+        // 64 hh + 63 into columns 64 + 32 hh (the scores are all in registers by now).  The
+        // row sum adds the rounded weights the P V product uses, so each output is a convex
+        // combination of the values (the rounding of P cancels in it).  Paired float32
+        // operations: two scores per FFMA2 and FADD2.
         float2 sum4[4];
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) sum4[g4] = make_float2(0.f, 0.f);
         const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
 #pragma unroll
-        for (int hh = 1; hh >= 0; --hh) {
-          if (hh == 0) load_half(0);
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(s[i >> 4][(2 * i) & 31]),
-                                                    __uint_as_float(s[i >> 4][(2 * i + 1) & 31])),
+            const uint32_t *v = s[2 * hh + (i >> 4)];
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])),
                                         c2, nm2);
             pk[i] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
             sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(__uint_as_float(pk[i] << 16),
