@@ -705,8 +705,9 @@ constexpr unsigned long long kPeerDrainNs = 200000ull;
 constexpr int kPairBN = 256;
 
 // Epilogues that leave through TMA stores: each epilogue warp stages 32 rows x 128 bytes of its
-// output in shared memory (two buffers) and one lane stores them as a box, instead of 32
-// scattered 16-byte stores per instruction, which slowed the copies feeding the next tile.
+// output in shared memory (two buffers) and one lane stores them as a box, instead of each
+// thread writing its row with 16-byte stores (32 rows per store instruction).  The epilogue
+// runs while the next tile's main loop does, so every instruction it saves helps that loop.
 // The staging space (32 KiB) takes one stage of the ring.
 template <int EPI>
 __host__ __device__ constexpr bool tma_store_epi() {
