@@ -273,6 +273,25 @@ __device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (
   for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
 }
 
+// 32-byte global accesses: one instruction moves a whole 32-byte sector, where
+// two 16-byte ones would each send half a sector (twice the requests and, for
+// stores, twice the bytes through the crossbar).  The address must be 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_global_v8(const void *p, uint32_t *v) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p)
+               : "memory");
+}
+
+__device__ __forceinline__ bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 // Epilogue of one tile by the 128 epilogue threads: each thread owns TMEM
 // lane `row_in_tile`, i.e. output row row0 + row_in_tile; `tb` addresses that
 // lane's quarter at the accumulator's first column.
@@ -296,12 +315,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const bool valid = row < g.rows_valid;
     float *out = static_cast<float *>(g.out) + t.slot * g.slot_stride +
                  static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
+    const bool wide = aligned32(out);  // rows of a multiple of 8 floats on a 32-byte base
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tb + c * 32, r);
       tmem_ld_wait();
-      if (valid) {
+      if (valid && wide) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_global_v8(out + c * 32 + 8 * j, r + 8 * j);
+      } else if (valid) {
         float4 *d = reinterpret_cast<float4 *>(out + c * 32);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -317,6 +340,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
     const float *addf = static_cast<const float *>(g.aux);
     const __nv_bfloat16 *addb = static_cast<const __nv_bfloat16 *>(g.aux2);
     __nv_bfloat16 *outb = static_cast<__nv_bfloat16 *>(g.out2);
+    // the float32 rows (output and residual) move 32 bytes at a time when aligned
+    const bool wide = aligned32(out) && (!addf || aligned32(addf + off));
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -326,7 +351,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      if (addf) {
+      if (addf && wide) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t x[8];
+          ld_global_v8(addf + off + c * 32 + 8 * j, x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[8 * j + k] += __uint_as_float(x[k]);
+        }
+      } else if (addf) {
         const float4 *a = reinterpret_cast<const float4 *>(addf + off + c * 32);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -350,9 +383,19 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
           }
         }
       }
-      float4 *d = reinterpret_cast<float4 *>(out + c * 32);
+      if (wide) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int j = 0; j < 4; ++j) {
+          uint32_t x[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[k] = __float_as_uint(v[8 * j + k]);
+          st_global_v8(out + c * 32 + 8 * j, x);
+        }
+      } else {
+        float4 *d = reinterpret_cast<float4 *>(out + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
       if (outb) {
         uint32_t vb[32];
 #pragma unroll

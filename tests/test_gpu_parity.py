@@ -341,6 +341,31 @@ def test_outputs_stay_inside_their_buffers(tp, act, M, H, F, T, variant):
         assert normwise_error(Z.cpu().numpy(), Zref) <= TOL_F32_NORMWISE
 
 
+@pytest.mark.parametrize("M,variant", [(64, "tmem_acc"), (64, "partials"), (300, "tmem_acc")])
+def test_float32_output_on_16_byte_boundary_matches_32(tp, M, variant):
+    """The float32 epilogue stores 32 bytes at a time where the output rows are
+    32-byte aligned and 16 at a time otherwise; Z at a 16-byte offset (legal:
+    device pointers need 16-byte alignment) gives bit-identical results."""
+    import torch
+    H, F, T = 256, 1024, 2
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=5, x_rows=M)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
+    Y = tp.tp_colpar_forward(s, to_device(d["X"]))
+    za = torch.full((M * H + 8,), float("nan"), dtype=torch.float32, device="cuda")
+    zb = torch.full((M * H + 8,), float("nan"), dtype=torch.float32, device="cuda")
+    Za = za[:M * H].view(M, H)           # the allocation's start: 32-byte aligned
+    Zb = zb[4:4 + M * H].view(M, H)      # 16 bytes further
+    assert Za.data_ptr() % 32 == 0 and Zb.data_ptr() % 32 == 16
+    tp.tp_rowpar_forward(s, Y, variant, Za)
+    tp.tp_rowpar_forward(s, Y, variant, Zb)
+    _sync()
+    assert tp.tp_last_device_status() == 0
+    assert torch.equal(Za, Zb)
+    assert torch.isnan(zb[:4]).all() and torch.isnan(zb[4 + M * H:]).all()
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")
+    assert rowwise_rms_error(Za.cpu().numpy(), Zref) <= TOL_BF16_ROW_RMS
+
+
 # ---- reduce-scatter, all-gather, bf16 all-reduce (bit exact) -----------------------
 
 @pytest.mark.parametrize("T,n", [(2, 4096), (4, 1 << 20), (8, 8 * 1001), (3, 3 * 77), (8, 8 * 4096)])
