@@ -23,7 +23,7 @@
 //   warps 2..5  softmax of tile A, warps 6..9 of tile B: one thread per query
 //               row (TMEM lane = row) reads the row of S into registers, takes
 //               its maximum, writes P = 2^(t - m_r) as bf16 over the upper 64
-//               columns of the same TMEM buffer, and adds the rounded weights
+//               columns of the same TMEM buffer, and adds the float32 weights
 //               to the row sum.
 // Each query tile has one S/P buffer: the next S into it is issued after the
 // P V that reads it, and tcgen05 MMAs of one thread run in issue order.  The
@@ -98,6 +98,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// One 32-byte global store (a whole sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // Position in a ring of n buffers: buffer index and phase parity, stepped per use.
@@ -413,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         // P = 2^(t - m) as bf16 pairs over the upper 64 columns of the S buffer: keys 64 hh ..
         // 64 hh + 63 into columns 64 + 32 hh (the scores are all in registers by now).  The
-        // row sum adds the rounded weights the P V product uses, so each output is a convex
-        // combination of the values (the rounding of P cancels in it).  Paired float32
-        // operations: two scores per FFMA2 and FADD2.
+        // row sum adds the float32 weights before their rounding to bf16 for the P V product;
+        // the roundings (2^-9 relative each, independent) move an output by far less than its
+        // own bf16 rounding.  Paired float32 operations: two scores per FFMA2 and FADD2.
         float2 sum4[4];
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) sum4[g4] = make_float2(0.f, 0.f);
@@ -428,9 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t *v = s[2 * hh + (i >> 4)];
             const float2 t = __ffma2_rn(make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])),
                                         c2, nm2);
-            pk[i] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
-            sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(__uint_as_float(pk[i] << 16),
-                                                               __uint_as_float(pk[i] & 0xFFFF0000u)));
+            const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            pk[i] = pack_bf16x2(e.x, e.y);
+            sum4[i & 3] = __fadd2_rn(sum4[i & 3], e);
           }
           tmem_st32(sb + 64 + hh * 32, pk);
         }
@@ -462,8 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = 1.0f / l_run;
       const bool in_row = TP_CHECK((t.head + 1) * static_cast<long long>(kAttnHeadDim) <= a.ldo, a.status);
-      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.O) + static_cast<long long>(row) * a.ldo +
-                                             static_cast<long long>(t.head) * kAttnHeadDim);
+      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.O) + static_cast<long long>(row) * a.ldo +
+                            static_cast<long long>(t.head) * kAttnHeadDim;
+      uint4 *dst = reinterpret_cast<uint4 *>(orow);
+      // 32-byte stores (whole sectors) where the row is 32-byte aligned, else 16-byte ones
+      const bool wide = (reinterpret_cast<uintptr_t>(orow) & 31u) == 0;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
@@ -471,13 +481,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         tmem_reg_fence(r);
         if (row < a.M && in_row) {
+          uint32_t p[16];
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4)
-            dst[cc * 4 + g4] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * g4]) * inv, __uint_as_float(r[8 * g4 + 1]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * inv, __uint_as_float(r[8 * g4 + 3]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * inv, __uint_as_float(r[8 * g4 + 5]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * inv, __uint_as_float(r[8 * g4 + 7]) * inv));
+          for (int i = 0; i < 16; ++i)
+            p[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          if (wide) {
+            st_global_v8(orow + cc * 32, p);
+            st_global_v8(orow + cc * 32 + 16, p + 8);
+          } else {
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4)
+              dst[cc * 4 + g4] = make_uint4(p[4 * g4], p[4 * g4 + 1], p[4 * g4 + 2], p[4 * g4 + 3]);
+          }
         }
       }
       tc_fence_before();

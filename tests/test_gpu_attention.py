@@ -105,10 +105,16 @@ def test_attention_deterministic_and_strided_output(tp):
     b = tp.tp_attention_forward(Q, K, V)
     wide = torch.full((M, nh * 128 + 64), 7.0, dtype=torch.bfloat16, device="cuda")
     tp.tp_attention_forward(Q, K, V, out=wide[:, : nh * 128])
+    # rows of 264 bf16 (528 bytes): every other row starts on a 16-byte, not a
+    # 32-byte, boundary, so both output store widths run
+    odd = torch.full((M, nh * 128 + 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    tp.tp_attention_forward(Q, K, V, out=odd[:, : nh * 128])
     _sync()
     assert torch.equal(a, b)
     assert torch.equal(wide[:, : nh * 128], a)
     assert torch.all(wide[:, nh * 128:] == 7.0)
+    assert torch.equal(odd[:, : nh * 128], a)
+    assert torch.all(odd[:, nh * 128:] == 7.0)
 
 
 def test_attention_edge_cases_and_errors(tp):
