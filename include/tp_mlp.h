@@ -229,11 +229,19 @@ TP_API tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp
  *   Its scratch is a fixed 16 MiB device array inside the library, which
  *   every GPU that loads the library holds until the process exits.  Calls
  *   whose workspace (tp_mlp_workspace_bytes(s, M, TP_VAR_AUTO)) exceeds
- *   16 MiB are rejected with TP_ERR_WORKSPACE; the memory-bound decode
- *   shapes (M <= 16 tokens) of an H = 8192, F = 28672, T = 8 MLP fit.
+ *   16 MiB are rejected with TP_ERR_WORKSPACE.  That size depends on the
+ *   GPU's SM count, because the AUTO plan splits K to fill the SMs: on a
+ *   152-SM GB300 the memory-bound decode shapes (M <= 16 tokens) of an
+ *   H = 8192, F = 28672, T = 8 MLP need at most about 12.4 MiB and fit; on
+ *   other parts query tp_mlp_workspace_bytes() first.
  *   The first call on a device looks up the scratch's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
- *   `s` must have been made on the current device (else TP_ERR_ARG), and
+ *   (cudaGetSymbolAddress) and keeps it for the life of the process; make
+ *   that first call before any stream capture.  cudaDeviceReset() is not
+ *   supported afterwards (the address, like the library's other per-device
+ *   state, would be stale).
+ *   `s` must have been made on the current device (else TP_ERR_ARG: making a
+ *   handle creates the device state this call needs, so a handle from
+ *   another device is the only way to reach it without that state), and
  *   X, Z are as for tp_mlp_forward.
  *   All calls share the one scratch array and it keeps the last call's
  *   contents; every byte a call reads from it is written earlier in the same

@@ -24,10 +24,29 @@ def rowwise_rms_error(Z: np.ndarray, Zref: np.ndarray) -> float:
     return float(np.max(np.abs(np.asarray(Z, np.float64) - Zref) / np.maximum(rms, 1e-300)))
 
 
-def global_rms_error(Z: np.ndarray, Zref: np.ndarray) -> float:
-    """max |Z - Zref| / RMS(Zref) over the whole output (reported, not gated)."""
-    rms = np.sqrt(np.mean(np.asarray(Zref, np.float64) ** 2))
+def global_rms_error(Z: np.ndarray, Zref: np.ndarray, rms: float | None = None) -> float:
+    """max |Z - Zref| / RMS: the tolerance normalised by one RMS for the
+    whole output.  `rms` is the whole output's RMS when only sampled rows are
+    compared (see stratified_rms); default: the RMS of Zref itself."""
+    if rms is None:
+        rms = float(np.sqrt(np.mean(np.asarray(Zref, np.float64) ** 2)))
     return float(np.max(np.abs(np.asarray(Z, np.float64) - Zref)) / max(rms, 1e-300))
+
+
+def stratified_rms(Zref_rows: np.ndarray, is_outlier: np.ndarray, n_outliers: int, M: int) -> float:
+    """RMS of a whole [M x H] output from sampled rows, one stratum for the
+    `n_outliers` outlier rows and one for the rest: the mean square of each
+    stratum is taken from its sampled rows and weighted by its share of M."""
+    ms = np.mean(np.asarray(Zref_rows, np.float64) ** 2, axis=1)
+    is_outlier = np.asarray(is_outlier, bool)
+    total = 0.0
+    if n_outliers:
+        if not is_outlier.any():
+            raise ValueError("no outlier row among the samples")
+        total += n_outliers / M * float(np.mean(ms[is_outlier]))
+    if n_outliers < M:
+        total += (M - n_outliers) / M * float(np.mean(ms[~is_outlier]))
+    return float(np.sqrt(total))
 
 
 def normwise_error(Z: np.ndarray, Zref: np.ndarray) -> float:
@@ -40,6 +59,18 @@ def normwise_error(Z: np.ndarray, Zref: np.ndarray) -> float:
 # float32 inputs: normwise relative error <= 1e-4.
 TOL_BF16_ROW_RMS = 2e-2
 TOL_F32_NORMWISE = 1e-4
+
+# The same measure normalised by the RMS of the whole output (the literal
+# reading), on a workload with 1 % of its token rows scaled x20.  SwiGLU is
+# quadratic in x, so an outlier row's output RMS is about 10x the whole
+# output's RMS, and the ordinary bf16 rounding of its h (the same share of
+# that row's own RMS as in every row) reads 10x larger here.  Emulating only
+# that rounding in numpy on the large SwiGLU workload's sampled rows (fp64
+# otherwise) gives 7.2e-3 of an outlier row's own RMS, 0.069 of the whole
+# output's.  Held to 0.1: on the outlier rows this is a per-row bound of about
+# 1e-2, half the row-RMS tolerance, so a regression confined to the outlier
+# rows cannot hide inside their own (large) normalisation.
+TOL_BF16_GLOBAL_RMS_OUTLIERS = 0.1
 
 # Gradients of the training path: the chain to dW1 and dX passes three bf16
 # roundings (the saved pre-activation, dP = dH * act'(P) and, for dW, the

@@ -68,10 +68,13 @@ def test_block_small(tp, causal, act, M, nh, T, variant):
 
 def test_block_attention_projection_workload(tp):
     """The attention-projection workload's shapes (M = 4096 tokens, 32 heads
-    of 128, T = 8) with a SwiGLU MLP of F = 4H, rows sampled among the first
-    512 tokens (the oracle then needs K and V of 512 tokens only)."""
+    of 128, T = 8) with a SwiGLU MLP of F = 4H, rows sampled across all 4096
+    tokens, the last one included: late queries attend over up to 4096 keys
+    (the oracle then needs K and V of every token)."""
     M, nh, hd, T = 4096, 32, 128, 8
     H, F = nh * hd, 4 * nh * hd
     d = _weights(M, H, F, "swiglu", seed=7)
-    rows = np.unique(np.concatenate([[0, 511], np.random.default_rng(2).choice(512, 6, replace=False)]))
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, 127, 128, 511, 2047, 2048, 4094, 4095],
+                                     rng.choice(M, 8, replace=False)]))
     _check(tp, d, M, H, F, nh, hd, T, "swiglu", True, "auto", rows)

@@ -1,14 +1,18 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times, on sampled output rows (a row of Z depends only on that
 row of X, so the oracle computes the sampled rows alone).  Tolerance: bf16
-row-RMS measure (tests/gpu_util.py); the global-RMS figure is printed."""
+row-RMS measure (tests/gpu_util.py), every variant (float32 partials with
+the shard-sum, one TMEM accumulator over all shards, and the planner's
+choice).  The global-RMS reading of the tolerance is asserted too: against
+2e-2 where there are no outlier rows, and against its own bound on the
+large SwiGLU workload (tests/gpu_util.py, TOL_BF16_GLOBAL_RMS_OUTLIERS)."""
 import numpy as np
 import pytest
 
 import oracle
 from synth import WORKLOADS, attn_inputs, mlp_inputs
-from tests.gpu_util import (TOL_BF16_ROW_RMS, bf16_bits, global_rms_error, rowwise_rms_error,
-                            to_device)
+from tests.gpu_util import (TOL_BF16_GLOBAL_RMS_OUTLIERS, TOL_BF16_ROW_RMS, bf16_bits,
+                            global_rms_error, rowwise_rms_error, stratified_rms, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +35,7 @@ def _sample_rows(M, k, seed, must=()):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-def _mlp_check(tp, name, variants, k_rows=24):
+def _mlp_check(tp, name, variants, k_rows=24, global_tol=TOL_BF16_ROW_RMS):
     import torch
     w = WORKLOADS[name]
     d = mlp_inputs(M=w["M"], H=w["H"], F=w["F"], act=w["act"], dtype=w["dtype"], seed=0,
@@ -43,14 +47,20 @@ def _mlp_check(tp, name, variants, k_rows=24):
     out = d["outlier_rows"]
     rows = _sample_rows(w["M"], k_rows, seed=1, must=out[: min(8, out.size)])
     Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], w["act"], rows=rows)
+    # RMS of the whole output, estimated per stratum (outlier rows, other rows)
+    # from the oracle's sampled rows
+    rms_all = stratified_rms(Zref, np.isin(rows, out), out.size, w["M"])
     for v in variants:
         Z = tp.tp_mlp_forward(s, X, variant=v)
         torch.cuda.synchronize()
         assert tp.tp_last_device_status() == 0
         Zs = Z[torch.from_numpy(rows).cuda()].cpu().numpy()
         err = rowwise_rms_error(Zs, Zref)
-        print(f"{name} {v}: row-RMS err {err:.3e}, global-RMS err {global_rms_error(Zs, Zref):.3e}")
+        gerr = global_rms_error(Zs, Zref, rms=rms_all)
+        print(f"{name} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}")
         assert err <= TOL_BF16_ROW_RMS
+        assert gerr <= global_tol
+        del Z
     return d, s
 
 
@@ -60,7 +70,8 @@ def test_prefill_gelu_full(tp):
 
 def test_large_prefill_swiglu_full(tp):
     name = "prefill_swiglu_m8192_h8192_f28672_t8_outliers"
-    d, s = _mlp_check(tp, name, ["auto", "partials"], k_rows=24)
+    d, s = _mlp_check(tp, name, ["auto", "partials", "tmem_acc"], k_rows=24,
+                      global_tol=TOL_BF16_GLOBAL_RMS_OUTLIERS)
     w = WORKLOADS[name]
     assert d["outlier_rows"].size == 82
     # shard layout bit exact at full size, first and last shard
@@ -79,13 +90,14 @@ def test_decode_swiglu_full(tp):
     Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu")
     for M in w["decode_m"]:
         X = to_device(d["X"][:M])
-        for v in ("auto", "partials"):
+        for v in ("auto", "partials", "tmem_acc"):
             Z = tp.tp_mlp_forward(s, X, variant=v)
             torch.cuda.synchronize()
             assert tp.tp_last_device_status() == 0
             err = rowwise_rms_error(Z.cpu().numpy(), Zref[:M])
-            print(f"decode M={M} {v}: row-RMS err {err:.3e}")
-            assert err <= TOL_BF16_ROW_RMS
+            gerr = global_rms_error(Z.cpu().numpy(), Zref[:M])
+            print(f"decode M={M} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}")
+            assert err <= TOL_BF16_ROW_RMS and gerr <= TOL_BF16_ROW_RMS
 
 
 def test_attn_proj_full(tp):
@@ -102,8 +114,9 @@ def test_attn_proj_full(tp):
         torch.cuda.synchronize()
         assert tp.tp_last_device_status() == 0
         err = rowwise_rms_error(Z[ridx].cpu().numpy(), Zref)
-        print(f"attn o-proj {v}: row-RMS err {err:.3e}")
-        assert err <= TOL_BF16_ROW_RMS
+        gerr = global_rms_error(Z[ridx].cpu().numpy(), Zref)
+        print(f"attn o-proj {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}")
+        assert err <= TOL_BF16_ROW_RMS and gerr <= TOL_BF16_ROW_RMS
     q = bf16_bits(QKV[:, ridx])
     for i in range(w["T"]):
         ref = oracle.qkv_shard(d["X"], d["Wqkv"], w["n_heads"], w["head_dim"], w["T"], i, rows=rows)
