@@ -43,18 +43,26 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--variant", choices=("auto", "partials", "tmem_acc"), default="auto")
-    p.add_argument("--extras", choices=("none", "default", "full"), default="default",
-                   help="secondary measurements at N=1: decode + shard-sum (default), "
-                        "plus attention projections and the large SwiGLU prefill (full)")
+    p.add_argument("--extras", choices=("none", "all"), default="all",
+                   help="secondary measurements at N=1 (all): decode, training, shard-sum, the "
+                        "attention projections and the large SwiGLU prefill with every all-reduce "
+                        "variant, the attention core and the transformer block")
     p.add_argument("--cpu-rows", type=int, default=64, help="rows of the oracle CPU-baseline sample")
-    p.add_argument("--case", choices=("prefill", "decode", "shard_sum", "train", "block", "attention"),
+    p.add_argument("--case", choices=("prefill", "decode", "shard_sum", "train", "block", "attention",
+                                      "mlp", "oproj"),
                    default="prefill",
                    help="prefill: the headline step (default); decode / shard_sum: time only the "
                         "memory-bound decode MLP (H=8192, F=28672, T=8, SwiGLU, --decode-m tokens) "
                         "or the standalone shard-sum (T=8, n=8192*8192); train: the backward of the "
                         "prefill MLP; block: one transformer block (M=4096, 32x128 heads, T=8, "
                         "SwiGLU F=4H, causal); attention: the block's fused causal attention core "
-                        "(M=4096, 32 heads of 128); for profiling")
+                        "(M=4096, 32 heads of 128); mlp: tp_mlp_forward on --mlp-workload with "
+                        "--variant; oproj: the row-parallel output projection of the attention "
+                        "projections (M=4096, H=4096, T=8) with --variant; for profiling")
+    p.add_argument("--mlp-workload", choices=("prefill_gelu", "prefill_swiglu_large"),
+                   default="prefill_gelu",
+                   help="--case mlp: M=2048 H=4096 F=16384 T=4 GeLU, or M=8192 H=8192 F=28672 T=8 "
+                        "SwiGLU")
     p.add_argument("--decode-m", type=int, default=16)
     return p.parse_args(argv)
 
@@ -118,9 +126,10 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs
+    (the fallback when NVML cannot be loaded in-process)."""
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
         self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
                     "-i", str(gpu_index), "-lms", str(period_ms)]
@@ -133,6 +142,12 @@ class ClockSampler:
         except OSError:
             self.proc = None
         return self
+
+    def mark(self) -> float:
+        return time.time()
+
+    def window(self, t0: float, t1: float) -> dict:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no per-region samples (nvidia-smi)"]}
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -151,24 +166,113 @@ class ClockSampler:
                     rows.append(parts)
         os.unlink(self.path)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        sm, mx, pw = [], [], []
+        samples = []
         for r in rows:
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-                pw.append(float(r[3]))
+                sm, mx, pw = float(r[1]), float(r[2]), float(r[3])
             except ValueError:
                 continue
-            for name, flag in zip(names, r[5:9]):
-                if flag.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [c for c, p in zip(sm, pw) if p >= 0.3 * max(pw)] or sm
-        loaded.sort()
-        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(pw)}
+            reasons = {name for name, flag in zip(names, r[5:9]) if flag.lower().startswith("active")}
+            samples.append((0.0, sm, mx, pw, reasons))
+        return summarize_clocks(samples)
+
+
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def summarize_clocks(samples) -> dict:
+    """Median SM clock under load (samples drawing >= 30 % of the peak power
+    seen), the maximum SM clock and every throttle reason seen."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    pw_max = max(s[3] for s in samples)
+    loaded = sorted(s[1] for s in samples if s[3] >= 0.3 * pw_max) or sorted(s[1] for s in samples)
+    reasons = set()
+    for s in samples:
+        reasons |= s[4]
+    return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": max(s[2] for s in samples),
+            "reasons": sorted(reasons), "samples": len(samples), "power_w_max": round(pw_max, 1)}
+
+
+class NvmlClockSampler:
+    """In-process NVML polling (ctypes, read-only queries) of the SM clock,
+    power and clock-event reasons every `period_s`, from a thread, so that
+    even a few-millisecond timed region gets samples.  window(t0, t1) returns
+    the summary of the samples taken between two mark() times; stop() the
+    summary of all, after one last sample."""
+
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML device handle")
+        self.reason_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.period = period_s
+        self.samples = []
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) != 0:
+            return
+        self.nvml.nvmlDeviceGetPowerUsage(self.dev, ct.byref(pw))
+        self.reason_fn(self.dev, ct.byref(rs))
+        reasons = {name for bit, name in NVML_REASONS.items() if rs.value & bit}
+        self.samples.append((time.time(), float(clk.value), self.max_mhz, pw.value / 1e3, reasons))
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread.start()
+        return self
+
+    def mark(self) -> float:
+        return time.time()
+
+    def window(self, t0: float, t1: float) -> dict:
+        snap = list(self.samples)
+        sel = [s for s in snap if t0 <= s[0] <= t1]
+        note = None
+        if not sel:  # a region shorter than the polling period: the first sample after it
+            sel = [s for s in snap if s[0] >= t1][:1]
+            note = "no sample inside the region; first sample after it"
+        out = summarize_clocks(sel)
+        if note:
+            out["note"] = note
+        return out
+
+    def stop(self) -> dict:
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        self._sample()
+        try:
+            self.nvml.nvmlShutdown()
+        except Exception:
+            pass
+        return summarize_clocks(self.samples)
+
+
+def clock_sampler(gpu_index: int):
+    try:
+        return NvmlClockSampler(gpu_index).start()
+    except (OSError, AttributeError):
+        return ClockSampler(gpu_index).start()
 
 
 def physical_gpu_index(local_rank: int) -> int:
@@ -256,6 +360,11 @@ def run_ours(args) -> dict | None:
     dist_init(world, "nccl")
     tp.load_library()
 
+    peaks, peak_src = measured_peaks()
+    if peak_src == "measured":
+        # the AUTO planners weigh partial traffic with this box's measured rates
+        tp.tp_set_machine_balance(peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9))
+
     w = WORKLOADS[WORKLOAD]
     M, H, F, T, act = w["M"], w["H"], w["F"], w["T"], w["act"]
     d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=rank)
@@ -269,18 +378,20 @@ def run_ours(args) -> dict | None:
     wrow = torch.empty(max(ws_row, 1), dtype=torch.uint8, device=device)
     launches_per_step = 1 + 1 + (1 if ws_row > 0 else 0)
     stream = torch.cuda.current_stream()
+    flops_step = 4.0 * M * H * F
 
     def step():
         tp.tp_colpar_forward(s, X, Y, workspace=wcol)
         tp.tp_rowpar_forward(s, Y, args.variant, Z, workspace=wrow)
 
-    clocks = ClockSampler(physical_gpu_index(local)).start()
+    clocks = clock_sampler(physical_gpu_index(local))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if tp.tp_last_device_status() != 0:
         raise RuntimeError("device status error during warm-up")
 
+    # ---- headline: K back-to-back steps (burst) ----
     K = args.steps
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -288,6 +399,7 @@ def run_ours(args) -> dict | None:
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(device)
     torch.cuda.synchronize()
+    c0 = clocks.mark()
     start.record(stream)
     for i in range(K):
         e0[i].record(stream)
@@ -297,17 +409,49 @@ def run_ours(args) -> dict | None:
         e2[i].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    c1 = clocks.mark()
     barrier(device)
-    clk = clocks.stop()
+    clk = clocks.window(c0, c1)
     status = tp.tp_last_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
 
     elapsed = start.elapsed_time(end) / 1e3
-    flops_step = 4.0 * M * H * F
     value, t_max = aggregate(elapsed, flops_step * K, device)
     col_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / K
     row_ms = sum(e1[i].elapsed_time(e2[i]) for i in range(K)) / K
+
+    # ---- the same steps with L2 flushed before each (a 256 MiB write) ----
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    f0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    f1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(device)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        f0[i].record(stream)
+        step()
+        f1[i].record(stream)
+    torch.cuda.synchronize()
+    flushed_s = sum(f0[i].elapsed_time(f1[i]) for i in range(K)) / 1e3
+    flushed_value, flushed_t = aggregate(flushed_s, flops_step * K, device)
+    del flush
+
+    # ---- sustained: >= 1 s of back-to-back steps, against the sustained peak ----
+    n_sus = max(K, int(math.ceil(1.2 / max(elapsed / K, 1e-6))))
+    ss0, ss1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize()
+    c2 = clocks.mark()
+    ss0.record(stream)
+    for _ in range(n_sus):
+        step()
+    ss1.record(stream)
+    torch.cuda.synchronize()
+    c3 = clocks.mark()
+    barrier(device)
+    sus_value, sus_t = aggregate(ss0.elapsed_time(ss1) / 1e3, flops_step * n_sus, device)
+    clk_sus = clocks.window(c2, c3)
 
     # end to end through the public host-buffer call: pinned X in, Z out.  Two
     # requests in flight on two streams (each with its own host and device
@@ -342,8 +486,8 @@ def run_ours(args) -> dict | None:
     if not torch.equal(Zh[0], Zh[1]) or not torch.isfinite(Zh[0]).all():
         raise RuntimeError("end-to-end results differ between the two in-flight buffers")
     e2e_value, _ = aggregate(hs.elapsed_time(he) / 1e3, flops_step * K, device)
+    clk_all = clocks.stop()
 
-    peaks, peak_src = measured_peaks()
     sustained = elapsed > 1.0
     peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     achieved = 2.0 * M * H * F / (col_ms / 1e3) / 1e12
@@ -364,7 +508,8 @@ def run_ours(args) -> dict | None:
         "config": {"workload": WORKLOAD, "M": M, "H": H, "F": F, "T": T, "act": "erf-gelu",
                    "variant": args.variant, "accumulate": "fp32", "output": "fp32",
                    "parallelism": f"{world} independent replica(s); T={T} shards per GPU",
-                   "l2": "inputs larger than L2 (256 MiB of weights read per step)"},
+                   "l2": "inputs larger than L2 (256 MiB of weights read per step); the same steps "
+                         "with a 256 MiB L2 flush before each are reported as l2_flushed"},
         "pct_bf16_peak": round(100.0 * value / 1e12 / world / peak, 1),
         "roofline": {"kernel": "tp_gemm_pair_kernel<EPI_GELU_BF16> (column-parallel GEMM + GeLU, "
                                "CTA-pair 256x256 tiles)",
@@ -373,16 +518,24 @@ def run_ours(args) -> dict | None:
                      "peak_source": f"{peak_src} ({'sustained' if sustained else 'burst'})",
                      "traffic": traffic, "avg_launch_ms": round(col_ms, 5)},
         "rowpar_ms": round(row_ms, 5),
+        "l2_flushed": {"value": round(flushed_value / 1e12, 2), "unit": "TFLOP/s",
+                       "ms_per_step": round(flushed_t * 1e3 / K, 5), "steps": K,
+                       "flush": "256 MiB write before every step, outside the step's events"},
+        "sustained": {"value": round(sus_value / 1e12, 2), "unit": "TFLOP/s", "steps": n_sus,
+                      "seconds": round(sus_t, 3), "peak": peaks["bf16_tflops_sustained"],
+                      "frac": round(sus_value / 1e12 / world / peaks["bf16_tflops_sustained"], 3),
+                      "peak_source": f"{peak_src} (sustained)", "clocks": clk_sus},
         "e2e": {"value": round(e2e_value / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 4,
                 "api": "tp_mlp_forward_host", "in_flight": n_inflight},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
+        "clocks_whole_run": clk_all,
         "context": {"ring_allreduce_bytes_per_rank_if_T_gpus": tp.ring_allreduce_bytes(M * H, T, 4)},
     }
     if world == 1 and rank == 0:
         if args.extras != "none":
-            line["extras"] = extras(args, tp, device, peaks, full=args.extras == "full")
+            line["extras"] = extras(args, tp, device, peaks)
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
     s.close()
     return line if rank == 0 else None
@@ -402,12 +555,27 @@ def _time_calls(fn, reps: int, warm: int = 3) -> float:
     return a.elapsed_time(b) / 1e3 / reps
 
 
-def extras(args, tp, device, peaks, full: bool) -> dict:
+def _auto_slots(ws_bytes: int, fixed_bytes: int, M: int, H: int) -> int:
+    """Accumulation slots of the row-parallel GEMM behind a workspace size:
+    the float32 partials take slots x M x H x 4 bytes beyond `fixed_bytes`
+    (1 slot: one TMEM accumulator over all shards, no partials)."""
+    extra = ws_bytes - fixed_bytes
+    return max(1, int(round(extra / (M * H * 4)))) if extra > 0 else 1
+
+
+def _r256(n: int) -> int:
+    return (n + 255) // 256 * 256
+
+
+def extras(args, tp, device, peaks) -> dict:
     """Secondary measurements (N = 1): the memory-bound decode shapes and the
-    standalone shard-sum against HBM bandwidth; with `full`, the attention
-    projections and the large SwiGLU prefill against tensor peak.  Inputs
-    for these timing-only runs are drawn on the device with a seeded
-    generator (same distributions as the parity workloads)."""
+    standalone shard-sum against HBM bandwidth; the training step; the
+    attention projections and the large SwiGLU prefill with each all-reduce
+    variant (float32 partials + shard-sum, one TMEM accumulator over all
+    shards, and the planner's AUTO pick, named) against tensor peak; the
+    attention core and one transformer block.  Inputs for these timing-only
+    runs are drawn on the device with a seeded generator (same distributions
+    as the parity workloads)."""
     import torch
     from synth import WORKLOADS
     out = {}
@@ -478,73 +646,92 @@ def extras(args, tp, device, peaks, full: bool) -> dict:
         torch.cuda.empty_cache()
     out["shard_sum"] = ss
     out["hbm_peak_gbs"] = hbm
+    burst = peaks["bf16_tflops"]
 
-    if full:
-        w = WORKLOADS["attn_proj_m4096_h4096_32x128_t8"]
-        M, H, T, nh, hd = w["M"], w["H"], w["T"], w["n_heads"], w["head_dim"]
-        s = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
-                                    nh, hd, T)
-        X, A = randn((M, H), 1.0), randn((M, H), 1.0)
-        QKV = torch.empty((T, M, 3 * H // T), dtype=torch.bfloat16, device=device)
-        Z = torch.empty((M, H), dtype=torch.float32, device=device)
-        res = {}
-        for v in ("auto", "partials", "tmem_acc"):
-            ws = torch.empty(max(tp.tp_attn_proj_workspace_bytes(s, M, v), 1), dtype=torch.uint8,
-                             device=device)
-            t_qkv = _time_calls(lambda: tp.tp_attn_proj_forward(s, X=X, variant=v, QKV=QKV), 20)
-            t_o = _time_calls(lambda: tp.tp_attn_proj_forward(s, A=A, variant=v, Z=Z, workspace=ws), 20)
-            res[v] = {"qkv_TFLOP/s": round(2 * M * H * 3 * H / t_qkv / 1e12, 1),
-                      "oproj_TFLOP/s": round(2 * M * H * H / t_o / 1e12, 1),
-                      "us_qkv": round(t_qkv * 1e6, 1), "us_oproj": round(t_o * 1e6, 1)}
-        out["attn_proj_m4096_h4096_32x128_t8"] = res
-        s.close()
-        torch.cuda.empty_cache()
+    w = WORKLOADS["attn_proj_m4096_h4096_32x128_t8"]
+    M, H, T, nh, hd = w["M"], w["H"], w["T"], w["n_heads"], w["head_dim"]
+    s = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                nh, hd, T)
+    X, A = randn((M, H), 1.0), randn((M, H), 1.0)
+    QKV = torch.empty((T, M, 3 * H // T), dtype=torch.bfloat16, device=device)
+    Z = torch.empty((M, H), dtype=torch.float32, device=device)
+    res = {}
+    variants = ("auto", "partials", "tmem_acc")
+    wss = {v: torch.empty(max(tp.tp_attn_proj_workspace_bytes(s, M, v), 1), dtype=torch.uint8, device=device)
+           for v in variants}
+    # the variants take turns, three rounds, and each keeps its median: the GPU's clock under its
+    # power cap drifts over a run, and this keeps that drift off any one variant
+    tq, to = {v: [] for v in variants}, {v: [] for v in variants}
+    for _ in range(3):
+        for v in variants:
+            tq[v].append(_time_calls(lambda: tp.tp_attn_proj_forward(s, X=X, variant=v, QKV=QKV), 10))
+            to[v].append(_time_calls(lambda: tp.tp_attn_proj_forward(s, A=A, variant=v, Z=Z,
+                                                                     workspace=wss[v]), 10))
+    for v in variants:
+        t_qkv, t_o = sorted(tq[v])[1], sorted(to[v])[1]
+        res[v] = {"qkv_TFLOP/s": round(2 * M * H * 3 * H / t_qkv / 1e12, 1),
+                  "oproj_TFLOP/s": round(2 * M * H * H / t_o / 1e12, 1),
+                  "us_qkv": round(t_qkv * 1e6, 1), "us_oproj": round(t_o * 1e6, 1),
+                  "oproj_frac_burst": round(2 * M * H * H / t_o / 1e12 / burst, 3)}
+    res["auto_oproj_slots"] = _auto_slots(tp.tp_attn_proj_workspace_bytes(s, M, "auto"), 0, M, H)
+    out["attn_proj_m4096_h4096_32x128_t8"] = res
+    s.close()
+    del wss, X, A, QKV, Z
+    torch.cuda.empty_cache()
 
-        # the block's fused causal attention core alone (4096 tokens, 32 heads of 128)
-        M, nh, hd = 4096, 32, 128
-        Qa, Ka, Va = (randn((nh, M, hd), 1.0) for _ in range(3))
-        Oa = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=device)
-        wsa = torch.empty(tp.tp_attention_workspace_bytes(M, nh, hd), dtype=torch.uint8, device=device)
-        t = _time_calls(lambda: tp.tp_attention_forward(Qa, Ka, Va, True, Oa, wsa), 20)
-        fl = 2 * 2 * nh * hd * M * (M + 1) / 2
-        out["attention_m4096_32x128_causal"] = {"us": round(t * 1e6, 1), "TFLOP/s": round(fl / t / 1e12, 1)}
-        del Qa, Ka, Va, Oa, wsa
+    # the block's fused causal attention core alone (4096 tokens, 32 heads of 128)
+    M, nh, hd = 4096, 32, 128
+    Qa, Ka, Va = (randn((nh, M, hd), 1.0) for _ in range(3))
+    Oa = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=device)
+    wsa = torch.empty(tp.tp_attention_workspace_bytes(M, nh, hd), dtype=torch.uint8, device=device)
+    t = _time_calls(lambda: tp.tp_attention_forward(Qa, Ka, Va, True, Oa, wsa), 20)
+    fl = 2 * 2 * nh * hd * M * (M + 1) / 2
+    out["attention_m4096_32x128_causal"] = {"us": round(t * 1e6, 1), "TFLOP/s": round(fl / t / 1e12, 1),
+                                             "frac_burst": round(fl / t / 1e12 / burst, 3)}
+    del Qa, Ka, Va, Oa, wsa
 
-        # one transformer block at the attention workload's shape, SwiGLU MLP with F = 4H
-        M, H, T, nh, hd = 4096, 4096, 8, 32, 128
-        F = 4 * H
-        a = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
-                                    nh, hd, T)
-        m = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
-                                "swiglu")
-        X = randn((M, H), 1.0)
-        ob = torch.empty((M, H), dtype=torch.float32, device=device)
-        ws = torch.empty(tp.tp_block_workspace_bytes(a, m, M, "auto"), dtype=torch.uint8, device=device)
-        t = _time_calls(lambda: tp.tp_block_forward(a, m, X, True, "auto", ob, None, ws), 10)
-        # algorithmic flop: projections, causal attention (the half below the diagonal), MLP
-        fl = 2 * M * H * 3 * H + 2 * 2 * nh * hd * M * (M + 1) / 2 + 2 * M * H * H + 6 * M * H * F
-        out["block_m4096_h4096_32x128_t8_swiglu_f16384"] = {"ms": round(t * 1e3, 3),
-                                                             "TFLOP/s": round(fl / t / 1e12, 1)}
-        a.close()
-        m.close()
-        del ws, ob, X
-        torch.cuda.empty_cache()
+    # one transformer block at the attention workload's shape, SwiGLU MLP with F = 4H
+    M, H, T, nh, hd = 4096, 4096, 8, 32, 128
+    F = 4 * H
+    a = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                nh, hd, T)
+    m = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                            "swiglu")
+    X = randn((M, H), 1.0)
+    ob = torch.empty((M, H), dtype=torch.float32, device=device)
+    ws = torch.empty(tp.tp_block_workspace_bytes(a, m, M, "auto"), dtype=torch.uint8, device=device)
+    t = _time_calls(lambda: tp.tp_block_forward(a, m, X, True, "auto", ob, None, ws), 10)
+    # algorithmic flop: projections, causal attention (the half below the diagonal), MLP
+    fl = 2 * M * H * 3 * H + 2 * 2 * nh * hd * M * (M + 1) / 2 + 2 * M * H * H + 6 * M * H * F
+    out["block_m4096_h4096_32x128_t8_swiglu_f16384"] = {"ms": round(t * 1e3, 3),
+                                                         "TFLOP/s": round(fl / t / 1e12, 1)}
+    a.close()
+    m.close()
+    del ws, ob, X
+    torch.cuda.empty_cache()
 
-        w = WORKLOADS["prefill_swiglu_m8192_h8192_f28672_t8_outliers"]
-        M, H, F, T = w["M"], w["H"], w["F"], w["T"]
-        s = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
-                                "swiglu")
-        X = randn((M, H), 1.0)
-        Z = torch.empty((M, H), dtype=torch.float32, device=device)
-        res = {}
-        for v in ("auto", "partials", "tmem_acc"):
+    w = WORKLOADS["prefill_swiglu_m8192_h8192_f28672_t8_outliers"]
+    M, H, F, T = w["M"], w["H"], w["F"], w["T"]
+    s = tp.tp_shard_weights(randn((H, 2 * F), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T,
+                            "swiglu")
+    X = randn((M, H), 1.0)
+    Z = torch.empty((M, H), dtype=torch.float32, device=device)
+    res = {}
+    variants = ("auto", "partials", "tmem_acc")
+    times = {v: [] for v in variants}
+    for _ in range(3):  # variants take turns (see the attention projections above)
+        for v in variants:
             ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, v), 1), dtype=torch.uint8, device=device)
-            t = _time_calls(lambda: tp.tp_mlp_forward(s, X, v, Z, ws), 5)
-            res[v] = {"ms": round(t * 1e3, 3), "TFLOP/s": round(6 * M * H * F / t / 1e12, 1)}
+            times[v].append(_time_calls(lambda: tp.tp_mlp_forward(s, X, v, Z, ws), 4, warm=2))
             del ws
-        out["prefill_swiglu_m8192_h8192_f28672_t8"] = res
-        s.close()
-        torch.cuda.empty_cache()
+    for v in variants:
+        t = sorted(times[v])[1]
+        res[v] = {"ms": round(t * 1e3, 3), "TFLOP/s": round(6 * M * H * F / t / 1e12, 1),
+                  "frac_burst": round(6 * M * H * F / t / 1e12 / burst, 3)}
+    res["auto_slots"] = _auto_slots(tp.tp_mlp_workspace_bytes(s, M, "auto"), _r256(M * F * 2), M, H)
+    out["prefill_swiglu_m8192_h8192_f28672_t8"] = res
+    s.close()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -604,6 +791,8 @@ def run_case(args) -> dict:
     device = torch.device("cuda", 0)
     tp.load_library()
     peaks, peak_src = measured_peaks()
+    if peak_src == "measured":
+        tp.tp_set_machine_balance(peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9))
     gen = torch.Generator(device=device)
     gen.manual_seed(0)
 
@@ -623,6 +812,43 @@ def run_case(args) -> dict:
         byts = 3 * H * F * 2 + M * H * (2 + 4)
         cfg = {"workload": "decode_swiglu_h8192_f28672_t8", "M": M, "H": H, "F": F, "T": T,
                "variant": args.variant}
+    elif args.case == "mlp":
+        name = (WORKLOAD if args.mlp_workload == "prefill_gelu"
+                else "prefill_swiglu_m8192_h8192_f28672_t8_outliers")
+        w = WORKLOADS[name]
+        M, H, F, T, act = w["M"], w["H"], w["F"], w["T"], w["act"]
+        ncols = 2 * F if act == "swiglu" else F
+        s = tp.tp_shard_weights(randn((H, ncols), 1 / math.sqrt(H)), randn((F, H), 1 / math.sqrt(F)), T, act)
+        X = randn((M, H), 1.0)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(max(tp.tp_mlp_workspace_bytes(s, M, args.variant), 1), dtype=torch.uint8,
+                         device=device)
+        fn = lambda: tp.tp_mlp_forward(s, X, args.variant, Z, ws)  # noqa: E731
+        t = _time_calls(fn, args.steps, warm=args.warmup)
+        if tp.tp_last_device_status() != 0:
+            raise RuntimeError("device status error")
+        fl = (6 if act == "swiglu" else 4) * M * H * F
+        return {"metric": "MLP forward TFLOP/s", "value": round(fl / t / 1e12, 1), "unit": "TFLOP/s",
+                "ms_per_call": round(t * 1e3, 4), "steps": args.steps, "warmup": args.warmup,
+                "config": {"workload": name, "variant": args.variant}}
+    elif args.case == "oproj":
+        w = WORKLOADS["attn_proj_m4096_h4096_32x128_t8"]
+        M, H, T, nh, hd = w["M"], w["H"], w["T"], w["n_heads"], w["head_dim"]
+        s = tp.tp_shard_weights_qkv(randn((H, 3 * H), 1 / math.sqrt(H)), randn((H, H), 1 / math.sqrt(H)),
+                                    nh, hd, T)
+        A = randn((M, H), 1.0)
+        Z = torch.empty((M, H), dtype=torch.float32, device=device)
+        ws = torch.empty(max(tp.tp_attn_proj_workspace_bytes(s, M, args.variant), 1), dtype=torch.uint8,
+                         device=device)
+        fn = lambda: tp.tp_attn_proj_forward(s, A=A, variant=args.variant, Z=Z, workspace=ws)  # noqa: E731
+        t = _time_calls(fn, args.steps, warm=args.warmup)
+        if tp.tp_last_device_status() != 0:
+            raise RuntimeError("device status error")
+        return {"metric": "O-projection TFLOP/s", "value": round(2 * M * H * H / t / 1e12, 1),
+                "unit": "TFLOP/s", "us_per_call": round(t * 1e6, 2), "steps": args.steps,
+                "warmup": args.warmup,
+                "config": {"workload": "attn_proj_m4096_h4096_32x128_t8 (O-projection)",
+                           "variant": args.variant}}
     elif args.case == "train":
         w = WORKLOADS[WORKLOAD]
         M, H, F, T = w["M"], w["H"], w["F"], w["T"]

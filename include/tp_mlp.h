@@ -434,6 +434,22 @@ TP_API tp_status_t tp_partial_sum_bf16(const float *const *Zi, int T, int64_t n,
 TP_API tp_status_t tp_last_device_status(void *stream);
 
 /*
+ * tp_set_machine_balance - the exchange rate, in dense bf16 tensor-core flop
+ * per byte of HBM traffic, that the AUTO planners (tp_mlp_forward,
+ * tp_attn_proj_forward, tp_block_forward and their workspace queries) use to
+ * weigh the row-parallel GEMM's work against the float32 partials that
+ * variant A writes and the shard-sum reads (the pages' "partial sums"
+ * completed by the all-reduce, "Slice the matrix itself", section
+ * "Mathematical formulation").  The default comes from the device's own
+ * figures: 8192 flop per SM per clock at the peak SM clock, against two
+ * transfers of the memory bus width per memory clock.  A caller that has
+ * measured both rates passes their ratio; 0 restores the default.  Negative,
+ * NaN or absurd values (> 1e6) -> TP_ERR_ARG.  Process-wide; affects plans
+ * made after the call (workspace sizes included).
+ */
+TP_API tp_status_t tp_set_machine_balance(double flop_per_byte);
+
+/*
  * tp_set_wait_limit_ns - limit on every device-side wait (default 2 s) in
  * kernels launched after this call, process-wide.  0 restores the default.
  * A limit below 1 ms is a test limit: the tensor-core kernels then first

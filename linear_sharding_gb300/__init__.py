@@ -38,7 +38,7 @@ EXPORTS = (
     "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
     "tp_block_workspace_bytes", "tp_block_forward", "tp_attention_workspace_bytes",
-    "tp_attention_forward", "tp_inject_alloc_failures",
+    "tp_attention_forward", "tp_inject_alloc_failures", "tp_set_machine_balance",
 )
 
 _lock = threading.Lock()
@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_last_device_status.argtypes = [vp]
         lib.tp_set_wait_limit_ns.argtypes = [u64]
         lib.tp_inject_alloc_failures.argtypes = [i32]
+        lib.tp_set_machine_balance.argtypes = [ctypes.c_double]
         lib.tp_colpar_workspace_bytes.restype = sz
         lib.tp_colpar_workspace_bytes.argtypes = [vp, i64]
         lib.tp_colpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
@@ -114,7 +115,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                      "tp_colpar_forward", "tp_rowpar_forward", "tp_mlp_forward_noalloc",
                      "tp_reduce_scatter", "tp_all_gather", "tp_partial_sum_bf16",
                      "tp_shards_enable_backward", "tp_mlp_forward_train", "tp_mlp_backward",
-                     "tp_block_forward", "tp_attention_forward", "tp_inject_alloc_failures"):
+                     "tp_block_forward", "tp_attention_forward", "tp_inject_alloc_failures",
+                     "tp_set_machine_balance"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -461,6 +463,12 @@ def tp_last_device_status(stream=None) -> int:
 
 def tp_set_wait_limit_ns(ns: int) -> None:
     _check(load_library().tp_set_wait_limit_ns(int(ns)), "tp_set_wait_limit_ns")
+
+
+def tp_set_machine_balance(flop_per_byte: float) -> None:
+    """Flop per HBM byte the AUTO planners weigh partial traffic with (0: the
+    device's own figures)."""
+    _check(load_library().tp_set_machine_balance(float(flop_per_byte)), "tp_set_machine_balance")
 
 
 def tp_inject_alloc_failures(count: int) -> None:

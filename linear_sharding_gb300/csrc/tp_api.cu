@@ -46,11 +46,22 @@ struct DevState {
   bool ready = false;
   int sms = 0;
   unsigned int *status = nullptr;
+  // Dense bf16 tensor flop per byte of HBM traffic from the device's own
+  // figures (peak SM clock, memory clock and bus width): the exchange rate
+  // the planners use between GEMM work and float32 partial traffic.
+  double queried_balance = 0.0;
 };
 
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+// tp_set_machine_balance: a caller's measured flop-per-byte figure (0: use
+// the queried one).
+std::atomic<double> g_balance_override{0.0};
+
+// Dense bf16 tensor-core flop per SM per clock (tcgen05.mma, kind::f16):
+// a 128 x 256 x 16 MMA every 128 cycles.
+constexpr double kFlopPerSmClock = 8192.0;
 
 // Failure injection (tp_inject_alloc_failures): device allocations still to fail.
 std::atomic<int> g_fail_allocs{0};
@@ -100,6 +111,14 @@ tp_status_t dev_state(DevState **out, int *dev_out = nullptr) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return TP_ERR_CUDA;
     if (major != 10 || minor != 3) return TP_ERR_ARCH;
+    int clk_khz = 0, mem_khz = 0, bus_bits = 0;
+    cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev);
+    cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, dev);
+    cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev);
+    // Double data rate: two transfers of bus_bits per memory clock.
+    const double flops = kFlopPerSmClock * sms * clk_khz * 1e3;
+    const double bytes = 2.0 * mem_khz * 1e3 * bus_bits / 8.0;
+    d.queried_balance = (flops > 0.0 && bytes > 0.0) ? flops / bytes : 300.0;
     unsigned int *st = nullptr;
     if (lib_malloc(reinterpret_cast<void **>(&st), 256) != cudaSuccess) return TP_ERR_OOM;
     if (cudaMemset(st, 0, 256) != cudaSuccess) {
@@ -175,6 +194,15 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Cost of one byte of float32 partials (written once, read by the
+// shard-sum) in k-tiles of a 128 x bn tensor-core tile: the machine balance
+// (flop per HBM byte) over the flop of one k-tile.
+double ktile_per_partial_byte(const DevState *d, int bn) {
+  const double o = g_balance_override.load();
+  const double balance = o > 0.0 ? o : d->queried_balance;
+  return balance / (2.0 * 128.0 * bn * 64.0);
+}
+
 GemmArgs base_args(const DevState *d) {
   GemmArgs g;
   std::memset(&g, 0, sizeof g);
@@ -226,8 +254,10 @@ struct MlpPlan {
   size_t total() const { return round256(y_bytes) + round256(col_bytes) + round256(row_bytes); }
 };
 
-tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, int sms, MlpPlan *p) {
+tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, const DevState *d, MlpPlan *p) {
   *p = MlpPlan();
+  const int sms = d->sms;
+  const double per_byte_tc = ktile_per_partial_byte(d, s->bn2);
   const int64_t H = s->H, Fs = s->Fs, T = s->T, R1 = s->R1;
   const size_t eb = esize(s->dt);
   p->y_bytes = static_cast<size_t>(T * M * Fs) * eb;
@@ -257,10 +287,8 @@ tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, int sms, Mlp
       p->slots2 = static_cast<int>(T);
     else {
       // Tensor-bound: one k-tile of a 128 x bn2 tile is 2*128*bn2*64 flop; a
-      // partial byte costs (peak flop/s per SM) / (HBM bytes/s per SM).
-      const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
-      const double per_byte = (1.9e15 / 6.5e12) / flop_per_ktile;
-      p->slots2 = choose_slots(cdiv(M, 128) * (H / s->bn2), static_cast<int>(T), kps, sms, per_byte,
+      // partial byte costs the machine balance in flop.
+      p->slots2 = choose_slots(cdiv(M, 128) * (H / s->bn2), static_cast<int>(T), kps, sms, per_byte_tc,
                                static_cast<int64_t>(M * H * 4), false);
     }
   }
@@ -569,11 +597,11 @@ struct TrainPlan {
   size_t bwd_total() const { return round256(dP) + round256(dx_part); }
 };
 
-void plan_train(const tp_shards *s, int64_t M, tp_variant_t v, int sms, TrainPlan *p) {
+void plan_train(const tp_shards *s, int64_t M, tp_variant_t v, const DevState *d, TrainPlan *p) {
   *p = TrainPlan();
   const int64_t H = s->H, Fs = s->Fs, T = s->T;
   MlpPlan fp;
-  plan_mlp(s, M > kDecodeMaxM ? M : kDecodeMaxM + 1, v, sms, &fp);
+  plan_mlp(s, M > kDecodeMaxM ? M : kDecodeMaxM + 1, v, d, &fp);
   p->slots2 = fp.slots2;
   p->fwd_row = p->slots2 > 1 ? static_cast<size_t>(p->slots2 * M * H) * 4 : 0;
   p->nseg = static_cast<int>(s->act == TP_ACT_SWIGLU ? 2 * T : T);
@@ -594,7 +622,7 @@ tp_status_t mlp_forward_train_impl(tp_shards *s, const void *X, int64_t M, tp_ac
   if (act != TP_ACT_IDENTITY && (!Psave || !aligned16(Psave))) return TP_ERR_ARG;
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   TrainPlan p;
-  plan_train(s, M, v, d->sms, &p);
+  plan_train(s, M, v, d, &p);
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.fwd_total(), st));
   const int64_t H = s->H, T = s->T, Fs = s->Fs;
@@ -644,7 +672,7 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   if (s->act != TP_ACT_IDENTITY && (!Psave || !aligned16(Psave))) return TP_ERR_ARG;
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   TrainPlan p;
-  plan_train(s, M, v, d->sms, &p);
+  plan_train(s, M, v, d, &p);
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.bwd_total(), st));
   const int64_t H = s->H, T = s->T, Fs = s->Fs, F = s->F;
@@ -761,7 +789,7 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
   if (!X || !Z || !aligned16(X) || !aligned16(Z)) return TP_ERR_ARG;
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   MlpPlan p;
-  TP_TRY(plan_mlp(s, M, v, d->sms, &p));
+  TP_TRY(plan_mlp(s, M, v, d, &p));
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
   char *Y = w.ptr;
@@ -808,11 +836,11 @@ struct BlockPlan {
   }
 };
 
-void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t v, int sms, BlockPlan *p) {
+void plan_block(const tp_shards *a, const tp_shards *m, int64_t M, tp_variant_t v, const DevState *d, BlockPlan *p) {
   *p = BlockPlan();
   const int64_t H = a->H;
   p->slots_o = v == TP_VAR_PARTIALS ? a->T : 1;
-  plan_mlp(m, M, v, sms, &p->mlp);
+  plan_mlp(m, M, v, d, &p->mlp);
   p->qkv = static_cast<size_t>(3 * H * M) * 2;  // Q, K and V head-major
   p->O = static_cast<size_t>(M * H) * 2;
   p->opart = p->slots_o > 1 ? static_cast<size_t>(p->slots_o * M * H) * 4 : 0;
@@ -833,7 +861,7 @@ tp_status_t block_forward_impl(tp_shards *a, tp_shards *m, const void *X, int64_
   if (!X || !out || !aligned16(X) || !aligned16(out) || (h_out && !aligned16(h_out))) return TP_ERR_ARG;
   if (M > (1LL << 24)) return TP_ERR_UNSUPPORTED;
   BlockPlan p;
-  plan_block(a, m, M, v, d->sms, &p);
+  plan_block(a, m, M, v, d, &p);
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
   const int64_t H = a->H, nh = a->n_heads, hd = a->head_dim;
@@ -937,6 +965,12 @@ int tp_abi_version(void) { return TP_ABI_VERSION; }
 tp_status_t tp_inject_alloc_failures(int count) {
   if (count < 0) return TP_ERR_ARG;
   g_fail_allocs.store(count);
+  return TP_OK;
+}
+
+tp_status_t tp_set_machine_balance(double flop_per_byte) {
+  if (!(flop_per_byte >= 0.0) || flop_per_byte > 1e6) return TP_ERR_ARG;
+  g_balance_override.store(flop_per_byte);
   return TP_OK;
 }
 
@@ -1142,7 +1176,7 @@ size_t tp_mlp_train_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
   DevState *d = nullptr;
   if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
   TrainPlan p;
-  plan_train(s, M, v, d->sms, &p);
+  plan_train(s, M, v, d, &p);
   return p.fwd_total();
 }
 
@@ -1157,7 +1191,7 @@ size_t tp_mlp_backward_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v)
   DevState *d = nullptr;
   if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
   TrainPlan p;
-  plan_train(s, M, v, d->sms, &p);
+  plan_train(s, M, v, d, &p);
   return p.bwd_total();
 }
 
@@ -1172,7 +1206,7 @@ size_t tp_mlp_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
   DevState *d = nullptr;
   if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
   MlpPlan p;
-  if (plan_mlp(s, M, v, d->sms, &p) != TP_OK) return 0;
+  if (plan_mlp(s, M, v, d, &p) != TP_OK) return 0;
   return p.total();
 }
 
@@ -1180,7 +1214,7 @@ size_t tp_colpar_workspace_bytes(tp_shards_t s, int64_t M) {
   DevState *d = nullptr;
   if (!s || s->kind != 0 || M <= 0 || dev_state(&d) != TP_OK) return 0;
   MlpPlan p;
-  if (plan_mlp(s, M, TP_VAR_AUTO, d->sms, &p) != TP_OK) return 0;
+  if (plan_mlp(s, M, TP_VAR_AUTO, d, &p) != TP_OK) return 0;
   return p.col_bytes;
 }
 
@@ -1194,7 +1228,7 @@ tp_status_t tp_colpar_forward(tp_shards_t s, const void *X, int64_t M, tp_act_t 
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MlpPlan p;
-  TP_TRY(plan_mlp(s, M, TP_VAR_AUTO, d->sms, &p));
+  TP_TRY(plan_mlp(s, M, TP_VAR_AUTO, d, &p));
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.col_bytes, st));
   return colpar_any(s, d, p, X, M, act, Y, w.ptr, st);
@@ -1204,7 +1238,7 @@ size_t tp_rowpar_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
   DevState *d = nullptr;
   if (!s || s->kind != 0 || M <= 0 || !valid_variant(v) || dev_state(&d) != TP_OK) return 0;
   MlpPlan p;
-  if (plan_mlp(s, M, v, d->sms, &p) != TP_OK) return 0;
+  if (plan_mlp(s, M, v, d, &p) != TP_OK) return 0;
   return p.row_bytes;
 }
 
@@ -1218,7 +1252,7 @@ tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp_varian
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MlpPlan p;
-  TP_TRY(plan_mlp(s, M, v, d->sms, &p));
+  TP_TRY(plan_mlp(s, M, v, d, &p));
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.row_bytes, st));
   return rowpar_any(s, d, p, Y, M, Z, w.ptr, st);
@@ -1264,9 +1298,8 @@ size_t tp_attn_proj_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
   int slots = 1;
   if (v == TP_VAR_PARTIALS) slots = s->T;
   if (v == TP_VAR_AUTO) {
-    const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
     slots = choose_slots(cdiv(M, 128) * (s->H / s->bn2), s->T, static_cast<int>(s->Fs / 64), d->sms,
-                         (1.9e15 / 6.5e12) / flop_per_ktile, M * s->H * 4, false);
+                         ktile_per_partial_byte(d, s->bn2), M * s->H * 4, false);
   }
   return slots > 1 ? round256(static_cast<size_t>(slots * M * s->H) * 4) : 0;
 }
@@ -1287,9 +1320,8 @@ tp_status_t tp_attn_proj_forward(tp_shards_t s, const void *X, const void *A, in
     int slots = 1;
     if (v == TP_VAR_PARTIALS) slots = s->T;
     if (v == TP_VAR_AUTO) {
-      const double flop_per_ktile = 2.0 * 128.0 * s->bn2 * 64.0;
       slots = choose_slots(cdiv(M, 128) * (s->H / s->bn2), s->T, static_cast<int>(s->Fs / 64), d->sms,
-                           (1.9e15 / 6.5e12) / flop_per_ktile, M * s->H * 4, false);
+                           ktile_per_partial_byte(d, s->bn2), M * s->H * 4, false);
     }
     const size_t need = slots > 1 ? round256(static_cast<size_t>(slots * M * s->H) * 4) : 0;
     Workspace w;
@@ -1307,7 +1339,7 @@ size_t tp_block_workspace_bytes(tp_shards_t attn, tp_shards_t mlp, int64_t M, tp
       dev_state(&d) != TP_OK)
     return 0;
   BlockPlan p;
-  plan_block(attn, mlp, M, v, d->sms, &p);
+  plan_block(attn, mlp, M, v, d, &p);
   return p.total();
 }
 

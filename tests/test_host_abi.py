@@ -76,6 +76,11 @@ def test_argument_errors_are_status_codes(lib):
     assert lib.tp_attention_workspace_bytes(100, 2, 64) == 0
     assert lib.tp_inject_alloc_failures(-1) == 1
     assert lib.tp_inject_alloc_failures(3) == 0 and lib.tp_inject_alloc_failures(0) == 0
+    lib.tp_set_machine_balance.argtypes = [ctypes.c_double]
+    assert lib.tp_set_machine_balance(-1.0) == 1
+    assert lib.tp_set_machine_balance(float("nan")) == 1
+    assert lib.tp_set_machine_balance(2e6) == 1
+    assert lib.tp_set_machine_balance(280.0) == 0 and lib.tp_set_machine_balance(0.0) == 0
     lib.tp_shards_destroy(None)
 
 
