@@ -810,7 +810,7 @@ tp_status_t attention_core(const DevState *d, const void *Q, const void *K, cons
   const int64_t hd = kAttnHeadDim;
   CUtensorMap mq, mk, mv;
   TP_TRY(make_map(&mq, Q, hd, M, heads, hd * 2, M * hd * 2, 128));
-  TP_TRY(make_map(&mk, K, hd, M, heads, hd * 2, M * hd * 2, 128));
+  TP_TRY(make_map(&mk, K, hd, M, heads, hd * 2, M * hd * 2, static_cast<uint32_t>(attention_key_box_rows())));
   TP_TRY(make_map(&mv, V, hd, M, heads, hd * 2, M * hd * 2, 64));
   AttnArgs g;
   std::memset(&g, 0, sizeof g);

@@ -333,6 +333,19 @@ __device__ __forceinline__ void tc_mma2_bf16(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// Pair MMA with A in tensor memory: D (each CTA's TMEM, its 128 rows) (+)= A
+// (each CTA's TMEM, its 128 rows x 16, bf16 pairs per 32-bit column) * B^T
+// (N/2 rows in each CTA's smem).
+__device__ __forceinline__ void tc_mma2_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the barrier at the same offset in every CTA of `cta_mask`
 // when the pair MMAs issued so far have completed.
 __device__ __forceinline__ void tc_commit2_multicast(uint32_t bar, uint16_t cta_mask) {

@@ -100,13 +100,13 @@ cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, con
 // Fused attention core over `heads` independent heads of dimension 128:
 // O_h[r] = sum over keys j (j <= r when causal, j < M) of
 // softmax_j(q_r . k_j * scale) v_j, for every token r < M.  Q, K and V are
-// head-major [heads][M][128] bf16 tensor maps (Q and K box 64 x 128 rows, V
-// box 64 x 64 rows; keys past M read as zeros); O is bf16 [M][ldo] with head h
-// in columns [128 h, 128 h + 128).
+// head-major [heads][M][128] bf16 tensor maps (Q box 64 x 128 rows, K box
+// 64 x attention_key_box_rows(), V box 64 x 64 rows; rows past M read as
+// zeros); O is bf16 [M][ldo] with head h in columns [128 h, 128 h + 128).
 struct AttnArgs {
   int M;
   int heads;
-  int m_tiles;        // query tiles of 128 rows
+  int m_tiles;        // key tiles of 128, ceil(M / 128)
   int causal;
   float scale_log2;   // scale * log2(e)
   void *O;
@@ -115,6 +115,9 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
 };
 constexpr int kAttnHeadDim = 128;
+// Rows (keys) of the K tensor map's box: the kernel runs on CTA pairs, each
+// CTA loading half of every 128-key tile.
+int attention_key_box_rows();
 cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapV,
                              const AttnArgs &args, int num_sms, cudaStream_t stream);
 

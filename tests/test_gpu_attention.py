@@ -71,15 +71,18 @@ def test_attention_peaky_and_drifting_scores(tp, q_scale, key_ramp):
 
 
 def test_attention_more_units_than_sms(tp):
-    """16 heads x 16 query tiles = 256 units: CTAs take several units each, in
-    snake order, with the pipeline carried across unit boundaries."""
-    M, nh = 2048, 16
+    """16 heads x 6 pairs of 256-row query tiles = 96 units on at most 76 CTA
+    pairs: pairs take several units each, in snake order, with the pipeline
+    carried across unit boundaries; 3000 tokens leave a ragged last tile
+    (rows 2816..2999, CTA 1's rows of it partly past M)."""
+    M, nh = 3000, 16
     d = attention_inputs(M, nh, seed=21)
     rng = np.random.default_rng(3)
-    rows = np.unique(np.concatenate([[0, 127, 128, 1023, 2046, 2047], rng.choice(M, 120, replace=False)]))
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, 1023, 2815, 2816, 2943, 2944, 2998, 2999],
+                                     rng.choice(M, 120, replace=False)]))
     for causal in (True, False):
         got, ref, _ = _run(tp, d, causal, rows=rows)
-        assert _ok(got, ref, f"M=2048 nh=16 causal={causal}")
+        assert _ok(got, ref, f"M=3000 nh=16 causal={causal}")
 
 
 def test_attention_full_workload_sampled_rows(tp):
