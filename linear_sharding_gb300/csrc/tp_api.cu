@@ -169,6 +169,23 @@ tp_status_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
   return r == CUDA_SUCCESS ? TP_OK : TP_ERR_CUDA;
 }
 
+// 4-D bf16 tensor map of an MN-major GEMM operand stored [segs][K][mn] (mn
+// elements per segment, a multiple of 64): dims {64, K, mn / 64, segs}, byte
+// strides {mn x 2, 128, K x mn x 2}, box {64, 64, kMnPairBox, 1}, 128-byte
+// swizzle, zero fill past K.  See kMnPairBox.
+tp_status_t make_map_mn_pairs(CUtensorMap *m, const void *base, uint64_t mn, uint64_t K, uint64_t segs) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) return TP_ERR_CUDA;
+  const cuuint64_t dims[4] = {64, K, mn / 64, segs};
+  const cuuint64_t strides[3] = {mn * 2, 128, K * mn * 2};
+  const cuuint32_t box[4] = {64, 64, static_cast<cuuint32_t>(kMnPairBox), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TP_OK : TP_ERR_CUDA;
+}
+
 // Tensor maps of the k-tile-blocked bf16 weights (operand mode kKtileBlocked:
 // coordinate (0, row, k-tile)).  W1: k-tile kt of all T R1 rows; W2: k-tile
 // kt of shard i is plane i (Ks/64) + kt of H rows.  Ks is the per-shard K of W2.
@@ -735,14 +752,26 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   // 3. dW2 = H^T dZ  [F x H];  4. dW1 = X^T dP  [H x ncols].  K is the token axis, so every
   // operand is read MN-major straight from its [tokens][features] layout (64 x 64 boxes; the
   // copies fill tokens past M with zeros): per-shard H and dP as [segments][M][Fs].
+  // Where every 128-row group of a tile's MN rows lies inside one segment (per-shard widths
+  // a multiple of 128), each copy fetches two 64-row blocks (4-D maps, kMnPairBox): half the
+  // copy instructions per stage, which is what bounds these GEMMs' loads.
+  const bool pairs = Fs % 128 == 0;
   CUtensorMap m_h, m_x, m_dz, m_dp;
-  TP_TRY(make_map(&m_h, Hsave, Fs, M, T, Fs * 2, M * Fs * 2, 64));
-  TP_TRY(make_map(&m_x, X, H, M, 1, H * 2, M * H * 2, 64));
-  TP_TRY(make_map(&m_dz, dZ, H, M, 1, H * 2, M * H * 2, 64));
-  TP_TRY(make_map(&m_dp, dP, Fs, M, p.nseg, Fs * 2, M * Fs * 2, 64));
+  if (pairs) {
+    TP_TRY(make_map_mn_pairs(&m_h, Hsave, Fs, M, T));
+    TP_TRY(make_map_mn_pairs(&m_x, X, H, M, 1));
+    TP_TRY(make_map_mn_pairs(&m_dz, dZ, H, M, 1));
+    TP_TRY(make_map_mn_pairs(&m_dp, dP, Fs, M, p.nseg));
+  } else {
+    TP_TRY(make_map(&m_h, Hsave, Fs, M, T, Fs * 2, M * Fs * 2, 64));
+    TP_TRY(make_map(&m_x, X, H, M, 1, H * 2, M * H * 2, 64));
+    TP_TRY(make_map(&m_dz, dZ, H, M, 1, H * 2, M * H * 2, 64));
+    TP_TRY(make_map(&m_dp, dP, Fs, M, p.nseg, Fs * 2, M * Fs * 2, 64));
+  }
   const int ktok = static_cast<int>(cdiv(M, 64));
   {
     GemmArgs g = base_args(d);
+    g.mn_pairs = pairs ? 1 : 0;
     g.out = dW2;
     g.ld_out = H;
     GemmCall c;
@@ -758,6 +787,7 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   }
   {
     GemmArgs g = base_args(d);
+    g.mn_pairs = pairs ? 1 : 0;
     g.out = dW1;
     g.ld_out = ncols;
     GemmCall c;

@@ -3,50 +3,39 @@
 // block": heads are sharded across ranks, so each head's attention is local
 // to the shard that owns it and needs no communication).
 //
-// For each query row r of a head,
+// One CTA per SM walks units (head, pair of adjacent 128-query tiles A and B)
+// and computes, for each query row r,
 //   O[r] = sum_{j allowed} 2^(t_rj - m_r) v_j / sum_{j allowed} 2^(t_rj - m_r),
 //   t_rj = (q_r . k_j / sqrt(128)) log2(e),
-// the softmax-weighted sum of the values for any shift m_r.  Keys are visited
-// 128 at a time and neither scores nor probabilities leave the SM.
-//
-// The kernel runs on CTA pairs (clusters of 2, tcgen05 cta_group::2).  A unit
-// is (head, two adjacent 256-row query tiles A and B); CTA r of the pair owns
-// rows [128 r, 128 r + 128) of each query tile.  Per 128-key tile the pair
-// issues, from one thread of CTA 0,
-//   S_A = Q_A K^T and S_B = Q_B K^T   (M = 256, N = 128 keys, K = 128),
-//   O_A += P_A V   and O_B += P_B V    (M = 256, N = 128 head dims, K = 128 keys),
-// where CTA r holds only HALF of each B operand in its shared memory: keys
-// [64 r, 64 r + 64) of the K tile, head dims [64 r, 64 r + 64) of the V tile.
-// Against one CTA per 128 rows this halves the operand bytes that the tensor
-// core reads from shared memory per flop, and the bytes the copy engine
-// writes there: a single CTA's 128 x 128 x 16 MMA with both operands in shared
-// memory alone reads 128 bytes per clock, the whole shared-memory bandwidth.
-//   warp 0      TMA producer of each CTA: its Q rows once per unit, its half
-//               of every K and V tile through 4- and 3-deep rings, keys one
-//               tile ahead of values.  All copies of the pair complete on CTA
-//               0's barriers, which CTA 0 arms for both halves;
-//   warp 1      TMEM allocation (both CTAs, 512 columns each); in CTA 0 one
-//               thread issues the pair's MMAs, per key tile j:
+// which is the softmax-weighted sum of the values for any shift m_r.  Keys
+// are visited 128 at a time and neither scores nor probabilities leave the
+// SM, or even reach shared memory:
+//   warp 0      TMA producer: both Q tiles once per unit; K and V tiles of
+//               128 keys (shared by the two query tiles) through a 3-deep and
+//               a 2-deep ring, keys one tile ahead of values.  Q, K and V are
+//               all head-major [heads][M][128]; V is the P V product's B
+//               operand read MN-major (its K, the key axis, is the outer one);
+//   warp 1      TMEM allocation; one thread issues, per key tile j,
 //               O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
-//               S_B = Q_B K_{j+1}^T, so the tensor core works on one tile
-//               while the other tile's probabilities are made;
-//   warps 2..5  softmax of tile A, warps 6..9 of tile B, in each CTA: one
-//               thread per query row (TMEM lane = row) reads the row of S,
-//               takes its maximum, writes P = 2^(t - m_r) as bf16 over the
-//               upper 64 columns of the same TMEM buffer (the P V product's A
-//               operand), adds the float32 weights to the row sum, and
-//               releases the tile to CTA 0's MMA thread (one arrival per warp).
+//               S_B = Q_B K_{j+1}^T (tcgen05, 128 x 128, K = 128; P read from
+//               TMEM, the rest from shared memory), so the tensor core works
+//               on one tile while the other tile's probabilities are made;
+//   warps 2..5  softmax of tile A, warps 6..9 of tile B: one thread per query
+//               row (TMEM lane = row) reads the row of S into registers, takes
+//               its maximum, writes P = 2^(t - m_r) as bf16 over the upper 64
+//               columns of the same TMEM buffer, and adds the float32 weights
+//               to the row sum.
 // Each query tile has one S/P buffer: the next S into it is issued after the
 // P V that reads it, and tcgen05 MMAs of one thread run in issue order.  The
 // shift m_r is raised only when a tile's maximum exceeds it by more than 8 (so
 // P <= 2^8): then the row's sum and its accumulator are scaled by
 // 2^(m_old - m_new).  The previous P V is complete at that point, because the
 // commit that signalled this S covers every MMA issued before it.
-// Causal: a 256-row query tile t needs key tiles 0 .. 2t + 1; CTA 0's rows
-// need one fewer, and on that last key tile its warps write zero weights
-// without computing them.  Units run heaviest first and are dealt to the
-// pairs in snake order.  Waits poll and are bounded like the GEMM's; on a
-// timeout a CTA drains what it issued and reports through the status word.
+// Units run heaviest first (causal: the last query tiles) and are dealt to
+// the CTAs in snake order, so CTA loads stay even.  Waits poll (the S ->
+// softmax -> P V hand-off is on the critical path, and a suspended wait wakes
+// too late) and are bounded like the GEMM's; on a timeout the CTA drains what
+// it issued and reports through the status word.
 #include <cuda_bf16.h>
 
 #include "tp_device.cuh"
@@ -55,25 +44,17 @@
 namespace tp {
 namespace {
 
-constexpr int kTile = 128;                 // keys per step; query rows per CTA per tile
-constexpr int kQRows = 256;                // query rows of a pair's tile
+constexpr int kTile = 128;                // queries per tile, keys per step
 constexpr int kThreads = 320;
-constexpr int kWarpsPerTile = 4;           // softmax warps per query tile in each CTA
-constexpr uint32_t kSub = 128 * 128;       // 128 rows x 64 bf16 in the 128-byte swizzle: 16 KiB
-constexpr uint32_t kBox = 64 * 128;        // 64 rows x 64 bf16: 8 KiB
-constexpr uint32_t kQBytes = 2 * kSub;     // this CTA's 128 query rows x 128 head dims
-constexpr uint32_t kKBytes = 2 * kBox;     // this CTA's 64 keys x 128 head dims
-constexpr uint32_t kVBytes = 2 * kBox;     // 128 keys x this CTA's 64 head dims
-constexpr int kKst = 4, kVst = 3;          // K and V halves in shared memory
-constexpr int kBars = 26;
-constexpr float kRescaleGap = 8.0f;        // log2 of the largest unnormalised probability
-// Time CTA 1 leaves its in-flight copies to land after an abort (they complete on CTA 0's barriers).
-constexpr unsigned long long kPeerDrainNs = 200000ull;
+constexpr int kSoftmaxThreads = 128;      // per query tile
+constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
+constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
+constexpr int kKst = 3, kVst = 2;         // K and V tiles in shared memory
+constexpr int kBars = 28;
+constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
 // Q[2] | K[kKst] | V[kVst] | barriers
-constexpr size_t kSmemBytes =
-    1024 + 2 * static_cast<size_t>(kQBytes) + kKst * static_cast<size_t>(kKBytes) +
-    kVst * static_cast<size_t>(kVBytes) + kBars * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + (2 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "attention tiles exceed the shared memory of one CTA");
 
 // TMEM columns: S/P of tile A 0..127, of tile B 128..255, O_A 256..383, O_B 384..511
@@ -81,30 +62,25 @@ constexpr uint32_t kOcol = 256;
 
 struct AttnUnit {
   int head;
-  int mt[2];   // 256-row query tiles A and B (B = -1 when the last pair has one tile)
-  int nkt[2];  // key tiles the pair visits for each (0 for an absent tile)
+  int mt[2];   // query tiles A and B (B = -1 when the last pair has one tile)
+  int nkt[2];  // key tiles each one visits (0 for an absent tile)
   int nk;      // key tiles the unit visits: max(nkt)
 };
 
-__device__ __forceinline__ int query_tiles(const AttnArgs &a) { return (a.M + kQRows - 1) / kQRows; }
-
-// k-th unit of pair b among G pairs: snake order over the heaviest-first list.
+// k-th unit of CTA b among G CTAs: snake order over the heaviest-first list.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? G - 1 - b : b); }
 
 __device__ __forceinline__ AttnUnit decode(int u, const AttnArgs &a) {
-  const int qt = query_tiles(a);
-  const int pairs = (qt + 1) / 2;
+  const int pairs = (a.m_tiles + 1) / 2;
   AttnUnit t;
   const int p = pairs - 1 - u / a.heads;
   t.head = u % a.heads;
   t.mt[0] = 2 * p;
-  t.mt[1] = 2 * p + 1 < qt ? 2 * p + 1 : -1;
-  for (int w = 0; w < 2; ++w) {
-    const int need = a.causal ? 2 * t.mt[w] + 2 : a.m_tiles;  // causal: keys up to the tile's last row
-    t.nkt[w] = t.mt[w] < 0 ? 0 : (need < a.m_tiles ? need : a.m_tiles);
-  }
+  t.mt[1] = 2 * p + 1 < a.m_tiles ? 2 * p + 1 : -1;
+  for (int w = 0; w < 2; ++w)
+    t.nkt[w] = t.mt[w] < 0 ? 0 : (a.causal ? t.mt[w] + 1 : a.m_tiles);
   t.nk = t.nkt[0] > t.nkt[1] ? t.nkt[0] : t.nkt[1];
-  if (!TP_CHECK(t.head < a.heads && t.mt[0] >= 0 && t.mt[1] < qt && t.nk >= 1 && t.nk <= a.m_tiles,
+  if (!TP_CHECK(t.head < a.heads && t.mt[0] >= 0 && t.mt[1] < a.m_tiles && t.nk >= 1 && t.nk <= a.m_tiles,
                 a.status)) {
     t.mt[1] = -1;  // keep the unit's shape sane: tile A alone over one key tile
     t.nkt[0] = t.nk = 1;
@@ -145,37 +121,34 @@ struct Ring {
 
 // 320 threads: the 10 warps leave 3 on two of the 4 SM sub-partitions, whose 16K registers
 // each then cap a thread at 168
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                         const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
-  constexpr uint32_t IDESC_S = idesc_bf16_f32(256, 128);
-  constexpr uint32_t IDESC_PV = IDESC_S | kIdescMnB;  // V is read MN-major: [keys][head_dim]
-  constexpr int kPairArrivals = 2 * kWarpsPerTile;    // one per softmax warp of a tile, both CTAs
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                    const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+  constexpr uint32_t IDESC_PV = IDESC | kIdescMnB;  // V is read MN-major: [keys][head_dim]
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem;                  // 2 query tiles (this CTA's rows)
-  uint8_t *sK = sQ + 2 * kQBytes;
-  uint8_t *sV = sK + kKst * kKBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + kVst * kVBytes);
+  uint8_t *sQ = smem;                  // 2 tiles
+  uint8_t *sK = sQ + 2 * kTileBytes;
+  uint8_t *sV = sK + kKst * kTileBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sV + kVst * kTileBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
   const uint32_t b0 = smem_u32(bars);
-  // barrier i at b0 + 8 i; the same offsets in both CTAs
+  // barrier i at b0 + 8 i
   const uint32_t q_full = b0, q_empty = b0 + 8;
   auto k_full = [&](int s) { return b0 + 16 + 8u * s; };    // kKst
-  auto k_empty = [&](int s) { return b0 + 48 + 8u * s; };   // kKst
-  auto v_full = [&](int s) { return b0 + 80 + 8u * s; };    // kVst
-  auto v_empty = [&](int s) { return b0 + 104 + 8u * s; };  // kVst
-  auto s_full = [&](int w) { return b0 + 128 + 8u * w; };   // S of tile w computed (both CTAs)
-  auto p_full = [&](int w) { return b0 + 144 + 8u * w; };   // P of tile w written (CTA 0's counts both)
-  auto o_full = [&](int w) { return b0 + 160 + 8u * w; };   // tile w's last P V of the unit done
-  auto o_free = [&](int w) { return b0 + 176 + 8u * w; };   // tile w's O read out (CTA 0's counts both)
-  const uint32_t drain = b0 + 192, never = b0 + 200;
+  auto k_empty = [&](int s) { return b0 + 40 + 8u * s; };   // kKst
+  auto v_full = [&](int s) { return b0 + 64 + 8u * s; };    // kVst
+  auto v_empty = [&](int s) { return b0 + 80 + 8u * s; };   // kVst
+  auto s_full = [&](int w) { return b0 + 96 + 8u * w; };    // S of tile w computed
+  auto p_full = [&](int w) { return b0 + 112 + 8u * w; };   // P of tile w written over its S
+  auto o_full = [&](int w) { return b0 + 128 + 8u * w; };   // tile w's last P V of the unit done
+  auto o_free = [&](int w) { return b0 + 144 + 8u * w; };   // tile w's O read out
+  const uint32_t drain = b0 + 160, never = b0 + 168;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -189,9 +162,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(s_full(w), 1);
-      mbar_init(p_full(w), kPairArrivals);
+      mbar_init(p_full(w), kSoftmaxThreads);
       mbar_init(o_full(w), 1);
-      mbar_init(o_free(w), kPairArrivals);
+      mbar_init(o_free(w), kSoftmaxThreads);
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
@@ -204,52 +177,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapV);
   }
   if (warp == 1) {
-    tmem_alloc2(smem_u32(tmem_slot), 512);
-    tmem_relinquish2();
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // the set-up above overlaps the previous kernel's tail; Q, K and V are read only from here on
   pdl_trigger();
   pdl_wait();
   const WaitCtl w{abort_flag, a.status, a.wait_limit_ns};
-  const int units = a.heads * ((query_tiles(a) + 1) / 2);
-  const int G = static_cast<int>(gridDim.x >> 1), b = static_cast<int>(blockIdx.x >> 1);
+  const int units = a.heads * ((a.m_tiles + 1) / 2);
+  const int G = gridDim.x, b = blockIdx.x;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer (each CTA its own rows and halves) ----
+      // ---- TMA producer ----
       // Loads per unit, in order: Q_A and Q_B, K_0, then for each j: K_{j+1} (if any), V_j.
       int kc = 0, vc = 0, qc = 0;  // K, V tiles and Q pairs issued so far
       Ring kr, vr;
       bool ok = true;
-      // this CTA's copy, completing on CTA 0's barrier `bar` (armed by CTA 0 for both CTAs)
-      auto load = [&](uint8_t *dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2) {
-        if (leader)
-          tma_load_3d(smem_u32(dst), m, bar, c0, c1, c2);
-        else
-          tma_load_3d_pair(smem_u32(dst), m, map_to_rank(bar, 0), c0, c1, c2);
-      };
       auto load_k = [&](const AttnUnit &t, int j) -> bool {
         if (!wait_bar_spin(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
-        if (leader) mbar_arrive_expect_tx(k_full(kr.buf), 2 * kKBytes);
-        // keys 128 j + 64 rank .. + 63, head dims 64 kb .. + 63 (8 KiB kb)
+        mbar_arrive_expect_tx(k_full(kr.buf), kTileBytes);
         for (int kb = 0; kb < 2; ++kb)
-          load(sK + kr.buf * kKBytes + kb * kBox, &mapK, k_full(kr.buf), kb * 64,
-               j * kTile + 64 * static_cast<int>(rank), t.head);
+          tma_load_3d(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
+                      t.head);
         ++kc;
         kr.next(kKst);
         return true;
       };
       auto load_v = [&](const AttnUnit &t, int j) -> bool {
         if (!wait_bar_spin(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
-        if (leader) mbar_arrive_expect_tx(v_full(vr.buf), 2 * kVBytes);
-        // head dims 64 rank .. + 63, keys 128 j + 64 h .. + 63 (8 KiB h)
+        mbar_arrive_expect_tx(v_full(vr.buf), kTileBytes);
+        // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
         for (int h = 0; h < 2; ++h)
-          load(sV + vr.buf * kVBytes + h * kBox, &mapV, v_full(vr.buf), 64 * static_cast<int>(rank),
-               j * kTile + 64 * h, t.head);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf), c * 64,
+                        j * kTile + h * 64, t.head);
         ++vc;
         vr.next(kVst);
         return true;
@@ -259,12 +225,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
         if (!wait_bar_spin(q_empty, (qc & 1u) ^ 1u, w)) break;
-        if (leader) mbar_arrive_expect_tx(q_full, (t.mt[1] >= 0 ? 2 : 1) * 2 * kQBytes);
+        mbar_arrive_expect_tx(q_full, (t.mt[1] >= 0 ? 2 : 1) * kTileBytes);
         for (int q = 0; q < 2; ++q) {
           if (t.mt[q] < 0) continue;
           for (int kb = 0; kb < 2; ++kb)
-            load(sQ + q * kQBytes + kb * kSub, &mapQ, q_full, kb * 64,
-                 t.mt[q] * kQRows + kTile * static_cast<int>(rank), t.head);
+            tma_load_3d(smem_u32(sQ + q * kTileBytes + kb * kSub), &mapQ, q_full, kb * 64, t.mt[q] * kTile,
+                        t.head);
         }
         ++qc;
         if (!load_k(t, 0)) break;
@@ -279,29 +245,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Every copy issued completes on CTA 0's full barrier, consumed or not (after an abort
-      // some are not).  CTA 0 waits for the last phase of each; CTA 1 cannot see those barriers
-      // and leaves its copies a bounded time to land.
-      if (leader) {
-        if (qc > 0) drain_bar(q_full, (qc - 1) & 1u, a.status);
-        for (int s = 0; s < kKst; ++s) {
-          const int n = (kc - s + kKst - 1) / kKst;  // loads issued into stage s
-          if (n > 0) drain_bar(k_full(s), (n - 1) & 1u, a.status);
-        }
-        for (int s = 0; s < kVst; ++s) {
-          const int n = (vc - s + kVst - 1) / kVst;
-          if (n > 0) drain_bar(v_full(s), (n - 1) & 1u, a.status);
-        }
-      } else if (*abort_flag) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < kPeerDrainNs) {
-        }
+      // Every copy issued completes on its full barrier, consumed or not (after an abort
+      // some are not): wait for the last phase of each before the CTA may exit.
+      if (qc > 0) drain_bar(q_full, (qc - 1) & 1u, a.status);
+      for (int s = 0; s < kKst; ++s) {
+        const int n = (kc - s + kKst - 1) / kKst;  // loads issued into stage s
+        if (n > 0) drain_bar(k_full(s), (n - 1) & 1u, a.status);
+      }
+      for (int s = 0; s < kVst; ++s) {
+        const int n = (vc - s + kVst - 1) / kVst;
+        if (n > 0) drain_bar(v_full(s), (n - 1) & 1u, a.status);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ---- MMA issuer (CTA 0 only) ----
+    if (lane == 0) {
+      // ---- MMA issuer ----
       int uc = 0;                            // units started
       Ring kr, vr;                           // K tile of the next S, V tile of the next P V
       uint32_t sph[2] = {0u, 0u};            // phase of tile q's next p_full wait
@@ -312,21 +271,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + q * 128;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + q * kQBytes + kb * kSub));
-          const uint64_t bd = sw128_kmajor_desc(kbase + kb * kBox);
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + q * kTileBytes + kb * kSub));
+          const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, IDESC_S, (kb | k) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) tc_mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) ? 1u : 0u);
         }
-        tc_commit2_multicast(s_full(q), 0x3);
+        tc_commit(s_full(q));
       };
       // S of both tiles for key tile j (tiles that visit it), then release K_j
       auto issue_s_pair = [&](const AttnUnit &t, int j) -> bool {
         if (!wait_bar_spin(k_full(kr.buf), kr.phase, w)) return false;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + kr.buf * kKBytes);
+        const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
         for (int q = 0; q < 2; ++q)
           if (j < t.nkt[q]) issue_s(q, kbase);
-        tc_commit2_multicast(k_empty(kr.buf), 0x3);
+        tc_commit(k_empty(kr.buf));
         kr.next(kKst);
         return true;
       };
@@ -337,17 +296,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!wait_bar_spin(q_full, uc & 1u, w)) break;
         tc_fence_after();
         if (!issue_s_pair(t, 0)) break;
-        if (t.nk == 1) tc_commit2_multicast(q_empty, 0x3);
+        if (t.nk == 1) tc_commit(q_empty);
         for (int j = 0; j < t.nk && ok; ++j) {
           if (!wait_bar_spin(v_full(vr.buf), vr.phase, w)) {
             ok = false;
             break;
           }
-          const uint64_t vd = sw128_mnmajor_desc(smem_u32(sV + vr.buf * kVBytes));
+          const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
           bool k_next_ready = false;
           for (int q = 0; q < 2 && ok; ++q) {
             if (j >= t.nkt[q]) continue;
-            // O_q += P_q V_j once both CTAs' softmax warps have written P_q (and, for the unit's
+            // O_q += P_q V_j once the softmax threads have written P_q (and, for the unit's
             // first key tile, read out the previous unit's O_q)
             if (!wait_bar_spin(p_full(q), sph[q], w) || (j == 0 && !wait_bar_spin(o_free(q), ofp[q] ^ 1u, w))) {
               ok = false;
@@ -357,10 +316,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t pa = tmem + q * 128 + 64;  // P: the upper 64 columns, bf16 pairs
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // keys 16 kk ..: 2 KiB per 16 keys of this CTA's V half
-              tc_mma2_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, vd + 128u * kk, IDESC_PV,
-                                  (j | kk) ? 1u : 0u);
-            if (j + 1 == t.nkt[q]) tc_commit2_multicast(o_full(q), 0x3);
+            for (int kk = 0; kk < 8; ++kk) {
+              // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
+              const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
+              tc_mma_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV,
+                                 (j | kk) ? 1u : 0u);
+            }
+            if (j + 1 == t.nkt[q]) tc_commit(o_full(q));
             // then this tile's S for key tile j + 1, so the other tile's P V overlaps its softmax
             if (j + 1 < t.nkt[q]) {
               if (!k_next_ready) {
@@ -371,23 +333,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 k_next_ready = true;
               }
-              issue_s(q, smem_u32(sK + kr.buf * kKBytes));
+              issue_s(q, smem_u32(sK + kr.buf * kTileBytes));
             }
           }
           if (!ok) break;
-          tc_commit2_multicast(v_empty(vr.buf), 0x3);
+          tc_commit(v_empty(vr.buf));
           vr.next(kVst);
           if (k_next_ready) {
-            tc_commit2_multicast(k_empty(kr.buf), 0x3);
+            tc_commit(k_empty(kr.buf));
             kr.next(kKst);
           }
-          if (j + 2 == t.nk) tc_commit2_multicast(q_empty, 0x3);  // every S of this unit is issued
+          if (j + 2 == t.nk) tc_commit(q_empty);  // every S of this unit is issued
         }
         ++uc;
         for (int q = 0; q < 2; ++q)
           if (t.nkt[q] > 0) ofp[q] ^= 1u;
       }
-      tc_commit2(drain);
+      tc_commit(drain);
       drain_bar(drain, 0u, a.status);
     }
     __syncwarp();
@@ -399,7 +361,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t sb = tmem + lane_base + q * 128;
     const uint32_t ob = tmem + lane_base + kOcol + q * 128;
-    const uint32_t p_done = map_to_rank(p_full(q), 0), o_done = map_to_rank(o_free(q), 0);
     const float c = a.scale_log2;
     uint32_t sph = 0, uc = 0;  // phase of the next s_full wait; units this tile took part in
     bool ok = true;
@@ -407,18 +368,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool got = wait_bar_spin(bar, parity, w);
       return __all_sync(0xffffffffu, got);
     };
-    // one arrival per warp on CTA 0's barrier, after the warp's TMEM accesses are complete
-    auto release = [&](uint32_t bar_cluster) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar_cluster);
-    };
     for (int k = 0; ok; ++k) {
       const int u = unit_of(k, b, G);
       if (u >= units) break;
       const AttnUnit t = decode(u, a);
       if (t.nkt[q] == 0) continue;  // the last pair's missing tile B
-      const int row = t.mt[q] * kQRows + kTile * static_cast<int>(rank) + row_in_tile;
+      const int row = t.mt[q] * kTile + row_in_tile;
       float m_used = -INFINITY, l_run = 0.f;
       for (int j = 0; j < t.nkt[q]; ++j) {
         if (!wait_all(s_full(q), sph)) {
@@ -431,19 +386,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int key0 = j * kTile;
         int kmax = a.M - 1 - key0;
         if (a.causal && row - key0 < kmax) kmax = row - key0;
-        if (__all_sync(0xffffffffu, kmax < 0)) {
-          // no allowed key for any row of this warp (CTA 0's rows on the pair's last causal key
-          // tile): zero weights, nothing to add
-          uint32_t z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
-          tmem_st32(sb + 64, z);
-          tmem_st32(sb + 96, z);
-          tmem_st_wait();
-          release(p_done);
-          continue;
-        }
         const bool masked = kmax < kTile - 1;
+        // every key tile a row visits holds at least one allowed key (its own, or key < M)
+        if (!TP_CHECK(kmax >= 0, a.status)) kmax = 0;
         // the whole row of S_j (128 scores) in registers: its maximum, then the weights
         uint32_t s[4][32];
 #pragma unroll
@@ -468,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mx4[cc] = m;
         }
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_tile = mx * c;  // -inf for a row with no allowed key here: never raises
+        const float m_tile = mx * c;
         const bool raise = m_tile > m_used + kRescaleGap;
         const float m_new = raise ? m_tile : m_used;
         const float alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
@@ -488,9 +433,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const uint32_t *v = s[2 * hh + (i >> 4)];
-            const float2 t2 = __ffma2_rn(
-                make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])), c2, nm2);
-            const float2 e = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])),
+                                        c2, nm2);
+            const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             pk[i] = pack_bf16x2(e.x, e.y);
             sum4[i & 3] = __fadd2_rn(sum4[i & 3], e);
           }
@@ -514,7 +459,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         tmem_st_wait();
-        release(p_done);
+        tc_fence_before();
+        mbar_arrive(p_full(q));
       }
       if (!ok) break;
       // read out O / l once this tile's last P V of the unit is done
@@ -549,51 +495,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      release(o_done);
+      tc_fence_before();
+      mbar_arrive(o_free(q));
     }
   }
 
   tc_fence_before();
-  cluster_sync();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc2(tmem, 512);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 }  // namespace
 
-int attention_key_box_rows() { return 64; }
+int attention_key_box_rows() { return kTile; }
 
 cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapV,
                              const AttnArgs &args, int num_sms, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long qt = (static_cast<long long>(args.M) + kQRows - 1) / kQRows;
-  const long long units = static_cast<long long>(args.heads) * ((qt + 1) / 2);
+  const long long units = static_cast<long long>(args.heads) * ((args.m_tiles + 1) / 2);
   if (units <= 0) return cudaSuccess;
-  // Pairs that fit on the GPU at once (two SMs with room for one CTA each), per device.
-  static int max_clusters[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int &mc = max_clusters[dev & 63];
-  if (mc <= 0) {
-    cudaLaunchConfig_t occ = {};
-    occ.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)), 1, 1);
-    occ.blockDim = dim3(kThreads, 1, 1);
-    occ.dynamicSmemBytes = kSmemBytes;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_pair_kernel, &occ) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = num_sms / 2;
-    }
-    mc = n;
-  }
-  const int clusters = static_cast<int>(units < mc ? units : mc);
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   // launched as a programmatic dependent of the previous kernel (the QKV projection)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -602,7 +531,7 @@ cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_fwd_pair_kernel, mapQ, mapK, mapV, args);
+  return cudaLaunchKernelEx(&cfg, attn_fwd_kernel, mapQ, mapK, mapV, args);
 }
 
 }  // namespace tp

@@ -57,6 +57,8 @@ struct GemmArgs {
   int kt_total, kt_per_seg, kt_per_slot;
   int a_seg, b_seg;
   int a_mn_seg, b_mn_seg;  // EPI_F32_MN: MN rows per segment of A / B (0: one segment)
+  int mn_pairs;            // EPI_F32_MN: the A and B maps are 4-D (see kMnPairBox): one copy
+                           // fetches two adjacent 64-row MN blocks of a segment
   int group_m;          // raster: m-tiles per group (L2 reuse of B tiles)
   int rows_valid;       // valid output rows along A (M, or features when swapped)
   int cols_valid;       // valid output columns along B (N, or tokens when swapped)
@@ -72,6 +74,13 @@ struct GemmArgs {
   int head_dim;             // EPI_QKV_HEADS_BF16: columns per head
   int n_heads;              // EPI_QKV_HEADS_BF16: heads over all shards
 };
+
+// MN-major operands (EPI_F32_MN) as 4-D tensor maps: dims {64 MN elements, K
+// (tokens), MN blocks of 64 per segment, segments}, byte strides {MN per
+// segment x 2, 128, K x MN per segment x 2}, box {64, 64, kMnPairBox, 1}.
+// One copy then lands kMnPairBox 64 x 64 blocks, 8 KiB apart, exactly where
+// kMnPairBox single-block copies of the 3-D map would put them.
+constexpr int kMnPairBox = 2;
 
 // Tile configurations the GEMM is instantiated for.
 enum GemmCfg : int {
@@ -115,8 +124,7 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
 };
 constexpr int kAttnHeadDim = 128;
-// Rows (keys) of the K tensor map's box: the kernel runs on CTA pairs, each
-// CTA loading half of every 128-key tile.
+// Rows (keys) of the K tensor map's box: one 128-key tile per copy.
 int attention_key_box_rows();
 cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, const CUtensorMap &mapV,
                              const AttnArgs &args, int num_sms, cudaStream_t stream);

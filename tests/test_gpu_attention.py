@@ -71,10 +71,10 @@ def test_attention_peaky_and_drifting_scores(tp, q_scale, key_ramp):
 
 
 def test_attention_more_units_than_sms(tp):
-    """16 heads x 6 pairs of 256-row query tiles = 96 units on at most 76 CTA
-    pairs: pairs take several units each, in snake order, with the pipeline
+    """16 heads x 12 pairs of 128-row query tiles = 192 units on at most 152
+    CTAs: CTAs take several units each, in snake order, with the pipeline
     carried across unit boundaries; 3000 tokens leave a ragged last tile
-    (rows 2816..2999, CTA 1's rows of it partly past M)."""
+    (rows 2944..2999)."""
     M, nh = 3000, 16
     d = attention_inputs(M, nh, seed=21)
     rng = np.random.default_rng(3)
