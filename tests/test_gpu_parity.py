@@ -256,6 +256,35 @@ def test_variants_agree_and_are_deterministic(tp):
         assert rowwise_rms_error(outs[v], Zref) <= TOL_BF16_ROW_RMS
 
 
+def test_machine_balance_steers_the_auto_plan(tp):
+    """tp_set_machine_balance: with partial traffic nearly free (1e-3 flop per
+    byte) AUTO splits the row-parallel GEMM over float32 partials (a larger
+    workspace); with it dear (1e5) it keeps one TMEM accumulator.  Either
+    plan's output stays within tolerance of the oracle; 0 restores the
+    device's own figure."""
+    M, H, F, T = 256, 512, 2048, 4  # 4 output tiles of 128 x 256: few waves, long K per tile
+    d = mlp_inputs(M=M, H=H, F=F, act="gelu", dtype="bf16", seed=23)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, "gelu")
+    X = to_device(d["X"])
+    Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "gelu")
+    y_bytes = T * M * (F // T) * 2
+    sizes = {}
+    try:
+        for bal in (1e-3, 1e5):
+            tp.tp_set_machine_balance(bal)
+            sizes[bal] = tp.tp_mlp_workspace_bytes(s, M, "auto")
+            Z = tp.tp_mlp_forward(s, X, variant="auto").cpu().numpy()
+            assert tp.tp_last_device_status() == 0
+            assert rowwise_rms_error(Z, Zref) <= TOL_BF16_ROW_RMS
+    finally:
+        tp.tp_set_machine_balance(0)
+    assert sizes[1e-3] >= y_bytes + 2 * M * H * 4  # at least two float32 partial slots
+    assert sizes[1e5] == (y_bytes + 255) // 256 * 256  # Y alone: one accumulator
+    with pytest.raises(tp.TPError):
+        tp.tp_set_machine_balance(-1.0)
+    s.close()
+
+
 def test_host_buffer_forward(tp):
     """tp_mlp_forward_host: pinned host X in, host Z out, same result."""
     import torch
