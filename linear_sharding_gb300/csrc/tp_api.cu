@@ -752,26 +752,18 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   // 3. dW2 = H^T dZ  [F x H];  4. dW1 = X^T dP  [H x ncols].  K is the token axis, so every
   // operand is read MN-major straight from its [tokens][features] layout (64 x 64 boxes; the
   // copies fill tokens past M with zeros): per-shard H and dP as [segments][M][Fs].
-  // Where every 128-row group of a tile's MN rows lies inside one segment (per-shard widths
-  // a multiple of 128), each copy fetches two 64-row blocks (4-D maps, kMnPairBox): half the
-  // copy instructions per stage, which is what bounds these GEMMs' loads.
-  const bool pairs = Fs % 128 == 0;
+  // Each copy fetches two 64-row MN blocks (4-D maps, kMnPairBox): half the copy instructions
+  // per stage, which is what bounds these GEMMs' loads.  Both blocks lie in one segment, since
+  // shard widths and H are multiples of 128 (tp_shard_weights requires it for bf16).
+  if (Fs % 128 != 0 || H % 128 != 0) return TP_ERR_UNSUPPORTED;
   CUtensorMap m_h, m_x, m_dz, m_dp;
-  if (pairs) {
-    TP_TRY(make_map_mn_pairs(&m_h, Hsave, Fs, M, T));
-    TP_TRY(make_map_mn_pairs(&m_x, X, H, M, 1));
-    TP_TRY(make_map_mn_pairs(&m_dz, dZ, H, M, 1));
-    TP_TRY(make_map_mn_pairs(&m_dp, dP, Fs, M, p.nseg));
-  } else {
-    TP_TRY(make_map(&m_h, Hsave, Fs, M, T, Fs * 2, M * Fs * 2, 64));
-    TP_TRY(make_map(&m_x, X, H, M, 1, H * 2, M * H * 2, 64));
-    TP_TRY(make_map(&m_dz, dZ, H, M, 1, H * 2, M * H * 2, 64));
-    TP_TRY(make_map(&m_dp, dP, Fs, M, p.nseg, Fs * 2, M * Fs * 2, 64));
-  }
+  TP_TRY(make_map_mn_pairs(&m_h, Hsave, Fs, M, T));
+  TP_TRY(make_map_mn_pairs(&m_x, X, H, M, 1));
+  TP_TRY(make_map_mn_pairs(&m_dz, dZ, H, M, 1));
+  TP_TRY(make_map_mn_pairs(&m_dp, dP, Fs, M, p.nseg));
   const int ktok = static_cast<int>(cdiv(M, 64));
   {
     GemmArgs g = base_args(d);
-    g.mn_pairs = pairs ? 1 : 0;
     g.out = dW2;
     g.ld_out = H;
     GemmCall c;
@@ -787,7 +779,6 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
   }
   {
     GemmArgs g = base_args(d);
-    g.mn_pairs = pairs ? 1 : 0;
     g.out = dW1;
     g.ld_out = ncols;
     GemmCall c;

@@ -619,32 +619,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           kc.coords(g.a_seg, ak, az);
           kc.coords(g.b_seg, bk, bz);
           if constexpr (amn) {
-            if (g.mn_pairs) {
+            // two 64-row MN blocks per copy (kMnPairBox)
 #pragma unroll
-              for (int i = 0; i < BM / 64; i += kMnPairBox)
-                tma_load_4d(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, fb, 0, kc.kflat,
-                            ablk.x[i] / 64, ablk.z[i]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_3d(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, fb, ablk.x[i], kc.kflat,
-                            ablk.z[i]);
-            }
+            for (int i = 0; i < BM / 64; i += kMnPairBox)
+              tma_load_4d(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, fb, 0, kc.kflat,
+                          ablk.x[i] / 64, ablk.z[i]);
           } else {
             tma_load_3d(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, t.m * BM, az);
           }
-          if constexpr (bmn && BN >= 64) {
-            if (g.mn_pairs) {
+          if constexpr (bmn && BN >= 128) {
 #pragma unroll
-              for (int i = 0; i < kBBlocks; i += kMnPairBox)
-                tma_load_4d(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, fb, 0, kc.kflat,
-                            bblk.x[i] / 64, bblk.z[i]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < kBBlocks; ++i)
-                tma_load_3d(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, fb, bblk.x[i], kc.kflat,
-                            bblk.z[i]);
-            }
+            for (int i = 0; i < kBBlocks; i += kMnPairBox)
+              tma_load_4d(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, fb, 0, kc.kflat,
+                          bblk.x[i] / 64, bblk.z[i]);
           } else {
             tma_load_3d(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, t.n * BN, bz);
           }
@@ -971,29 +958,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // this CTA's copies complete on CTA 0's stage barrier, which CTA 0 arms for both
             const uint32_t fb = leader ? full_bar(stage) : map_to_rank(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(fb, 2u * (A_BYTES + B_BYTES));
-            auto load = [&](uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2) {
-              if (leader)
-                tma_load_3d(dst, map, fb, c0, c1, c2);
-              else
-                tma_load_3d_pair(dst, map, fb, c0, c1, c2);
-            };
-            if (g.mn_pairs) {
-              // both 64-row blocks of this CTA's 128 rows in one copy per operand
-              if (leader) {
-                tma_load_4d(smem_u32(sA + stage * A_BYTES), &mapA, fb, 0, kc.kflat, ablk.x[0] / 64, ablk.z[0]);
-                tma_load_4d(smem_u32(sB + stage * B_BYTES), &mapB, fb, 0, kc.kflat, bblk.x[0] / 64, bblk.z[0]);
-              } else {
-                tma_load_4d_pair(smem_u32(sA + stage * A_BYTES), &mapA, fb, 0, kc.kflat, ablk.x[0] / 64,
-                                 ablk.z[0]);
-                tma_load_4d_pair(smem_u32(sB + stage * B_BYTES), &mapB, fb, 0, kc.kflat, bblk.x[0] / 64,
-                                 bblk.z[0]);
-              }
+            // both 64-row MN blocks of this CTA's 128 rows in one copy per operand (kMnPairBox)
+            if (leader) {
+              tma_load_4d(smem_u32(sA + stage * A_BYTES), &mapA, fb, 0, kc.kflat, ablk.x[0] / 64, ablk.z[0]);
+              tma_load_4d(smem_u32(sB + stage * B_BYTES), &mapB, fb, 0, kc.kflat, bblk.x[0] / 64, bblk.z[0]);
             } else {
-#pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                load(smem_u32(sA + stage * A_BYTES + i * kMnBlockBytes), &mapA, ablk.x[i], kc.kflat, ablk.z[i]);
-                load(smem_u32(sB + stage * B_BYTES + i * kMnBlockBytes), &mapB, bblk.x[i], kc.kflat, bblk.z[i]);
-              }
+              tma_load_4d_pair(smem_u32(sA + stage * A_BYTES), &mapA, fb, 0, kc.kflat, ablk.x[0] / 64, ablk.z[0]);
+              tma_load_4d_pair(smem_u32(sB + stage * B_BYTES), &mapB, fb, 0, kc.kflat, bblk.x[0] / 64, bblk.z[0]);
             }
           } else if (leader) {
             const uint32_t fb = full_bar(stage);

@@ -30,9 +30,9 @@ enum Epi : int {
   EPI_F32_RESID = 10,        // one slot: out = acc (+ aux, float32) (+ aux2, bf16), same layout as out;
                              // with out2, also out2 = bf16(out) (a residual add fused into the GEMM)
   EPI_F32_MN = 11            // as EPI_F32, with both operands MN-major (the weight gradients, whose K
-                             // is the token axis): A and B tensor maps are [segments][K][MN per
-                             // segment] with 64 x 64 boxes; a_mn_seg / b_mn_seg are the MN rows per
-                             // segment (0: one segment)
+                             // is the token axis): A and B are [segments][K][MN per segment] in
+                             // memory, read through 4-D maps (kMnPairBox); a_mn_seg / b_mn_seg are
+                             // the MN rows per segment (0: one segment)
 };
 
 // Packed rows of a SwiGLU shard alternate 128 gate rows and 128 up rows, so
@@ -47,8 +47,8 @@ constexpr int kSwigluGranule = 128;
 // kt / kt_per_seg); a flat operand (0) is [1][rows][K] and reads (kt * 64,
 // row, 0); a k-tile-blocked operand (kKtileBlocked, the packed bf16 weights)
 // is [k-tiles][rows][64] and reads (0, row, kt).  With EPI_F32_MN both operands
-// are MN-major and k-tile kt reads, for each 64 rows of the tile, (row %
-// mn_seg, kt * 64, row / mn_seg).  Slot s covers k-tiles [s*kt_per_slot,
+// are MN-major and k-tile kt reads, for each 128 rows of the tile, (0, kt * 64,
+// (row % mn_seg) / 64, row / mn_seg) of a 4-D map (kMnPairBox).  Slot s covers k-tiles [s*kt_per_slot,
 // min(kt_total, (s+1)*kt_per_slot)).
 constexpr int kKtileBlocked = 2;
 
@@ -57,8 +57,6 @@ struct GemmArgs {
   int kt_total, kt_per_seg, kt_per_slot;
   int a_seg, b_seg;
   int a_mn_seg, b_mn_seg;  // EPI_F32_MN: MN rows per segment of A / B (0: one segment)
-  int mn_pairs;            // EPI_F32_MN: the A and B maps are 4-D (see kMnPairBox): one copy
-                           // fetches two adjacent 64-row MN blocks of a segment
   int group_m;          // raster: m-tiles per group (L2 reuse of B tiles)
   int rows_valid;       // valid output rows along A (M, or features when swapped)
   int cols_valid;       // valid output columns along B (N, or tokens when swapped)
@@ -75,11 +73,11 @@ struct GemmArgs {
   int n_heads;              // EPI_QKV_HEADS_BF16: heads over all shards
 };
 
-// MN-major operands (EPI_F32_MN) as 4-D tensor maps: dims {64 MN elements, K
+// MN-major operands (EPI_F32_MN) are 4-D tensor maps: dims {64 MN elements, K
 // (tokens), MN blocks of 64 per segment, segments}, byte strides {MN per
 // segment x 2, 128, K x MN per segment x 2}, box {64, 64, kMnPairBox, 1}.
-// One copy then lands kMnPairBox 64 x 64 blocks, 8 KiB apart, exactly where
-// kMnPairBox single-block copies of the 3-D map would put them.
+// One copy lands kMnPairBox 64 x 64 blocks, 8 KiB apart; both lie in one
+// segment because segments (shard widths) and tile rows are multiples of 128.
 constexpr int kMnPairBox = 2;
 
 // Tile configurations the GEMM is instantiated for.
