@@ -34,7 +34,8 @@ def _rank_main(rank, world, port, out):
 def test_replicas_aggregate_over_gloo():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    # spawn, not fork: the test process may already run threads (the oracle's OpenMP pool)
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
