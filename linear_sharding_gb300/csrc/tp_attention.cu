@@ -3,39 +3,41 @@
 // block": heads are sharded across ranks, so each head's attention is local
 // to the shard that owns it and needs no communication).
 //
-// One CTA per SM walks units (head, pair of adjacent 128-query tiles A and B)
-// and computes, for each query row r,
+// One CTA per SM walks units (head, 128-query tile) and computes, for each
+// query row r,
 //   O[r] = sum_{j allowed} 2^(t_rj - m_r) v_j / sum_{j allowed} 2^(t_rj - m_r),
 //   t_rj = (q_r . k_j / sqrt(128)) log2(e),
 // which is the softmax-weighted sum of the values for any shift m_r.  Keys
 // are visited 128 at a time and neither scores nor probabilities leave the
 // SM, or even reach shared memory:
-//   warp 0      TMA producer: both Q tiles once per unit; K and V tiles of
-//               128 keys (shared by the two query tiles) through a 3-deep and
-//               a 2-deep ring, keys one tile ahead of values.  Q, K and V are
-//               all head-major [heads][M][128]; V is the P V product's B
-//               operand read MN-major (its K, the key axis, is the outer one);
-//   warp 1      TMEM allocation; one thread issues, per key tile j,
-//               O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
-//               S_B = Q_B K_{j+1}^T (tcgen05, 128 x 128, K = 128; P read from
-//               TMEM, the rest from shared memory), so the tensor core works
-//               on one tile while the other tile's probabilities are made;
-//   warps 2..5  softmax of tile A, warps 6..9 of tile B: one thread per query
-//               row (TMEM lane = row) reads the row of S into registers, takes
-//               its maximum, writes P = 2^(t - m_r) as bf16 over the upper 64
-//               columns of the same TMEM buffer, and adds the float32 weights
-//               to the row sum.
-// Each query tile has one S/P buffer: the next S into it is issued after the
-// P V that reads it, and tcgen05 MMAs of one thread run in issue order.  The
-// shift m_r is raised only when a tile's maximum exceeds it by more than 8 (so
+//   warp 0      TMA producer: the Q tile once per unit; K and V tiles of 128
+//               keys through 3-deep rings, keys up to three tiles ahead of
+//               values.  Q, K and V are all head-major [heads][M][128]; V is
+//               the P V product's B operand read MN-major (its K, the key
+//               axis, is the outer one);
+//   warp 1      TMEM allocation; one thread issues S_j = Q K_j^T (tcgen05,
+//               128 x 128, K = 128) into one of three S/P buffers, up to three
+//               key tiles ahead: S_{j+3} goes into buffer j % 3 once P_j V_j
+//               has read it;
+//   warp 6      one thread issues O += P_j V_j (P read from TMEM, V from
+//               shared memory).  Two issuing threads: each one's waits and
+//               commits overlap the other's MMAs, so the tensor core is fed
+//               while either waits;
+//   warps 2..5  softmax: one thread per query row (TMEM lane = row) reads the
+//               row of S_j, takes its maximum, writes P = 2^(t - m_r) as bf16
+//               over the upper 64 columns of the same buffer, and adds the
+//               float32 weights to the row sum.
+// With S computed ahead, the softmax of key tile j + 1 starts as soon as that
+// of tile j ends: neither waits for the other's hand-off, and the tensor core
+// has a whole S and P V (1024 cycles) per 128-key step beside it.  The shift
+// m_r is raised only when a tile's maximum exceeds it by more than 8 (so
 // P <= 2^8): then the row's sum and its accumulator are scaled by
-// 2^(m_old - m_new).  The previous P V is complete at that point, because the
-// commit that signalled this S covers every MMA issued before it.
-// Units run heaviest first (causal: the last query tiles) and are dealt to
-// the CTAs in snake order, so CTA loads stay even.  Waits poll (the S ->
-// softmax -> P V hand-off is on the critical path, and a suspended wait wakes
-// too late) and are bounded like the GEMM's; on a timeout the CTA drains what
-// it issued and reports through the status word.
+// 2^(m_old - m_new), after the P V product issued before is complete (the
+// barrier that frees its buffer says so).  Units run heaviest first (causal: the
+// last query tiles) and are dealt to the CTAs in snake order.  Waits poll (the
+// hand-offs are on the critical path, and a suspended wait wakes too late) and
+// are bounded like the GEMM's; on a timeout the CTA drains what it issued and
+// reports through the status word.
 #include <cuda_bf16.h>
 
 #include "tp_device.cuh"
@@ -45,46 +47,40 @@ namespace tp {
 namespace {
 
 constexpr int kTile = 128;                // queries per tile, keys per step
-constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 128;      // per query tile
+constexpr int kThreads = 224;             // producer, S issuer, 4 softmax warps, P V issuer
+constexpr int kSoftmaxThreads = 128;
+constexpr int kSbuf = 3;                  // S/P buffers in tensor memory: S runs up to 3 steps ahead
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
 constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
-constexpr int kKst = 3, kVst = 2;         // K and V tiles in shared memory
-constexpr int kBars = 28;
+constexpr int kKst = 3, kVst = 3;         // K and V tiles in shared memory
+constexpr int kBars = 32;
 constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
-// Q[2] | K[kKst] | V[kVst] | barriers
-constexpr size_t kSmemBytes = 1024 + (2 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
+// Q | K[kKst] | V[kVst] | barriers
+constexpr size_t kSmemBytes = 1024 + (1 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "attention tiles exceed the shared memory of one CTA");
 
-// TMEM columns: S/P of tile A 0..127, of tile B 128..255, O_A 256..383, O_B 384..511
-constexpr uint32_t kOcol = 256;
+// TMEM columns: S/P buffer b at 128 b (b < 3), O at 384
+constexpr uint32_t kOcol = kSbuf * 128;
+static_assert(kOcol + 128 <= 512, "S/P buffers and O exceed tensor memory");
 
 struct AttnUnit {
   int head;
-  int mt[2];   // query tiles A and B (B = -1 when the last pair has one tile)
-  int nkt[2];  // key tiles each one visits (0 for an absent tile)
-  int nk;      // key tiles the unit visits: max(nkt)
+  int mt;  // query tile
+  int nk;  // key tiles it visits
 };
 
 // k-th unit of CTA b among G CTAs: snake order over the heaviest-first list.
 __device__ __forceinline__ int unit_of(int k, int b, int G) { return k * G + ((k & 1) ? G - 1 - b : b); }
 
 __device__ __forceinline__ AttnUnit decode(int u, const AttnArgs &a) {
-  const int pairs = (a.m_tiles + 1) / 2;
   AttnUnit t;
-  const int p = pairs - 1 - u / a.heads;
+  t.mt = a.m_tiles - 1 - u / a.heads;
   t.head = u % a.heads;
-  t.mt[0] = 2 * p;
-  t.mt[1] = 2 * p + 1 < a.m_tiles ? 2 * p + 1 : -1;
-  for (int w = 0; w < 2; ++w)
-    t.nkt[w] = t.mt[w] < 0 ? 0 : (a.causal ? t.mt[w] + 1 : a.m_tiles);
-  t.nk = t.nkt[0] > t.nkt[1] ? t.nkt[0] : t.nkt[1];
-  if (!TP_CHECK(t.head < a.heads && t.mt[0] >= 0 && t.mt[1] < a.m_tiles && t.nk >= 1 && t.nk <= a.m_tiles,
-                a.status)) {
-    t.mt[1] = -1;  // keep the unit's shape sane: tile A alone over one key tile
-    t.nkt[0] = t.nk = 1;
-    t.nkt[1] = 0;
+  t.nk = a.causal ? t.mt + 1 : a.m_tiles;
+  if (!TP_CHECK(t.head < a.heads && t.mt >= 0 && t.nk >= 1 && t.nk <= a.m_tiles, a.status)) {
+    t.mt = 0;  // keep the unit's shape sane: one key tile
+    t.nk = 1;
   }
   return t;
 }
@@ -119,8 +115,6 @@ struct Ring {
   }
 };
 
-// 320 threads: the 10 warps leave 3 on two of the 4 SM sub-partitions, whose 16K registers
-// each then cap a thread at 168
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                     const __grid_constant__ CUtensorMap mapV, const AttnArgs a) {
@@ -129,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem;                  // 2 tiles
-  uint8_t *sK = sQ + 2 * kTileBytes;
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + kTileBytes;
   uint8_t *sV = sK + kKst * kTileBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sV + kVst * kTileBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
@@ -141,12 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto k_full = [&](int s) { return b0 + 16 + 8u * s; };    // kKst
   auto k_empty = [&](int s) { return b0 + 40 + 8u * s; };   // kKst
   auto v_full = [&](int s) { return b0 + 64 + 8u * s; };    // kVst
-  auto v_empty = [&](int s) { return b0 + 80 + 8u * s; };   // kVst
-  auto s_full = [&](int w) { return b0 + 96 + 8u * w; };    // S of tile w computed
-  auto p_full = [&](int w) { return b0 + 112 + 8u * w; };   // P of tile w written over its S
-  auto o_full = [&](int w) { return b0 + 128 + 8u * w; };   // tile w's last P V of the unit done
-  auto o_free = [&](int w) { return b0 + 144 + 8u * w; };   // tile w's O read out
-  const uint32_t drain = b0 + 160, never = b0 + 168;
+  auto v_empty = [&](int s) { return b0 + 88 + 8u * s; };   // kVst
+  auto s_full = [&](int b) { return b0 + 112 + 8u * b; };   // kSbuf: S in buffer b computed
+  auto p_full = [&](int b) { return b0 + 136 + 8u * b; };   // kSbuf: P written over it
+  auto s_free = [&](int b) { return b0 + 160 + 8u * b; };   // kSbuf: P V of buffer b done (P read)
+  const uint32_t o_full = b0 + 184, o_free = b0 + 192;      // the unit's last P V done; O read out
+  const uint32_t drain = b0 + 200, drain_pv = b0 + 208, never = b0 + 216;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -160,13 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(s_full(w), 1);
-      mbar_init(p_full(w), kSoftmaxThreads);
-      mbar_init(o_full(w), 1);
-      mbar_init(o_free(w), kSoftmaxThreads);
+    for (int b = 0; b < kSbuf; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), kSoftmaxThreads);
+      mbar_init(s_free(b), 1);
     }
+    mbar_init(o_full, 1);
+    mbar_init(o_free, kSoftmaxThreads);
     mbar_init(drain, 1);
+    mbar_init(drain_pv, 1);
     mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -188,14 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   pdl_wait();
   const WaitCtl w{abort_flag, a.status, a.wait_limit_ns};
-  const int units = a.heads * ((a.m_tiles + 1) / 2);
+  const int units = a.heads * a.m_tiles;
   const int G = gridDim.x, b = blockIdx.x;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer ----
-      // Loads per unit, in order: Q_A and Q_B, K_0, then for each j: K_{j+1} (if any), V_j.
-      int kc = 0, vc = 0, qc = 0;  // K, V tiles and Q pairs issued so far
+      // Loads per unit: Q, K_0 .. K_2, then for each j: V_j, K_{j+3} (if any).
+      int kc = 0, vc = 0, qc = 0;  // K, V and Q tiles issued so far
       Ring kr, vr;
       bool ok = true;
       auto load_k = [&](const AttnUnit &t, int j) -> bool {
@@ -225,24 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
         if (!wait_bar_spin(q_empty, (qc & 1u) ^ 1u, w)) break;
-        mbar_arrive_expect_tx(q_full, (t.mt[1] >= 0 ? 2 : 1) * kTileBytes);
-        for (int q = 0; q < 2; ++q) {
-          if (t.mt[q] < 0) continue;
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_3d(smem_u32(sQ + q * kTileBytes + kb * kSub), &mapQ, q_full, kb * 64, t.mt[q] * kTile,
-                        t.head);
-        }
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
         ++qc;
-        if (!load_k(t, 0)) break;
-        for (int j = 0; j < t.nk; ++j) {
-          if (j + 1 < t.nk && !load_k(t, j + 1)) {
-            ok = false;
-            break;
-          }
-          if (!load_v(t, j)) {
-            ok = false;
-            break;
-          }
+        const int pre = t.nk < kSbuf ? t.nk : kSbuf;
+        for (int j = 0; j < pre && ok; ++j) ok = load_k(t, j);
+        for (int j = 0; j < t.nk && ok; ++j) {
+          ok = load_v(t, j);
+          if (ok && j + kSbuf < t.nk) ok = load_k(t, j + kSbuf);
         }
       }
       // Every copy issued completes on its full barrier, consumed or not (after an abort
@@ -260,109 +247,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer ----
-      int uc = 0;                            // units started
-      Ring kr, vr;                           // K tile of the next S, V tile of the next P V
-      uint32_t sph[2] = {0u, 0u};            // phase of tile q's next p_full wait
-      uint32_t ofp[2] = {0u, 0u};            // units tile q took part in (o_free phases)
+      // ---- S issuer: S_j = Q K_j^T into buffer j % 3, once P V has read that buffer's P_{j-3} ----
+      int uc = 0;                          // units started
+      Ring kr;                             // K tile of the next S
+      // bit b: parity of buffer b's next s_free wait (a fresh barrier's previous phase counts as
+      // complete).  Per-buffer phases live in bits of a register, not in an indexed array.
+      uint32_t fph = (1u << kSbuf) - 1u;
       bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_spin(never, 0u, w);
-      auto issue_s = [&](int q, const uint32_t kbase) {
-        // S_q = Q_q K^T over head_dim 128: two 64-wide sub-tiles x four K = 16 steps
-        const uint32_t d = tmem + q * 128;
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + q * kTileBytes + kb * kSub));
-          const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tc_mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb | k) ? 1u : 0u);
-        }
-        tc_commit(s_full(q));
-      };
-      // S of both tiles for key tile j (tiles that visit it), then release K_j
-      auto issue_s_pair = [&](const AttnUnit &t, int j) -> bool {
-        if (!wait_bar_spin(k_full(kr.buf), kr.phase, w)) return false;
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
-        for (int q = 0; q < 2; ++q)
-          if (j < t.nkt[q]) issue_s(q, kbase);
-        tc_commit(k_empty(kr.buf));
-        kr.next(kKst);
-        return true;
-      };
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k, b, G);
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
         if (!wait_bar_spin(q_full, uc & 1u, w)) break;
-        tc_fence_after();
-        if (!issue_s_pair(t, 0)) break;
-        if (t.nk == 1) tc_commit(q_empty);
-        for (int j = 0; j < t.nk && ok; ++j) {
-          if (!wait_bar_spin(v_full(vr.buf), vr.phase, w)) {
+        for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+          if (!wait_bar_spin(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_spin(k_full(kr.buf), kr.phase, w)) {
             ok = false;
             break;
           }
-          const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
-          bool k_next_ready = false;
-          for (int q = 0; q < 2 && ok; ++q) {
-            if (j >= t.nkt[q]) continue;
-            // O_q += P_q V_j once the softmax threads have written P_q (and, for the unit's
-            // first key tile, read out the previous unit's O_q)
-            if (!wait_bar_spin(p_full(q), sph[q], w) || (j == 0 && !wait_bar_spin(o_free(q), ofp[q] ^ 1u, w))) {
-              ok = false;
-              break;
-            }
-            sph[q] ^= 1u;
-            tc_fence_after();
-            const uint32_t pa = tmem + q * 128 + 64;  // P: the upper 64 columns, bf16 pairs
+          fph ^= 1u << sb;
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
+          const uint32_t d = tmem + sb * 128;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
-              const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
-              tc_mma_bf16_tmem_a(tmem + kOcol + q * 128, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV,
-                                 (j | kk) ? 1u : 0u);
-            }
-            if (j + 1 == t.nkt[q]) tc_commit(o_full(q));
-            // then this tile's S for key tile j + 1, so the other tile's P V overlaps its softmax
-            if (j + 1 < t.nkt[q]) {
-              if (!k_next_ready) {
-                if (!wait_bar_spin(k_full(kr.buf), kr.phase, w)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                k_next_ready = true;
-              }
-              issue_s(q, smem_u32(sK + kr.buf * kTileBytes));
-            }
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + kb * kSub));
+            const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) tc_mma_bf16(d, ad + 2u * kq, bd + 2u * kq, IDESC, (kb | kq) ? 1u : 0u);
           }
-          if (!ok) break;
-          tc_commit(v_empty(vr.buf));
-          vr.next(kVst);
-          if (k_next_ready) {
-            tc_commit(k_empty(kr.buf));
-            kr.next(kKst);
-          }
-          if (j + 2 == t.nk) tc_commit(q_empty);  // every S of this unit is issued
+          tc_commit(s_full(sb));
+          tc_commit(k_empty(kr.buf));
+          kr.next(kKst);
         }
+        if (!ok) break;
+        tc_commit(q_empty);  // every S of this unit is issued
         ++uc;
-        for (int q = 0; q < 2; ++q)
-          if (t.nkt[q] > 0) ofp[q] ^= 1u;
       }
       tc_commit(drain);
       drain_bar(drain, 0u, a.status);
     }
     __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // ---- P V issuer: O += P_j V_j once the softmax threads have written P_j ----
+      int uc = 0;
+      Ring vr;
+      uint32_t pph = 0;                    // bit b: phase of buffer b's next p_full wait
+      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_spin(never, 0u, w);
+      for (int k = 0; ok; ++k) {
+        const int u = unit_of(k, b, G);
+        if (u >= units) break;
+        const AttnUnit t = decode(u, a);
+        for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+          // (for the unit's first key tile, also once the previous unit's O is read out)
+          if (!wait_bar_spin(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_spin(o_free, (uc & 1u) ^ 1u, w)) ||
+              !wait_bar_spin(v_full(vr.buf), vr.phase, w)) {
+            ok = false;
+            break;
+          }
+          pph ^= 1u << sb;
+          tc_fence_after();
+          const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
+          const uint32_t pa = tmem + sb * 128 + 64;  // P: the upper 64 columns, bf16 pairs
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
+            const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
+            tc_mma_bf16_tmem_a(tmem + kOcol, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV, (j | kk) ? 1u : 0u);
+          }
+          tc_commit(s_free(sb));
+          tc_commit(v_empty(vr.buf));
+          vr.next(kVst);
+          if (j + 1 == t.nk) tc_commit(o_full);
+        }
+        if (!ok) break;
+        ++uc;
+      }
+      tc_commit(drain_pv);
+      drain_bar(drain_pv, 0u, a.status);
+    }
+    __syncwarp();
   } else {
-    // ---- softmax and output: warps 2..5 tile A, 6..9 tile B (warp v reads TMEM lanes
-    // 32 (v % 4) .. + 31) ----
-    const int q = (warp - 2) >> 2;
+    // ---- softmax and output: warps 2..5 (warp v reads TMEM lanes 32 (v % 4) .. + 31) ----
     const int row_in_tile = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t sb = tmem + lane_base + q * 128;
-    const uint32_t ob = tmem + lane_base + kOcol + q * 128;
+    const uint32_t ob = tmem + lane_base + kOcol;
     const float c = a.scale_log2;
-    uint32_t sph = 0, uc = 0;  // phase of the next s_full wait; units this tile took part in
+    uint32_t sph = 0;                    // bit b: phase of buffer b's next s_full wait
+    uint32_t uc = 0;                     // units done
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       const bool got = wait_bar_spin(bar, parity, w);
@@ -372,15 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_of(k, b, G);
       if (u >= units) break;
       const AttnUnit t = decode(u, a);
-      if (t.nkt[q] == 0) continue;  // the last pair's missing tile B
-      const int row = t.mt[q] * kTile + row_in_tile;
+      const int row = t.mt * kTile + row_in_tile;
       float m_used = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < t.nkt[q]; ++j) {
-        if (!wait_all(s_full(q), sph)) {
+      for (int j = 0, sbuf = 0, prev = kSbuf - 1; j < t.nk; ++j, prev = sbuf, sbuf = sbuf + 1 == kSbuf ? 0 : sbuf + 1) {
+        const uint32_t sb = tmem + lane_base + sbuf * 128;
+        if (!wait_all(s_full(sbuf), (sph >> sbuf) & 1u)) {
           ok = false;
           break;
         }
-        sph ^= 1u;
+        sph ^= 1u << sbuf;
         tc_fence_after();
         // allowed keys of this tile: key0 + i for i <= kmax (causal: key <= row; always key < M)
         const int key0 = j * kTile;
@@ -403,21 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
         }
-        // row maximum: four independent chains of three-input maxima
-        float mx4[4];
+        // row maximum: sixteen chains of four three-input maxima over 8 scores each, then a tree
+        // (seven dependent steps in all, where one chain per 32 scores took sixteen)
+        float m16[16];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float m = fmaxf(__uint_as_float(s[cc][0]), __uint_as_float(s[cc][1]));
-#pragma unroll
-          for (int i = 2; i < 32; i += 2) m = fmax3(m, __uint_as_float(s[cc][i]), __uint_as_float(s[cc][i + 1]));
-          mx4[cc] = m;
+        for (int q = 0; q < 16; ++q) {
+          const uint32_t *v = s[q >> 2] + (q & 3) * 8;
+          float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          m = fmax3(m, __uint_as_float(v[3]), __uint_as_float(v[4]));
+          m = fmax3(m, __uint_as_float(v[5]), __uint_as_float(v[6]));
+          m16[q] = fmaxf(m, __uint_as_float(v[7]));
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float m6[6];
+#pragma unroll
+        for (int q = 0; q < 5; ++q) m6[q] = fmax3(m16[3 * q], m16[3 * q + 1], m16[3 * q + 2]);
+        m6[5] = m16[15];
+        const float mx = fmaxf(fmax3(m6[0], m6[1], m6[2]), fmax3(m6[3], m6[4], m6[5]));
         const float m_tile = mx * c;
         const bool raise = m_tile > m_used + kRescaleGap;
         const float m_new = raise ? m_tile : m_used;
         const float alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
-        m_used = m_new;
         // P = 2^(t - m) as bf16 pairs over the upper 64 columns of the S buffer: keys 64 hh ..
         // 64 hh + 63 into columns 64 + 32 hh (the scores are all in registers by now).  The
         // row sum adds the float32 weights before their rounding to bf16 for the P V product;
@@ -433,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const uint32_t *v = s[2 * hh + (i >> 4)];
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])),
-                                        c2, nm2);
-            const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            const float2 t2 = __ffma2_rn(
+                make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])), c2, nm2);
+            const float2 e = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
             pk[i] = pack_bf16x2(e.x, e.y);
             sum4[i & 3] = __fadd2_rn(sum4[i & 3], e);
           }
@@ -444,9 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sum = ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
                           ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
         l_run = fmaf(l_run, alpha, sum);
-        // a raised shift also scales the accumulated O; the previous P V is already in it
-        // (the commit that signalled this S covered it)
+        // A raised shift also scales the accumulated O, once every P V issued before this step
+        // is complete.  The last of them, P_{j-1} V_{j-1}, completes the phase of
+        // s_free(buffer of j - 1) whose parity is that of the s_full phase step j - 1 waited on.
+        // That barrier's previous phase is complete already (S_{j-1} was issued after it), and
+        // its next one needs P_{j+2}, which this step precedes: the parity names one phase.
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          if (!wait_all(s_free(prev), ((sph >> prev) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t r[32];
@@ -458,13 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(ob + cc * 32, r);
           }
         }
+        m_used = m_new;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(q));
+        mbar_arrive(p_full(sbuf));
       }
       if (!ok) break;
-      // read out O / l once this tile's last P V of the unit is done
-      if (!wait_all(o_full(q), uc & 1u)) break;
+      // read out O / l once the unit's last P V is done
+      if (!wait_all(o_full, uc & 1u)) break;
       ++uc;
       tc_fence_after();
       const float inv = 1.0f / l_run;
@@ -496,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free(q));
+      mbar_arrive(o_free);
     }
   }
 
@@ -517,7 +503,7 @@ cudaError_t launch_attention(const CUtensorMap &mapQ, const CUtensorMap &mapK, c
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(args.heads) * ((args.m_tiles + 1) / 2);
+  const long long units = static_cast<long long>(args.heads) * args.m_tiles;
   if (units <= 0) return cudaSuccess;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   // launched as a programmatic dependent of the previous kernel (the QKV projection)
