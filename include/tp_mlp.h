@@ -227,13 +227,17 @@ TP_API tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp
  * device and take unbounded time), or a host runtime that hands out all
  * device memory itself and has none to lend as workspace.
  *   Its scratch is a fixed 16 MiB device array inside the library, which
- *   every GPU that loads the library holds until the process exits.  Calls
- *   whose workspace (tp_mlp_workspace_bytes(s, M, TP_VAR_AUTO)) exceeds
- *   16 MiB are rejected with TP_ERR_WORKSPACE.  That size depends on the
- *   GPU's SM count, because the AUTO plan splits K to fill the SMs: on a
- *   152-SM GB300 the memory-bound decode shapes (M <= 16 tokens) of an
- *   H = 8192, F = 28672, T = 8 MLP need at most about 12.4 MiB and fit; on
- *   other parts query tp_mlp_workspace_bytes() first.
+ *   every GPU that loads the library holds until the process exits.  The
+ *   call runs the AUTO plan when its workspace (tp_mlp_workspace_bytes(s,
+ *   M, TP_VAR_AUTO)) fits in 16 MiB; that size depends on the GPU's SM
+ *   count, because the AUTO plan splits K to fill the SMs.  Where it does
+ *   not fit, the call refits the plan to the scratch: no float32 partials of
+ *   the second layer (all shards summed in one TMEM accumulator, as
+ *   TP_VAR_TMEM_ACC) and, for decode, as many first-layer split-K slots as
+ *   fit.  Only a call whose Y ([T x M x F/T]) and one set of first-layer
+ *   partials alone exceed 16 MiB is rejected, with TP_ERR_WORKSPACE.  The
+ *   memory-bound decode shapes (M <= 16 tokens) of an H = 8192, F = 28672,
+ *   T = 8 MLP fit on any SM count.
  *   The first call on a device looks up the scratch's device address
  *   (cudaGetSymbolAddress) and keeps it for the life of the process; make
  *   that first call before any stream capture.  cudaDeviceReset() is not

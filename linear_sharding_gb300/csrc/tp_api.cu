@@ -238,12 +238,12 @@ GemmArgs base_args(const DevState *d) {
 // float32 partial traffic (written once, read by the shard-sum) expressed in
 // k-tile units.
 int choose_slots(int64_t tiles, int T, int kt_per_seg, int sms, double ktile_per_partial_byte,
-                 int64_t partial_bytes, bool sub_ok) {
+                 int64_t partial_bytes, bool sub_ok, int max_slots = 1 << 30) {
   int best = 1;
   double best_cost = 1e300;
   auto consider = [&](int S) {
     const int64_t kt_total = static_cast<int64_t>(T) * kt_per_seg;
-    if (kt_total % S) return;
+    if (kt_total % S || S > max_slots) return;
     const int64_t units = tiles * S;
     const int64_t waves = cdiv(units, sms);
     double cost = static_cast<double>(waves) * static_cast<double>(kt_total / S);
@@ -271,7 +271,11 @@ struct MlpPlan {
   size_t total() const { return round256(y_bytes) + round256(col_bytes) + round256(row_bytes); }
 };
 
-tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, const DevState *d, MlpPlan *p) {
+// budget > 0 (AUTO only): when the AUTO plan's workspace exceeds `budget` bytes, refit it: no
+// second-layer partials (all shards in one TMEM accumulator) and, for decode, as many first-layer
+// split-K slots as fit.  A plan that fits is left as it is.
+tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, const DevState *d, MlpPlan *p,
+                     size_t budget = 0) {
   *p = MlpPlan();
   const int sms = d->sms;
   const double per_byte_tc = ktile_per_partial_byte(d, s->bn2);
@@ -310,6 +314,19 @@ tp_status_t plan_mlp(const tp_shards *s, int64_t M, tp_variant_t v, const DevSta
     }
   }
   p->row_bytes = p->slots2 > 1 ? static_cast<size_t>(p->slots2 * M * H) * 4 : 0;
+  if (budget > 0 && v == TP_VAR_AUTO && p->total() > budget) {
+    p->slots2 = 1;
+    p->row_bytes = 0;
+    if (p->decode) {
+      const size_t per_slot = static_cast<size_t>(M * T * R1) * 4;
+      const size_t fixed = round256(p->y_bytes) + 255;
+      const int64_t fit = budget > fixed ? static_cast<int64_t>((budget - fixed) / per_slot) : 0;
+      const int cap = static_cast<int>(fit < 1 ? 1 : (fit > p->slots1 ? p->slots1 : fit));
+      p->slots1 = choose_slots((T * R1) / 128, 1, static_cast<int>(H / 64), sms, 1.0 / (128.0 * 64.0 * 2.0),
+                               static_cast<int64_t>(M * T * R1 * 4), true, cap);
+      p->col_bytes = static_cast<size_t>(p->slots1) * per_slot;
+    }
+  }
   return TP_OK;
 }
 
@@ -802,7 +819,7 @@ bool act_ok(const tp_shards *s, tp_act_t act) {
 
 tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t act, tp_variant_t v,
                              float *Z, void *workspace, size_t ws_bytes, cudaStream_t st,
-                             const Residual &res = Residual()) {
+                             const Residual &res = Residual(), size_t budget = 0) {
   DevState *d = nullptr;
   TP_TRY(check_handle(s, 0, &d));
   if (M < 0 || !valid_variant(v) || !act_ok(s, act)) return TP_ERR_ARG;
@@ -810,7 +827,7 @@ tp_status_t mlp_forward_impl(tp_shards *s, const void *X, int64_t M, tp_act_t ac
   if (!X || !Z || !aligned16(X) || !aligned16(Z)) return TP_ERR_ARG;
   if (M > (1LL << 30)) return TP_ERR_UNSUPPORTED;
   MlpPlan p;
-  TP_TRY(plan_mlp(s, M, v, d, &p));
+  TP_TRY(plan_mlp(s, M, v, d, &p, budget));
   Workspace w;
   TP_TRY(get_ws(&w, workspace, ws_bytes, p.total(), st));
   char *Y = w.ptr;
@@ -948,6 +965,20 @@ bool tp::encode_store_map(CUtensorMap *m, const void *base, int elem_bytes, uint
            const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t tp::mlp_workspace_within(tp_shards *s, int64_t M, size_t budget) {
+  DevState *d = nullptr;
+  if (!s || s->kind != 0 || M <= 0 || budget == 0 || dev_state(&d) != TP_OK) return 0;
+  MlpPlan p;
+  if (plan_mlp(s, M, TP_VAR_AUTO, d, &p, budget) != TP_OK) return 0;
+  return p.total();
+}
+
+tp_status_t tp::mlp_forward_within(tp_shards *s, const void *X, int64_t M, tp_act_t act, float *Z, void *ws,
+                                   size_t budget, cudaStream_t st) {
+  if (budget == 0) return TP_ERR_ARG;
+  return mlp_forward_impl(s, X, M, act, TP_VAR_AUTO, Z, ws, budget, st, Residual(), budget);
 }
 
 bool tp::handle_ready_on_current_device(const tp_shards *s) {

@@ -201,4 +201,13 @@ cudaError_t launch_decode_act(const float *P, int slots, long long slot_stride, 
 // state already exists (checked without creating it, so without allocating).
 bool handle_ready_on_current_device(const tp_shards *s);
 
+// The AUTO MLP plan fitted to a workspace of `budget` bytes: as tp_mlp_workspace_bytes(s, M,
+// AUTO) when that fits; else the plan with no second-layer partials and, for decode, as many
+// first-layer split-K slots as fit.  mlp_workspace_within returns its workspace bytes (0 on a
+// bad argument; more than `budget` when even the smallest plan does not fit);
+// mlp_forward_within runs it with `ws` (at least `budget` bytes) as the workspace.
+size_t mlp_workspace_within(tp_shards *s, int64_t M, size_t budget);
+tp_status_t mlp_forward_within(tp_shards *s, const void *X, int64_t M, tp_act_t act, float *Z, void *ws,
+                               size_t budget, cudaStream_t st);
+
 }  // namespace tp

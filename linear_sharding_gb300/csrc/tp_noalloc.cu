@@ -46,11 +46,13 @@ extern "C" TP_API tp_status_t tp_mlp_forward_noalloc(tp_shards_t s, const void *
   // A handle made on this device means the library's per-device state exists,
   // so neither the size query nor the forward pass below allocates.
   if (!tp::handle_ready_on_current_device(s)) return TP_ERR_ARG;
-  const size_t need = tp_mlp_workspace_bytes(s, M, TP_VAR_AUTO);
+  // The AUTO plan, or, where its workspace exceeds the scratch (it grows with the SM count's
+  // split-K choice), the same pass refitted to the scratch.
+  const size_t need = tp::mlp_workspace_within(s, M, kNoAllocScratchBytes);
   if (need == 0) return TP_ERR_ARG;
   if (need > kNoAllocScratchBytes) return TP_ERR_WORKSPACE;
   void *scratch = nullptr;
   const tp_status_t st = scratch_address(dev, &scratch);
   if (st != TP_OK) return st;
-  return tp_mlp_forward(s, X, M, act, TP_VAR_AUTO, Z, scratch, kNoAllocScratchBytes, stream);
+  return tp::mlp_forward_within(s, X, M, act, Z, scratch, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
 }

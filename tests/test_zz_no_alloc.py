@@ -1,10 +1,11 @@
 """tp_mlp_forward_noalloc: the forward pass for callers that cannot allocate
 device memory during a call (a decode loop under CUDA graph capture or a
 real-time scheduler, a runtime that owns all device memory).  Its scratch is
-a fixed array inside the library.  It runs the same plan and kernels as
-tp_mlp_forward with variant AUTO, so its output must equal that call's bit
-for bit, call after call, and match the fp64 oracle within the bf16
-tolerance.  Between the two compared calls another shape and other inputs
+a fixed array inside the library.  Where the AUTO plan's workspace fits it,
+it runs the same plan and kernels as tp_mlp_forward with variant AUTO, so
+its output must equal that call's bit for bit, call after call, and match
+the fp64 oracle within the bf16 tolerance; where it does not, it runs the
+plan refitted to the scratch.  Between the two compared calls another shape and other inputs
 run through the same scratch, so bytes a call reads without writing them
 first would show up as a difference.  This file is collected last so that a
 run stopping at the first failure has run every other test before it."""
@@ -94,6 +95,42 @@ def test_noalloc_decode_shape_fits_and_matches():
     ref = tp.tp_mlp_forward(s, X, variant="auto")
     torch.cuda.synchronize()
     ref = ref.cpu().numpy()
+    for _ in range(2):
+        assert np.array_equal(_run(lib, tp, s, X, "swiglu", H), ref)
+    s.close()
+
+
+def test_noalloc_refits_a_plan_beyond_its_scratch():
+    """Where the AUTO plan's workspace exceeds the scratch, the call runs the
+    same pass refitted to it: no float32 partials of the second layer (all
+    shards summed in one TMEM accumulator) and as many first-layer split-K
+    slots as fit.  H = 16384, F = 57344, T = 8, SwiGLU at M = 16 needs about
+    41 MiB under AUTO on a 152-SM GB300 (its second layer splits into 32
+    partial slots); the refitted plan is then the TMEM-accumulator plan, so
+    the call equals tp_mlp_forward(variant "tmem_acc") bit for bit."""
+    import torch
+    import linear_sharding_gb300 as tp
+    lib = tp.load_library()
+    H, F, T, M = 16384, 57344, 8, 16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    W1 = (torch.randn((H, 2 * F), generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    W2 = (torch.randn((F, H), generator=g, device="cuda") * F ** -0.5).to(torch.bfloat16)
+    s = tp.tp_shard_weights(W1, W2, T, "swiglu")
+    del W1, W2
+    torch.cuda.empty_cache()
+    need_auto = tp.tp_mlp_workspace_bytes(s, M)
+    need_tmem = tp.tp_mlp_workspace_bytes(s, M, "tmem_acc")
+    print(f"refit M={M}: AUTO workspace {need_auto} bytes, TMEM accumulator {need_tmem} bytes")
+    if need_auto <= SCRATCH_BYTES:
+        s.close()
+        pytest.skip("the AUTO plan fits the scratch on this GPU: nothing to refit")
+    assert 0 < need_tmem <= SCRATCH_BYTES
+    X = (torch.randn((M, H), generator=g, device="cuda")).to(torch.bfloat16)
+    ref = tp.tp_mlp_forward(s, X, variant="tmem_acc")
+    torch.cuda.synchronize()
+    ref = ref.cpu().numpy()
+    assert np.isfinite(ref).all()
     for _ in range(2):
         assert np.array_equal(_run(lib, tp, s, X, "swiglu", H), ref)
     s.close()
