@@ -53,6 +53,7 @@ constexpr int kSbuf = 3;                  // S/P buffers in tensor memory: S run
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
 constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
 constexpr int kKst = 3, kVst = 3;         // K and V tiles in shared memory
+static_assert(kSbuf <= kKst, "the producer copies K up to kSbuf tiles ahead, into a ring of kKst");
 constexpr int kBars = 32;
 constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
