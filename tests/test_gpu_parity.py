@@ -108,6 +108,9 @@ def _run_mlp(tp, d, T, act, variant, M=None):
     ("swiglu", 200, 512, 2048, 8),    # Fs = 256: one gate/up tile per shard
     ("identity", 129, 256, 1024, 2),  # one row into the second M tile
     ("gelu", 517, 384, 1152, 3),      # T = 3, 128-wide tiles in both GEMMs (Fs = H = 384)
+    ("swiglu", 260, 512, 1024, 1),    # T = 1: one shard, the all-reduce sums a single term
+    ("gelu", 12, 256, 1024, 1),       # T = 1 on the decode path
+    ("gelu", 200, 256, 2048, 16),     # T = 16 shards of 128 columns
 ])
 def test_mlp_bf16_small(tp, variant, act, M, H, F, T):
     d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=M)
