@@ -56,6 +56,7 @@ def _run(tp, d, dZ, T, act, variant):
     ("identity", 64, 256, 1024, 2),   # single-CTA tiles
     ("gelu", 300, 384, 1152, 3),      # 128-wide tiles everywhere, T = 3
     ("gelu", 96, 256, 768, 2),        # 256-wide weight-gradient tiles that span two shards of 384
+    ("swiglu", 160, 256, 1024, 1),    # T = 1: the backward all-reduce sums a single term
 ])
 def test_training_forward_and_backward_small(tp, variant, act, M, H, F, T):
     d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=M + T)

@@ -57,6 +57,7 @@ def _check(tp, d, M, H, F, nh, hd, T, act, causal, variant, rows):
     ("gelu", 300, 4, 2, "auto"),      # ragged M: 300 keys, scores padded to 512
     ("swiglu", 256, 4, 4, "partials"),
     ("gelu", 100, 2, 2, "tmem_acc"),  # single-CTA tiles everywhere
+    ("swiglu", 200, 2, 1, "auto"),    # T = 1: one shard, both all-reduces sum a single term
 ])
 def test_block_small(tp, causal, act, M, nh, T, variant):
     hd = 128
