@@ -69,6 +69,7 @@ def _load():
         lib.orc_colpar_full.argtypes = [vp, vp, i32, i64, i64, i64, i32, vp, i64, dp]
         lib.orc_colpar_shard.argtypes = [vp, vp, i32, i64, i64, i64, i32, i32, i32, vp, i64, dp]
         lib.orc_mlp_unsharded.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp]
+        lib.orc_mlp_unsharded_hbf16.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32, vp, i64, dp]
         lib.orc_mlp_sharded.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32, i32, vp, i64, dp]
         lib.orc_qkv_shard.argtypes = [vp, vp, i32, i64, i64, i32, i32, i32, i32, vp, i64, dp]
         lib.orc_oproj_sharded.argtypes = [vp, vp, i32, i64, i64, i32, i32, i32, vp, i64, dp]
@@ -98,7 +99,7 @@ def _load():
         lib.orc_partial_sum_bf16.argtypes = [vp, i32, i64, vp]
         for name in ("orc_shard_w1", "orc_shard_w2", "orc_shard_wqkv", "orc_shard_wo",
                      "orc_linear", "orc_colpar_full", "orc_colpar_shard",
-                     "orc_mlp_unsharded", "orc_mlp_sharded", "orc_qkv_shard",
+                     "orc_mlp_unsharded", "orc_mlp_unsharded_hbf16", "orc_mlp_sharded", "orc_qkv_shard",
                      "orc_oproj_sharded"):
             getattr(lib, name).restype = i32
         _lib = lib
@@ -268,6 +269,19 @@ def mlp_unsharded(X, W1, W2, act: str, rows=None) -> np.ndarray:
     out = np.empty((r.size, H), dtype=np.float64)
     _check(_load().orc_mlp_unsharded(_ptr(X), _ptr(W1), _ptr(W2), _dt(X), M, H, F, ACTS[act],
                                      _ptr(r), r.size, _ptr(out)), "mlp_unsharded")
+    return out
+
+
+def mlp_unsharded_hbf16(X, W1, W2, act: str, rows=None) -> np.ndarray:
+    """Z = bf16(act(X W1)) W2 on the selected rows: the first layer's output
+    rounded to float32 and then bfloat16 (nearest even) before the second
+    layer, as the workloads store it; otherwise fp64 like mlp_unsharded."""
+    X, W1, W2 = _c(X), _c(W1), _c(W2)
+    M, H, F = _mlp_shapes(X, W1, W2, act)
+    r = _rows(rows, M)
+    out = np.empty((r.size, H), dtype=np.float64)
+    _check(_load().orc_mlp_unsharded_hbf16(_ptr(X), _ptr(W1), _ptr(W2), _dt(X), M, H, F, ACTS[act],
+                                           _ptr(r), r.size, _ptr(out)), "mlp_unsharded_hbf16")
     return out
 
 

@@ -90,6 +90,11 @@ double orc_value(const void *base, int64_t idx, int dt)
     return (double)f;
 }
 
+uint16_t orc_f32_to_bf16(float f);
+
+/* Value of a bfloat16 bit pattern. */
+static double bf16_bits_value(uint16_t b) { return orc_value(&b, 0, ORC_BF16); }
+
 /* ---- activations ------------------------------------------------------- */
 
 /* GeLU(y) = y * Phi(y), Phi the standard normal CDF, via erf. */
@@ -326,11 +331,11 @@ int orc_colpar_shard(const void *X, const void *W1, int dt, int64_t M, int64_t H
     return err;
 }
 
-/* Unsharded MLP on selected rows: Z[r] = act(X[rows[r]] W1) W2, H values per
- * row.  This is the dense result that the sharded computation must equal. */
-int orc_mlp_unsharded(const void *X, const void *W1, const void *W2, int dt, int64_t M,
-                      int64_t H, int64_t F, int act, const int64_t *rows, int64_t n_rows,
-                      double *Z)
+/* Unsharded MLP on selected rows (orc_mlp_unsharded, orc_mlp_unsharded_hbf16):
+ * h = act(X W1) per row, optionally rounded to bfloat16 (round_h), then h W2. */
+static int mlp_unsharded(const void *X, const void *W1, const void *W2, int dt, int64_t M,
+                         int64_t H, int64_t F, int act, int round_h, const int64_t *rows,
+                         int64_t n_rows, double *Z)
 {
     if (!W2 || !Z)
         return ORC_ERR_ARG;
@@ -344,11 +349,39 @@ int orc_mlp_unsharded(const void *X, const void *W1, const void *W2, int dt, int
         free(Y);
         return e;
     }
+    if (round_h)
+        for (int64_t k = 0; k < n_rows * F; ++k)
+            Y[k] = bf16_bits_value(orc_f32_to_bf16((float)Y[k]));
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < n_rows; ++r)
         drow_times_matrix(Y + r * F, F, W2, dt, H, Z + r * H);
     free(Y);
     return ORC_OK;
+}
+
+/* Unsharded MLP on selected rows: Z[r] = act(X[rows[r]] W1) W2, H values per
+ * row.  This is the dense result that the sharded computation must equal. */
+int orc_mlp_unsharded(const void *X, const void *W1, const void *W2, int dt, int64_t M,
+                      int64_t H, int64_t F, int act, const int64_t *rows, int64_t n_rows,
+                      double *Z)
+{
+    return mlp_unsharded(X, W1, W2, dt, M, H, F, act, 0, rows, n_rows, Z);
+}
+
+/* The same MLP with the first layer's output rounded to bfloat16 before the
+ * second layer reads it, as the workloads store it: the column-parallel
+ * output Y_i = act(X W1_i) is the row-parallel layer's input ("Tensor
+ * Parallelism in Action", section 1, "Row Parallel (W2)"), a bfloat16 tensor
+ * here.  Each fp64 h is rounded to float32 and then to bfloat16, both to
+ * nearest even; the second layer is fp64 on those values.  A diagnostic
+ * beside orc_mlp_unsharded, which keeps h in fp64: it leaves out the one
+ * rounding the method's dtype prescribes, so what remains of a kernel's error
+ * is its own arithmetic. */
+int orc_mlp_unsharded_hbf16(const void *X, const void *W1, const void *W2, int dt, int64_t M,
+                            int64_t H, int64_t F, int act, const int64_t *rows, int64_t n_rows,
+                            double *Z)
+{
+    return mlp_unsharded(X, W1, W2, dt, M, H, F, act, 1, rows, n_rows, Z);
 }
 
 /* Sharded MLP: for each shard i (ascending), Y_i = act(X W1_i) and the

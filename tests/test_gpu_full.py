@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from synth import WORKLOADS, attn_inputs, mlp_inputs
-from tests.gpu_util import (TOL_BF16_GLOBAL_RMS_OUTLIERS, TOL_BF16_ROW_RMS, bf16_bits,
+from tests.gpu_util import (TOL_BF16_GLOBAL_RMS_OUTLIERS, TOL_BF16_ROW_RMS, BF16H_ERROR_RATIO, bf16_bits,
                             global_rms_error, rowwise_rms_error, stratified_rms, to_device)
 
 pytestmark = pytest.mark.gpu
@@ -47,6 +47,7 @@ def _mlp_check(tp, name, variants, k_rows=24, global_tol=TOL_BF16_ROW_RMS):
     out = d["outlier_rows"]
     rows = _sample_rows(w["M"], k_rows, seed=1, must=out[: min(8, out.size)])
     Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], w["act"], rows=rows)
+    Zref_h = oracle.mlp_unsharded_hbf16(d["X"], d["W1"], d["W2"], w["act"], rows=rows)
     # RMS of the whole output, estimated per stratum (outlier rows, other rows)
     # from the oracle's sampled rows
     rms_all = stratified_rms(Zref, np.isin(rows, out), out.size, w["M"])
@@ -57,9 +58,11 @@ def _mlp_check(tp, name, variants, k_rows=24, global_tol=TOL_BF16_ROW_RMS):
         Zs = Z[torch.from_numpy(rows).cuda()].cpu().numpy()
         err = rowwise_rms_error(Zs, Zref)
         gerr = global_rms_error(Zs, Zref, rms=rms_all)
-        print(f"{name} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}")
+        herr = rowwise_rms_error(Zs, Zref_h)
+        print(f"{name} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}, against bf16 h {herr:.3e}")
         assert err <= TOL_BF16_ROW_RMS
         assert gerr <= global_tol
+        assert herr <= BF16H_ERROR_RATIO * err
         del Z
     return d, s
 
@@ -88,6 +91,7 @@ def test_decode_swiglu_full(tp):
     d = mlp_inputs(M=16, H=w["H"], F=w["F"], act="swiglu", dtype="bf16", seed=0, x_rows=16)
     s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), w["T"], "swiglu")
     Zref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], "swiglu")
+    Zref_h = oracle.mlp_unsharded_hbf16(d["X"], d["W1"], d["W2"], "swiglu")
     for M in w["decode_m"]:
         X = to_device(d["X"][:M])
         for v in ("auto", "partials", "tmem_acc"):
@@ -96,8 +100,9 @@ def test_decode_swiglu_full(tp):
             assert tp.tp_last_device_status() == 0
             err = rowwise_rms_error(Z.cpu().numpy(), Zref[:M])
             gerr = global_rms_error(Z.cpu().numpy(), Zref[:M])
-            print(f"decode M={M} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}")
-            assert err <= TOL_BF16_ROW_RMS and gerr <= TOL_BF16_ROW_RMS
+            herr = rowwise_rms_error(Z.cpu().numpy(), Zref_h[:M])
+            print(f"decode M={M} {v}: row-RMS err {err:.3e}, global-RMS err {gerr:.3e}, against bf16 h {herr:.3e}")
+            assert err <= TOL_BF16_ROW_RMS and gerr <= TOL_BF16_ROW_RMS and herr <= BF16H_ERROR_RATIO * err
 
 
 def test_attn_proj_full(tp):

@@ -603,3 +603,49 @@ def test_block_attention_is_the_attention_core():
     heads = lambda A: A.reshape(M, nh, hd).transpose(1, 0, 2).copy()  # noqa: E731
     Q, K, V = (heads(X @ Wqkv[:, i * H:(i + 1) * H]) for i in range(3))
     assert _normwise(h - X, oracle.attention(Q, K, V, causal=True)) <= 1e-13
+
+
+# ---- the MLP with its first-layer output in bfloat16 ---------------------------------
+
+def test_mlp_hbf16_rounds_each_h_to_nearest_even():
+    """mlp_unsharded_hbf16 rounds every first-layer output h (not Z) to
+    bfloat16, to nearest with ties to even.  Identity activation, X = [1],
+    W2 = ones: Z is the sum of the rounded h values, known in closed form."""
+    h = [1 + 2 ** -8 + 2 ** -10,     # above the midpoint of 1 and 1 + 2^-7: up
+         1 + 2 ** -8,                # the midpoint: to even, 1
+         1 + 3 * 2 ** -8,            # the midpoint of 1 + 2^-7 and 1 + 2^-6: to even, 1 + 2^-6
+         -(1 + 2 ** -8 + 2 ** -10)]  # negative: -(1 + 2^-7)
+    X = np.array([[1.0]], dtype=np.float32)
+    W1 = np.array([h], dtype=np.float32)
+    W2 = np.ones((4, 1), dtype=np.float32)
+    Z = oracle.mlp_unsharded_hbf16(X, W1, W2, "identity")
+    assert Z[0, 0] == (1 + 2 ** -7) + 1 + (1 + 2 ** -6) - (1 + 2 ** -7)
+    # only h is rounded: with one h the rounded Z is that h's rounding
+    Z1 = oracle.mlp_unsharded_hbf16(X, W1[:, :1], np.array([[3.0]], dtype=np.float32), "identity")
+    assert Z1[0, 0] == 3 * (1 + 2 ** -7)
+
+
+def test_mlp_hbf16_equals_fp64_h_when_h_is_bf16_exact():
+    """Small integer inputs make every h an integer below 256, exact in
+    bfloat16: then the two oracles agree exactly, for any W2."""
+    rng = np.random.default_rng(4)
+    X = rng.integers(-3, 4, size=(6, 8)).astype(np.float32)
+    W1 = rng.integers(-3, 4, size=(8, 12)).astype(np.float32)
+    W2 = rng.standard_normal((12, 8)).astype(np.float32)
+    assert np.array_equal(oracle.mlp_unsharded_hbf16(X, W1, W2, "identity"),
+                          oracle.mlp_unsharded(X, W1, W2, "identity"))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_mlp_hbf16_within_the_rounding_bound(act):
+    """Rounding h to bfloat16 moves each h by at most 2^-8 of itself (2^-9
+    to float32 and then bfloat16, with a float32 step below that), so the two
+    oracles differ by at most 2^-8 (|h| |W2|) elementwise, and do differ."""
+    d = mlp_inputs(M=5, H=64, F=256, act=act, dtype="bf16", seed=11)
+    Za = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    Zb = oracle.mlp_unsharded_hbf16(d["X"], d["W1"], d["W2"], act)
+    h = oracle.colpar_full(d["X"], d["W1"], d["W2"].shape[0], act)
+    W2 = (d["W2"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bound = 2.0 ** -8 * (np.abs(h) @ np.abs(W2))
+    assert np.all(np.abs(Zb - Za) <= bound)
+    assert np.any(Zb != Za)

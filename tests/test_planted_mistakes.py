@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 from synth import attention_inputs, mlp_inputs, partials_inputs
-from tests.gpu_util import TOL_BF16_ROW_RMS, attention_elementwise_ok, rowwise_rms_error
+from tests.gpu_util import TOL_BF16_ROW_RMS, BF16H_ERROR_RATIO, attention_elementwise_ok, rowwise_rms_error
 
 
 def _normwise(a, b):
@@ -110,3 +110,21 @@ def test_misplaced_shard_column_is_caught(T):
     shifted = W1[:, F // T: 2 * F // T]
     assert np.array_equal(good, W1[:, : F // T])
     assert not np.array_equal(good, shifted)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_unrounded_or_truncated_h_is_caught(act):
+    """The diagnostic against the oracle that rounds h to bfloat16 (to
+    nearest even): a computation that kept h unrounded, or truncated it to
+    bfloat16, is not closer to that oracle than to the fp64-h one by the
+    required ratio."""
+    d = mlp_inputs(M=16, H=512, F=2048, act=act, dtype="bf16", seed=5)
+    F = d["W2"].shape[0]
+    ref = oracle.mlp_unsharded_hbf16(d["X"], d["W1"], d["W2"], act)
+    unrounded = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    h = oracle.colpar_full(d["X"], d["W1"], F, act)
+    W2 = (d["W2"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    truncated = (h.astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64) @ W2
+    exact = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act)
+    for bad in (unrounded, truncated):
+        assert rowwise_rms_error(bad, ref) > BF16H_ERROR_RATIO * rowwise_rms_error(bad, exact)
