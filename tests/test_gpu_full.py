@@ -127,3 +127,36 @@ def test_attn_proj_full(tp):
         ref = oracle.qkv_shard(d["X"], d["Wqkv"], w["n_heads"], w["head_dim"], w["T"], i, rows=rows)
         got = (q[i].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         assert rowwise_rms_error(got, ref) <= TOL_BF16_ROW_RMS
+
+
+def test_more_than_2_31_elements_in_y(tp):
+    """Maximum sizes: M = 65636 (a ragged last tile), H = 1024, F = 36864,
+    T = 4 makes the first layer's output Y 2.42e9 bf16 elements (4.8 GB),
+    past 2^31: element offsets must not wrap.  Rows on both sides of 2^31 / F
+    and of the halfway point, and the last rows, every variant."""
+    import torch
+    M, H, F, T = 65636, 1024, 36864, 4
+    assert M * F > 2 ** 31
+    g = torch.Generator(device="cuda")
+    g.manual_seed(21)
+    X = torch.randn((M, H), generator=g, device="cuda").to(torch.bfloat16)
+    W1 = (torch.randn((H, F), generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    W2 = (torch.randn((F, H), generator=g, device="cuda") * F ** -0.5).to(torch.bfloat16)
+    s = tp.tp_shard_weights(W1, W2, T, "gelu")
+    r31 = 2 ** 31 // F  # the first row with Y elements past 2^31 (T F_s = F columns a row)
+    rows = np.array([0, 1, M // 2 - 1, M // 2, r31 - 1, r31, r31 + 1, M - 2, M - 1], dtype=np.int64)
+    bits = lambda a: a.cpu().view(torch.int16).numpy().view(np.uint16)
+    Xs = bits(X[torch.from_numpy(rows).cuda()])
+    Zref = oracle.mlp_unsharded(Xs, bits(W1), bits(W2), "gelu")
+    Zref_h = oracle.mlp_unsharded_hbf16(Xs, bits(W1), bits(W2), "gelu")
+    del W1, W2
+    for v in ("auto", "partials", "tmem_acc"):
+        Z = tp.tp_mlp_forward(s, X, variant=v)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0
+        Zs = Z[torch.from_numpy(rows).cuda()].cpu().numpy()
+        del Z
+        err, herr = rowwise_rms_error(Zs, Zref), rowwise_rms_error(Zs, Zref_h)
+        print(f"Y of {M * F} elements, {v}: row-RMS err {err:.3e}, against bf16 h {herr:.3e}")
+        assert err <= TOL_BF16_ROW_RMS and herr <= BF16H_ERROR_RATIO * err
+    s.close()
