@@ -34,10 +34,12 @@
 // P <= 2^8): then the row's sum and its accumulator are scaled by
 // 2^(m_old - m_new), after the P V product issued before is complete (the
 // barrier that frees its buffer says so).  Units run heaviest first (causal: the
-// last query tiles) and are dealt to the CTAs in snake order.  Waits poll (the
-// hand-offs are on the critical path, and a suspended wait wakes too late) and
-// are bounded like the GEMM's; on a timeout the CTA drains what it issued and
-// reports through the status word.
+// last query tiles) and are dealt to the CTAs in snake order.  The hand-offs
+// are on the critical path, so waits probe with try_wait and no suspend hint
+// (the thread wakes when the phase completes: faster than polling with
+// test_wait, where a long hint woke too late); they are bounded like the
+// GEMM's, and on a timeout the CTA drains what it issued and reports through
+// the status word.
 #include <cuda_bf16.h>
 
 #include "tp_device.cuh"
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Ring kr, vr;
       bool ok = true;
       auto load_k = [&](const AttnUnit &t, int j) -> bool {
-        if (!wait_bar_spin(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
+        if (!wait_bar_wake(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
         mbar_arrive_expect_tx(k_full(kr.buf), kTileBytes);
         for (int kb = 0; kb < 2; ++kb)
           tma_load_3d(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto load_v = [&](const AttnUnit &t, int j) -> bool {
-        if (!wait_bar_spin(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
+        if (!wait_bar_wake(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
         mbar_arrive_expect_tx(v_full(vr.buf), kTileBytes);
         // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
         for (int h = 0; h < 2; ++h)
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = unit_of(k, b, G);
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
-        if (!wait_bar_spin(q_empty, (qc & 1u) ^ 1u, w)) break;
+        if (!wait_bar_wake(q_empty, (qc & 1u) ^ 1u, w)) break;
         mbar_arrive_expect_tx(q_full, kTileBytes);
         for (int kb = 0; kb < 2; ++kb)
           tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
@@ -263,14 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bit b: parity of buffer b's next s_free wait (a fresh barrier's previous phase counts as
       // complete).  Per-buffer phases live in bits of a register, not in an indexed array.
       uint32_t fph = (1u << kSbuf) - 1u;
-      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_spin(never, 0u, w);
+      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k, b, G);
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
-        if (!wait_bar_spin(q_full, uc & 1u, w)) break;
+        if (!wait_bar_wake(q_full, uc & 1u, w)) break;
         for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
-          if (!wait_bar_spin(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_spin(k_full(kr.buf), kr.phase, w)) {
+          if (!wait_bar_wake(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_wake(k_full(kr.buf), kr.phase, w)) {
             ok = false;
             break;
           }
@@ -303,15 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int uc = 0;
       Ring vr;
       uint32_t pph = 0;                    // bit b: phase of buffer b's next p_full wait
-      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_spin(never, 0u, w);
+      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k, b, G);
         if (u >= units) break;
         const AttnUnit t = decode(u, a);
         for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
           // (for the unit's first key tile, also once the previous unit's O is read out)
-          if (!wait_bar_spin(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_spin(o_free, (uc & 1u) ^ 1u, w)) ||
-              !wait_bar_spin(v_full(vr.buf), vr.phase, w)) {
+          if (!wait_bar_wake(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_wake(o_free, (uc & 1u) ^ 1u, w)) ||
+              !wait_bar_wake(v_full(vr.buf), vr.phase, w)) {
             ok = false;
             break;
           }
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t uc = 0;                     // units done
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-      const bool got = wait_bar_spin(bar, parity, w);
+      const bool got = wait_bar_wake(bar, parity, w);
       return __all_sync(0xffffffffu, got);
     };
     for (int k = 0; ok; ++k) {
