@@ -387,51 +387,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (cc * 32 + i > kmax) s[cc][i] = __float_as_uint(-INFINITY);
         }
-        // row maximum: sixteen chains of four three-input maxima over 8 scores each, then a tree
-        // (seven dependent steps in all, where one chain per 32 scores took sixteen)
-        float m16[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const uint32_t *v = s[q >> 2] + (q & 3) * 8;
-          float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-          m = fmax3(m, __uint_as_float(v[3]), __uint_as_float(v[4]));
-          m = fmax3(m, __uint_as_float(v[5]), __uint_as_float(v[6]));
-          m16[q] = fmaxf(m, __uint_as_float(v[7]));
-        }
-        float m6[6];
-#pragma unroll
-        for (int q = 0; q < 5; ++q) m6[q] = fmax3(m16[3 * q], m16[3 * q + 1], m16[3 * q + 2]);
-        m6[5] = m16[15];
-        const float mx = fmaxf(fmax3(m6[0], m6[1], m6[2]), fmax3(m6[3], m6[4], m6[5]));
-        const float m_tile = mx * c;
-        const bool raise = m_tile > m_used + kRescaleGap;
-        const float m_new = raise ? m_tile : m_used;
-        const float alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
         // P = 2^(t - m) as bf16 pairs over the upper 64 columns of the S buffer: keys 64 hh ..
         // 64 hh + 63 into columns 64 + 32 hh (the scores are all in registers by now).  The
         // row sum adds the float32 weights before their rounding to bf16 for the P V product;
         // the roundings (2^-9 relative each, independent) move an output by far less than its
         // own bf16 rounding.  Paired float32 operations: two scores per FFMA2 and FADD2.
-        float2 sum4[4];
+        // Returns the row sum; with `watch`, also the largest exponent argument t - m (targ).
+        auto make_p = [&](float m_sh, bool watch, float &targ) -> float {
+          float2 sum4[4];
+          float tm4[4];
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) sum4[g4] = make_float2(0.f, 0.f);
-        const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t *v = s[2 * hh + (i >> 4)];
-            const float2 t2 = __ffma2_rn(
-                make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])), c2, nm2);
-            const float2 e = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
-            pk[i] = pack_bf16x2(e.x, e.y);
-            sum4[i & 3] = __fadd2_rn(sum4[i & 3], e);
+          for (int g4 = 0; g4 < 4; ++g4) {
+            sum4[g4] = make_float2(0.f, 0.f);
+            tm4[g4] = -INFINITY;
           }
-          tmem_st32(sb + 64 + hh * 32, pk);
+          const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_sh, -m_sh);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t *v = s[2 * hh + (i >> 4)];
+              const float2 t2 = __ffma2_rn(
+                  make_float2(__uint_as_float(v[(2 * i) & 31]), __uint_as_float(v[(2 * i + 1) & 31])), c2, nm2);
+              if (watch) tm4[i & 3] = fmax3(tm4[i & 3], t2.x, t2.y);
+              const float2 e = make_float2(ex2_approx(t2.x), ex2_approx(t2.y));
+              pk[i] = pack_bf16x2(e.x, e.y);
+              sum4[i & 3] = __fadd2_rn(sum4[i & 3], e);
+            }
+            tmem_st32(sb + 64 + hh * 32, pk);
+          }
+          targ = fmaxf(fmaxf(tm4[0], tm4[1]), fmaxf(tm4[2], tm4[3]));
+          return ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
+                 ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
+        };
+        // The unit's first key tile sets the shift from the tile's maximum.  A later tile first
+        // makes P against the current shift, watching the largest exponent argument alongside
+        // (its maxima run on the ALU beside the exponentials on the XU); only where some score
+        // would exceed 2^8 is the tile made again from its maximum, as the first one is (lanes
+        // whose shift stays then make the same P again).
+        float sum = 0.f, alpha = 1.0f, m_new = m_used, targ = 0.f;
+        bool raise = false;
+        bool redo = j == 0;
+        if (!redo) {
+          sum = make_p(m_used, true, targ);
+          redo = __any_sync(0xffffffffu, targ > kRescaleGap);
         }
-        const float sum = ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) +
-                          ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
+        if (redo) {
+          // row maximum: sixteen chains of four three-input maxima over 8 scores each, then a tree
+          float m16[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t *v = s[q >> 2] + (q & 3) * 8;
+            float m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+            m = fmax3(m, __uint_as_float(v[3]), __uint_as_float(v[4]));
+            m = fmax3(m, __uint_as_float(v[5]), __uint_as_float(v[6]));
+            m16[q] = fmaxf(m, __uint_as_float(v[7]));
+          }
+          float m6[6];
+#pragma unroll
+          for (int q = 0; q < 5; ++q) m6[q] = fmax3(m16[3 * q], m16[3 * q + 1], m16[3 * q + 2]);
+          m6[5] = m16[15];
+          const float mx = fmaxf(fmax3(m6[0], m6[1], m6[2]), fmax3(m6[3], m6[4], m6[5]));
+          const float m_tile = mx * c;
+          raise = m_tile > m_used + kRescaleGap;
+          m_new = raise ? m_tile : m_used;
+          alpha = raise ? ex2_approx(m_used - m_new) : 1.0f;  // 0 on the first tile
+          sum = make_p(m_new, false, targ);
+        }
         l_run = fmaf(l_run, alpha, sum);
         // A raised shift also scales the accumulated O, once every P V issued before this step
         // is complete.  The last of them, P_{j-1} V_{j-1}, completes the phase of
