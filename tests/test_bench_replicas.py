@@ -56,3 +56,24 @@ def test_bench_arguments_default_to_one_gpu():
     import bench
     a = bench.parse_args([])
     assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3 and a.steps >= 1
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """The reference arm launched like the scaling runs (torchrun, two ranks
+    on this host): rank 0 alone times the oracle and prints one line; the
+    other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    from pathlib import Path
+    root = Path(__file__).resolve().parent.parent
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           str(root / "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
