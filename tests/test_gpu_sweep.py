@@ -1,0 +1,73 @@
+"""Seeded random sweeps over the shapes the API accepts: the fused attention
+core and the MLP forward, each case against the fp64 oracle on a few sampled
+rows (always the first and the last).  The fixed parity cases pin chosen
+tile boundaries; these cover the combinations between them (ragged M of
+every size class, shard counts, head counts, causal or not, every all-reduce
+variant, score scales that make the online softmax raise its shift), and
+would show a barrier-phase or work-split slip that only some shapes reach.
+Same tolerances as the fixed cases."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import attention_inputs, mlp_inputs
+from tests.gpu_util import (TOL_ATTN_ELEMENT, TOL_BF16_GRAD_ROW_RMS, TOL_BF16_ROW_RMS, attention_elementwise_ok,
+                            rowwise_rms_error, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import linear_sharding_gb300 as tp
+    tp.load_library()
+    return tp
+
+
+def _rows(rng, M, k=4):
+    rows = {0, M - 1}
+    rows.update(int(r) for r in rng.integers(0, M, size=k))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def test_attention_random_shapes(tp):
+    import torch
+    rng = np.random.default_rng(2024)
+    for case in range(200):
+        M = int(rng.integers(1, 2049))
+        nh = int(rng.integers(1, 9))
+        causal = bool(rng.integers(0, 2))
+        q_scale = float(rng.choice([0.5, 1.0, 2.0, 3.0]))
+        d = attention_inputs(M, nh, seed=case, q_scale=q_scale)
+        O = tp.tp_attention_forward(to_device(d["Q"]), to_device(d["K"]), to_device(d["V"]), causal)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0, (M, nh, causal)
+        rows = _rows(rng, M)
+        got = (O[torch.from_numpy(rows).cuda()].cpu().view(torch.int16).numpy().view(np.uint16)
+               .astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = oracle.attention(d["Q"], d["K"], d["V"], causal, rows=rows)
+        e, el = rowwise_rms_error(got, ref), attention_elementwise_ok(got, ref)
+        assert e <= TOL_BF16_GRAD_ROW_RMS and el <= TOL_ATTN_ELEMENT, (case, M, nh, causal, q_scale, e, el)
+
+
+def test_mlp_random_shapes(tp):
+    import torch
+    rng = np.random.default_rng(2025)
+    for case in range(120):
+        act = str(rng.choice(["gelu", "swiglu", "identity"]))
+        T = int(rng.choice([1, 2, 3, 4, 8]))
+        Fs = 128 * int(rng.integers(1, 5))
+        H = 128 * int(rng.integers(2, 9))
+        M = int(rng.choice([int(rng.integers(1, 17)), int(rng.integers(17, 1200))]))
+        variant = str(rng.choice(["auto", "partials", "tmem_acc"]))
+        d = mlp_inputs(M=M, H=H, F=Fs * T, act=act, dtype="bf16", seed=case, x_rows=max(M, 16))
+        s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+        Z = tp.tp_mlp_forward(s, to_device(d["X"][:M]), variant=variant)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0, (act, M, H, Fs, T, variant)
+        rows = _rows(rng, M)
+        got = Z[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+        ref = oracle.mlp_unsharded(d["X"][:M], d["W1"], d["W2"], act, rows=rows)
+        e = rowwise_rms_error(got, ref)
+        assert e <= TOL_BF16_ROW_RMS, (case, act, M, H, Fs, T, variant, e)
+        s.close()
