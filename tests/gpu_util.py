@@ -91,8 +91,15 @@ TOL_BF16_GLOBAL_RMS_OUTLIERS = 0.1
 # roundings (the saved pre-activation, dP = dH * act'(P) and, for dW, the
 # transposed operands are exact copies) against the forward's one (Y); the
 # forward's measured row-RMS error is about 8e-3 per rounding, so the
-# gradients are held to 3e-2.
+# gradients are held to 3e-2.  That assumes the weight gradients sum over
+# enough tokens for those roundings (2^-9 relative each) to average: an exact
+# float32 emulation of the same rounding chain (SwiGLU, H = 384, F = 512)
+# puts dW1 at 1.3e-2 with 512 or 2048 tokens, 2.0e-2 with 128 and 2.5-3.2e-2
+# with 44, where a few tokens' terms dominate each dW1 element.  The bound
+# is asserted for sums over at least 64 tokens (GRAD_MIN_TOKENS), as all
+# the backward tests run.
 TOL_BF16_GRAD_ROW_RMS = 3e-2
+GRAD_MIN_TOKENS = 64
 
 # The attention output passes through two bf16 roundings: the probabilities P
 # (each weight relative 2^-9, rounded once before the P V product) and the

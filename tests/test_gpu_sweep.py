@@ -11,8 +11,8 @@ import pytest
 
 import oracle
 from synth import attention_inputs, mlp_inputs
-from tests.gpu_util import (TOL_ATTN_ELEMENT, TOL_BF16_GRAD_ROW_RMS, TOL_BF16_ROW_RMS, attention_elementwise_ok,
-                            rowwise_rms_error, to_device)
+from tests.gpu_util import (GRAD_MIN_TOKENS, TOL_ATTN_ELEMENT, TOL_BF16_GRAD_ROW_RMS, TOL_BF16_ROW_RMS,
+                            attention_elementwise_ok, rowwise_rms_error, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,4 +70,35 @@ def test_mlp_random_shapes(tp):
         ref = oracle.mlp_unsharded(d["X"][:M], d["W1"], d["W2"], act, rows=rows)
         e = rowwise_rms_error(got, ref)
         assert e <= TOL_BF16_ROW_RMS, (case, act, M, H, Fs, T, variant, e)
+        s.close()
+
+
+def test_training_backward_random_shapes(tp):
+    """The training forward and the backward (dX, dW1, dW2) on random shapes,
+    every element against the fp64 backward oracle (token counts from
+    GRAD_MIN_TOKENS up, the domain of the gradient bound)."""
+    import torch
+    from synth import f32_to_bf16_bits
+    rng = np.random.default_rng(2026)
+    for case in range(30):
+        act = str(rng.choice(["gelu", "swiglu", "identity"]))
+        T = int(rng.choice([1, 2, 3, 4]))
+        Fs = 128 * int(rng.integers(1, 4))
+        H = 128 * int(rng.integers(2, 5))
+        M = int(rng.integers(GRAD_MIN_TOKENS, 401))
+        variant = str(rng.choice(["auto", "partials"]))
+        d = mlp_inputs(M=M, H=H, F=Fs * T, act=act, dtype="bf16", seed=100 + case)
+        dZ = f32_to_bf16_bits(rng.standard_normal((M, H)).astype(np.float32))
+        s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+        tp.tp_shards_enable_backward(s, to_device(d["W1"]), to_device(d["W2"]))
+        X = to_device(d["X"])
+        Z, Hs, Ps = tp.tp_mlp_forward_train(s, X, variant)
+        dX, dW1, dW2 = tp.tp_mlp_backward(s, X, Hs, Ps, to_device(dZ), variant)
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0, (act, M, H, Fs, T, variant)
+        dx_ref = oracle.mlp_backward_dx(d["X"], d["W1"], d["W2"], dZ, act)
+        dw1_ref, dw2_ref = oracle.mlp_backward_dw(d["X"], d["W1"], d["W2"], dZ, act)
+        e = max(rowwise_rms_error(dX.cpu().numpy(), dx_ref), rowwise_rms_error(dW1.cpu().numpy(), dw1_ref),
+                rowwise_rms_error(dW2.cpu().numpy(), dw2_ref))
+        assert e <= TOL_BF16_GRAD_ROW_RMS, (case, act, M, H, Fs, T, variant, e)
         s.close()
