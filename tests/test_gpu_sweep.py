@@ -102,3 +102,22 @@ def test_training_backward_random_shapes(tp):
                 rowwise_rms_error(dW2.cpu().numpy(), dw2_ref))
         assert e <= TOL_BF16_GRAD_ROW_RMS, (case, act, M, H, Fs, T, variant, e)
         s.close()
+
+
+def test_block_random_shapes(tp):
+    """One transformer block (QKV, attention, O-projection with its residual,
+    the MLP with its residual) on random shapes, sampled rows against the
+    block oracle."""
+    from tests.test_gpu_block import _check, _weights
+    rng = np.random.default_rng(2027)
+    for case in range(16):
+        nh = int(rng.choice([1, 2, 3, 4, 6, 8]))
+        T = int(rng.choice([t for t in (1, 2, 3, 4, 8) if nh % t == 0]))
+        H = nh * 128
+        F = 128 * int(rng.integers(1, 5)) * T
+        M = int(rng.integers(2, 701))
+        act = str(rng.choice(["gelu", "swiglu", "identity"]))
+        causal = bool(rng.integers(0, 2))
+        variant = str(rng.choice(["auto", "partials", "tmem_acc"]))
+        d = _weights(M, H, F, act, seed=300 + case)
+        _check(tp, d, M, H, F, nh, 128, T, act, causal, variant, _rows(rng, M, k=6))
