@@ -27,6 +27,7 @@
 // MMAs finish and releasing its tensor memory.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstring>
 #include <utility>
 
@@ -1125,11 +1126,14 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
   if (units <= 0) return cudaSuccess;
-  // Clusters that fit on the GPU at once (pairs of SMs with room for one CTA each).
-  static int max_clusters[64][4];
+  // Clusters that fit on the GPU at once (pairs of SMs with room for one CTA each), per device,
+  // found on the first launch there (one array per epilogue: this is a template).  Atomic, as
+  // host threads may launch concurrently; they would store the same value.
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int &mc = max_clusters[dev & 63][EPI & 3];
+  std::atomic<int> &slot = max_clusters[dev & 63];
+  int mc = slot.load(std::memory_order_relaxed);
   if (mc <= 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -1141,6 +1145,7 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
       n = num_sms / 2;
     }
     mc = n;
+    slot.store(n, std::memory_order_relaxed);
   }
   const int clusters = static_cast<int>(units < mc ? units : mc);
   return launch_dependent(kern, dim3(2 * clusters), smem, stream, a, b, o, g);
