@@ -48,3 +48,65 @@ def test_forward_replays_from_a_cuda_graph(tp, M, H, F, T, act, variant):
     assert torch.equal(Z, eager2)
     assert tp.tp_last_device_status() == 0
     s.close()
+
+
+def test_attention_replays_from_a_cuda_graph(tp):
+    """The fused attention core allocates nothing: captured once, replayed
+    with Q, K and V refilled in place."""
+    import torch
+    from synth import attention_inputs
+    a1, a2 = attention_inputs(700, 3, seed=51), attention_inputs(700, 3, seed=52)
+    Q, K, V = (to_device(a1[k]) for k in "QKV")
+    eager1 = tp.tp_attention_forward(Q, K, V, True).clone()
+    Q2, K2, V2 = (to_device(a2[k]) for k in "QKV")
+    eager2 = tp.tp_attention_forward(Q2, K2, V2, True).clone()
+    torch.cuda.synchronize()
+    O = torch.empty_like(eager1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tp.tp_attention_forward(Q, K, V, True, O)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(O, eager1)
+    Q.copy_(Q2)
+    K.copy_(K2)
+    V.copy_(V2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(O, eager2)
+    assert tp.tp_last_device_status() == 0
+
+
+def test_block_replays_from_a_cuda_graph(tp):
+    """One transformer block with a caller-provided workspace, captured once
+    and replayed with the input refilled in place."""
+    import torch
+    from tests.test_gpu_block import _weights
+    M, nh, T, act = 300, 4, 2, "swiglu"
+    H, F = nh * 128, 4 * nh * 128
+    d = _weights(M, H, F, act, seed=61)
+    d2 = _weights(M, H, F, act, seed=62)
+    a = tp.tp_shard_weights_qkv(to_device(d["Wqkv"]), to_device(d["Wo"]), nh, 128, T)
+    m = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    ws = torch.empty(max(tp.tp_block_workspace_bytes(a, m, M), 16), dtype=torch.uint8, device="cuda")
+    X, X2 = to_device(d["X"]), to_device(d2["X"])
+    e1, _ = tp.tp_block_forward(a, m, X, workspace=ws)
+    e1 = e1.clone()
+    e2, _ = tp.tp_block_forward(a, m, X2, workspace=ws)
+    e2 = e2.clone()
+    torch.cuda.synchronize()
+    Xin = X.clone()
+    out = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tp.tp_block_forward(a, m, Xin, out=out, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, e1)
+    Xin.copy_(X2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, e2)
+    assert tp.tp_last_device_status() == 0
+    a.close()
+    m.close()

@@ -136,6 +136,35 @@ def test_noalloc_refits_a_plan_beyond_its_scratch():
     s.close()
 
 
+def test_noalloc_replays_from_a_cuda_graph():
+    """The use it exists for: a decode step captured into a CUDA graph with no
+    workspace at all (after a first call on the device, as documented), then
+    replayed with the input refilled in place; bit-identical to eager calls."""
+    import torch
+    import linear_sharding_gb300 as tp
+    lib = tp.load_library()
+    H, F, T, M = 2048, 7168, 8, 16
+    d, s, X = _problem(tp, "swiglu", M, H, F, T, seed=71)
+    d2 = mlp_inputs(M=M, H=H, F=F, act="swiglu", dtype="bf16", seed=72, x_rows=16)
+    X2 = to_device(d2["X"])
+    e1 = _run(lib, tp, s, X, "swiglu", H)
+    e2 = _run(lib, tp, s, X2, "swiglu", H)
+    Xin = X.clone()
+    Z = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert _noalloc(lib, s, Xin, Z, "swiglu") == 0
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(Z.cpu().numpy(), e1)
+    Xin.copy_(X2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(Z.cpu().numpy(), e2)
+    assert tp.tp_last_device_status() == 0
+    s.close()
+
+
 def test_noalloc_rejects_work_beyond_its_scratch():
     import torch
     import linear_sharding_gb300 as tp
