@@ -454,6 +454,22 @@ TP_API tp_status_t tp_last_device_status(void *stream);
 TP_API tp_status_t tp_set_machine_balance(double flop_per_byte);
 
 /*
+ * tp_set_rowpar_schedule - how the row-parallel GEMM with one TMEM accumulator
+ * over all shards (the all-reduce-sum inside the accumulator, "Slice the
+ * matrix itself", section "Mathematical formulation") lays its output tiles
+ * over the GPU's CTA pairs.  1 (default): where 256-column tiles would need
+ * more than one round of the pairs and tiles of 288..448 columns (plus one
+ * narrow tile per 256 rows, two of those per pair) fit in one round with at
+ * most 90 % of the columns per pair, the wider tiles (at M = 2048, H = 4096
+ * on a 152-SM GB300: 448 columns instead of two rounds of 256).  0: always
+ * 256-column tiles.  Both sum every output element over the same K order in
+ * one accumulator, so they give identical results.  Other values ->
+ * TP_ERR_ARG.  Process-wide; affects calls made after it (workspace sizes do
+ * not depend on it).
+ */
+TP_API tp_status_t tp_set_rowpar_schedule(int wide);
+
+/*
  * tp_set_wait_limit_ns - limit on every device-side wait (default 2 s) in
  * kernels launched after this call, process-wide.  0 restores the default.
  * A limit below 1 ms is a test limit: the tensor-core kernels then first

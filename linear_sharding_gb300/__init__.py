@@ -38,7 +38,7 @@ EXPORTS = (
     "tp_partial_sum_bf16", "tp_shards_enable_backward", "tp_mlp_train_workspace_bytes",
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
     "tp_block_workspace_bytes", "tp_block_forward", "tp_attention_workspace_bytes",
-    "tp_attention_forward", "tp_inject_alloc_failures", "tp_set_machine_balance",
+    "tp_attention_forward", "tp_inject_alloc_failures", "tp_set_machine_balance", "tp_set_rowpar_schedule",
 )
 
 _lock = threading.Lock()
@@ -86,6 +86,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_set_wait_limit_ns.argtypes = [u64]
         lib.tp_inject_alloc_failures.argtypes = [i32]
         lib.tp_set_machine_balance.argtypes = [ctypes.c_double]
+        lib.tp_set_rowpar_schedule.argtypes = [i32]
         lib.tp_colpar_workspace_bytes.restype = sz
         lib.tp_colpar_workspace_bytes.argtypes = [vp, i64]
         lib.tp_colpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
@@ -469,6 +470,13 @@ def tp_set_machine_balance(flop_per_byte: float) -> None:
     """Flop per HBM byte the AUTO planners weigh partial traffic with (0: the
     device's own figures)."""
     _check(load_library().tp_set_machine_balance(float(flop_per_byte)), "tp_set_machine_balance")
+
+
+def tp_set_rowpar_schedule(wide: bool) -> None:
+    """Let the row-parallel GEMM with one accumulator use wide output tiles
+    where they fit one round of CTA pairs (True, the default), or always
+    256-column tiles (False).  The results are identical."""
+    _check(load_library().tp_set_rowpar_schedule(1 if wide else 0), "tp_set_rowpar_schedule")
 
 
 def tp_inject_alloc_failures(count: int) -> None:

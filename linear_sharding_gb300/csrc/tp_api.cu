@@ -58,6 +58,8 @@ std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 // tp_set_machine_balance: a caller's measured flop-per-byte figure (0: use
 // the queried one).
 std::atomic<double> g_balance_override{0.0};
+// tp_set_rowpar_schedule: whether the row-parallel GEMM may use the wide tiles.
+std::atomic<int> g_rowpar_wide{1};
 
 // Dense bf16 tensor-core flop per SM per clock (tcgen05.mma, kind::f16):
 // a 128 x 256 x 16 MMA every 128 cycles.
@@ -361,6 +363,38 @@ tp_status_t apply_residual(const DevState *d, float *Z, int64_t n, const Residua
   return TP_OK;
 }
 
+// Wide schedule of a row-parallel CTA-pair GEMM with one accumulation slot (launch_gemm_wide):
+// each of the m_tiles 256-row blocks of H columns is cut into q tiles whose widths are multiples
+// of 32 that differ by at most 32 (nb of bn columns, q - nb of bn - 32), with q as large as the
+// clusters allow (one tile each, all at once), every tile wider than 256 columns (two MMAs per
+// k-step into two accumulators) and at most kWideMaxN.  Chosen when its widest tile is narrower
+// than the columns the 256-column tiles put on one cluster over their rounds; bn = 0: none.
+// At M = 2048, H = 4096 on 76 clusters: 128 tiles of 256 columns take two rounds (512 columns a
+// cluster); 8 x 9 tiles of 480 and 448 columns take one (480).
+struct WidePlan {
+  int bn = 0, nb = 0, q = 0;
+};
+WidePlan plan_wide(int m_tiles, int64_t H, int clusters) {
+  WidePlan p;
+  if (m_tiles < 1 || H % 256 != 0 || clusters < m_tiles) return p;
+  const int64_t units = H / 32;  // 32-column units of a row block
+  const int64_t rounds = cdiv(static_cast<int64_t>(m_tiles) * (H / 256), clusters);
+  for (int64_t q = clusters / m_tiles; q >= 1; --q) {
+    const int64_t w1 = cdiv(units, q);        // widest tile, in units
+    const int64_t nb = units - q * (w1 - 1);  // tiles of w1 units; the others have w1 - 1
+    const int64_t narrowest = nb == q ? w1 : w1 - 1;
+    if (32 * narrowest <= 256) continue;      // a tile this narrow has one MMA: fewer, wider tiles
+    if (32 * w1 > kWideMaxN) break;           // fewer tiles would only be wider
+    if (32 * w1 < rounds * 256) {
+      p.bn = static_cast<int>(32 * w1);
+      p.nb = static_cast<int>(nb);
+      p.q = static_cast<int>(q);
+    }
+    break;
+  }
+  return p;
+}
+
 // Row-parallel GEMM over T shards into Z, with `slots` accumulation slots
 // (slots > 1: float32 partials in P, then the shard-sum).  A residual is fused
 // into the GEMM's epilogue with one slot, and applied after the shard-sum otherwise.
@@ -389,9 +423,31 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
     g.aux2 = res.add_bf16;
     g.out2 = res.out_bf16;
   }
-  if (pair)
+  bool done = false;
+  if (pair && epi == EPI_F32 && slots == 1 && g_rowpar_wide.load() != 0) {
+    const WidePlan wp = plan_wide(g.m_tiles, H, d->sms / 2);
+    if (wp.bn > 0) {
+      // the same k-tile-blocked W2 with the row counts of the tiles' second B pieces as boxes
+      CUtensorMap mb2, mbr;
+      TP_TRY(make_map(&mb2, s->w2p, 64, H, g.kt_total, 128, H * 128, (wp.bn - 256) / 2));
+      if (wp.nb < wp.q)
+        TP_TRY(make_map(&mbr, s->w2p, 64, H, g.kt_total, 128, H * 128, (wp.bn - 288) / 2));
+      else
+        mbr = mb2;
+      GemmArgs gw = g;
+      gw.wide_bn = wp.bn;
+      gw.wide_nb = wp.nb;
+      gw.wide_q = wp.q;
+      const cudaError_t e = launch_gemm_wide(mapA, s->map_w2_a, mb2, mbr, gw, d->sms, st);
+      // fewer clusters fit at once than the schedule needs (a GPU shared with other work):
+      // the 256-column tiles below
+      if (e != cudaErrorInvalidConfiguration) TP_CUDA(e);
+      done = e == cudaSuccess;
+    }
+  }
+  if (!done && pair)
     TP_CUDA(launch_gemm(CFG_PAIR_N256, epi, mapA, s->map_w2_a, g, d->sms, st));
-  else
+  else if (!done)
     TP_CUDA(launch_gemm(cfg_for(s->bn2), epi, mapA, s->map_w2_b, g, d->sms, st));
   if (slots > 1) {
     TP_CUDA(launch_shard_sum_strided(P, slots, M * H, M * H, Z, d->sms, st));
@@ -1023,6 +1079,12 @@ tp_status_t tp_inject_alloc_failures(int count) {
 tp_status_t tp_set_machine_balance(double flop_per_byte) {
   if (!(flop_per_byte >= 0.0) || flop_per_byte > 1e6) return TP_ERR_ARG;
   g_balance_override.store(flop_per_byte);
+  return TP_OK;
+}
+
+tp_status_t tp_set_rowpar_schedule(int wide) {
+  if (wide != 0 && wide != 1) return TP_ERR_ARG;
+  g_rowpar_wide.store(wide);
   return TP_OK;
 }
 

@@ -759,17 +759,68 @@ __host__ __device__ constexpr bool tma_store_epi() {
   return EPI == EPI_GELU_BF16 || EPI == EPI_IDENT_BF16 || EPI == EPI_F32 || EPI == EPI_SWIGLU_BF16;
 }
 constexpr uint32_t kStoreBufBytes = 32 * 128;  // 32 rows x 128 B, 128-byte swizzle
-template <int EPI>
+// Stages of the ring; the wide schedule's stages hold up to kWideMaxN / 2 B rows per CTA.
+template <int EPI, bool WIDE = false>
 __host__ __device__ constexpr int pair_stages() {
-  return tma_store_epi<EPI>() ? kPairStages - 1 : kPairStages;
+  return WIDE ? 4 : tma_store_epi<EPI>() ? kPairStages - 1 : kPairStages;
 }
-template <int EPI>
+template <bool WIDE = false>
+__host__ __device__ constexpr uint32_t pair_b_bytes() {
+  return static_cast<uint32_t>(WIDE ? kWideMaxN / 2 : kPairBN / 2) * BK * 2;
+}
+template <int EPI, bool WIDE = false>
 __host__ __device__ constexpr size_t pair_smem_bytes() {
-  return 1024 + static_cast<size_t>(pair_stages<EPI>()) * (128 * BK * 2 + (kPairBN / 2) * BK * 2) +
+  return 1024 + static_cast<size_t>(pair_stages<EPI, WIDE>()) * (128 * BK * 2 + pair_b_bytes<WIDE>()) +
          (tma_store_epi<EPI>() ? 8 * kStoreBufBytes : 0) + 512;
 }
 static_assert(pair_smem_bytes<EPI_F32_RESID>() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
 static_assert(pair_smem_bytes<EPI_F32>() <= 232448, "pair kernel exceeds 227 KiB of shared memory");
+static_assert(pair_smem_bytes<EPI_F32, true>() <= 232448, "wide pair kernel exceeds 227 KiB of shared memory");
+static_assert(kWideMaxN > 256 && kWideMaxN <= 512 && kWideMaxN % 32 == 0, "wide tiles: two MMAs, one TMEM allocation");
+
+// One cluster's work on the wide schedule (GemmArgs::wide_*): `width` columns from n0 of
+// 256-row block m0.  The row blocks of one column range run side by side (they share its B
+// tiles through L2).
+struct WideUnit {
+  int m0, n0, width;
+};
+__device__ __forceinline__ WideUnit decode_wide(int u, const GemmArgs &g) {
+  WideUnit r;
+  r.m0 = u % g.m_tiles;
+  const int j = u / g.m_tiles;  // tile of the row block: wide_nb of wide_bn columns, then 32 fewer
+  const int narrow = j - g.wide_nb;
+  r.width = narrow < 0 ? g.wide_bn : g.wide_bn - 32;
+  r.n0 = narrow < 0 ? j * g.wide_bn : g.wide_nb * g.wide_bn + narrow * (g.wide_bn - 32);
+  return r;
+}
+
+// Float32 epilogue of `ncols` columns (a multiple of 32) of one accumulator through the warp's
+// staging buffers and TMA stores (output columns x0 ..; TMEM lanes = rows wrow .. wrow + 31).
+__device__ __forceinline__ void epilogue_f32_cols(uint32_t tb, int x0, int ncols, int wrow, int lane,
+                                                  const GemmArgs &g, const CUtensorMap *mapO, uint8_t *bufs,
+                                                  uint32_t &nstore) {
+  const bool rows_in = wrow < g.rows_valid;
+#pragma unroll 1
+  for (int c = 0; c < ncols / 32; ++c) {
+    uint8_t *buf = bufs + (nstore & 1u) * kStoreBufBytes;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done with it
+    __syncwarp();
+    uint32_t w[32];
+    tmem_ld32(tb + c * 32, w);
+    tmem_ld_wait();
+    tmem_reg_fence(w);
+    uint4 *row = reinterpret_cast<uint4 *>(buf + lane * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) row[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (rows_in) tma_store_3d(mapO, smem_u32(buf), x0 + c * 32, wrow, 0);
+      bulk_commit();
+    }
+    ++nstore;
+  }
+}
 
 // Epilogue of one 256-column accumulator by one warp through TMA stores: TMEM lanes
 // [32 q, 32 q + 32) are output rows wrow .. wrow + 31; 128-byte column chunks (64 bf16 or 32
@@ -858,15 +909,22 @@ __device__ __forceinline__ void epilogue_tile_tma(uint32_t tb, const Unit &t, in
   }
 }
 
-template <int EPI>
+// WIDE: the wide row-parallel schedule (EPI_F32 only): one tile per cluster, of up to kWideMaxN
+// columns, as two MMAs per k-step (256 columns into TMEM columns 0 .., the rest into 256 ..),
+// each CTA loading its half of both B pieces (mapB: 128 rows; the second piece's half with mapB2
+// for the wide_bn-column tiles, mapBr for the 32 narrower ones).
+template <int EPI, bool WIDE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tp_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB,
-                        const __grid_constant__ CUtensorMap mapO, const GemmArgs g) {
-  constexpr int STAGES = pair_stages<EPI>();
+                        const __grid_constant__ CUtensorMap mapO,
+                        const __grid_constant__ CUtensorMap mapB2,
+                        const __grid_constant__ CUtensorMap mapBr, const GemmArgs g) {
+  static_assert(!WIDE || EPI == EPI_F32, "the wide schedule has the float32 epilogue only");
+  constexpr int STAGES = pair_stages<EPI, WIDE>();
   constexpr int BN = kPairBN;
   constexpr uint32_t A_BYTES = 128 * BK * 2;
-  constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
+  constexpr uint32_t B_BYTES = pair_b_bytes<WIDE>();
   constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
   constexpr int kReleaseArrivals = 8;  // 4 epilogue warps in each CTA
@@ -912,6 +970,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapA);
     prefetch_tmap(&mapB);
     if constexpr (tma_store_epi<EPI>()) prefetch_tmap(&mapO);
+    if constexpr (WIDE) {
+      prefetch_tmap(&mapB2);
+      prefetch_tmap(&mapBr);
+    }
   }
   if (warp == 1) {
     tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
@@ -926,7 +988,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   pdl_wait();
 
   const WaitCtl w{abort_flag, g.status, g.wait_limit_ns};
-  const int units = g.slots * g.m_tiles * g.n_tiles;
+  const int units = WIDE ? g.m_tiles * g.wide_q : g.slots * g.m_tiles * g.n_tiles;
   const int cluster_id = static_cast<int>(blockIdx.x >> 1);
   const int nclusters = static_cast<int>(gridDim.x >> 1);
 
@@ -938,7 +1000,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       const bool leader = rank == 0;
       constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
+      auto advance = [&]() {
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      };
+      if constexpr (WIDE) {
+        // One tile per cluster, over the whole K range: A, and B in two pieces (the second at
+        // 128 rows into the stage's B space).
+        const WideUnit wu = decode_wide(cluster_id, g);
+        const int h2 = (wu.width - 256) / 2;  // this CTA's rows of the second B piece
+        const CUtensorMap *mb2 = wu.width == g.wide_bn ? &mapB2 : &mapBr;
+        const int brow1 = wu.n0 + 128 * static_cast<int>(rank);
+        const int brow2 = wu.n0 + 256 + h2 * static_cast<int>(rank);
+        const int arow = wu.m0 * 256 + 128 * static_cast<int>(rank);
+        const uint32_t tx = 2u * (A_BYTES + static_cast<uint32_t>(128 + h2) * BK * 2);  // both CTAs' bytes
+        KCursor kc;
+        kc.start(0, g);
+        for (int kt = 0; cluster_id < units && kt < g.kt_total; ++kt, kc.next()) {
+          if (!wait_bar_spin(empty_bar(stage), phase ^ 1u, w)) {
+            ok = false;
+            break;
+          }
+          int ak, az, bk, bz;
+          kc.coords(g.a_seg, ak, az);
+          kc.coords(g.b_seg, bk, bz);
+          const uint32_t da = smem_u32(sA + stage * A_BYTES), db = smem_u32(sB + stage * B_BYTES);
+          if (leader) {
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, tx);
+            tma_load_3d(da, &mapA, fb, ak, arow, az);
+            tma_load_3d(db, &mapB, fb, bk, brow1, bz);
+            tma_load_3d(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
+          } else {
+            const uint32_t fb = map_to_rank(full_bar(stage), 0);
+            tma_load_3d_pair(da, &mapA, fb, ak, arow, az);
+            tma_load_3d_pair(db, &mapB, fb, bk, brow1, bz);
+            tma_load_3d_pair(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
+          }
+          advance();
+        }
+      }
+      for (int u = cluster_id; !WIDE && u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
         const int arow = t.m * 256 + 128 * static_cast<int>(rank);
         const int brow = t.n * BN + (BN / 2) * static_cast<int>(rank);
@@ -977,12 +1083,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_3d_pair(smem_u32(sA + stage * A_BYTES), &mapA, fb, ak, arow, az);
             tma_load_3d_pair(smem_u32(sB + stage * B_BYTES), &mapB, fb, bk, brow, bz);
           }
-          issued |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          advance();
         }
       }
       if (!ok && issued) {
@@ -1006,7 +1107,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr bool amn = EPI == EPI_F32_MN, bmn = EPI == EPI_F32_MN;
       constexpr uint32_t idesc = IDESC | (amn ? kIdescMnA : 0u) | (bmn ? kIdescMnB : 0u);
       constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
-      for (int u = cluster_id; u < units && ok; u += nclusters) {
+      if constexpr (WIDE) {
+        // The tile's first 256 columns accumulate at TMEM column 0, the rest at 256: each k-step's
+        // two MMAs write different accumulators, so neither waits for the other's result.
+        const WideUnit wu = decode_wide(cluster_id, g);
+        constexpr uint32_t id1 = idesc_bf16_f32(256, 256);
+        const uint32_t id2 = idesc_bf16_f32(256, wu.width - 256);
+        const uint32_t d = tmem_base;
+        for (int kt = 0; cluster_id < units && kt < g.kt_total; ++kt) {
+          if (!wait_bar_spin(full_bar(stage), phase, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * A_BYTES), sb = smem_u32(sB + stage * B_BYTES);
+          const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sb);
+          const uint64_t bd2 = sw128_kmajor_desc(sb + 128 * BK * 2);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint32_t accum = (kt > 0 || k > 0) ? 1u : 0u;
+            tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, id1, accum);
+            tc_mma2_bf16(d + 256u, ad + 2u * k, bd2 + 2u * k, id2, accum);
+          }
+          tc_commit2_multicast(empty_bar(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok && cluster_id < units) tc_commit2_multicast(tfull_bar(0), 0x3);
+      }
+      for (int u = cluster_id; !WIDE && u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
         if (!wait_bar_spin(tempty_bar(acc), acc_phase ^ 1u, w)) break;
         tc_fence_after();
@@ -1047,7 +1178,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t nstore = 0;  // TMA-store chunks this warp issued
-    for (int u = cluster_id; u < units; u += nclusters) {
+    if constexpr (WIDE) {
+      const WideUnit wu = decode_wide(cluster_id, g);
+      const bool ok = cluster_id < units && wait_bar_cluster(tfull_bar(0), 0u, w);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        epilogue_f32_cols(tb, wu.n0, wu.width, wu.m0 * 256 + 128 * static_cast<int>(rank) + q * 32, lane, g, &mapO,
+                          sO + q * 2 * kStoreBufBytes, nstore);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(0), 0));
+      }
+    }
+    for (int u = cluster_id; !WIDE && u < units; u += nclusters) {
       const Unit t = decode_unit(u, g);
       const bool ok = wait_bar_cluster(tfull_bar(acc), acc_phase, w);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -1098,11 +1242,37 @@ cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-template <int EPI>
+// Clusters of the pair kernel <EPI, WIDE> that fit on the GPU at once (pairs of SMs with room for
+// one CTA each), per device, found on the first launch there (one array per instantiation).
+// Atomic, as host threads may launch concurrently; they would store the same value.
+template <int EPI, bool WIDE>
+int pair_capacity(int num_sms) {
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::atomic<int> &slot = max_clusters[dev & 63];
+  int mc = slot.load(std::memory_order_relaxed);
+  if (mc <= 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pair_smem_bytes<EPI, WIDE>();
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tp_gemm_pair_kernel<EPI, WIDE>, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = num_sms / 2;
+    }
+    mc = n;
+    slot.store(n, std::memory_order_relaxed);
+  }
+  return mc;
+}
+
+template <int EPI, bool WIDE = false>
 cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmArgs &g, int num_sms,
-                        cudaStream_t stream) {
-  constexpr size_t smem = pair_smem_bytes<EPI>();
-  auto kern = tp_gemm_pair_kernel<EPI>;
+                        cudaStream_t stream, const CUtensorMap *b2 = nullptr, const CUtensorMap *br = nullptr) {
+  constexpr size_t smem = pair_smem_bytes<EPI, WIDE>();
+  auto kern = tp_gemm_pair_kernel<EPI, WIDE>;
   CUtensorMap o;
   std::memset(&o, 0, sizeof o);
   if constexpr (tma_store_epi<EPI>()) {
@@ -1124,31 +1294,14 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
+  const long long units = WIDE ? static_cast<long long>(g.m_tiles) * g.wide_q
+                               : static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
   if (units <= 0) return cudaSuccess;
-  // Clusters that fit on the GPU at once (pairs of SMs with room for one CTA each), per device,
-  // found on the first launch there (one array per epilogue: this is a template).  Atomic, as
-  // host threads may launch concurrently; they would store the same value.
-  static std::atomic<int> max_clusters[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::atomic<int> &slot = max_clusters[dev & 63];
-  int mc = slot.load(std::memory_order_relaxed);
-  if (mc <= 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = num_sms / 2;
-    }
-    mc = n;
-    slot.store(n, std::memory_order_relaxed);
-  }
+  const int mc = pair_capacity<EPI, WIDE>(num_sms);
+  // the wide schedule runs every unit at once, one per cluster
+  if (WIDE && units > mc) return cudaErrorInvalidConfiguration;
   const int clusters = static_cast<int>(units < mc ? units : mc);
-  return launch_dependent(kern, dim3(2 * clusters), smem, stream, a, b, o, g);
+  return launch_dependent(kern, dim3(2 * clusters), smem, stream, a, b, o, b2 ? *b2 : b, br ? *br : b, g);
 }
 
 template <int BN, int EPI>

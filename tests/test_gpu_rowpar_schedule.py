@@ -1,0 +1,88 @@
+"""The row-parallel GEMM's two tile schedules (tp_set_rowpar_schedule): with
+one TMEM accumulator over all shards, 256-column tiles in rounds of the
+GPU's CTA pairs, or, where they fit one round, wider tiles (two MMAs per
+k-step into two accumulators) of near-equal widths.  Both add every output
+element's products over the same K order in one accumulator, so Z must be
+the same bit for bit; and Z must match the fp64 oracle on sampled rows
+within the bf16 tolerance.  The shapes are ones where the wide schedule
+applies on a 152-SM GB300 (76 CTA pairs): the planner is restated below to
+say which tiles it picks, and on another GPU the comparison still holds."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import mlp_inputs
+from tests.gpu_util import TOL_BF16_ROW_RMS, rowwise_rms_error, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _wide_plan(m_tiles, H, clusters):
+    """Restated schedule choice: each 256-row block cut into q tiles of
+    widths (multiples of 32, differing by at most 32) as many as the clusters
+    allow, each over 256 and at most 480 columns, if the widest is narrower
+    than the columns 256-column tiles put on one cluster.  Returns (widest,
+    tiles of that width, tiles per block) or None."""
+    units = H // 32
+    rounds = -(-m_tiles * (H // 256) // clusters)
+    for q in range(clusters // m_tiles, 0, -1):
+        w1 = -(-units // q)
+        nb = units - q * (w1 - 1)
+        narrowest = w1 if nb == q else w1 - 1
+        if 32 * narrowest <= 256:
+            continue
+        if 32 * w1 > 480:
+            return None
+        return (32 * w1, nb, q) if 32 * w1 < rounds * 256 else None
+    return None
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import linear_sharding_gb300 as tp
+    tp.load_library()
+    yield tp
+    tp.tp_set_rowpar_schedule(True)
+
+
+@pytest.mark.parametrize("act,M,H,F,T", [
+    ("gelu", 2048, 4096, 4096, 4),      # 8 row blocks: 2 tiles of 480 and 7 of 448 each
+    ("swiglu", 1100, 4096, 2048, 2),    # 5 row blocks, ragged: tiles of 320 and 288
+    ("identity", 700, 8192, 1024, 1),   # 3 row blocks: tiles of 352 and 320, T = 1
+    ("gelu", 1900, 4096, 3072, 3),      # ragged last row block, T = 3
+])
+def test_wide_tiles_equal_256_column_tiles(tp, act, M, H, F, T):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    print(f"M={M} H={H}: wide plan on {sms // 2} pairs: {_wide_plan(-(-M // 256), H, sms // 2)}")
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=M + T)
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    X = to_device(d["X"])
+    out = {}
+    for wide in (True, False, True):
+        tp.tp_set_rowpar_schedule(wide)
+        Z = tp.tp_mlp_forward(s, X, variant="tmem_acc")
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0
+        z = Z.cpu().numpy()
+        if wide in out:
+            assert np.array_equal(z, out[wide]), "the wide schedule is not deterministic"
+        out[wide] = z
+    tp.tp_set_rowpar_schedule(True)
+    assert np.array_equal(out[True], out[False]), "wide and 256-column tiles differ"
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([[0, 255, 256, M - 1], rng.choice(M, 12, replace=False)]))
+    ref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act, rows=rows)
+    err = rowwise_rms_error(out[True][rows], ref)
+    print(f"{act} M={M} H={H} T={T}: row-RMS err {err:.3e}")
+    assert err <= TOL_BF16_ROW_RMS
+    s.close()
+
+
+def test_wide_plan_restatement_matches_documented_cases():
+    """The restated planner picks the tiles the header documents (host only)."""
+    assert _wide_plan(8, 4096, 76) == (480, 2, 9)
+    assert _wide_plan(5, 4096, 76) == (320, 2, 14)
+    assert _wide_plan(3, 8192, 76) == (352, 6, 25)
+    assert _wide_plan(16, 4096, 76) is None      # needs more than one round at any width
+    assert _wide_plan(4, 4096, 76) is None       # 64 tiles of 256 already fit one round

@@ -81,6 +81,9 @@ def test_argument_errors_are_status_codes(lib):
     assert lib.tp_set_machine_balance(float("nan")) == 1
     assert lib.tp_set_machine_balance(2e6) == 1
     assert lib.tp_set_machine_balance(280.0) == 0 and lib.tp_set_machine_balance(0.0) == 0
+    lib.tp_set_rowpar_schedule.argtypes = [ctypes.c_int]
+    assert lib.tp_set_rowpar_schedule(2) == 1 and lib.tp_set_rowpar_schedule(-1) == 1
+    assert lib.tp_set_rowpar_schedule(0) == 0 and lib.tp_set_rowpar_schedule(1) == 0
     lib.tp_shards_destroy(None)
 
 
