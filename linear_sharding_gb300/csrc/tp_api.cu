@@ -395,6 +395,42 @@ WidePlan plan_wide(int m_tiles, int64_t H, int clusters) {
   return p;
 }
 
+// A B operand's 3-D tensor as make_map takes it (base, dims, byte strides), for tensor maps of
+// other box heights over it.
+struct BTensor {
+  const void *base;
+  uint64_t d0, d1, d2, s1, s2;
+};
+
+// Launch a CTA-pair GEMM with float32 output and one slot (EPI_F32; its output columns N along
+// B's rows) on the wide schedule when plan_wide has one and tp_set_rowpar_schedule allows it;
+// *done says whether it ran.  b128: the B map with the 128-row box, over `bt`.
+tp_status_t try_wide(const DevState *d, const GemmArgs &g, int64_t N, const CUtensorMap &mapA,
+                     const CUtensorMap &b128, const BTensor &bt, cudaStream_t st, bool *done) {
+  *done = false;
+  if (g_rowpar_wide.load() == 0) return TP_OK;
+  const WidePlan wp = plan_wide(g.m_tiles, N, d->sms / 2);
+  if (wp.bn == 0) return TP_OK;
+  // the same tensor with the row counts of the tiles' second B pieces as boxes
+  CUtensorMap mb2, mbr;
+  TP_TRY(make_map(&mb2, bt.base, bt.d0, bt.d1, bt.d2, bt.s1, bt.s2, static_cast<uint32_t>(wp.bn - 256) / 2));
+  if (wp.nb < wp.q)
+    TP_TRY(make_map(&mbr, bt.base, bt.d0, bt.d1, bt.d2, bt.s1, bt.s2, static_cast<uint32_t>(wp.bn - 288) / 2));
+  else
+    mbr = mb2;
+  GemmArgs gw = g;
+  gw.wide_bn = wp.bn;
+  gw.wide_nb = wp.nb;
+  gw.wide_q = wp.q;
+  const cudaError_t e = launch_gemm_wide(mapA, b128, mb2, mbr, gw, d->sms, st);
+  // fewer clusters fit at once than the schedule needs (a GPU shared with other work): the
+  // caller's 256-column tiles
+  if (e == cudaErrorInvalidConfiguration) return TP_OK;
+  TP_CUDA(e);
+  *done = true;
+  return TP_OK;
+}
+
 // Row-parallel GEMM over T shards into Z, with `slots` accumulation slots
 // (slots > 1: float32 partials in P, then the shard-sum).  A residual is fused
 // into the GEMM's epilogue with one slot, and applied after the shard-sum otherwise.
@@ -424,27 +460,11 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
     g.out2 = res.out_bf16;
   }
   bool done = false;
-  if (pair && epi == EPI_F32 && slots == 1 && g_rowpar_wide.load() != 0) {
-    const WidePlan wp = plan_wide(g.m_tiles, H, d->sms / 2);
-    if (wp.bn > 0) {
-      // the same k-tile-blocked W2 with the row counts of the tiles' second B pieces as boxes
-      CUtensorMap mb2, mbr;
-      TP_TRY(make_map(&mb2, s->w2p, 64, H, g.kt_total, 128, H * 128, (wp.bn - 256) / 2));
-      if (wp.nb < wp.q)
-        TP_TRY(make_map(&mbr, s->w2p, 64, H, g.kt_total, 128, H * 128, (wp.bn - 288) / 2));
-      else
-        mbr = mb2;
-      GemmArgs gw = g;
-      gw.wide_bn = wp.bn;
-      gw.wide_nb = wp.nb;
-      gw.wide_q = wp.q;
-      const cudaError_t e = launch_gemm_wide(mapA, s->map_w2_a, mb2, mbr, gw, d->sms, st);
-      // fewer clusters fit at once than the schedule needs (a GPU shared with other work):
-      // the 256-column tiles below
-      if (e != cudaErrorInvalidConfiguration) TP_CUDA(e);
-      done = e == cudaSuccess;
-    }
-  }
+  if (pair && epi == EPI_F32 && slots == 1)
+    TP_TRY(try_wide(d, g, H, mapA, s->map_w2_a, BTensor{s->w2p, 64, static_cast<uint64_t>(H),
+                                                       static_cast<uint64_t>(g.kt_total), 128,
+                                                       static_cast<uint64_t>(H) * 128},
+                    st, &done));
   if (!done && pair)
     TP_CUDA(launch_gemm(CFG_PAIR_N256, epi, mapA, s->map_w2_a, g, d->sms, st));
   else if (!done)
@@ -654,6 +674,7 @@ struct GemmCall {
   int64_t rows = 0, N = 0;
   int bn = 256, kps = 0, nseg = 1, slots = 1;
   Epi epi = EPI_F32;
+  BTensor bt{};  // B's tensor (base non-null): EPI_F32 with one slot may take the wide schedule
 };
 
 tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStream_t st) {
@@ -670,6 +691,9 @@ tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStrea
   g.b_mn_seg = c.b_mn_seg;
   g.rows_valid = static_cast<int>(c.rows);
   g.cols_valid = static_cast<int>(c.N);
+  bool done = false;
+  if (pair && c.epi == EPI_F32 && c.slots == 1 && c.bt.base) TP_TRY(try_wide(d, g, c.N, *c.a, *c.b_128, c.bt, st, &done));
+  if (done) return TP_OK;
   if (pair) TP_CUDA(launch_gemm(CFG_PAIR_N256, c.epi, *c.a, *c.b_128, g, d->sms, st));
   else TP_CUDA(launch_gemm(cfg_for(c.bn), c.epi, *c.a, *c.b_bn, g, d->sms, st));
   return TP_OK;
@@ -813,6 +837,8 @@ tp_status_t mlp_backward_impl(tp_shards *s, const void *X, const void *Hsave, co
     c.a_seg = 1;
     c.b_bn = &s->map_w1o_bn;
     c.b_128 = &s->map_w1o_128;
+    c.bt = BTensor{s->w1o, static_cast<uint64_t>(ncols), static_cast<uint64_t>(H), 1, static_cast<uint64_t>(ncols) * 2,
+                   static_cast<uint64_t>(H * ncols) * 2};
     c.rows = M;
     c.N = H;
     c.bn = s->bn2;

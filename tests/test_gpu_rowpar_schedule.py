@@ -86,3 +86,29 @@ def test_wide_plan_restatement_matches_documented_cases():
     assert _wide_plan(3, 8192, 76) == (352, 6, 25)
     assert _wide_plan(16, 4096, 76) is None      # needs more than one round at any width
     assert _wide_plan(4, 4096, 76) is None       # 64 tiles of 256 already fit one round
+
+
+def test_backward_dx_wide_tiles_equal_256_column_tiles(tp):
+    """The backward's dX = sum over shards of dP_i W1_i^T has the row-parallel
+    shape and takes the same schedules: dX (and dW1, dW2, which do not depend
+    on it) bit-identical between them."""
+    import torch
+    from synth import f32_to_bf16_bits
+    M, H, F, T, act = 2048, 4096, 4096, 4, "gelu"
+    d = mlp_inputs(M=M, H=H, F=F, act=act, dtype="bf16", seed=9)
+    dZ = to_device(f32_to_bf16_bits(np.random.default_rng(9).standard_normal((M, H)).astype(np.float32)))
+    s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+    tp.tp_shards_enable_backward(s, to_device(d["W1"]), to_device(d["W2"]))
+    X = to_device(d["X"])
+    out = {}
+    for wide in (True, False):
+        tp.tp_set_rowpar_schedule(wide)
+        Z, Hs, Ps = tp.tp_mlp_forward_train(s, X, "auto")
+        grads = tp.tp_mlp_backward(s, X, Hs, Ps, dZ, "auto")
+        torch.cuda.synchronize()
+        assert tp.tp_last_device_status() == 0
+        out[wide] = [Z.cpu().numpy()] + [t.cpu().numpy() for t in grads]
+    tp.tp_set_rowpar_schedule(True)
+    for a, b in zip(out[True], out[False]):
+        assert np.array_equal(a, b)
+    s.close()
