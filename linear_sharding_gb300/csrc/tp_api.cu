@@ -365,34 +365,44 @@ tp_status_t apply_residual(const DevState *d, float *Z, int64_t n, const Residua
 
 // Wide schedule of a row-parallel CTA-pair GEMM with one accumulation slot (launch_gemm_wide):
 // each of the m_tiles 256-row blocks of H columns is cut into q tiles whose widths are multiples
-// of 32 that differ by at most 32 (nb of bn columns, q - nb of bn - 32), with q as large as the
-// clusters allow (one tile each, all at once), every tile wider than 256 columns (two MMAs per
-// k-step into two accumulators) and at most kWideMaxN.  Chosen when its widest tile is narrower
-// than the columns the 256-column tiles put on one cluster over their rounds; bn = 0: none.
-// At M = 2048, H = 4096 on 76 clusters: 128 tiles of 256 columns take two rounds (512 columns a
-// cluster); 8 x 9 tiles of 480 and 448 columns take one (480).
+// of 32 that differ by at most 32 (nb of bn columns, q - nb of bn - 32), every tile wider than 256
+// columns (two MMAs per k-step into two accumulators) and at most kWideMaxN, in one or two rounds
+// of the clusters, q as large as that allows.  A cluster's single accumulator of up to
+// kWideMaxN columns is drained before its next tile starts, so each round after the first
+// exposes one epilogue (priced as 6 k-tiles of a 480-column tile).  Against the 256-column tiles
+// in rounds (their epilogues hidden behind the next tile), with the tensor-pipe activity
+// measured for each form at this size (about 90 % and 80 %), priced in column-k-tiles.  kt: the
+// k-tiles of one tile.  bn = 0: the 256-column tiles.  At M = 2048, H = 4096 on 76 clusters:
+// 128 tiles of 256 columns take two rounds, 8 x 9 tiles of 480 and 448 columns one.
 struct WidePlan {
   int bn = 0, nb = 0, q = 0;
 };
-WidePlan plan_wide(int m_tiles, int64_t H, int clusters) {
-  WidePlan p;
-  if (m_tiles < 1 || H % 256 != 0 || clusters < m_tiles) return p;
+WidePlan plan_wide(int m_tiles, int64_t H, int clusters, int64_t kt) {
+  WidePlan best;
+  if (m_tiles < 1 || H % 256 != 0 || clusters < m_tiles || kt < 1) return best;
   const int64_t units = H / 32;  // 32-column units of a row block
-  const int64_t rounds = cdiv(static_cast<int64_t>(m_tiles) * (H / 256), clusters);
-  for (int64_t q = clusters / m_tiles; q >= 1; --q) {
-    const int64_t w1 = cdiv(units, q);        // widest tile, in units
-    const int64_t nb = units - q * (w1 - 1);  // tiles of w1 units; the others have w1 - 1
-    const int64_t narrowest = nb == q ? w1 : w1 - 1;
-    if (32 * narrowest <= 256) continue;      // a tile this narrow has one MMA: fewer, wider tiles
-    if (32 * w1 > kWideMaxN) break;           // fewer tiles would only be wider
-    if (32 * w1 < rounds * 256) {
-      p.bn = static_cast<int>(32 * w1);
-      p.nb = static_cast<int>(nb);
-      p.q = static_cast<int>(q);
+  const int64_t rounds_u = cdiv(static_cast<int64_t>(m_tiles) * (H / 256), clusters);
+  const double cost_u = static_cast<double>(rounds_u) * 256.0 * kt / 0.80;
+  double best_cost = 0.95 * cost_u;  // the wide tiles must win by 5 %
+  for (int rounds = 1; rounds <= 2; ++rounds) {
+    for (int64_t q = rounds * clusters / m_tiles; q >= 1; --q) {
+      const int64_t w1 = cdiv(units, q);        // widest tile, in units
+      const int64_t nb = units - q * (w1 - 1);  // tiles of w1 units; the others have w1 - 1
+      const int64_t narrowest = nb == q ? w1 : w1 - 1;
+      if (32 * narrowest <= 256) continue;      // a tile this narrow has one MMA: fewer, wider tiles
+      if (32 * w1 > kWideMaxN) break;           // fewer tiles would only be wider
+      const int64_t rounds_w = cdiv(static_cast<int64_t>(m_tiles) * q, clusters);
+      const double cost = static_cast<double>(rounds_w) * 32.0 * w1 * kt / 0.90 + (rounds_w - 1) * 6.0 * 480.0;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best.bn = static_cast<int>(32 * w1);
+        best.nb = static_cast<int>(nb);
+        best.q = static_cast<int>(q);
+      }
+      break;
     }
-    break;
   }
-  return p;
+  return best;
 }
 
 // A B operand's 3-D tensor as make_map takes it (base, dims, byte strides), for tensor maps of
@@ -402,14 +412,15 @@ struct BTensor {
   uint64_t d0, d1, d2, s1, s2;
 };
 
-// Launch a CTA-pair GEMM with float32 output and one slot (EPI_F32; its output columns N along
-// B's rows) on the wide schedule when plan_wide has one and tp_set_rowpar_schedule allows it;
-// *done says whether it ran.  b128: the B map with the 128-row box, over `bt`.
-tp_status_t try_wide(const DevState *d, const GemmArgs &g, int64_t N, const CUtensorMap &mapA,
+// Launch a CTA-pair GEMM with float32 output and one slot (epi EPI_F32 or EPI_F32_RESID; its
+// output columns N along B's rows) on the wide schedule when plan_wide has one and
+// tp_set_rowpar_schedule allows it; *done says whether it ran.  b128: the B map with the
+// 128-row box, over `bt`.
+tp_status_t try_wide(const DevState *d, Epi epi, const GemmArgs &g, int64_t N, const CUtensorMap &mapA,
                      const CUtensorMap &b128, const BTensor &bt, cudaStream_t st, bool *done) {
   *done = false;
   if (g_rowpar_wide.load() == 0) return TP_OK;
-  const WidePlan wp = plan_wide(g.m_tiles, N, d->sms / 2);
+  const WidePlan wp = plan_wide(g.m_tiles, N, d->sms / 2, g.kt_total);
   if (wp.bn == 0) return TP_OK;
   // the same tensor with the row counts of the tiles' second B pieces as boxes
   CUtensorMap mb2, mbr;
@@ -422,11 +433,7 @@ tp_status_t try_wide(const DevState *d, const GemmArgs &g, int64_t N, const CUte
   gw.wide_bn = wp.bn;
   gw.wide_nb = wp.nb;
   gw.wide_q = wp.q;
-  const cudaError_t e = launch_gemm_wide(mapA, b128, mb2, mbr, gw, d->sms, st);
-  // fewer clusters fit at once than the schedule needs (a GPU shared with other work): the
-  // caller's 256-column tiles
-  if (e == cudaErrorInvalidConfiguration) return TP_OK;
-  TP_CUDA(e);
+  TP_CUDA(launch_gemm_wide(epi, mapA, b128, mb2, mbr, gw, d->sms, st));
   *done = true;
   return TP_OK;
 }
@@ -460,8 +467,8 @@ tp_status_t rowpar_tc(const tp_shards *s, const DevState *d, const CUtensorMap &
     g.out2 = res.out_bf16;
   }
   bool done = false;
-  if (pair && epi == EPI_F32 && slots == 1)
-    TP_TRY(try_wide(d, g, H, mapA, s->map_w2_a, BTensor{s->w2p, 64, static_cast<uint64_t>(H),
+  if (pair && slots == 1)
+    TP_TRY(try_wide(d, epi, g, H, mapA, s->map_w2_a, BTensor{s->w2p, 64, static_cast<uint64_t>(H),
                                                        static_cast<uint64_t>(g.kt_total), 128,
                                                        static_cast<uint64_t>(H) * 128},
                     st, &done));
@@ -692,7 +699,8 @@ tp_status_t run_gemm(const DevState *d, const GemmCall &c, GemmArgs g, cudaStrea
   g.rows_valid = static_cast<int>(c.rows);
   g.cols_valid = static_cast<int>(c.N);
   bool done = false;
-  if (pair && c.epi == EPI_F32 && c.slots == 1 && c.bt.base) TP_TRY(try_wide(d, g, c.N, *c.a, *c.b_128, c.bt, st, &done));
+  if (pair && c.epi == EPI_F32 && c.slots == 1 && c.bt.base)
+    TP_TRY(try_wide(d, c.epi, g, c.N, *c.a, *c.b_128, c.bt, st, &done));
   if (done) return TP_OK;
   if (pair) TP_CUDA(launch_gemm(CFG_PAIR_N256, c.epi, *c.a, *c.b_128, g, d->sms, st));
   else TP_CUDA(launch_gemm(cfg_for(c.bn), c.epi, *c.a, *c.b_bn, g, d->sms, st));

@@ -45,14 +45,17 @@ cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUt
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm_wide(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapB2,
+cudaError_t launch_gemm_wide(Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapB2,
                              const CUtensorMap &mapBr, const GemmArgs &args, int num_sms, cudaStream_t stream) {
   // every tile two MMAs (256 columns, then 32 .. kWideMaxN - 256), the widths multiples of 32
   const int narrowest = args.wide_nb == args.wide_q ? args.wide_bn : args.wide_bn - 32;
   if (narrowest <= 256 || args.wide_bn > kWideMaxN || args.wide_bn % 32 != 0 || args.wide_nb < 1 ||
       args.wide_nb > args.wide_q || args.slots != 1)
     return cudaErrorInvalidValue;
-  return launch_pair<EPI_F32, true>(mapA, mapB, args, num_sms, stream, &mapB2, &mapBr);
+  if (epi == EPI_F32) return launch_pair<EPI_F32, true>(mapA, mapB, args, num_sms, stream, &mapB2, &mapBr);
+  if (epi == EPI_F32_RESID)
+    return launch_pair<EPI_F32_RESID, true>(mapA, mapB, args, num_sms, stream, &mapB2, &mapBr);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace tp

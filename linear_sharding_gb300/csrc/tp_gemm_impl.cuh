@@ -293,6 +293,82 @@ __device__ __forceinline__ void ld_global_v8(const void *p, uint32_t *v) {
 
 __device__ __forceinline__ bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
+// Float32 output with the residual of a row-parallel layer (EPI_F32_RESID): `ncols` columns (a
+// multiple of 32) of one accumulator, output row `row` (this thread's TMEM lane), columns
+// n0 .. : out = acc (+ float32 residual aux) (+ bf16 residual aux2), and with out2 its bf16.
+__device__ __forceinline__ void epilogue_resid_cols(uint32_t tb, int row, long long n0, int ncols,
+                                                    const GemmArgs &g) {
+  const bool valid = row < g.rows_valid;
+  const long long off = static_cast<long long>(row) * g.ld_out + n0;
+  float *out = static_cast<float *>(g.out) + off;
+  const float *addf = static_cast<const float *>(g.aux);
+  const __nv_bfloat16 *addb = static_cast<const __nv_bfloat16 *>(g.aux2);
+  __nv_bfloat16 *outb = static_cast<__nv_bfloat16 *>(g.out2);
+  // the float32 rows (output and residual) move 32 bytes at a time when aligned
+  const bool wide = aligned32(out) && (!addf || aligned32(addf + off));
+#pragma unroll 1
+  for (int c = 0; c < ncols / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tb + c * 32, r);
+    tmem_ld_wait();
+    if (!valid) continue;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if (addf && wide) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t x[8];
+        ld_global_v8(addf + off + c * 32 + 8 * j, x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[8 * j + k] += __uint_as_float(x[k]);
+      }
+    } else if (addf) {
+      const float4 *a = reinterpret_cast<const float4 *>(addf + off + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = a[j];
+        v[4 * j] += x.x;
+        v[4 * j + 1] += x.y;
+        v[4 * j + 2] += x.z;
+        v[4 * j + 3] += x.w;
+      }
+    }
+    if (addb) {
+      const uint4 *a = reinterpret_cast<const uint4 *>(addb + off + c * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = a[j];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * j + 2 * k] += __uint_as_float(w[k] << 16);
+          v[8 * j + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      }
+    }
+    if (wide) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = __float_as_uint(v[8 * j + k]);
+        st_global_v8(out + c * 32 + 8 * j, x);
+      }
+    } else {
+      float4 *d = reinterpret_cast<float4 *>(out + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (outb) {
+      uint32_t vb[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) vb[j] = __float_as_uint(v[j]);
+      store_act32<EPI_IDENT_BF16>(outb + off + c * 32, vb);
+    }
+  }
+}
+
 // Epilogue of one tile by the 128 epilogue threads: each thread owns TMEM
 // lane `row_in_tile`, i.e. output row row0 + row_in_tile; `tb` addresses that
 // lane's quarter at the accumulator's first column.
@@ -334,76 +410,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
       }
     }
   } else if constexpr (EPI == EPI_F32_RESID) {
-    const int row = row0 + row_in_tile;
-    const bool valid = row < g.rows_valid;
-    const long long off = static_cast<long long>(row) * g.ld_out + static_cast<long long>(t.n) * BN;
-    float *out = static_cast<float *>(g.out) + off;
-    const float *addf = static_cast<const float *>(g.aux);
-    const __nv_bfloat16 *addb = static_cast<const __nv_bfloat16 *>(g.aux2);
-    __nv_bfloat16 *outb = static_cast<__nv_bfloat16 *>(g.out2);
-    // the float32 rows (output and residual) move 32 bytes at a time when aligned
-    const bool wide = aligned32(out) && (!addf || aligned32(addf + off));
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tb + c * 32, r);
-      tmem_ld_wait();
-      if (!valid) continue;
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      if (addf && wide) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t x[8];
-          ld_global_v8(addf + off + c * 32 + 8 * j, x);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) v[8 * j + k] += __uint_as_float(x[k]);
-        }
-      } else if (addf) {
-        const float4 *a = reinterpret_cast<const float4 *>(addf + off + c * 32);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 x = a[j];
-          v[4 * j] += x.x;
-          v[4 * j + 1] += x.y;
-          v[4 * j + 2] += x.z;
-          v[4 * j + 3] += x.w;
-        }
-      }
-      if (addb) {
-        const uint4 *a = reinterpret_cast<const uint4 *>(addb + off + c * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 x = a[j];
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[8 * j + 2 * k] += __uint_as_float(w[k] << 16);
-            v[8 * j + 2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
-          }
-        }
-      }
-      if (wide) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t x[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) x[k] = __float_as_uint(v[8 * j + k]);
-          st_global_v8(out + c * 32 + 8 * j, x);
-        }
-      } else {
-        float4 *d = reinterpret_cast<float4 *>(out + c * 32);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      }
-      if (outb) {
-        uint32_t vb[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) vb[j] = __float_as_uint(v[j]);
-        store_act32<EPI_IDENT_BF16>(outb + off + c * 32, vb);
-      }
-    }
+    epilogue_resid_cols(tb, row0 + row_in_tile, t.n * BN, BN, g);
   } else if constexpr (EPI == EPI_SWIGLU_BF16) {
     constexpr int HALF = BN / 2;
     const int row = row0 + row_in_tile;
@@ -909,10 +916,10 @@ __device__ __forceinline__ void epilogue_tile_tma(uint32_t tb, const Unit &t, in
   }
 }
 
-// WIDE: the wide row-parallel schedule (EPI_F32 only): one tile per cluster, of up to kWideMaxN
-// columns, as two MMAs per k-step (256 columns into TMEM columns 0 .., the rest into 256 ..),
-// each CTA loading its half of both B pieces (mapB: 128 rows; the second piece's half with mapB2
-// for the wide_bn-column tiles, mapBr for the 32 narrower ones).
+// WIDE: the wide row-parallel schedule (EPI_F32 and EPI_F32_RESID): tiles of up to kWideMaxN
+// columns, one per cluster at a time, as two MMAs per k-step (256 columns into TMEM columns 0 ..,
+// the rest into 256 ..), each CTA loading its half of both B pieces (mapB: 128 rows; the second
+// piece's half with mapB2 for the wide_bn-column tiles, mapBr for the 32 narrower ones).
 template <int EPI, bool WIDE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tp_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -920,7 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapO,
                         const __grid_constant__ CUtensorMap mapB2,
                         const __grid_constant__ CUtensorMap mapBr, const GemmArgs g) {
-  static_assert(!WIDE || EPI == EPI_F32, "the wide schedule has the float32 epilogue only");
+  static_assert(!WIDE || EPI == EPI_F32 || EPI == EPI_F32_RESID, "the wide schedule has the float32 epilogues only");
   constexpr int STAGES = pair_stages<EPI, WIDE>();
   constexpr int BN = kPairBN;
   constexpr uint32_t A_BYTES = 128 * BK * 2;
@@ -1009,39 +1016,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       };
       if constexpr (WIDE) {
-        // One tile per cluster, over the whole K range: A, and B in two pieces (the second at
-        // 128 rows into the stage's B space).
-        const WideUnit wu = decode_wide(cluster_id, g);
-        const int h2 = (wu.width - 256) / 2;  // this CTA's rows of the second B piece
-        const CUtensorMap *mb2 = wu.width == g.wide_bn ? &mapB2 : &mapBr;
-        const int brow1 = wu.n0 + 128 * static_cast<int>(rank);
-        const int brow2 = wu.n0 + 256 + h2 * static_cast<int>(rank);
-        const int arow = wu.m0 * 256 + 128 * static_cast<int>(rank);
-        const uint32_t tx = 2u * (A_BYTES + static_cast<uint32_t>(128 + h2) * BK * 2);  // both CTAs' bytes
-        KCursor kc;
-        kc.start(0, g);
-        for (int kt = 0; cluster_id < units && kt < g.kt_total; ++kt, kc.next()) {
-          if (!wait_bar_spin(empty_bar(stage), phase ^ 1u, w)) {
-            ok = false;
-            break;
+        // Each unit (tile) over the whole K range: A, and B in two pieces (the second at 128
+        // rows into the stage's B space).
+        for (int u = cluster_id; u < units && ok; u += nclusters) {
+          const WideUnit wu = decode_wide(u, g);
+          const int h2 = (wu.width - 256) / 2;  // this CTA's rows of the second B piece
+          const CUtensorMap *mb2 = wu.width == g.wide_bn ? &mapB2 : &mapBr;
+          const int brow1 = wu.n0 + 128 * static_cast<int>(rank);
+          const int brow2 = wu.n0 + 256 + h2 * static_cast<int>(rank);
+          const int arow = wu.m0 * 256 + 128 * static_cast<int>(rank);
+          const uint32_t tx = 2u * (A_BYTES + static_cast<uint32_t>(128 + h2) * BK * 2);  // both CTAs' bytes
+          KCursor kc;
+          kc.start(0, g);
+          for (int kt = 0; kt < g.kt_total; ++kt, kc.next()) {
+            if (!wait_bar_spin(empty_bar(stage), phase ^ 1u, w)) {
+              ok = false;
+              break;
+            }
+            int ak, az, bk, bz;
+            kc.coords(g.a_seg, ak, az);
+            kc.coords(g.b_seg, bk, bz);
+            const uint32_t da = smem_u32(sA + stage * A_BYTES), db = smem_u32(sB + stage * B_BYTES);
+            if (leader) {
+              const uint32_t fb = full_bar(stage);
+              mbar_arrive_expect_tx(fb, tx);
+              tma_load_3d(da, &mapA, fb, ak, arow, az);
+              tma_load_3d(db, &mapB, fb, bk, brow1, bz);
+              tma_load_3d(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
+            } else {
+              const uint32_t fb = map_to_rank(full_bar(stage), 0);
+              tma_load_3d_pair(da, &mapA, fb, ak, arow, az);
+              tma_load_3d_pair(db, &mapB, fb, bk, brow1, bz);
+              tma_load_3d_pair(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
+            }
+            advance();
           }
-          int ak, az, bk, bz;
-          kc.coords(g.a_seg, ak, az);
-          kc.coords(g.b_seg, bk, bz);
-          const uint32_t da = smem_u32(sA + stage * A_BYTES), db = smem_u32(sB + stage * B_BYTES);
-          if (leader) {
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, tx);
-            tma_load_3d(da, &mapA, fb, ak, arow, az);
-            tma_load_3d(db, &mapB, fb, bk, brow1, bz);
-            tma_load_3d(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
-          } else {
-            const uint32_t fb = map_to_rank(full_bar(stage), 0);
-            tma_load_3d_pair(da, &mapA, fb, ak, arow, az);
-            tma_load_3d_pair(db, &mapB, fb, bk, brow1, bz);
-            tma_load_3d_pair(db + 128 * BK * 2, mb2, fb, bk, brow2, bz);
-          }
-          advance();
         }
       }
       for (int u = cluster_id; !WIDE && u < units && ok; u += nclusters) {
@@ -1108,34 +1117,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = IDESC | (amn ? kIdescMnA : 0u) | (bmn ? kIdescMnB : 0u);
       constexpr uint32_t astep = amn ? 128u : 2u, bstep = bmn ? 128u : 2u;
       if constexpr (WIDE) {
-        // The tile's first 256 columns accumulate at TMEM column 0, the rest at 256: each k-step's
-        // two MMAs write different accumulators, so neither waits for the other's result.
-        const WideUnit wu = decode_wide(cluster_id, g);
+        // A tile's first 256 columns accumulate at TMEM column 0, the rest at 256: each k-step's
+        // two MMAs write different accumulators, so neither waits for the other's result.  One
+        // accumulator of up to kWideMaxN columns: a unit after the first waits until the
+        // epilogue has drained the one before.
         constexpr uint32_t id1 = idesc_bf16_f32(256, 256);
-        const uint32_t id2 = idesc_bf16_f32(256, wu.width - 256);
         const uint32_t d = tmem_base;
-        for (int kt = 0; cluster_id < units && kt < g.kt_total; ++kt) {
-          if (!wait_bar_spin(full_bar(stage), phase, w)) {
-            ok = false;
-            break;
-          }
+        uint32_t tphase = 0;
+        for (int u = cluster_id; u < units && ok; u += nclusters) {
+          const WideUnit wu = decode_wide(u, g);
+          const uint32_t id2 = idesc_bf16_f32(256, wu.width - 256);
+          if (!wait_bar_spin(tempty_bar(0), tphase ^ 1u, w)) break;
           tc_fence_after();
-          const uint32_t sa = smem_u32(sA + stage * A_BYTES), sb = smem_u32(sB + stage * B_BYTES);
-          const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sb);
-          const uint64_t bd2 = sw128_kmajor_desc(sb + 128 * BK * 2);
+          for (int kt = 0; kt < g.kt_total; ++kt) {
+            if (!wait_bar_spin(full_bar(stage), phase, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sA + stage * A_BYTES), sb = smem_u32(sB + stage * B_BYTES);
+            const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sb);
+            const uint64_t bd2 = sw128_kmajor_desc(sb + 128 * BK * 2);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint32_t accum = (kt > 0 || k > 0) ? 1u : 0u;
-            tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, id1, accum);
-            tc_mma2_bf16(d + 256u, ad + 2u * k, bd2 + 2u * k, id2, accum);
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint32_t accum = (kt > 0 || k > 0) ? 1u : 0u;
+              tc_mma2_bf16(d, ad + 2u * k, bd + 2u * k, id1, accum);
+              tc_mma2_bf16(d + 256u, ad + 2u * k, bd2 + 2u * k, id2, accum);
+            }
+            tc_commit2_multicast(empty_bar(stage), 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit2_multicast(empty_bar(stage), 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit2_multicast(tfull_bar(0), 0x3);
+          tphase ^= 1u;
         }
-        if (ok && cluster_id < units) tc_commit2_multicast(tfull_bar(0), 0x3);
       }
       for (int u = cluster_id; !WIDE && u < units && ok; u += nclusters) {
         const Unit t = decode_unit(u, g);
@@ -1179,16 +1197,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t nstore = 0;  // TMA-store chunks this warp issued
     if constexpr (WIDE) {
-      const WideUnit wu = decode_wide(cluster_id, g);
-      const bool ok = cluster_id < units && wait_bar_cluster(tfull_bar(0), 0u, w);
-      if (__all_sync(0xffffffffu, ok)) {
+      uint32_t tphase = 0;
+      for (int u = cluster_id; u < units; u += nclusters) {
+        const WideUnit wu = decode_wide(u, g);
+        const bool ok = wait_bar_cluster(tfull_bar(0), tphase, w);
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        epilogue_f32_cols(tb, wu.n0, wu.width, wu.m0 * 256 + 128 * static_cast<int>(rank) + q * 32, lane, g, &mapO,
-                          sO + q * 2 * kStoreBufBytes, nstore);
+        if constexpr (EPI == EPI_F32)
+          epilogue_f32_cols(tb, wu.n0, wu.width, wu.m0 * 256 + 128 * static_cast<int>(rank) + q * 32, lane, g,
+                            &mapO, sO + q * 2 * kStoreBufBytes, nstore);
+        else
+          epilogue_resid_cols(tb, wu.m0 * 256 + 128 * static_cast<int>(rank) + row_in_tile, wu.n0, wu.width, g);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(0), 0));
+        tphase ^= 1u;
       }
     }
     for (int u = cluster_id; !WIDE && u < units; u += nclusters) {
@@ -1298,8 +1322,6 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const GemmAr
                                : static_cast<long long>(g.slots) * g.m_tiles * g.n_tiles;
   if (units <= 0) return cudaSuccess;
   const int mc = pair_capacity<EPI, WIDE>(num_sms);
-  // the wide schedule runs every unit at once, one per cluster
-  if (WIDE && units > mc) return cudaErrorInvalidConfiguration;
   const int clusters = static_cast<int>(units < mc ? units : mc);
   return launch_dependent(kern, dim3(2 * clusters), smem, stream, a, b, o, b2 ? *b2 : b, br ? *br : b, g);
 }

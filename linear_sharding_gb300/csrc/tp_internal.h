@@ -72,8 +72,8 @@ struct GemmArgs {
   int head_dim;             // EPI_QKV_HEADS_BF16: columns per head
   int n_heads;              // EPI_QKV_HEADS_BF16: heads over all shards
   // Wide row-parallel schedule (launch_gemm_wide): each 256-row block of the output is cut into
-  // wide_q tiles, wide_nb of wide_bn columns and the others of wide_bn - 32; every cluster runs
-  // one tile.
+  // wide_q tiles, wide_nb of wide_bn columns and the others of wide_bn - 32; a cluster runs one
+  // tile at a time.
   int wide_bn, wide_nb, wide_q;
 };
 
@@ -106,13 +106,12 @@ bool encode_store_map(CUtensorMap *m, const void *base, int elem_bytes, uint64_t
 // Launch the tensor-core GEMM.  Returns cudaSuccess or the launch error.
 cudaError_t launch_gemm(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
                         const GemmArgs &args, int num_sms, cudaStream_t stream);
-// The row-parallel GEMM with float32 output (EPI_F32, one slot) on the wide schedule of
-// GemmArgs::wide_*, in one round of CTA pairs.  mapB is the k-tile-blocked B operand with a
-// 128-row box; mapB2 the same tensor with a (wide_bn - 256) / 2-row box and mapBr one with a
-// (wide_bn - 288) / 2-row box (the second B piece of a tile, per CTA).  Returns
-// cudaErrorInvalidConfiguration, launching nothing, when the GPU holds fewer clusters at once
-// than the schedule has tiles.
-cudaError_t launch_gemm_wide(const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapB2,
+// The row-parallel GEMM with float32 output (epi EPI_F32 or EPI_F32_RESID, one slot) on the
+// wide schedule of GemmArgs::wide_*: the tiles in rounds of the CTA pairs that fit on the GPU at
+// once, one tile per pair at a time.  mapB is the k-tile-blocked B operand with a 128-row box;
+// mapB2 the same tensor with a (wide_bn - 256) / 2-row box and mapBr one with a
+// (wide_bn - 288) / 2-row box (the second B piece of a tile, per CTA).
+cudaError_t launch_gemm_wide(Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB, const CUtensorMap &mapB2,
                              const CUtensorMap &mapBr, const GemmArgs &args, int num_sms, cudaStream_t stream);
 // The training epilogues (EPI_*_SAVE_BF16, EPI_D*_BF16); launch_gemm forwards to it.
 cudaError_t launch_gemm_train(GemmCfg cfg, Epi epi, const CUtensorMap &mapA, const CUtensorMap &mapB,
