@@ -10,12 +10,12 @@
 // which is the softmax-weighted sum of the values for any shift m_r.  Keys
 // are visited 128 at a time and neither scores nor probabilities leave the
 // SM, or even reach shared memory:
-//   warp 0      TMA producer: the Q tile once per unit; K and V tiles of 128
+//   warp 4      TMA producer: the Q tile once per unit; K and V tiles of 128
 //               keys through 3-deep rings, keys up to three tiles ahead of
 //               values (odd units of a CTA walk their key tiles downwards).  Q, K and V are all head-major [heads][M][128]; V is
 //               the P V product's B operand read MN-major (its K, the key
 //               axis, is the outer one);
-//   warp 1      TMEM allocation; one thread issues S_j = Q K_j^T (tcgen05,
+//   warp 5      TMEM allocation; one thread issues S_j = Q K_j^T (tcgen05,
 //               128 x 128, K = 128) into one of three S/P buffers, up to three
 //               key tiles ahead: S_{j+3} goes into buffer j % 3 once P_j V_j
 //               has read it;
@@ -23,10 +23,17 @@
 //               shared memory).  Two issuing threads: each one's waits and
 //               commits overlap the other's MMAs, so the tensor core is fed
 //               while either waits;
-//   warps 2..5  softmax: one thread per query row (TMEM lane = row) reads the
+//   warps 0..3  softmax: one thread per query row (TMEM lane = row) reads the
 //               row of S_j, takes its maximum, writes P = 2^(t - m_r) as bf16
 //               over the upper 64 columns of the same buffer, and adds the
-//               float32 weights to the row sum.
+//               float32 weights to the row sum; at a unit's end it hands the
+//               row sum to the output warps and goes on to the next unit;
+//   warps 8..11 output: once a unit's last P V is done, read O out of tensor
+//               memory (which frees it for the next unit's first P V) and
+//               store O / l as bf16, while the softmax warps already work on
+//               the next unit (warp 7 is idle).
+// The softmax warpgroup runs with 256 registers a thread, the others with
+// fewer (setmaxnreg), within the 168 a thread the CTA is launched with.
 // With S computed ahead, the softmax of key tile j + 1 starts as soon as that
 // of tile j ends: neither waits for the other's hand-off, and the tensor core
 // has a whole S and P V (1024 cycles) per 128-key step beside it.  The shift
@@ -49,8 +56,13 @@ namespace tp {
 namespace {
 
 constexpr int kTile = 128;                // queries per tile, keys per step
-constexpr int kThreads = 224;             // producer, S issuer, 4 softmax warps, P V issuer
+constexpr int kThreads = 384;             // softmax | producer, S issuer, P V issuer, idle | output
 constexpr int kSoftmaxThreads = 128;
+constexpr int kOutThreads = 128;
+// registers a thread per warpgroup after setmaxnreg: softmax, issuers, output.  Their sum over
+// 128 threads each (63488) stays within the launch's 384 x 168 = 64512.
+constexpr int kRegsSoftmax = 256, kRegsIssue = 104, kRegsOut = 136;
+static_assert(128 * (kRegsSoftmax + kRegsIssue + kRegsOut) <= kThreads * 168, "register split exceeds the launch");
 constexpr int kSbuf = 3;                  // S/P buffers in tensor memory: S runs up to 3 steps ahead
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
 constexpr uint32_t kTileBytes = 2 * kSub; // 128 x 128 bf16
@@ -59,8 +71,8 @@ static_assert(kSbuf <= kKst, "the producer copies K up to kSbuf tiles ahead, int
 constexpr int kBars = 32;
 constexpr float kRescaleGap = 8.0f;       // log2 of the largest unnormalised probability
 
-// Q | K[kKst] | V[kVst] | barriers
-constexpr size_t kSmemBytes = 1024 + (1 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16;
+// Q | K[kKst] | V[kVst] | barriers | TMEM address, abort flag | row sums (2 x 128 floats)
+constexpr size_t kSmemBytes = 1024 + (1 + kKst + kVst) * static_cast<size_t>(kTileBytes) + kBars * 8 + 16 + 2 * 128 * 4;
 static_assert(kSmemBytes <= 232448, "attention tiles exceed the shared memory of one CTA");
 
 // TMEM columns: S/P buffer b at 128 b (b < 3), O at 384
@@ -139,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sV + kVst * kTileBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBars);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+  float *l_buf = reinterpret_cast<float *>(tmem_slot + 4);  // [2][128]: a unit's row sums
   const uint32_t b0 = smem_u32(bars);
   // barrier i at b0 + 8 i
   const uint32_t q_full = b0, q_empty = b0 + 8;
@@ -151,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_free = [&](int b) { return b0 + 160 + 8u * b; };   // kSbuf: P V of buffer b done (P read)
   const uint32_t o_full = b0 + 184, o_free = b0 + 192;      // the unit's last P V done; O read out
   const uint32_t drain = b0 + 200, drain_pv = b0 + 208, never = b0 + 216;
+  auto l_full = [&](uint32_t p) { return b0 + 224 + 8u * p; };   // 2: row sums of a unit written
+  auto l_empty = [&](uint32_t p) { return b0 + 240 + 8u * p; };  // 2: row sums read
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -170,19 +185,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_free(b), 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_free, kSoftmaxThreads);
+    mbar_init(o_free, kOutThreads);
+    for (uint32_t p = 0; p < 2; ++p) {
+      mbar_init(l_full(p), kSoftmaxThreads);
+      mbar_init(l_empty(p), kOutThreads);
+    }
     mbar_init(drain, 1);
     mbar_init(drain_pv, 1);
     mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 4 && lane == 0) {
     prefetch_tmap(&mapQ);
     prefetch_tmap(&mapK);
     prefetch_tmap(&mapV);
   }
-  if (warp == 1) {
+  if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -196,151 +215,156 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl w{abort_flag, a.status, a.wait_limit_ns};
   const int units = a.heads * a.m_tiles;
   const int G = gridDim.x, b = blockIdx.x;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer ----
-      // Loads per unit, by key step: Q, the K tiles of steps 0 .. 2, then for each step j its V
-      // tile and the K tile of step j + 3 (if any).
-      int kc = 0, vc = 0, qc = 0;  // K, V and Q tiles issued so far
-      Ring kr, vr;
-      bool ok = true;
-      auto load_k = [&](const AttnUnit &t, int j) -> bool {
-        if (!wait_bar_wake(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
-        mbar_arrive_expect_tx(k_full(kr.buf), kTileBytes);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
-                      t.head);
-        ++kc;
-        kr.next(kKst);
-        return true;
-      };
-      auto load_v = [&](const AttnUnit &t, int j) -> bool {
-        if (!wait_bar_wake(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
-        mbar_arrive_expect_tx(v_full(vr.buf), kTileBytes);
-        // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
-        for (int h = 0; h < 2; ++h)
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf), c * 64,
-                        j * kTile + h * 64, t.head);
-        ++vc;
-        vr.next(kVst);
-        return true;
-      };
-      for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, b, G);
-        if (u >= units) break;
-        const AttnUnit t = decode(u, a);
-        if (!wait_bar_wake(q_empty, (qc & 1u) ^ 1u, w)) break;
-        mbar_arrive_expect_tx(q_full, kTileBytes);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
-        ++qc;
-        // key step j visits key tile key_tile(k, t, j): every other unit walks down from its last
-        const int pre = t.nk < kSbuf ? t.nk : kSbuf;
-        for (int j = 0; j < pre && ok; ++j) ok = load_k(t, key_tile(k, t, j));
-        for (int j = 0; j < t.nk && ok; ++j) {
-          ok = load_v(t, key_tile(k, t, j));
-          if (ok && j + kSbuf < t.nk) ok = load_k(t, key_tile(k, t, j + kSbuf));
-        }
-      }
-      // Every copy issued completes on its full barrier, consumed or not (after an abort
-      // some are not): wait for the last phase of each before the CTA may exit.
-      if (qc > 0) drain_bar(q_full, (qc - 1) & 1u, a.status);
-      for (int s = 0; s < kKst; ++s) {
-        const int n = (kc - s + kKst - 1) / kKst;  // loads issued into stage s
-        if (n > 0) drain_bar(k_full(s), (n - 1) & 1u, a.status);
-      }
-      for (int s = 0; s < kVst; ++s) {
-        const int n = (vc - s + kVst - 1) / kVst;
-        if (n > 0) drain_bar(v_full(s), (n - 1) & 1u, a.status);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- S issuer: S_j = Q K_j^T into buffer j % 3, once P V has read that buffer's P_{j-3} ----
-      int uc = 0;                          // units started
-      Ring kr;                             // K tile of the next S
-      // bit b: parity of buffer b's next s_free wait (a fresh barrier's previous phase counts as
-      // complete).  Per-buffer phases live in bits of a register, not in an indexed array.
-      uint32_t fph = (1u << kSbuf) - 1u;
-      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
-      for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, b, G);
-        if (u >= units) break;
-        const AttnUnit t = decode(u, a);
-        if (!wait_bar_wake(q_full, uc & 1u, w)) break;
-        for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
-          if (!wait_bar_wake(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_wake(k_full(kr.buf), kr.phase, w)) {
-            ok = false;
-            break;
-          }
-          fph ^= 1u << sb;
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
-          const uint32_t d = tmem + sb * 128;
-#pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + kb * kSub));
-            const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
-#pragma unroll
-            for (int kq = 0; kq < 4; ++kq) tc_mma_bf16(d, ad + 2u * kq, bd + 2u * kq, IDESC, (kb | kq) ? 1u : 0u);
-          }
-          tc_commit(s_full(sb));
-          tc_commit(k_empty(kr.buf));
+  // Roles by warpgroup; each warpgroup first takes its register share (every warp of it, at one
+  // instruction; the softmax's increase waits for the others' decreases).
+  if (warp >= 4 && warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+    if (warp == 4) {
+      if (lane == 0) {
+        // ---- TMA producer ----
+        // Loads per unit, by key step: Q, the K tiles of steps 0 .. 2, then for each step j its V
+        // tile and the K tile of step j + 3 (if any).
+        int kc = 0, vc = 0, qc = 0;  // K, V and Q tiles issued so far
+        Ring kr, vr;
+        bool ok = true;
+        auto load_k = [&](const AttnUnit &t, int j) -> bool {
+          if (!wait_bar_wake(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
+          mbar_arrive_expect_tx(k_full(kr.buf), kTileBytes);
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_3d(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
+                        t.head);
+          ++kc;
           kr.next(kKst);
-        }
-        if (!ok) break;
-        tc_commit(q_empty);  // every S of this unit is issued
-        ++uc;
-      }
-      tc_commit(drain);
-      drain_bar(drain, 0u, a.status);
-    }
-    __syncwarp();
-  } else if (warp == 6) {
-    if (lane == 0) {
-      // ---- P V issuer: O += P_j V_j once the softmax threads have written P_j ----
-      int uc = 0;
-      Ring vr;
-      uint32_t pph = 0;                    // bit b: phase of buffer b's next p_full wait
-      bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
-      for (int k = 0; ok; ++k) {
-        const int u = unit_of(k, b, G);
-        if (u >= units) break;
-        const AttnUnit t = decode(u, a);
-        for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
-          // (for the unit's first key tile, also once the previous unit's O is read out)
-          if (!wait_bar_wake(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_wake(o_free, (uc & 1u) ^ 1u, w)) ||
-              !wait_bar_wake(v_full(vr.buf), vr.phase, w)) {
-            ok = false;
-            break;
-          }
-          pph ^= 1u << sb;
-          tc_fence_after();
-          const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
-          const uint32_t pa = tmem + sb * 128 + 64;  // P: the upper 64 columns, bf16 pairs
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
-            const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
-            tc_mma_bf16_tmem_a(tmem + kOcol, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV, (j | kk) ? 1u : 0u);
-          }
-          tc_commit(s_free(sb));
-          tc_commit(v_empty(vr.buf));
+          return true;
+        };
+        auto load_v = [&](const AttnUnit &t, int j) -> bool {
+          if (!wait_bar_wake(v_empty(vr.buf), vr.phase ^ 1u, w)) return false;
+          mbar_arrive_expect_tx(v_full(vr.buf), kTileBytes);
+          // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
+          for (int h = 0; h < 2; ++h)
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf), c * 64,
+                          j * kTile + h * 64, t.head);
+          ++vc;
           vr.next(kVst);
-          if (j + 1 == t.nk) tc_commit(o_full);
+          return true;
+        };
+        for (int k = 0; ok; ++k) {
+          const int u = unit_of(k, b, G);
+          if (u >= units) break;
+          const AttnUnit t = decode(u, a);
+          if (!wait_bar_wake(q_empty, (qc & 1u) ^ 1u, w)) break;
+          mbar_arrive_expect_tx(q_full, kTileBytes);
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
+          ++qc;
+          // key step j visits key tile key_tile(k, t, j): every other unit walks down from its last
+          const int pre = t.nk < kSbuf ? t.nk : kSbuf;
+          for (int j = 0; j < pre && ok; ++j) ok = load_k(t, key_tile(k, t, j));
+          for (int j = 0; j < t.nk && ok; ++j) {
+            ok = load_v(t, key_tile(k, t, j));
+            if (ok && j + kSbuf < t.nk) ok = load_k(t, key_tile(k, t, j + kSbuf));
+          }
         }
-        if (!ok) break;
-        ++uc;
+        // Every copy issued completes on its full barrier, consumed or not (after an abort
+        // some are not): wait for the last phase of each before the CTA may exit.
+        if (qc > 0) drain_bar(q_full, (qc - 1) & 1u, a.status);
+        for (int s = 0; s < kKst; ++s) {
+          const int n = (kc - s + kKst - 1) / kKst;  // loads issued into stage s
+          if (n > 0) drain_bar(k_full(s), (n - 1) & 1u, a.status);
+        }
+        for (int s = 0; s < kVst; ++s) {
+          const int n = (vc - s + kVst - 1) / kVst;
+          if (n > 0) drain_bar(v_full(s), (n - 1) & 1u, a.status);
+        }
       }
-      tc_commit(drain_pv);
-      drain_bar(drain_pv, 0u, a.status);
+      __syncwarp();
+    } else if (warp == 5) {
+      if (lane == 0) {
+        // ---- S issuer: S_j = Q K_j^T into buffer j % 3, once P V has read that buffer's P_{j-3} ----
+        int uc = 0;                          // units started
+        Ring kr;                             // K tile of the next S
+        // bit b: parity of buffer b's next s_free wait (a fresh barrier's previous phase counts as
+        // complete).  Per-buffer phases live in bits of a register, not in an indexed array.
+        uint32_t fph = (1u << kSbuf) - 1u;
+        bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
+        for (int k = 0; ok; ++k) {
+          const int u = unit_of(k, b, G);
+          if (u >= units) break;
+          const AttnUnit t = decode(u, a);
+          if (!wait_bar_wake(q_full, uc & 1u, w)) break;
+          for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+            if (!wait_bar_wake(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_wake(k_full(kr.buf), kr.phase, w)) {
+              ok = false;
+              break;
+            }
+            fph ^= 1u << sb;
+            tc_fence_after();
+            const uint32_t kbase = smem_u32(sK + kr.buf * kTileBytes);
+            const uint32_t d = tmem + sb * 128;
+  #pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+              const uint64_t ad = sw128_kmajor_desc(smem_u32(sQ + kb * kSub));
+              const uint64_t bd = sw128_kmajor_desc(kbase + kb * kSub);
+  #pragma unroll
+              for (int kq = 0; kq < 4; ++kq) tc_mma_bf16(d, ad + 2u * kq, bd + 2u * kq, IDESC, (kb | kq) ? 1u : 0u);
+            }
+            tc_commit(s_full(sb));
+            tc_commit(k_empty(kr.buf));
+            kr.next(kKst);
+          }
+          if (!ok) break;
+          tc_commit(q_empty);  // every S of this unit is issued
+          ++uc;
+        }
+        tc_commit(drain);
+        drain_bar(drain, 0u, a.status);
+      }
+      __syncwarp();
+    } else if (warp == 6) {
+      if (lane == 0) {
+        // ---- P V issuer: O += P_j V_j once the softmax threads have written P_j ----
+        int uc = 0;
+        Ring vr;
+        uint32_t pph = 0;                    // bit b: phase of buffer b's next p_full wait
+        bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
+        for (int k = 0; ok; ++k) {
+          const int u = unit_of(k, b, G);
+          if (u >= units) break;
+          const AttnUnit t = decode(u, a);
+          for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+            // (for the unit's first key tile, also once the previous unit's O is read out)
+            if (!wait_bar_wake(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_wake(o_free, (uc & 1u) ^ 1u, w)) ||
+                !wait_bar_wake(v_full(vr.buf), vr.phase, w)) {
+              ok = false;
+              break;
+            }
+            pph ^= 1u << sb;
+            tc_fence_after();
+            const uint32_t vbase = smem_u32(sV + vr.buf * kTileBytes);
+            const uint32_t pa = tmem + sb * 128 + 64;  // P: the upper 64 columns, bf16 pairs
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // keys 16 kk ..: their 64-key half, then 2 KiB per 16 keys
+              const uint64_t bd = sw128_mnmajor_desc(vbase + (kk >> 2) * kSub);
+              tc_mma_bf16_tmem_a(tmem + kOcol, pa + 8u * kk, bd + 128u * (kk & 3), IDESC_PV, (j | kk) ? 1u : 0u);
+            }
+            tc_commit(s_free(sb));
+            tc_commit(v_empty(vr.buf));
+            vr.next(kVst);
+            if (j + 1 == t.nk) tc_commit(o_full);
+          }
+          if (!ok) break;
+          ++uc;
+        }
+        tc_commit(drain_pv);
+        drain_bar(drain_pv, 0u, a.status);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else {
-    // ---- softmax and output: warps 2..5 (warp v reads TMEM lanes 32 (v % 4) .. + 31) ----
+  } else if (warp < 4) {
+    // ---- softmax: warps 0..3 (warp v reads TMEM lanes 32 v .. + 31) ----
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int row_in_tile = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ob = tmem + lane_base + kOcol;
@@ -484,11 +508,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(p_full(sbuf));
       }
       if (!ok) break;
-      // read out O / l once the unit's last P V is done
-      if (!wait_all(o_full, uc & 1u)) break;
+      // the row sum to the output warps, through slot uc % 2 (once they have read that slot's
+      // sum of two units before: a fresh barrier's previous phase counts as complete)
+      const uint32_t par = uc & 1u;
+      if (!wait_all(l_empty(par), ((uc >> 1) & 1u) ^ 1u)) break;
+      l_buf[par * 128 + row_in_tile] = l_run;
+      mbar_arrive(l_full(par));
       ++uc;
+    }
+  } else if (warp >= 8) {
+    // ---- output: warps 8..11 (warp v reads TMEM lanes 32 (v % 4) .. + 31) ----
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOut));
+    const int row_in_tile = (warp & 3) * 32 + lane;
+    const uint32_t ob = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kOcol;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool got = wait_bar_wake(bar, parity, w);
+      return __all_sync(0xffffffffu, got);
+    };
+    uint32_t uc = 0;  // units read out
+    for (int k = 0;; ++k) {
+      const int u = unit_of(k, b, G);
+      if (u >= units) break;
+      const AttnUnit t = decode(u, a);
+      const int row = t.mt * kTile + row_in_tile;
+      const uint32_t par = uc & 1u;
+      if (!wait_all(o_full, uc & 1u) || !wait_all(l_full(par), (uc >> 1) & 1u)) break;
       tc_fence_after();
-      const float inv = 1.0f / l_run;
+      const float inv = 1.0f / l_buf[par * 128 + row_in_tile];
+      mbar_arrive(l_empty(par));
       const bool in_row = TP_CHECK((t.head + 1) * static_cast<long long>(kAttnHeadDim) <= a.ldo, a.status);
       __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.O) + static_cast<long long>(row) * a.ldo +
                             static_cast<long long>(t.head) * kAttnHeadDim;
@@ -501,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ob + cc * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
+        if (cc == 3) {
+          // O is read out: the next unit's first P V may overwrite it
+          tc_fence_before();
+          mbar_arrive(o_free);
+        }
         if (row < a.M && in_row) {
           uint32_t p[16];
 #pragma unroll
@@ -516,14 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(o_free);
+      ++uc;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
