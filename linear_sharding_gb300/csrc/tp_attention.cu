@@ -17,8 +17,9 @@
 //               axis, is the outer one);
 //   warp 5      TMEM allocation; one thread issues S_j = Q K_j^T (tcgen05,
 //               128 x 128, K = 128) into one of three S/P buffers, up to three
-//               key tiles ahead: S_{j+3} goes into buffer j % 3 once P_j V_j
-//               has read it;
+//               key tiles ahead: the buffers form one ring over all of a
+//               CTA's key steps, unit after unit, and S_{j+3} goes into the
+//               buffer of S_j once P_j V_j has read it;
 //   warp 6      one thread issues O += P_j V_j (P read from TMEM, V from
 //               shared memory).  Two issuing threads: each one's waits and
 //               commits overlap the other's MMAs, so the tensor core is fed
@@ -61,7 +62,7 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kOutThreads = 128;
 // registers a thread per warpgroup after setmaxnreg: softmax, issuers, output.  Their sum over
 // 128 threads each (63488) stays within the launch's 384 x 168 = 64512.
-constexpr int kRegsSoftmax = 256, kRegsIssue = 104, kRegsOut = 136;
+constexpr int kRegsSoftmax = 248, kRegsIssue = 104, kRegsOut = 144;
 static_assert(128 * (kRegsSoftmax + kRegsIssue + kRegsOut) <= kThreads * 168, "register split exceeds the launch");
 constexpr int kSbuf = 3;                  // S/P buffers in tensor memory: S runs up to 3 steps ahead
 constexpr uint32_t kSub = 128 * 128;      // 128 rows x 64 bf16, swizzled (16 KiB)
@@ -281,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == 5) {
       if (lane == 0) {
-        // ---- S issuer: S_j = Q K_j^T into buffer j % 3, once P V has read that buffer's P_{j-3} ----
+        // ---- S issuer: S_j = Q K_j^T into the next buffer of the ring, once P V has read the
+        // P made three key steps before in that buffer ----
         int uc = 0;                          // units started
+        int sb = 0;                          // buffer of the next S (the ring runs on across units)
         Ring kr;                             // K tile of the next S
         // bit b: parity of buffer b's next s_free wait (a fresh barrier's previous phase counts as
         // complete).  Per-buffer phases live in bits of a register, not in an indexed array.
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u >= units) break;
           const AttnUnit t = decode(u, a);
           if (!wait_bar_wake(q_full, uc & 1u, w)) break;
-          for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+          for (int j = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
             if (!wait_bar_wake(s_free(sb), (fph >> sb) & 1u, w) || !wait_bar_wake(k_full(kr.buf), kr.phase, w)) {
               ok = false;
               break;
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ---- P V issuer: O += P_j V_j once the softmax threads have written P_j ----
         int uc = 0;
+        int sb = 0;                          // buffer of the next P, in the S issuer's order
         Ring vr;
         uint32_t pph = 0;                    // bit b: phase of buffer b's next p_full wait
         bool ok = !(a.wait_limit_ns < kShortLimitNs) || wait_bar_wake(never, 0u, w);
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int u = unit_of(k, b, G);
           if (u >= units) break;
           const AttnUnit t = decode(u, a);
-          for (int j = 0, sb = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
+          for (int j = 0; j < t.nk; ++j, sb = sb + 1 == kSbuf ? 0 : sb + 1) {
             // (for the unit's first key tile, also once the previous unit's O is read out)
             if (!wait_bar_wake(p_full(sb), (pph >> sb) & 1u, w) || (j == 0 && !wait_bar_wake(o_free, (uc & 1u) ^ 1u, w)) ||
                 !wait_bar_wake(v_full(vr.buf), vr.phase, w)) {
@@ -376,13 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = wait_bar_wake(bar, parity, w);
       return __all_sync(0xffffffffu, got);
     };
+    int sbuf = 0, prev = kSbuf - 1;      // buffer of this key step and of the one before (one ring)
     for (int k = 0; ok; ++k) {
       const int u = unit_of(k, b, G);
       if (u >= units) break;
       const AttnUnit t = decode(u, a);
       const int row = t.mt * kTile + row_in_tile;
       float m_used = -INFINITY, l_run = 0.f;
-      for (int j = 0, sbuf = 0, prev = kSbuf - 1; j < t.nk; ++j, prev = sbuf, sbuf = sbuf + 1 == kSbuf ? 0 : sbuf + 1) {
+      for (int j = 0; j < t.nk; ++j, prev = sbuf, sbuf = sbuf + 1 == kSbuf ? 0 : sbuf + 1) {
         const uint32_t sb = tmem + lane_base + sbuf * 128;
         if (!wait_all(s_full(sbuf), (sph >> sbuf) & 1u)) {
           ok = false;
@@ -542,30 +547,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 *dst = reinterpret_cast<uint4 *>(orow);
       // 32-byte stores (whole sectors) where the row is 32-byte aligned, else 16-byte ones
       const bool wide = (reinterpret_cast<uintptr_t>(orow) & 31u) == 0;
+      // the row of O / l as bf16 pairs (64 registers), a chunk of 32 columns at a time; then O is
+      // free for the next unit's first P V, and the stores follow
+      uint32_t p[64];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
         tmem_ld32(ob + cc * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
-        if (cc == 3) {
-          // O is read out: the next unit's first P V may overwrite it
-          tc_fence_before();
-          mbar_arrive(o_free);
-        }
-        if (row < a.M && in_row) {
-          uint32_t p[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            p[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          if (wide) {
-            st_global_v8(orow + cc * 32, p);
-            st_global_v8(orow + cc * 32 + 16, p + 8);
-          } else {
+        for (int i = 0; i < 16; ++i)
+          p[16 * cc + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+      }
+      tc_fence_before();
+      mbar_arrive(o_free);
+      if (row < a.M && in_row) {
+        if (wide) {
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4)
-              dst[cc * 4 + g4] = make_uint4(p[4 * g4], p[4 * g4 + 1], p[4 * g4 + 2], p[4 * g4 + 3]);
-          }
+          for (int q = 0; q < 8; ++q) st_global_v8(orow + 16 * q, p + 8 * q);
+        } else {
+#pragma unroll
+          for (int g4 = 0; g4 < 16; ++g4) dst[g4] = make_uint4(p[4 * g4], p[4 * g4 + 1], p[4 * g4 + 2], p[4 * g4 + 3]);
         }
       }
       ++uc;
