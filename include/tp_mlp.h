@@ -457,15 +457,18 @@ TP_API tp_status_t tp_set_machine_balance(double flop_per_byte);
  * tp_set_rowpar_schedule - how the row-parallel GEMM with one TMEM accumulator
  * over all shards (the all-reduce-sum inside the accumulator, "Slice the
  * matrix itself", section "Mathematical formulation") lays its output tiles
- * over the GPU's CTA pairs.  1 (default): where 256-column tiles would need
- * more than one round of the pairs and tiles of 288..448 columns (plus one
- * narrow tile per 256 rows, two of those per pair) fit in one round with at
- * most 90 % of the columns per pair, the wider tiles (at M = 2048, H = 4096
- * on a 152-SM GB300: 448 columns instead of two rounds of 256).  0: always
- * 256-column tiles.  Both sum every output element over the same K order in
- * one accumulator, so they give identical results.  Other values ->
- * TP_ERR_ARG.  Process-wide; affects calls made after it (workspace sizes do
- * not depend on it).
+ * over the GPU's CTA pairs.  1 (default): where it pays, each 256-row block of
+ * the output is cut into tiles of 288..480 columns (near-equal widths, two
+ * MMAs per k-step into two accumulators) run in one or two rounds of the
+ * pairs, instead of 256-column tiles in more rounds (at M = 2048, H = 4096 on
+ * a 152-SM GB300: one round of 480- and 448-column tiles against two rounds
+ * of 256; at M = 4096, two rounds against four).  Applies to the MLP's
+ * second layer, the training backward's dX, the attention output
+ * projection and the block's row-parallel layers.  0: always 256-column
+ * tiles.  Both sum every output element over the same K order in one
+ * accumulator, so they give identical results.  Other values -> TP_ERR_ARG.
+ * Process-wide; affects calls made after it (workspace sizes do not depend on
+ * it).
  */
 TP_API tp_status_t tp_set_rowpar_schedule(int wide);
 
