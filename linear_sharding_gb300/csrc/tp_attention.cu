@@ -226,14 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Loads per unit, by key step: Q, the K tiles of steps 0 .. 2, then for each step j its V
         // tile and the K tile of step j + 3 (if any).
         int kc = 0, vc = 0, qc = 0;  // K, V and Q tiles issued so far
+        // L2 hints: K and V tiles are read again by the other query tiles of their head (kept),
+        // a Q tile by its unit only
+        const uint64_t keep = policy_evict_last(), once = policy_evict_first();
         Ring kr, vr;
         bool ok = true;
         auto load_k = [&](const AttnUnit &t, int j) -> bool {
           if (!wait_bar_wake(k_empty(kr.buf), kr.phase ^ 1u, w)) return false;
           mbar_arrive_expect_tx(k_full(kr.buf), kTileBytes);
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_3d(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
-                        t.head);
+            tma_load_3d_hint(smem_u32(sK + kr.buf * kTileBytes + kb * kSub), &mapK, k_full(kr.buf), kb * 64, j * kTile,
+                             t.head, keep);
           ++kc;
           kr.next(kKst);
           return true;
@@ -244,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // V_j as four 64 x 64 boxes: keys 64 h .. (16 KiB h), head_dim 64 c .. (8 KiB c)
           for (int h = 0; h < 2; ++h)
             for (int c = 0; c < 2; ++c)
-              tma_load_3d(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf), c * 64,
-                          j * kTile + h * 64, t.head);
+              tma_load_3d_hint(smem_u32(sV + vr.buf * kTileBytes + h * kSub + c * kSub / 2), &mapV, v_full(vr.buf),
+                               c * 64, j * kTile + h * 64, t.head, keep);
           ++vc;
           vr.next(kVst);
           return true;
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar_wake(q_empty, (qc & 1u) ^ 1u, w)) break;
           mbar_arrive_expect_tx(q_full, kTileBytes);
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_3d(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head);
+            tma_load_3d_hint(smem_u32(sQ + kb * kSub), &mapQ, q_full, kb * 64, t.mt * kTile, t.head, once);
           ++qc;
           // key step j visits key tile key_tile(k, t, j): every other unit walks down from its last
           const int pre = t.nk < kSbuf ? t.nk : kSbuf;
