@@ -471,16 +471,6 @@ __device__ __forceinline__ void tmem_reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-// 32 lanes x 2 consecutive columns of 32-bit (thread t gets its lane's two).
-__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t &r0, uint32_t &r1) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
-}
-
-// 32 lanes x 1 column of 32-bit from a register (complete with tmem_st_wait).
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r0) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r0) : "memory");
-}
-
 // 32 lanes x 32 consecutive columns of 32-bit from registers (the inverse of
 // tmem_ld32); complete with tmem_st_wait.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
