@@ -713,7 +713,9 @@ def extras(args, tp, device, peaks) -> dict:
     Qa, Ka, Va = (randn((nh, M, hd), 1.0) for _ in range(3))
     Oa = torch.empty((M, nh * hd), dtype=torch.bfloat16, device=device)
     wsa = torch.empty(tp.tp_attention_workspace_bytes(M, nh, hd), dtype=torch.uint8, device=device)
-    t = _time_calls(lambda: tp.tp_attention_forward(Qa, Ka, Va, True, Oa, wsa), 20)
+    # 200 calls (20 ms) after 20 untimed ones, so that the GPU's clock has settled after the
+    # large GEMMs before it
+    t = _time_calls(lambda: tp.tp_attention_forward(Qa, Ka, Va, True, Oa, wsa), 200, warm=20)
     fl = 2 * 2 * nh * hd * M * (M + 1) / 2
     out["attention_m4096_32x128_causal"] = {"us": round(t * 1e6, 1), "TFLOP/s": round(fl / t / 1e12, 1),
                                              "frac_burst": round(fl / t / 1e12 / burst, 3)}
