@@ -150,3 +150,40 @@ def test_block_wide_tiles_equal_256_column_tiles(tp):
     assert np.array_equal(out[True][0], out[False][0]), "block output differs"
     a.close()
     m.close()
+
+
+def test_random_shapes_both_schedules_agree(tp):
+    """Random shapes around the sizes where the wide tiles apply (256-row blocks from 3 to 16,
+    H from 2048 to 8192, ragged M, every activation, T from 1 to 8): Z from the wide tiles
+    equals Z from 256-column tiles bit for bit, and two sampled rows match the oracle."""
+    import torch
+    rng = np.random.default_rng(2028)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wide_cases = 0
+    for case in range(24):
+        m_tiles = int(rng.integers(3, 17))
+        M = int(rng.integers(256 * (m_tiles - 1) + 1, 256 * m_tiles + 1))
+        H = 256 * int(rng.integers(8, 33))
+        T = int(rng.choice([1, 2, 4, 8]))
+        Fs = 128 * int(rng.integers(1, 4))
+        act = str(rng.choice(["gelu", "swiglu", "identity"]))
+        plan = _wide_plan(m_tiles, H, sms // 2, Fs * T // 64)
+        wide_cases += plan is not None
+        d = mlp_inputs(M=M, H=H, F=Fs * T, act=act, dtype="bf16", seed=500 + case)
+        s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), T, act)
+        X = to_device(d["X"])
+        out = {}
+        for wide in (True, False):
+            tp.tp_set_rowpar_schedule(wide)
+            Z = tp.tp_mlp_forward(s, X, variant="tmem_acc")
+            torch.cuda.synchronize()
+            assert tp.tp_last_device_status() == 0
+            out[wide] = Z.cpu().numpy()
+        tp.tp_set_rowpar_schedule(True)
+        assert np.array_equal(out[True], out[False]), (case, M, H, T, Fs, act, plan)
+        rows = np.array([0, M - 1])
+        ref = oracle.mlp_unsharded(d["X"], d["W1"], d["W2"], act, rows=rows)
+        assert rowwise_rms_error(out[True][rows], ref) <= TOL_BF16_ROW_RMS, (case, M, H, T, act)
+        s.close()
+    print(f"{wide_cases} of 24 random shapes on wide tiles")
+    assert wide_cases >= 6
