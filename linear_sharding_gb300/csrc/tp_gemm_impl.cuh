@@ -798,6 +798,15 @@ __device__ __forceinline__ WideUnit decode_wide(int u, const GemmArgs &g) {
   const int narrow = j - g.wide_nb;
   r.width = narrow < 0 ? g.wide_bn : g.wide_bn - 32;
   r.n0 = narrow < 0 ? j * g.wide_bn : g.wide_nb * g.wide_bn + narrow * (g.wide_bn - 32);
+  // a tile outside the output or of a width the kernel cannot take is a bug in the plan:
+  // report it and run the first tile instead
+  if (!TP_CHECK(r.m0 < g.m_tiles && j < g.wide_q && r.width > 256 && r.width <= kWideMaxN &&
+                    r.n0 + r.width <= g.cols_valid,
+                g.status)) {
+    r.m0 = 0;
+    r.n0 = 0;
+    r.width = g.wide_bn;
+  }
   return r;
 }
 

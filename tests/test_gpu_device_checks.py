@@ -46,6 +46,12 @@ dZ = to_device(mlp_inputs(M=300, H=512, F=2048, act="gelu", dtype="bf16", seed=2
 done("train", Z, Hs, Ps, *tp.tp_mlp_backward(s, X, Hs, Ps, dZ))
 s.close()
 
+# the row-parallel GEMM on wide tiles (three 256-row blocks, H = 8192: 352- and 320-column tiles)
+d = mlp_inputs(M=700, H=8192, F=1024, act="identity", dtype="bf16", seed=8, x_rows=700)
+s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), 1, "identity")
+done("mlp_wide", tp.tp_mlp_forward(s, to_device(d["X"]), "tmem_acc"))
+s.close()
+
 d = mlp_inputs(M=3, H=512, F=2048, act="swiglu", dtype="bf16", seed=3, x_rows=16)
 s = tp.tp_shard_weights(to_device(d["W1"]), to_device(d["W2"]), 4, "swiglu")
 done("decode", tp.tp_mlp_forward(s, to_device(d["X"])))
