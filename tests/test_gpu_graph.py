@@ -23,6 +23,7 @@ def tp():
     (16, 1024, 4096, 4, "swiglu", "auto"),      # decode kernels (split-K, weights as the MMA's A)
     (256, 1024, 4096, 4, "gelu", "tmem_acc"),   # CTA-pair prefill tiles
     (256, 1024, 4096, 4, "gelu", "partials"),   # partials + shard-sum
+    (700, 8192, 1024, 1, "identity", "tmem_acc"),  # wide row-parallel tiles (tensor maps made per call)
 ])
 def test_forward_replays_from_a_cuda_graph(tp, M, H, F, T, act, variant):
     import torch

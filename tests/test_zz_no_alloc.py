@@ -100,6 +100,25 @@ def test_noalloc_decode_shape_fits_and_matches():
     s.close()
 
 
+def test_noalloc_on_wide_row_parallel_tiles():
+    """A prefill shape whose row-parallel GEMM takes the wide tiles (three 256-row blocks,
+    H = 8192): the call equals tp_mlp_forward bit for bit, twice, with another shape run
+    through the scratch in between."""
+    import torch
+    import linear_sharding_gb300 as tp
+    lib = tp.load_library()
+    d, s, X = _problem(tp, "identity", 700, 8192, 1024, 1, seed=91)
+    d2, s2, X2 = _problem(tp, "gelu", 16, 2048, 7168, 8, seed=92)
+    ref = tp.tp_mlp_forward(s, X, variant="auto")
+    torch.cuda.synchronize()
+    ref = ref.cpu().numpy()
+    for _ in range(2):
+        _run(lib, tp, s2, X2, "gelu", 2048)
+        assert np.array_equal(_run(lib, tp, s, X, "identity", 8192), ref)
+    s.close()
+    s2.close()
+
+
 def test_noalloc_refits_a_plan_beyond_its_scratch():
     """Where the AUTO plan's workspace exceeds the scratch, the call runs the
     same pass refitted to it: no float32 partials of the second layer (all
