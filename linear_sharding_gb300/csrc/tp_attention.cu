@@ -12,9 +12,11 @@
 // SM, or even reach shared memory:
 //   warp 4      TMA producer: the Q tile once per unit; K and V tiles of 128
 //               keys through 3-deep rings, keys up to three tiles ahead of
-//               values (odd units of a CTA walk their key tiles downwards).  Q, K and V are all head-major [heads][M][128]; V is
-//               the P V product's B operand read MN-major (its K, the key
-//               axis, is the outer one);
+//               values (odd units of a CTA walk their key tiles downwards);
+//               L2 hints keep K and V (other query tiles of the head read
+//               them again) and not Q.  Q, K and V are all head-major
+//               [heads][M][128]; V is the P V product's B operand read
+//               MN-major (its K, the key axis, is the outer one);
 //   warp 5      TMEM allocation; one thread issues S_j = Q K_j^T (tcgen05,
 //               128 x 128, K = 128) into one of three S/P buffers, up to three
 //               key tiles ahead: the buffers form one ring over all of a
@@ -30,10 +32,10 @@
 //               float32 weights to the row sum; at a unit's end it hands the
 //               row sum to the output warps and goes on to the next unit;
 //   warps 8..11 output: once a unit's last P V is done, read O out of tensor
-//               memory (which frees it for the next unit's first P V) and
-//               store O / l as bf16, while the softmax warps already work on
-//               the next unit (warp 7 is idle).
-// The softmax warpgroup runs with 256 registers a thread, the others with
+//               memory as bf16 O / l (which frees it for the next unit's
+//               first P V) and store it, while the softmax warps already work
+//               on the next unit (warp 7 is idle).
+// The softmax warpgroup runs with 248 registers a thread, the others with
 // fewer (setmaxnreg), within the 168 a thread the CTA is launched with.
 // With S computed ahead, the softmax of key tile j + 1 starts as soon as that
 // of tile j ends: neither waits for the other's hand-off, and the tensor core
