@@ -473,6 +473,18 @@ TP_API tp_status_t tp_set_machine_balance(double flop_per_byte);
 TP_API tp_status_t tp_set_rowpar_schedule(int wide);
 
 /*
+ * tp_rowpar_tiles - the tiles tp_mlp_forward's row-parallel GEMM would use
+ * for M tokens with variant v on the current device and schedule (see
+ * tp_set_rowpar_schedule).  out[3] (host memory): the widest tile's columns,
+ * the number of such tiles per 256-row block, and the tiles per block (the
+ * others 32 columns narrower), or three zeros where the call takes any other
+ * form (256-column tiles, float32 partials, the decode or CUDA-core path).
+ * A query only: nothing is launched.  NULL or foreign handle, M <= 0 or a bad
+ * variant -> TP_ERR_ARG.
+ */
+TP_API tp_status_t tp_rowpar_tiles(tp_shards_t s, int64_t M, tp_variant_t v, int32_t *out);
+
+/*
  * tp_set_wait_limit_ns - limit on every device-side wait (default 2 s) in
  * kernels launched after this call, process-wide.  0 restores the default.
  * A limit below 1 ms is a test limit: the tensor-core kernels then first

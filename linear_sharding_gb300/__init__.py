@@ -39,6 +39,7 @@ EXPORTS = (
     "tp_mlp_forward_train", "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
     "tp_block_workspace_bytes", "tp_block_forward", "tp_attention_workspace_bytes",
     "tp_attention_forward", "tp_inject_alloc_failures", "tp_set_machine_balance", "tp_set_rowpar_schedule",
+    "tp_rowpar_tiles",
 )
 
 _lock = threading.Lock()
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.tp_inject_alloc_failures.argtypes = [i32]
         lib.tp_set_machine_balance.argtypes = [ctypes.c_double]
         lib.tp_set_rowpar_schedule.argtypes = [i32]
+        lib.tp_rowpar_tiles.argtypes = [vp, i64, i32, vp]
         lib.tp_colpar_workspace_bytes.restype = sz
         lib.tp_colpar_workspace_bytes.argtypes = [vp, i64]
         lib.tp_colpar_forward.argtypes = [vp, vp, i64, i32, vp, vp, sz, vp]
@@ -477,6 +479,15 @@ def tp_set_rowpar_schedule(wide: bool) -> None:
     where they fit one round of CTA pairs (True, the default), or always
     256-column tiles (False).  The results are identical."""
     _check(load_library().tp_set_rowpar_schedule(1 if wide else 0), "tp_set_rowpar_schedule")
+
+
+def tp_rowpar_tiles(s: Shards, M: int, variant: str = "auto"):
+    """The row-parallel GEMM's wide tiles for M tokens: (widest tile's columns, tiles of that
+    width per 256-row block, tiles per block), or None where it takes another form."""
+    out = (ctypes.c_int32 * 3)()
+    _check(load_library().tp_rowpar_tiles(s.handle, int(M), VARIANT[variant], ctypes.cast(out, ctypes.c_void_p)),
+           "tp_rowpar_tiles")
+    return tuple(out) if out[0] else None
 
 
 def tp_inject_alloc_failures(count: int) -> None:

@@ -1390,6 +1390,23 @@ size_t tp_rowpar_workspace_bytes(tp_shards_t s, int64_t M, tp_variant_t v) {
   return p.row_bytes;
 }
 
+tp_status_t tp_rowpar_tiles(tp_shards_t s, int64_t M, tp_variant_t v, int32_t *out) {
+  if (!out) return TP_ERR_ARG;
+  out[0] = out[1] = out[2] = 0;
+  DevState *d = nullptr;
+  TP_TRY(check_handle(s, 0, &d));
+  if (M <= 0 || !valid_variant(v)) return TP_ERR_ARG;
+  MlpPlan p;
+  TP_TRY(plan_mlp(s, M, v, d, &p));
+  // the path rowpar_tc takes: tensor cores, CTA pairs, one accumulation slot, float32 output
+  if (p.simt || p.decode || p.slots2 != 1 || !use_pair(s->bn2, M) || g_rowpar_wide.load() == 0) return TP_OK;
+  const WidePlan wp = plan_wide(static_cast<int>(cdiv(M, 256)), s->H, d->sms / 2, s->T * (s->Fs / 64));
+  out[0] = wp.bn;
+  out[1] = wp.nb;
+  out[2] = wp.q;
+  return TP_OK;
+}
+
 tp_status_t tp_rowpar_forward(tp_shards_t s, const void *Y, int64_t M, tp_variant_t v, float *Z,
                               void *workspace, size_t ws_bytes, void *stream) {
   DevState *d = nullptr;

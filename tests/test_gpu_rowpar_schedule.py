@@ -187,3 +187,32 @@ def test_random_shapes_both_schedules_agree(tp):
         s.close()
     print(f"{wide_cases} of 24 random shapes on wide tiles")
     assert wide_cases >= 6
+
+
+def test_library_plan_matches_restatement(tp):
+    """The library's own tile plan (tp_rowpar_tiles) against the restated planner, on 40 random
+    shapes with one TMEM accumulator (M from 257 to 4096, H a multiple of 256 up to 8192), and
+    none under tp_set_rowpar_schedule(False) or on the decode path."""
+    import torch
+    rng = np.random.default_rng(2029)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hits = 0
+    for case in range(40):
+        M = int(rng.integers(257, 4097))
+        H = 256 * int(rng.integers(4, 33))
+        T = int(rng.choice([1, 2, 4, 8]))
+        Fs = 128 * int(rng.integers(1, 4))
+        W1 = torch.zeros((H, Fs * T), dtype=torch.bfloat16, device="cuda")
+        W2 = torch.zeros((Fs * T, H), dtype=torch.bfloat16, device="cuda")
+        s = tp.tp_shard_weights(W1, W2, T, "gelu")
+        want = _wide_plan(-(-M // 256), H, sms // 2, Fs * T // 64)
+        got = tp.tp_rowpar_tiles(s, M, "tmem_acc")
+        assert got == want, (case, M, H, T, Fs, got, want)
+        hits += got is not None
+        tp.tp_set_rowpar_schedule(False)
+        assert tp.tp_rowpar_tiles(s, M, "tmem_acc") is None
+        tp.tp_set_rowpar_schedule(True)
+        assert tp.tp_rowpar_tiles(s, 16, "tmem_acc") is None   # decode path
+        s.close()
+    print(f"{hits} of 40 shapes planned on wide tiles")
+    assert hits >= 5

@@ -84,6 +84,10 @@ def test_argument_errors_are_status_codes(lib):
     lib.tp_set_rowpar_schedule.argtypes = [ctypes.c_int]
     assert lib.tp_set_rowpar_schedule(2) == 1 and lib.tp_set_rowpar_schedule(-1) == 1
     assert lib.tp_set_rowpar_schedule(0) == 0 and lib.tp_set_rowpar_schedule(1) == 0
+    lib.tp_rowpar_tiles.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    out3 = (ctypes.c_int32 * 3)(7, 7, 7)
+    assert lib.tp_rowpar_tiles(None, 16, 0, out3) == 1 and list(out3) == [0, 0, 0]
+    assert lib.tp_rowpar_tiles(None, 16, 0, None) == 1
     lib.tp_shards_destroy(None)
 
 
