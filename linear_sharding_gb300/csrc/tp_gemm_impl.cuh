@@ -236,44 +236,6 @@ __device__ __forceinline__ float silu_grad(float g) {
   return s * (1.0f + g * (1.0f - s));
 }
 
-// 32 consecutive bf16 (16-byte aligned) -> float.
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *src, float (&v)[32]) {
-  const uint4 *p = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 q = p[j];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[8 * j + 2 * k] = __uint_as_float(w[k] << 16);
-      v[8 * j + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// 32 float32 values of one row -> activation -> 32 bf16 at dst (16 B aligned).
-template <int EPI>
-__device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
-  uint32_t p[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-    if (EPI == EPI_GELU_BF16) {
-      a = gelu_erf(a);
-      b = gelu_erf(b);
-    }
-    p[j] = pack_bf16x2(a, b);
-  }
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-}
-
 // 32-byte global accesses: one instruction moves a whole 32-byte sector, where
 // two 16-byte ones would each send half a sector (twice the requests and, for
 // stores, twice the bytes through the crossbar).  The address must be 32-byte
@@ -292,6 +254,60 @@ __device__ __forceinline__ void ld_global_v8(const void *p, uint32_t *v) {
 }
 
 __device__ __forceinline__ bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// 32 consecutive bf16 (16-byte aligned) -> float; two 32-byte loads where the
+// address allows.
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *src, float (&v)[32]) {
+  uint32_t w[16];
+  if (aligned32(src)) {
+    ld_global_v8(src, w);
+    ld_global_v8(src + 16, w + 8);
+  } else {
+    const uint4 *p = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = p[j];
+      w[4 * j] = q.x;
+      w[4 * j + 1] = q.y;
+      w[4 * j + 2] = q.z;
+      w[4 * j + 3] = q.w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    v[2 * k] = __uint_as_float(w[k] << 16);
+    v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 32 float32 values of one row -> activation -> 32 bf16 at dst (16 B aligned;
+// two 32-byte stores where the address allows).
+template <int EPI>
+__device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
+  uint32_t p[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+    if (EPI == EPI_GELU_BF16) {
+      a = gelu_erf(a);
+      b = gelu_erf(b);
+    }
+    p[j] = pack_bf16x2(a, b);
+  }
+  if (aligned32(dst)) {
+    st_global_v8(dst, p);
+    st_global_v8(dst + 16, p + 8);
+  } else {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+  }
+}
 
 // Float32 output with the residual of a row-parallel layer (EPI_F32_RESID): `ncols` columns (a
 // multiple of 32) of one accumulator, output row `row` (this thread's TMEM lane), columns
