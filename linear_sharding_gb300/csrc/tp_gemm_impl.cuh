@@ -152,7 +152,7 @@ constexpr uint32_t kMnBlockBytes = 64 * BK * 2;  // one 64 x 64 box
 // the result to bfloat16, 2^-9 relative); erf(-u) = -erf(u).  Two MUFU operations and a few
 // FMA-pipe ones per value, about half the library erff: the epilogue warps share their SM
 // sub-partitions with the copy-issuing and MMA-issuing threads, so their arithmetic slows the
-// main loop.  gelu_erf and gelu_erf2 (two values with paired float32 operations) round alike.
+// main loop.
 namespace as7126 {
 constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
                 kA4 = -1.453152027f, kA5 = 1.061405429f;
@@ -164,21 +164,7 @@ __device__ __forceinline__ float rcp(float d) {
 }
 }  // namespace as7126
 
-__device__ __forceinline__ float gelu_erf(float x) {
-  using namespace as7126;
-  const float u = x * kRsqrt2, au = fabsf(u);
-  const float t = rcp(fmaf(kP, au, 1.0f));
-  float p = fmaf(t, kA5, kA4);
-  p = fmaf(t, p, kA3);
-  p = fmaf(t, p, kA2);
-  p = fmaf(t, p, kA1);
-  p = p * t;
-  const float e = ex2_approx((au * au) * kNegLog2e);  // e^(-u^2)
-  const float q = fmaf(p, e, -1.0f);                  // -erf(|u|)
-  const float h = x * 0.5f;
-  return fmaf(h, copysignf(fabsf(q), u), h);
-}
-
+// Two values at a time, with paired float32 operations.
 __device__ __forceinline__ float2 gelu_erf2(float2 x) {
   using namespace as7126;
   const float2 u = __fmul2_rn(x, make_float2(kRsqrt2, kRsqrt2));
@@ -209,31 +195,39 @@ __device__ __forceinline__ float2 silu2(float2 g) {
   return __fmul2_rn(g, r);
 }
 
-// GeLU'(y) = Phi(y) + y phi(y);  SiLU'(g) = s (1 + g (1 - s)), s = sigmoid(g).
-// erf(u) by the same formula 7.1.26 as gelu_erf.
-__device__ __forceinline__ float erf_as7126(float u) {
+// GeLU'(y) = Phi(y) + y phi(y), Phi(y) = (1 + erf(y / sqrt 2)) / 2, phi(y) = e^(-y^2 / 2) /
+// sqrt(2 pi); erf by the same formula 7.1.26 as gelu_erf2.  With u = y / sqrt 2 the formula's
+// e^(-u^2) is e^(-y^2 / 2), so one exponential serves both terms: for u >= 0, Phi(y) = 1 - c and
+// for u < 0, Phi(y) = c, where c = (a1 t + ... + a5 t^5) e^(-u^2) / 2 (the coefficients halved,
+// which is exact).  Two values at a time with paired float32 operations.
+namespace as7126 {
+constexpr float kH1 = 0.5f * kA1, kH2 = 0.5f * kA2, kH3 = 0.5f * kA3, kH4 = 0.5f * kA4, kH5 = 0.5f * kA5;
+constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+}  // namespace as7126
+
+__device__ __forceinline__ float2 gelu_grad2(float2 y) {
   using namespace as7126;
-  const float au = fabsf(u);
-  const float t = rcp(fmaf(kP, au, 1.0f));
-  float p = fmaf(t, kA5, kA4);
-  p = fmaf(t, p, kA3);
-  p = fmaf(t, p, kA2);
-  p = fmaf(t, p, kA1);
-  p = p * t;
-  const float q = fmaf(p, ex2_approx((au * au) * kNegLog2e), -1.0f);  // -erf(|u|)
-  return copysignf(fabsf(q), u);
+  const float2 u = __fmul2_rn(y, make_float2(kRsqrt2, kRsqrt2));
+  const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
+  const float2 d = __ffma2_rn(make_float2(kP, kP), au, make_float2(1.0f, 1.0f));
+  const float2 t = make_float2(rcp(d.x), rcp(d.y));
+  float2 p = __ffma2_rn(t, make_float2(kH5, kH5), make_float2(kH4, kH4));
+  p = __ffma2_rn(t, p, make_float2(kH3, kH3));
+  p = __ffma2_rn(t, p, make_float2(kH2, kH2));
+  p = __ffma2_rn(t, p, make_float2(kH1, kH1));
+  p = __fmul2_rn(p, t);
+  const float2 a = __fmul2_rn(__fmul2_rn(au, au), make_float2(kNegLog2e, kNegLog2e));
+  const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+  const float2 c = __fmul2_rn(p, e);
+  const float2 phi_cdf = make_float2(u.x >= 0.0f ? 1.0f - c.x : c.x, u.y >= 0.0f ? 1.0f - c.y : c.y);
+  return __ffma2_rn(__fmul2_rn(y, make_float2(kInvSqrt2Pi, kInvSqrt2Pi)), e, phi_cdf);
 }
 
-// GeLU'(y) = Phi(y) + y phi(y), with erf and the exponential as in the forward epilogue.
-__device__ __forceinline__ float gelu_grad(float y) {
-  return 0.5f * (1.0f + erf_as7126(y * as7126::kRsqrt2)) +
-         y * 0.39894228040143268f * ex2_approx((y * y) * (0.5f * as7126::kNegLog2e));
-}
-
-// SiLU'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g) by the ex2 and rcp approximations.
-__device__ __forceinline__ float silu_grad(float g) {
-  const float s = as7126::rcp(1.0f + ex2_approx(g * as7126::kNegLog2e));
-  return s * (1.0f + g * (1.0f - s));
+// s = sigmoid(g) = 1 / (1 + e^-g) for two values, by the ex2 and rcp approximations; the
+// SwiGLU backward takes SiLU(g) = g s and SiLU'(g) = s (1 + g (1 - s)) from it.
+__device__ __forceinline__ float2 sigmoid2(float2 g) {
+  const float2 a = __fmul2_rn(g, make_float2(as7126::kNegLog2e, as7126::kNegLog2e));
+  return make_float2(as7126::rcp(1.0f + ex2_approx(a.x)), as7126::rcp(1.0f + ex2_approx(a.y)));
 }
 
 // 32-byte global accesses: one instruction moves a whole 32-byte sector, where
@@ -292,12 +286,9 @@ __device__ __forceinline__ void store_act32(__nv_bfloat16 *dst, const uint32_t (
   uint32_t p[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-    if (EPI == EPI_GELU_BF16) {
-      a = gelu_erf(a);
-      b = gelu_erf(b);
-    }
-    p[j] = pack_bf16x2(a, b);
+    float2 v = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    if (EPI == EPI_GELU_BF16) v = gelu_erf2(v);
+    p[j] = pack_bf16x2(v.x, v.y);
   }
   if (aligned32(dst)) {
     st_global_v8(dst, p);
@@ -497,7 +488,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
         load_bf16x32(static_cast<const __nv_bfloat16 *>(g.aux) + off + c * 32, p);
         uint32_t d[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) d[j] = __float_as_uint(__uint_as_float(r[j]) * gelu_grad(p[j]));
+        for (int j = 0; j < 16; ++j) {
+          const float2 gd = __fmul2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                       gelu_grad2(make_float2(p[2 * j], p[2 * j + 1])));
+          d[2 * j] = __float_as_uint(gd.x);
+          d[2 * j + 1] = __float_as_uint(gd.y);
+        }
         store_act32<EPI_IDENT_BF16>(out, d);
       } else {
         float gv[32], uv[32];
@@ -505,10 +501,19 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tb, const Unit &t, int ro
         load_bf16x32(static_cast<const __nv_bfloat16 *>(g.aux2) + off + c * 32, uv);
         uint32_t dg[32], du[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float dh = __uint_as_float(r[j]);
-          dg[j] = __float_as_uint(dh * uv[j] * silu_grad(gv[j]));
-          du[j] = __float_as_uint(dh * silu(gv[j]));
+        for (int j = 0; j < 16; ++j) {
+          const float2 dh = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          const float2 g2 = make_float2(gv[2 * j], gv[2 * j + 1]), u2 = make_float2(uv[2 * j], uv[2 * j + 1]);
+          const float2 sg = sigmoid2(g2);
+          // dg = dh u SiLU'(g), SiLU'(g) = s (1 + g (1 - s));  du = dh SiLU(g) = dh g s
+          const float2 one = make_float2(1.0f, 1.0f);
+          const float2 d1 = __ffma2_rn(g2, __ffma2_rn(sg, make_float2(-1.0f, -1.0f), one), one);
+          const float2 a = __fmul2_rn(__fmul2_rn(dh, u2), __fmul2_rn(sg, d1));
+          const float2 b = __fmul2_rn(dh, __fmul2_rn(g2, sg));
+          dg[2 * j] = __float_as_uint(a.x);
+          dg[2 * j + 1] = __float_as_uint(a.y);
+          du[2 * j] = __float_as_uint(b.x);
+          du[2 * j + 1] = __float_as_uint(b.y);
         }
         store_act32<EPI_IDENT_BF16>(out, dg);
         store_act32<EPI_IDENT_BF16>(static_cast<__nv_bfloat16 *>(g.out2) + off + c * 32, du);
