@@ -121,3 +121,58 @@ def test_backward_full_size_sampled(tp, name):
     print(f"{name}: dW1 col-RMS err {e1:.3e}, dW2 row-RMS err {e2:.3e}")
     assert e1 <= TOL_BF16_GRAD_ROW_RMS and e2 <= TOL_BF16_GRAD_ROW_RMS
     s.close()
+
+
+@pytest.mark.parametrize("M", [256, 100])   # CTA-pair tiles; single-CTA tiles with a ragged M
+def test_activation_gradient_elementwise(tp, M):
+    """The dP epilogue element by element.  With H = F, T = 1 and W1 = W2 = I the
+    pre-activation is X itself, dH = dZ and dX = dP = bf16(dZ * GeLU'(X)), each a
+    single product term, so every element of dX must lie within one bf16 rounding
+    of the fp64 oracle's dZ * GeLU'(X).  X spans [-8, 8] on a grid that includes
+    0 and -0, where Phi(y) switches between its two forms; dZ is a seeded normal
+    draw, so both signs of each factor occur."""
+    H = 256
+    x = np.linspace(-8.0, 8.0, M * H).astype(np.float32).reshape(M, H)
+    x[0, :2] = (0.0, -0.0)
+    X = f32_to_bf16_bits(x)
+    eye = f32_to_bf16_bits(np.eye(H, dtype=np.float32))
+    dZ = _dz(M, H, seed=7 + M)
+    d = {"X": X, "W1": eye, "W2": eye}
+    s, Z, Hs, Ps, dX, dW1, dW2 = _run(tp, d, dZ, 1, "gelu", "auto")
+    ref = oracle.mlp_backward_dx(X, eye, eye, dZ, "gelu")
+    got = dX.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-6 * np.abs(_bits_to_f64(dZ))
+    print(f"M={M}: max |dX - ref| / bound = {np.max(err / np.maximum(bound, 1e-30)):.3f}")
+    assert np.all(err <= bound)
+    s.close()
+
+
+@pytest.mark.parametrize("M", [256, 100])
+def test_swiglu_gradient_elementwise(tp, M):
+    """The SwiGLU backward epilogue element by element.  With H = F, T = 1,
+    W1 = [I | I] and W2 = I, g = u = X and dH = dZ, so dX = bf16(dZ u SiLU'(g)) +
+    bf16(dZ SiLU(g)) summed in float32: each element within one bf16 rounding of
+    each of the two terms of the fp64 oracle's dX (the bound takes the terms'
+    magnitudes from the logistic function, the oracle gives their sum)."""
+    from scipy.special import expit
+    H = 256
+    x = np.linspace(-12.0, 12.0, M * H).astype(np.float32).reshape(M, H)
+    x[0, :2] = (0.0, -0.0)
+    X = f32_to_bf16_bits(x)
+    eye = np.eye(H, dtype=np.float32)
+    W1 = f32_to_bf16_bits(np.concatenate([eye, eye], axis=1))
+    W2 = f32_to_bf16_bits(eye)
+    dZ = _dz(M, H, seed=11 + M)
+    d = {"X": X, "W1": W1, "W2": W2}
+    s, Z, Hs, Ps, dX, dW1, dW2 = _run(tp, d, dZ, 1, "swiglu", "auto")
+    ref = oracle.mlp_backward_dx(X, W1, W2, dZ, "swiglu")
+    got = dX.cpu().numpy().astype(np.float64)
+    xv, dz = _bits_to_f64(X), _bits_to_f64(dZ)
+    sg = expit(xv)
+    terms = np.abs(dz) * (np.abs(xv * sg * (1.0 + xv * (1.0 - sg))) + np.abs(xv * sg))
+    bound = 2.0 ** -8 * terms + 1e-6 * np.abs(dz)
+    err = np.abs(got - ref)
+    print(f"M={M}: max |dX - ref| / bound = {np.max(err / np.maximum(bound, 1e-30)):.3f}")
+    assert np.all(err <= bound)
+    s.close()
