@@ -464,7 +464,10 @@ TP_API tp_status_t tp_set_machine_balance(double flop_per_byte);
  * a 152-SM GB300: one round of 480- and 448-column tiles against two rounds
  * of 256; at M = 4096, two rounds against four).  Applies to the MLP's
  * second layer, the training backward's dX, the attention output
- * projection and the block's row-parallel layers.  0: always 256-column
+ * projection and the block's row-parallel layers; a tile's epilogue is
+ * exposed once per round, so a layer that also adds a residual takes the
+ * wide tiles only where its K is long enough (in the block at M = 4096: the
+ * MLP's down-projection, not the output projection).  0: always 256-column
  * tiles.  Both sum every output element over the same K order in one
  * accumulator, so they give identical results.  Other values -> TP_ERR_ARG.
  * Process-wide; affects calls made after it (workspace sizes do not depend on

@@ -369,7 +369,11 @@ tp_status_t apply_residual(const DevState *d, float *Z, int64_t n, const Residua
 // columns (two MMAs per k-step into two accumulators) and at most kWideMaxN, in one or two rounds
 // of the clusters, q as large as that allows.  A cluster's single accumulator of up to
 // kWideMaxN columns is drained before its next tile starts, so each round after the first
-// exposes one epilogue (priced as 6 k-tiles of a 480-column tile).  Against the 256-column tiles
+// exposes one epilogue, priced as epi_ktiles k-tiles of a 480-column tile: 6 for the float32
+// output, 24 where the epilogue also reads a residual and writes its bf16 copy (timed on one
+// GPU: the block's O-projection, 64 k-tiles at M = 4096, ran faster on 256-column tiles and its
+// MLP down-projection, 256 k-tiles, on the wide ones; the float32 O-projection alone, on the
+// wide ones).  Against the 256-column tiles
 // in rounds (their epilogues hidden behind the next tile), with the tensor-pipe activity
 // measured for each form at this size (about 90 % and 80 %), priced in column-k-tiles.  kt: the
 // k-tiles of one tile.  bn = 0: the 256-column tiles.  At M = 2048, H = 4096 on 76 clusters:
@@ -377,7 +381,8 @@ tp_status_t apply_residual(const DevState *d, float *Z, int64_t n, const Residua
 struct WidePlan {
   int bn = 0, nb = 0, q = 0;
 };
-WidePlan plan_wide(int m_tiles, int64_t H, int clusters, int64_t kt) {
+constexpr double kEpiKtilesF32 = 6.0, kEpiKtilesResid = 24.0;
+WidePlan plan_wide(int m_tiles, int64_t H, int clusters, int64_t kt, double epi_ktiles = kEpiKtilesF32) {
   WidePlan best;
   if (m_tiles < 1 || H % 256 != 0 || clusters < m_tiles || kt < 1) return best;
   const int64_t units = H / 32;  // 32-column units of a row block
@@ -392,7 +397,7 @@ WidePlan plan_wide(int m_tiles, int64_t H, int clusters, int64_t kt) {
       if (32 * narrowest <= 256) continue;      // a tile this narrow has one MMA: fewer, wider tiles
       if (32 * w1 > kWideMaxN) break;           // fewer tiles would only be wider
       const int64_t rounds_w = cdiv(static_cast<int64_t>(m_tiles) * q, clusters);
-      const double cost = static_cast<double>(rounds_w) * 32.0 * w1 * kt / 0.90 + (rounds_w - 1) * 6.0 * 480.0;
+      const double cost = static_cast<double>(rounds_w) * 32.0 * w1 * kt / 0.90 + (rounds_w - 1) * epi_ktiles * 480.0;
       if (cost < best_cost) {
         best_cost = cost;
         best.bn = static_cast<int>(32 * w1);
@@ -420,7 +425,8 @@ tp_status_t try_wide(const DevState *d, Epi epi, const GemmArgs &g, int64_t N, c
                      const CUtensorMap &b128, const BTensor &bt, cudaStream_t st, bool *done) {
   *done = false;
   if (g_rowpar_wide.load() == 0) return TP_OK;
-  const WidePlan wp = plan_wide(g.m_tiles, N, d->sms / 2, g.kt_total);
+  const WidePlan wp = plan_wide(g.m_tiles, N, d->sms / 2, g.kt_total,
+                                epi == EPI_F32_RESID ? kEpiKtilesResid : kEpiKtilesF32);
   if (wp.bn == 0) return TP_OK;
   // the same tensor with the row counts of the tiles' second B pieces as boxes
   CUtensorMap mb2, mbr;

@@ -17,11 +17,12 @@ from tests.gpu_util import TOL_BF16_ROW_RMS, rowwise_rms_error, to_device
 pytestmark = pytest.mark.gpu
 
 
-def _wide_plan(m_tiles, H, clusters, kt):
+def _wide_plan(m_tiles, H, clusters, kt, epi_ktiles=6):
     """Restated schedule choice: each 256-row block cut into q tiles of
     widths (multiples of 32, differing by at most 32), each over 256 and at
     most 480 columns, in one or two rounds of the clusters, q as large as that
-    allows; priced as rounds x width x kt / 0.9 plus 6 x 480 per extra round,
+    allows; priced as rounds x width x kt / 0.9 plus epi_ktiles x 480 per extra
+    round (6 for the float32 output, 24 with a residual in the epilogue),
     against the 256-column tiles' rounds x 256 x kt / 0.8, and taken when at
     least 5 % cheaper.  Returns (widest, tiles of that width, tiles per
     block) or None."""
@@ -38,7 +39,7 @@ def _wide_plan(m_tiles, H, clusters, kt):
             if 32 * w1 > 480:
                 break
             rounds_w = -(-m_tiles * q // clusters)
-            cost = rounds_w * 32 * w1 * kt / 0.9 + (rounds_w - 1) * 6 * 480
+            cost = rounds_w * 32 * w1 * kt / 0.9 + (rounds_w - 1) * epi_ktiles * 480
             if cost < best_cost:
                 best, best_cost = (32 * w1, nb, q), cost
             break
@@ -96,6 +97,11 @@ def test_wide_plan_restatement_matches_documented_cases():
     assert _wide_plan(16, 4096, 76, 64) == (480, 2, 9)    # the block's O-projection
     assert _wide_plan(4, 4096, 76, 256) is None           # 64 tiles of 256 already fit one round
     assert _wide_plan(32, 8192, 76, 448) is None          # many rounds: no width fits two
+    # with a residual in the epilogue (the block at M = 4096): the down-projection's 256 k-tiles
+    # keep the wide tiles, the output projection's 64 do not
+    assert _wide_plan(16, 4096, 76, 256, epi_ktiles=24) == (480, 2, 9)
+    assert _wide_plan(16, 4096, 76, 64, epi_ktiles=24) is None
+    assert _wide_plan(8, 4096, 76, 64, epi_ktiles=24) == (480, 2, 9)   # one round: no exposed epilogue priced
 
 
 def test_backward_dx_wide_tiles_equal_256_column_tiles(tp):
@@ -126,10 +132,11 @@ def test_backward_dx_wide_tiles_equal_256_column_tiles(tp):
 
 def test_block_wide_tiles_equal_256_column_tiles(tp):
     """One transformer block at the attention-projection workload's shapes
-    (M = 4096, 32 heads of 128, T = 8, SwiGLU F = 4H): its O-projection and
-    MLP row-parallel GEMMs, with the residuals in their epilogues, run on two
-    rounds of wide tiles; the block's output and residual stream h must equal
-    the 256-column tiles' bit for bit."""
+    (M = 4096, 32 heads of 128, T = 8, SwiGLU F = 4H): its MLP row-parallel
+    GEMM, with the residual in its epilogue, runs on two rounds of wide tiles
+    (the O-projection, with a K of 64 k-tiles, on 256-column tiles either
+    way); the block's output and residual stream h must equal the 256-column
+    tiles' bit for bit."""
     import torch
     from tests.test_gpu_block import _weights
     M, nh, hd, T = 4096, 32, 128, 8
